@@ -1,0 +1,465 @@
+"""Float64 CPU oracle for sink + window KV attention with RoPE / YaRN.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, ``__graft_entry__.smoke()``
+and ``bench.py``'s CPU-baseline / reference leg may import this module.  The CUDA
+library (``sink_kv_attention_gb300``) never imports it, and this module imports
+nothing from the library: the two share no code.
+
+Everything here is a plain, slow restatement of what the source pages compute,
+in float64 numpy, one function per step, each citing the passage it follows.
+Page names used in the citations:
+
+* "RoPE, scaling, sliding window, attention sinks" (mlinterviewnotes, page 1)
+* "Inference & 128K Long Context" / "KV-Cache Engineering" (GPT-OSS-Lite, page 2)
+* "#2961 rope: --rope-scaling dynamic" (strata pull request, page 3)
+* "Attention Sink 与 Streaming KV Cache" (llm-glossary, page 4)
+
+Precision: float64 throughout, except where a floating-point value decides an
+integer (the int8 requantisation code).  The pages do not fix that precision, so
+the decision is taken in float32, the precision the CUDA kernel uses
+(``quantize_int8_rows``).
+
+Parity status: every function below is pinned by ``tests/test_oracle_*.py``
+against values the pages print, closed forms, invariants or library routines.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# O1. Rotary frequencies: plain RoPE and the YaRN blend.
+# ---------------------------------------------------------------------------
+
+def rope_inv_freq(rotary_dim: int, theta: float) -> np.ndarray:
+    """omega_i = theta ** (-2 i / r) for the r/2 rotary pairs i = 0 .. r/2-1.
+
+    "RoPE, scaling, sliding window, attention sinks", section on RoPE: the
+    ``_compute_inv_freq`` listing, 1 / base ** (arange(0, r, 2) / r).
+    """
+    i = np.arange(rotary_dim // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / rotary_dim)
+
+
+def yarn_correction_dim(num_rotations: float, rotary_dim: int, theta: float,
+                        orig_ctx: int) -> float:
+    """Pair index at which a pair turns ``num_rotations`` times in ``orig_ctx`` tokens.
+
+    "RoPE, scaling, sliding window, attention sinks", "YaRN, precisely":
+    d(n) = r * ln(L0 / (2 pi n)) / (2 ln b).
+    """
+    return (rotary_dim * math.log(orig_ctx / (num_rotations * 2.0 * math.pi))
+            / (2.0 * math.log(theta)))
+
+
+def yarn_correction_range(beta_fast: float, beta_slow: float, rotary_dim: int,
+                          theta: float, orig_ctx: int):
+    """(low, high) = (floor d(beta_fast), ceil d(beta_slow)), clamped to [0, r-1].
+
+    "RoPE, scaling, sliding window, attention sinks", "YaRN, precisely" (the worked
+    band "truncated to [20, 46]") and its first exercise (max(lo, 0), min(hi, r-1)).
+    """
+    low = math.floor(yarn_correction_dim(beta_fast, rotary_dim, theta, orig_ctx))
+    high = math.ceil(yarn_correction_dim(beta_slow, rotary_dim, theta, orig_ctx))
+    return max(low, 0), min(high, rotary_dim - 1)
+
+
+def yarn_linear_ramp(low: float, high: float, n: int) -> np.ndarray:
+    """clamp((i - low) / (high - low), 0, 1) for i < n; high += 0.001 when low == high.
+
+    "RoPE, scaling, sliding window, attention sinks", "YaRN, precisely"
+    (``yarn_linear_ramp_mask``).
+    """
+    if low == high:
+        high = high + 0.001
+    i = np.arange(n, dtype=np.float64)
+    return np.clip((i - low) / (high - low), 0.0, 1.0)
+
+
+def yarn_mscale(factor: float) -> float:
+    """mu = 1 for s <= 1, else 0.1 ln s + 1.
+
+    "RoPE, scaling, sliding window, attention sinks", "YaRN, precisely"
+    (``yarn_get_mscale``; mu(8) = 1.2079).
+    """
+    if factor <= 1.0:
+        return 1.0
+    return 0.1 * math.log(factor) + 1.0
+
+
+def yarn_inv_freq(rotary_dim: int, theta: float, factor: float, orig_ctx: int,
+                  beta_fast: float = 32.0, beta_slow: float = 1.0) -> np.ndarray:
+    """YaRN frequencies: blend of the extrapolated and the interpolated sets.
+
+    "RoPE, scaling, sliding window, attention sinks", "YaRN, precisely": with
+    pos_freq_i = b ** (2i / r), extrapolation = 1 / pos_freq, interpolation =
+    1 / (s pos_freq), mask = (1 - ramp) * extrapolation_factor (= 1), and
+    omega = interpolation * (1 - mask) + extrapolation * mask.
+    """
+    pos_freq = np.power(float(theta),
+                        np.arange(0, rotary_dim, 2, dtype=np.float64) / rotary_dim)
+    extrapolation = 1.0 / pos_freq
+    interpolation = 1.0 / (factor * pos_freq)
+    low, high = yarn_correction_range(beta_fast, beta_slow, rotary_dim, theta, orig_ctx)
+    mask = 1.0 - yarn_linear_ramp(low, high, rotary_dim // 2)
+    return interpolation * (1.0 - mask) + extrapolation * mask
+
+
+@dataclass(frozen=True)
+class RopeSpec:
+    """The rotary configuration: head_dim d_h, rotary_dim r <= d_h, base theta,
+    NeoX or GPT-J pairing, optional YaRN factor (<= 1 means plain RoPE)."""
+    head_dim: int
+    rotary_dim: int
+    theta: float
+    neox: bool = True
+    yarn_factor: float = 1.0
+    yarn_orig_ctx: int = 4096
+    beta_fast: float = 32.0
+    beta_slow: float = 1.0
+
+    def omega(self) -> np.ndarray:
+        """Plain frequencies when the factor is <= 1 ("none"), else the YaRN blend."""
+        if self.yarn_factor <= 1.0:
+            return rope_inv_freq(self.rotary_dim, self.theta)
+        return yarn_inv_freq(self.rotary_dim, self.theta, self.yarn_factor,
+                             self.yarn_orig_ctx, self.beta_fast, self.beta_slow)
+
+    def mscale(self) -> float:
+        return yarn_mscale(self.yarn_factor)
+
+    def with_factor(self, factor: float) -> "RopeSpec":
+        return RopeSpec(self.head_dim, self.rotary_dim, self.theta, self.neox, factor,
+                        self.yarn_orig_ctx, self.beta_fast, self.beta_slow)
+
+
+# ---------------------------------------------------------------------------
+# O2. Rotation of Q or K (never V).
+# ---------------------------------------------------------------------------
+
+def rotary_pairs(rotary_dim: int, neox: bool):
+    """Indices (first, second) of each rotary pair.
+
+    "RoPE, scaling, sliding window, attention sinks", section on RoPE: NeoX pairs
+    element j with j + r/2, GPT-J pairs 2j with 2j+1.
+    """
+    half = rotary_dim // 2
+    if neox:
+        return np.arange(half), np.arange(half) + half
+    return np.arange(0, rotary_dim, 2), np.arange(1, rotary_dim, 2)
+
+
+def rope_rotate(x: np.ndarray, positions: Sequence[int], omega: np.ndarray,
+                mscale: float, rotary_dim: int, neox: bool = True) -> np.ndarray:
+    """Rotate each rotary pair of x by angle P * omega_j and scale it by mscale.
+
+    x has shape [n_tok, H, D] (any H), positions has n_tok entries.  For pair j
+    with elements (x1, x2) and angle a = P omega_j:
+        o1 = mscale (x1 cos a - x2 sin a),  o2 = mscale (x2 cos a + x1 sin a);
+    dims [r, D) pass through unchanged.
+
+    "RoPE, scaling, sliding window, attention sinks": the rotation listing
+    (o1 = x1 cos - x2 sin, o2 = x2 cos + x1 sin), partial rotary (the tail passes
+    through) and the YaRN table whose cos and sin both carry mscale.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = x.copy()
+    first, second = rotary_pairs(rotary_dim, neox)
+    pos = np.asarray(positions, dtype=np.float64).reshape(-1, 1)
+    angle = pos * np.asarray(omega, dtype=np.float64).reshape(1, -1)     # [n_tok, r/2]
+    c = (np.cos(angle) * mscale)[:, None, :]
+    s = (np.sin(angle) * mscale)[:, None, :]
+    x1 = x[..., first]
+    x2 = x[..., second]
+    out[..., first] = x1 * c - x2 * s
+    out[..., second] = x2 * c + x1 * s
+    return out
+
+
+def rerotate(k_a: np.ndarray, positions: Sequence[int], spec_a: RopeSpec,
+             spec_b: RopeSpec) -> np.ndarray:
+    """Turn keys stored rotated under spec A into keys rotated under spec B.
+
+    "#2961 rope: --rope-scaling dynamic", "What it does": one more rotation of each
+    pair by p * (w_B - w_A) and the magnitude ratio mscale_B / mscale_A; this is
+    R_a R_b = R_{a+b} ("Attention Sink 与 Streaming KV Cache", RoPE section).
+    No raw key is needed.
+    """
+    delta = spec_b.omega() - spec_a.omega()
+    return rope_rotate(k_a, positions, delta, spec_b.mscale() / spec_a.mscale(),
+                       spec_a.rotary_dim, spec_a.neox)
+
+
+# ---------------------------------------------------------------------------
+# int8 keys with one float32 scale per row.
+# ---------------------------------------------------------------------------
+
+def quantize_int8_rows(x: np.ndarray):
+    """Symmetric absmax int8 codes with one scale per row (last axis).
+
+    scale = max_k |x_k| / 127 (a zero row gets scale 1 and codes 0);
+    code = clamp(rint(x / scale), -127, 127), rint rounding half to even.
+    The pages fix neither the rounding nor its precision ("#2961", "What it does":
+    dequantize, turn, requantize), so the decision is taken in float32, the
+    precision of the CUDA kernel: x is rounded to float32 first and the division
+    is an IEEE float32 division.
+    """
+    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+    amax = np.max(np.abs(x32), axis=-1, keepdims=True)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    scale = np.where(amax == 0, np.float32(1.0), scale).astype(np.float32)
+    q = np.rint((x32 / scale).astype(np.float32))
+    codes = np.clip(q, -127, 127).astype(np.int8)
+    return codes, scale[..., 0]
+
+
+def dequantize_int8_rows(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """x = code * scale in float64."""
+    return codes.astype(np.float64) * np.asarray(scale, dtype=np.float64)[..., None]
+
+
+def rerotate_int8(codes: np.ndarray, scale: np.ndarray, positions: Sequence[int],
+                  spec_a: RopeSpec, spec_b: RopeSpec):
+    """Dequantize, turn the rotary pairs (``rerotate``), requantize with a new scale.
+
+    "#2961 rope: --rope-scaling dynamic", "What it does" (int8 K without the
+    Hadamard: dequantize, turn the rotary pairs, requantize).  One scale per row
+    over all D dims, so the tail codes may change on requantisation.
+    codes: [n_tok, H, D] int8, scale: [n_tok, H].
+    """
+    x = dequantize_int8_rows(codes, scale)
+    turned = rerotate(x, positions, spec_a, spec_b)
+    new_codes, new_scale = quantize_int8_rows(turned)
+    return new_codes, new_scale, turned
+
+
+# ---------------------------------------------------------------------------
+# O4. Per-layer caches: ring with pinned sinks, and the global linear prefix.
+# ---------------------------------------------------------------------------
+
+class CapacityError(RuntimeError):
+    """A global-layer append past its capacity: a loud error, never a truncation
+    ("KV-Cache Engineering", 4.6 and 6: "The 4M cap is a loud cliff")."""
+
+
+class RingCache:
+    """One (sequence, layer) windowed cache: S pinned sink slots then a ring of W.
+
+    The ring follows "Inference & 128K Long Context", "MixedKVCache", windowed
+    layers (write at head, head = (head+1) % W, count = min(W, count+1); a chunk of
+    n >= W keeps its last W rows with head = 0, count = W), extended with S sink
+    slots that hold positions 0..S-1 and are never overwritten ("Attention Sink 与
+    Streaming KV Cache": sink + recent).  ``rows`` holds whatever per-token rows the
+    caller stores (K, V, ...); ``slot_pos`` records the logical position per slot.
+    """
+
+    def __init__(self, sinks: int, window: int):
+        assert sinks >= 0 and window >= 1
+        self.S = sinks
+        self.W = window
+        self.C = sinks + window
+        self.slots: List[object] = [None] * self.C
+        self.slot_pos = [-1] * self.C
+        self.pos = 0      # tokens seen = the next absolute position
+        self.head = 0     # next ring index to write, in [0, W)
+        self.count = 0    # valid ring entries, in [0, W]
+
+    def append(self, rows: Sequence[object]) -> None:
+        T = len(rows)
+        ring_items = []
+        for t in range(T):
+            P = self.pos + t
+            if P < self.S:
+                self.slots[P] = rows[t]
+                self.slot_pos[P] = P
+            else:
+                ring_items.append((P, rows[t]))
+        n = len(ring_items)
+        if n >= self.W:
+            for j, (P, row) in enumerate(ring_items[n - self.W:]):
+                self.slots[self.S + j] = row
+                self.slot_pos[self.S + j] = P
+            self.head = 0
+            self.count = self.W
+        else:
+            for t, (P, row) in enumerate(ring_items):
+                j = (self.head + t) % self.W
+                self.slots[self.S + j] = row
+                self.slot_pos[self.S + j] = P
+            self.head = (self.head + n) % self.W
+            self.count = min(self.W, self.count + n)
+        self.pos += T
+
+    def chronological_slots(self) -> List[int]:
+        """Slots in temporal order: the sinks, then ring[head:] + ring[:head] when
+        the ring is full, else ring[:count] ("Inference & 128K Long Context",
+        "MixedKVCache", read ordering)."""
+        sinks = list(range(min(self.pos, self.S)))
+        if self.count == self.W:
+            ring = list(range(self.head, self.W)) + list(range(0, self.head))
+        else:
+            ring = list(range(self.count))
+        return sinks + [self.S + j for j in ring]
+
+    def chronological_positions(self) -> List[int]:
+        return [self.slot_pos[s] for s in self.chronological_slots()]
+
+    def chronological_rows(self) -> List[object]:
+        return [self.slots[s] for s in self.chronological_slots()]
+
+
+class GlobalCache:
+    """A global layer's linear prefix: rows [0, len), an append writes at len and
+    advances it; past ``capacity`` it raises ("KV-Cache Engineering", 4.6 and 5.2,
+    global branch; the growth policy itself belongs to the host allocator)."""
+
+    def __init__(self, capacity: int):
+        self.capacity = capacity
+        self.rows: List[object] = []
+
+    @property
+    def pos(self) -> int:
+        return len(self.rows)
+
+    def append(self, rows: Sequence[object]) -> None:
+        if len(self.rows) + len(rows) > self.capacity:
+            raise CapacityError(f"global layer: {len(self.rows)} + {len(rows)} > "
+                                f"capacity {self.capacity}")
+        self.rows.extend(rows)
+
+    def chronological_positions(self) -> List[int]:
+        return list(range(len(self.rows)))
+
+    def chronological_rows(self) -> List[object]:
+        return list(self.rows)
+
+
+# ---------------------------------------------------------------------------
+# O5. The visible set of a query.
+# ---------------------------------------------------------------------------
+
+def visible_positions(P: int, capacity: int, sinks: int) -> List[int]:
+    """V(P) for capacity C, sinks S < C, recent W = C - S: all of 0..P when P < C,
+    else 0..S-1 together with max(S, P-W+1)..P.
+
+    "Attention Sink 与 Streaming KV Cache", "可见集合与容量定义" and the C=6, S=2,
+    T=10 worked example.
+    """
+    if P < capacity:
+        return list(range(P + 1))
+    recent = capacity - sinks
+    start = max(sinks, P - recent + 1)
+    return list(range(sinks)) + list(range(start, P + 1))
+
+
+def mask_allows(P: int, k: int, sinks: int, window: Optional[int]) -> bool:
+    """Mask rule for a query at absolute position P and a key at absolute k:
+    causal (k <= P) and either a sink (k < S) or recent (P - k < W).  window None
+    means a global layer (causal only).
+
+    "KV-Cache Engineering", 5.5: keys allowed where idx_q >= idx_k and
+    idx_q - idx_k < window; with sinks added as in "Attention Sink 与 Streaming KV
+    Cache" (sink ∪ recent).
+    """
+    if k > P:
+        return False
+    if window is None:
+        return True
+    return k < sinks or (P - k) < window
+
+
+# ---------------------------------------------------------------------------
+# O6. Attention.
+# ---------------------------------------------------------------------------
+
+def attend(q: np.ndarray, keys: np.ndarray, values: np.ndarray) -> np.ndarray:
+    """Softmax attention of one query row over a key/value set, with GQA.
+
+    q [H_q, D], keys and values [n, H_kv, D]; q head h reads kv head h // n_rep
+    ("KV-Cache Engineering", 5.5, ``repeat_kv``).  scores = q . k / sqrt(D), a
+    max-subtracted softmax in float64, out = sum_j p_j v_j ("Attention Sink 与
+    Streaming KV Cache", the experiment's ``incremental_sink``).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    keys = np.asarray(keys, dtype=np.float64)
+    values = np.asarray(values, dtype=np.float64)
+    Hq, D = q.shape
+    Hkv = keys.shape[1]
+    n_rep = Hq // Hkv
+    out = np.zeros((Hq, D), dtype=np.float64)
+    for h in range(Hq):
+        g = h // n_rep
+        s = keys[:, g, :] @ q[h] / math.sqrt(D)
+        s = s - s.max()
+        p = np.exp(s)
+        p = p / p.sum()
+        out[h] = p @ values[:, g, :]
+    return out
+
+
+def decode_attention(cache, q_rot: np.ndarray) -> np.ndarray:
+    """Decode attention of one new query over a cache after its own append:
+    the cache's chronological rows are exactly the visible set V(P).
+
+    Rows of the cache are (k_rot, v) pairs of shape [H_kv, D] each.
+    "Inference & 128K Long Context", "_attn_forward_layer" (append, get, attend).
+    """
+    rows = cache.chronological_rows()
+    keys = np.stack([r[0] for r in rows])
+    values = np.stack([r[1] for r in rows])
+    return attend(q_rot, keys, values)
+
+
+def prefill_attention(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray, p0: int,
+                      sinks: int, window: Optional[int],
+                      rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Masked attention of a prompt chunk over itself.
+
+    q_rot [T, H_q, D], k_rot and v [T, H_kv, D]; chunk index t has absolute
+    position p0 + t.  Query t sees key k iff ``mask_allows(p0+t, p0+k, S, W)``.
+    ``rows`` picks the query indices to evaluate (all by default).
+    Returns [len(rows), H_q, D].
+    """
+    T = q_rot.shape[0]
+    if rows is None:
+        rows = range(T)
+    out = []
+    for t in rows:
+        P = p0 + t
+        ks = [k for k in range(T) if mask_allows(P, p0 + k, sinks, window)]
+        out.append(attend(q_rot[t], k_rot[ks], v[ks]))
+    return np.stack(out)
+
+
+# ---------------------------------------------------------------------------
+# O7. Dynamic factor policy.
+# ---------------------------------------------------------------------------
+
+def dynamic_factor(total_positions: int, orig_ctx: int, step: float = 0.125,
+                   cap: Optional[float] = None) -> float:
+    """1 while the positions fit the trained context; past it, positions / L0
+    rounded up to ``step`` and capped.
+
+    "#2961 rope: --rope-scaling dynamic", "What it does", the factor.
+    """
+    if total_positions <= orig_ctx:
+        return 1.0
+    f = math.ceil((total_positions / orig_ctx) / step) * step
+    if cap is not None:
+        f = min(f, cap)
+    return f
+
+
+# ---------------------------------------------------------------------------
+# Measurement context.
+# ---------------------------------------------------------------------------
+
+def kv_bytes_per_token(n_layers: int, n_kv_heads: int, head_dim: int,
+                       elem_bytes: int) -> int:
+    """c = 2 L h_kv d_h bytes ("RoPE, scaling, sliding window, attention sinks",
+    sliding-window section: 128 KiB per token for the Llama-3-8B shape)."""
+    return 2 * n_layers * n_kv_heads * head_dim * elem_bytes
