@@ -1,0 +1,392 @@
+"""Benchmark of the sink + window KV attention hot path on GB300.
+
+Default workload (N=1): the windowed-layer decode step -- B=32 sequences, H_q=32,
+H_kv=8, d_h=r=128, theta=5e5, bf16, S=4 sinks + W=4092 ring (C=4096), positions
+U[4096, 32768] with the ring wrapped at a random head; each step rotates and appends
+one new token per sequence and runs split-K decode attention over the 4096 visible
+keys.  The metric is the KV bytes the attention must read per second.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload window|hybrid|rerotate|prefill]
+
+For N > 1 (torchrun, one rank per GPU) every rank runs its own replica: the path
+shards by sequence with no exchange step, so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sink+window decode attn KV-read GB/s (frac of HBM peak), tokens/s, keys/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.06 <= r[0] <= (self.t1 or 1e30) + 0.06]
+        used = inside if inside else [min(rows, key=lambda r: abs(r[0] - (self.t1 or r[0])))]
+        sm = [float(p[1]) for _, p in used if p[1].replace(".", "").isdigit()]
+        smax = [float(p[2]) for _, p in used if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, p in used for n, v in zip(names, p[5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(used), "in_region": bool(inside)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ---------------------------------------------------------------------------
+
+def _dist_init(n_gpus):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# windowed decode workload
+# ---------------------------------------------------------------------------
+
+def window_setup(seed_base=0, steps=1):
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    B, Hq, Hkv, D, S, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    tbl = sk.RopeTable(D, c["r"], c["theta"], c["pos_hi"] + steps + 64)
+    layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W)
+    synth.fill_normal_(layer.k, 11 + seed_base)
+    synth.fill_normal_(layer.v, 12 + seed_base)
+    pos, head, count = synth.window_state(13 + seed_base, B, W, c["pos_lo"], c["pos_hi"])
+    layer.pos.copy_(pos)
+    layer.head.copy_(head)
+    layer.count.copy_(count)
+    return tbl, layer, c
+
+
+def bench_window(args, rank, world):
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    steps, warm = args.steps, args.warmup
+    tbl, layer, c = window_setup(seed_base=100 * rank, steps=steps + warm + 2)
+    B, Hq, Hkv, D, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["W"]
+    n = steps + warm
+    # one fresh token per sequence per step, resident in HBM before timing
+    qs = synth.normal((n, B, 1, Hq, D), 14, torch.bfloat16, device="cuda")
+    ks = synth.normal((n, B, 1, Hkv, D), 15, torch.bfloat16, device="cuda")
+    vs = synth.normal((n, B, 1, Hkv, D), 16, torch.bfloat16, device="cuda")
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(sk.decode_workspace_bytes(layer, Hq), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        sk.kv_append(tbl, layer, qs[i], ks[i], vs[i])
+        if ev is not None:
+            ev[0].record(stream)
+        sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(warm):
+        step(i)
+    torch.cuda.synchronize()
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    _barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    t_start.record(stream)
+    for i in range(steps):
+        step(warm + i, dec_ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("end")
+    _barrier(world)
+    if rank == 0:
+        clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    ms = _max_over_ranks(ms, world)
+    dec_ms = sum(a.elapsed_time(b) for a, b in dec_ev) / steps
+    assert layer.error_bits() == 0
+
+    L = c["S"] + W  # visible keys per sequence (ring full)
+    kv_bytes = B * Hkv * L * D * 2 * 2
+    alg_bytes_decode = kv_bytes + 2 * (B * Hq * D * 2)          # + q read, out write
+    ms_step = ms / steps
+    value = world * kv_bytes / (ms_step * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers: pinned inputs copied in,
+    # the output copied out, every step
+    e2e = None
+    if True:
+        hq = torch.empty((steps, B, 1, Hq, D), dtype=torch.bfloat16).pin_memory()
+        hk = torch.empty((steps, B, 1, Hkv, D), dtype=torch.bfloat16).pin_memory()
+        hv = torch.empty((steps, B, 1, Hkv, D), dtype=torch.bfloat16).pin_memory()
+        hq.copy_(qs[:steps].cpu()); hk.copy_(ks[:steps].cpu()); hv.copy_(vs[:steps].cpu())
+        hout = torch.empty((steps, B, Hq, D), dtype=torch.bfloat16).pin_memory()
+        dq = torch.empty_like(qs[0]); dk = torch.empty_like(ks[0]); dv = torch.empty_like(vs[0])
+        tbl2, layer2, _ = window_setup(seed_base=100 * rank + 7, steps=steps + 2)
+        torch.cuda.synchronize()
+        _barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            dq.copy_(hq[i], non_blocking=True)
+            dk.copy_(hk[i], non_blocking=True)
+            dv.copy_(hv[i], non_blocking=True)
+            sk.kv_append(tbl2, layer2, dq, dk, dv)
+            sk.decode_attention(layer2, dq[:, 0], out=out, workspace=ws)
+            hout[i].copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world) / steps
+        h2d = (hq[0].numel() + hk[0].numel() + hv[0].numel()) * 2
+        e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout[0].numel() * 2,
+               "ms_per_step": round(e2e_ms, 5)}
+
+    hbm, _, _, peak_kind = _peaks()
+    achieved = alg_bytes_decode / (dec_ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "windowed-layer decode step (RoPE + append + split-K attention)",
+                   "batch_per_gpu": B, "H_q": Hq, "H_kv": Hkv, "d_h": D, "rotary_dim": c["r"],
+                   "theta": c["theta"], "sinks": c["S"], "window": W, "visible_keys": L,
+                   "positions": "U[4096, 32768], ring wrapped at random head",
+                   "l2": f"inputs larger than L2 (KV {kv_bytes / 1e6:.0f} MB per step > 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_hbm_peak": round(value / world / hbm, 4),
+        "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
+        "keys_per_s": round(world * B * L / (ms_step * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "decode attention (split-K + combine), per launch",
+                     "algorithmic_bytes_per_launch": alg_bytes_decode,
+                     "launch_ms": round(dec_ms, 5), "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": e2e,
+        "gpu_launches": steps * 3,
+    }
+    if rank == 0:
+        result["clocks"] = clocks.summary()
+    return result
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (single thread, in a subprocess)
+# ---------------------------------------------------------------------------
+
+def cpu_oracle_window(n_seq: int, seed_base: int = 0):
+    """Time the float64 oracle on n_seq sequences of the windowed decode step
+    (RoPE + append + attention) and return (seconds, kv_bytes)."""
+    import numpy as np
+    import torch
+    from oracle.sinkkv_oracle import RingCache, RopeSpec, decode_attention, rope_rotate
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    B, Hq, Hkv, D, S, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    pos, head, count = synth.window_state(13 + seed_base, B, W, c["pos_lo"], c["pos_hi"])
+    spec = RopeSpec(D, c["r"], c["theta"])
+    omega = spec.omega()
+    total = 0.0
+    for b in range(n_seq):
+        kb = synth.normal((Hkv, S + W, D), 1000 + b, torch.bfloat16).double().numpy()
+        vb = synth.normal((Hkv, S + W, D), 2000 + b, torch.bfloat16).double().numpy()
+        q = synth.normal((1, Hq, D), 3000 + b, torch.bfloat16).double().numpy()
+        k = synth.normal((1, Hkv, D), 4000 + b, torch.bfloat16).double().numpy()
+        v = synth.normal((Hkv, D), 5000 + b, torch.bfloat16).double().numpy()
+        t0 = time.perf_counter()
+        ring = RingCache(S, W)
+        ring.pos, ring.head, ring.count = int(pos[b]), int(head[b]), int(count[b])
+        for s in range(S + W):
+            ring.slots[s] = (kb[:, s], vb[:, s])
+        P = int(pos[b])
+        qr = rope_rotate(q, [P], omega, 1.0, D)
+        kr = rope_rotate(k, [P], omega, 1.0, D)
+        ring.append([(kr[0], v)])
+        decode_attention(ring, qr[0])
+        total += time.perf_counter() - t0
+    return total, n_seq * Hkv * (S + W) * D * 2 * 2
+
+
+def _cpu_worker(n_seq):
+    secs, kv = cpu_oracle_window(n_seq)
+    print(json.dumps({"secs": secs, "kv_bytes": kv}))
+
+
+def cpu_baseline(n_seq=32):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", str(n_seq)],
+                       capture_output=True, text=True, env=env, timeout=600)
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    gbs = d["kv_bytes"] / d["secs"] / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_seq} of 32 sequences of one windowed decode step (float64 numpy, "
+                      f"single thread, {d['secs']:.2f} s)"}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="window", choices=["window"])
+    ap.add_argument("--cpu-worker", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    if args.cpu_worker:
+        _cpu_worker(args.cpu_worker)
+        return
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        # The reference arm is the float64 CPU oracle, on rank 0 only.
+        if rank != 0:
+            return
+        steps, warm = args.steps, args.warmup
+        per_step = 2  # sequences of the 32 per step: a bounded sample
+        n = min(steps, 20)
+        for _ in range(min(warm, 2)):
+            cpu_oracle_window(1)
+        secs, kv = 0.0, 0
+        for i in range(n):
+            s, b = cpu_oracle_window(per_step, seed_base=i)
+            secs += s
+            kv += b
+        value = kv / secs / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": n, "warmup": min(warm, 2),
+                "ms_per_step": round(1e3 * secs / n, 3), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": "windowed-layer decode step (RoPE + append + split-K attention)",
+                           "sample_per_step": f"{per_step} of 32 sequences"},
+                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{per_step} of 32 sequences per step, {n} steps"},
+                "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    _, world_, _ = _dist_init(args.gpus)
+    result = bench_window(args, rank, world_)
+    if rank == 0:
+        if not args.no_cpu_baseline and world_ == 1:
+            try:
+                result["cpu_baseline"] = cpu_baseline()
+            except Exception as e:  # reported, never fatal
+                result["cpu_baseline"] = {"value": None, "error": str(e)[:200]}
+        print(json.dumps(result))
+    if world_ > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+/*
+ * sinkkv.h -- C ABI of libsinkkv: sink + sliding-window KV attention with RoPE/YaRN
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the problem statement of these pages:
+ *   [RoPE]   "RoPE, scaling, sliding window, attention sinks" (mlinterviewnotes)
+ *   [MIXED]  "Inference & 128K Long Context" / "KV-Cache Engineering" (GPT-OSS-Lite)
+ *   [DYN]    "#2961 rope: --rope-scaling dynamic" (strata pull request)
+ *   [SINK]   "Attention Sink 与 Streaming KV Cache" (llm-glossary)
+ *
+ * Conventions for every call
+ *   - Ownership: the caller owns every tensor, cache, state array and workspace.
+ *     The library owns only sk_rope_table objects (host and device memory).
+ *   - Pointers named "device" are CUDA device pointers of the current device;
+ *     "host" pointers are ordinary host memory.  `stream` is a cudaStream_t
+ *     (NULL = legacy default stream).  Every call is asynchronous on `stream`
+ *     except table create/rebuild, which synchronise `stream` before returning.
+ *   - Layouts are dense, row-major, innermost last, with no padding.
+ *   - Errors: host-side argument checks run before any launch and return an
+ *     sk_status; nothing is launched on error.  Conditions that depend on device
+ *     state (a position past the table, a global layer past its capacity) are
+ *     detected by the kernel, which then leaves that sequence untouched and ORs a
+ *     bit into the layer's device error word `err` (SK_DEVERR_*), if given.
+ *     Launch failures return SK_ERR_CUDA.  No call aborts or traps the GPU.
+ */
+#ifndef SINKKV_H
+#define SINKKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define SK_API __attribute__((visibility("default")))
+#else
+#define SK_API
+#endif
+
+typedef enum {
+    SK_OK = 0,
+    SK_ERR_ARG = 1,             /* a null pointer, bad shape or inconsistent argument */
+    SK_ERR_CAPACITY = 2,        /* a cache cannot hold what was asked */
+    SK_ERR_POSITION_RANGE = 3,  /* a position at or past the table's max_positions */
+    SK_ERR_UNSUPPORTED = 4,     /* a valid combination this build does not implement */
+    SK_ERR_CUDA = 5             /* a CUDA runtime call or launch failed */
+} sk_status;
+
+typedef enum { SK_BF16 = 0, SK_F32 = 1, SK_I8 = 2 } sk_dtype;
+
+typedef enum { SK_LAYER_RING = 0, SK_LAYER_GLOBAL = 1 } sk_layer_kind;
+
+/* Bits of a device error word (uint32_t, caller-owned, zeroed by the caller). */
+#define SK_DEVERR_POSITION_RANGE 0x1u  /* a position >= max_positions was skipped   */
+#define SK_DEVERR_CAPACITY       0x2u  /* a global-layer append past capacity was skipped */
+#define SK_DEVERR_TIMEOUT        0x4u  /* a bounded in-kernel wait gave up (never expected) */
+
+/*
+ * Rotary configuration.  [RoPE] "Let d_h be the head dimension, r <= d_h the rotary
+ * dimension ... b the base"; the frequencies omega_i = theta^(-2i/r) (the
+ * _compute_inv_freq listing); NeoX pairs (j, j + r/2), GPT-J pairs (2j, 2j+1).
+ * yarn_factor <= 1 means plain RoPE; otherwise the YaRN blend of [RoPE] "YaRN,
+ * precisely" with original context yarn_orig_ctx, beta_fast / beta_slow, and the
+ * mscale mu = 0.1 ln s + 1 folded into both cos and sin.
+ * Constraints: rotary_dim even, 16 <= rotary_dim <= head_dim, head_dim in {64, 128},
+ * rotary_dim a multiple of 16; max_positions >= 1.
+ */
+typedef struct {
+    int32_t head_dim;
+    int32_t rotary_dim;
+    int32_t neox;            /* 1 = NeoX pairing, 0 = GPT-J pairing */
+    int32_t reserved0;
+    double theta;            /* rope_theta, > 1 */
+    double yarn_factor;      /* <= 1: plain RoPE */
+    int64_t yarn_orig_ctx;   /* L0, used when yarn_factor > 1 */
+    double beta_fast;        /* default 32 */
+    double beta_slow;        /* default 1 */
+    int64_t max_positions;   /* table rows: positions 0 .. max_positions-1 */
+} sk_rope_config;
+
+/* Opaque, library-owned cos/sin table.  Its device buffer is
+ * float2[max_positions][rotary_dim/2] = (mu cos(P omega_j), mu sin(P omega_j)),
+ * computed in float64 on the host and rounded to float32 ([RoPE]: "a table of
+ * shape [max_position_embeddings, r] built once ... No trigonometry at runtime"). */
+typedef struct sk_rope_table sk_rope_table;
+
+/*
+ * One layer's KV cache for a batch of sequences.  All pointers are device pointers
+ * owned by the caller.
+ *   kind = SK_LAYER_RING   ([MIXED] "Windowed layers - ring buffer", extended with
+ *     [SINK]'s pinned sinks): slots [0, sinks) hold positions 0..sinks-1 and are
+ *     never overwritten; slots [sinks, sinks+window) are a ring with state
+ *     head[b] in [0, window) and count[b] in [0, window]; capacity = sinks + window.
+ *   kind = SK_LAYER_GLOBAL ([MIXED] "Global layers"): slot = position, rows [0, pos[b])
+ *     are valid; capacity = rows allocated per (sequence, kv head).
+ *   k, v:    [batch][n_kv_heads][capacity][head_dim] of k_dtype / v_dtype
+ *   k_scale: [batch][n_kv_heads][capacity] float, one scale per int8 K row (k_dtype
+ *            SK_I8 only, else NULL)
+ *   head, count: int32 [batch] (ring only; may be NULL for global layers)
+ *   pos:     int64 [batch], tokens seen so far = the next absolute position
+ *   err:     uint32 device error word, may be NULL
+ * k_dtype in {SK_BF16, SK_F32, SK_I8}; v_dtype in {SK_BF16, SK_F32}.
+ */
+typedef struct {
+    int32_t kind;
+    int32_t k_dtype;
+    int32_t v_dtype;
+    int32_t batch;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t sinks;
+    int32_t window;
+    int64_t capacity;
+    void* k;
+    void* v;
+    float* k_scale;
+    int32_t* head;
+    int32_t* count;
+    int64_t* pos;
+    uint32_t* err;
+} sk_kv_layer;
+
+/* ---- RoPE table (host float64 build, device float32 copy) ---------------------- */
+
+/* Build the table for `cfg` on the current device.  Allocates the device buffer;
+ * on success *out owns it.  Synchronises `stream`.  Errors: SK_ERR_ARG for a bad
+ * config or NULL pointer, SK_ERR_CUDA if the allocation or copy fails. */
+SK_API sk_status sk_rope_table_create(const sk_rope_config* cfg, void* stream, sk_rope_table** out);
+
+/* Rebuild the table in place for a new YaRN factor: same device pointer, so CUDA
+ * graphs captured against it read the new angles ([DYN] "The table. The cos/sin
+ * table is rebuilt in place ... so the captured CUDA graphs keep their pointer").
+ * The entries are computed independently on host threads, so the result is bitwise
+ * that of sk_rope_table_create with the new factor.  Ordered on `stream`
+ * (kernels already queued on it finish first) and synchronises it. */
+SK_API sk_status sk_rope_table_rebuild(sk_rope_table* table, double new_yarn_factor, void* stream);
+
+/* Free the table (device and host memory).  NULL is ignored.  The caller must
+ * ensure no queued kernel still reads it. */
+SK_API void sk_rope_table_destroy(sk_rope_table* table);
+
+/* Read back the table's config and its device buffer (float2 [max_positions][r/2]).
+ * Either output may be NULL. */
+SK_API sk_status sk_rope_table_info(const sk_rope_table* table, sk_rope_config* cfg_out,
+                             const void** device_cos_sin);
+
+/* ---- RoPE apply ------------------------------------------------------------------ */
+
+/* Rotate x in place: x [n_tok][n_heads][head_dim] (dtype SK_BF16 or SK_F32, device),
+ * row t at absolute position positions[t] (device int64 [n_tok]).
+ * [RoPE] the rotation listing: o1 = x1 cos - x2 sin, o2 = x2 cos + x1 sin, times mu;
+ * dims [r, d_h) untouched.  A row whose position is < 0 or >= max_positions is left
+ * unchanged and sets SK_DEVERR_POSITION_RANGE in *err (device, may be NULL). */
+SK_API sk_status sk_rope_apply(const sk_rope_table* table, void* x, int32_t dtype, int64_t n_tok,
+                        int32_t n_heads, const int64_t* positions, uint32_t* err, void* stream);
+
+/* ---- Fused RoPE + KV append -------------------------------------------------------- */
+
+/* Append T new tokens per sequence to `layer`, rotating Q and K on the way.
+ *   q: [batch][T][n_q_heads][head_dim] of io_dtype, device, may be NULL; rotated in place.
+ *   k: [batch][T][n_kv_heads][head_dim] of io_dtype, device; rotated in place, then
+ *      written to the cache (quantised per row for an int8 K cache).
+ *   v: [batch][T][n_kv_heads][head_dim] of io_dtype, device; written as is.
+ * Token t of sequence b has absolute position P = pos[b] + t: the same counter gives
+ * the angle and the slot ([RoPE] "Where the positions come from").
+ * Ring layers ([MIXED] MixedKVCache.append, with [SINK] sinks): P < sinks goes to
+ * slot P; of the remaining n tokens, n >= window keeps the last `window` at ring slots
+ * 0..window-1 with head = 0, count = window; otherwise they go to ring slot
+ * (head + u) % window, head = (head + n) % window, count = min(window, count + n).
+ * Global layers: slot = P; pos[b] + T > capacity skips the sequence and sets
+ * SK_DEVERR_CAPACITY.  pos[b] += T.  pos[b] + T > max_positions skips the sequence
+ * and sets SK_DEVERR_POSITION_RANGE.
+ * io_dtype: SK_BF16 or SK_F32.  Supported (io, k cache, v cache): (F32,F32,F32),
+ * (BF16,BF16,BF16), (BF16,I8,BF16); others return SK_ERR_UNSUPPORTED.
+ * n_q_heads must be a multiple of n_kv_heads when q is given. */
+SK_API sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer* layer, void* q,
+                       int32_t n_q_heads, void* k, const void* v, int32_t io_dtype, int32_t T,
+                       void* stream);
+
+/* ---- Decode attention (split-K over the visible set) ------------------------------ */
+
+/* Workspace bytes sk_decode_attention needs for `layer` and n_q_heads. */
+SK_API size_t sk_decode_workspace_bytes(const sk_kv_layer* layer, int32_t n_q_heads);
+
+/* One decode query per sequence against the visible set of its cache, after its own
+ * append.  [SINK] "可见集合与容量定义": V(P) = 0..P when P < C, else sinks 0..S-1 and
+ * max(S, P-W+1)..P; in a ring layer these are exactly the occupied slots
+ * [0, min(pos, S) + count).  Global layers read rows [0, pos).
+ * q head h reads kv head h / (n_q_heads / n_kv_heads) ([MIXED] 5.5 repeat_kv, done as an
+ * in-register broadcast).  scores = q.k / sqrt(d_h), softmax, out = sum p v
+ * ([SINK] the experiment's incremental_sink).
+ *   q_rot: [batch][n_q_heads][head_dim] of io_dtype (device); out: same shape and dtype.
+ *   workspace: device, >= sk_decode_workspace_bytes(layer, n_q_heads) bytes, 16-byte
+ *   aligned; its contents need no initialisation.
+ * Supported: io SK_F32 with an F32/F32 cache, io SK_BF16 with a BF16/BF16 cache;
+ * n_q_heads / n_kv_heads in {1, 2, 4} for head_dim 128 and {1, 2, 4, 8} for 64. */
+SK_API sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q_rot, int32_t n_q_heads,
+                              int32_t io_dtype, void* out, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/* ---- Prefill attention (causal + window + sinks) ---------------------------------- */
+
+/* Masked attention of a prompt chunk over itself on the tensor cores.
+ *   q_rot: [batch][T][n_q_heads][head_dim], k_rot, v: [batch][T][n_kv_heads][head_dim],
+ *   out: [batch][T][n_q_heads][head_dim]; all SK_BF16, device.
+ * Chunk index t has absolute position p0 + t.  Query t sees key k iff k <= t and
+ * (p0 + k < sinks or t - k < window) ([MIXED] 5.5: idx_q >= idx_k and
+ * idx_q - idx_k < window; [SINK] sink + recent).  window <= 0 means a global layer
+ * (causal only).  Tiles the mask rules out entirely are skipped.
+ * Supported: head_dim 128, SK_BF16. */
+SK_API sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
+                               int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                               int64_t p0, int32_t sinks, int32_t window, void* out, void* stream);
+
+/* ---- Cached-key rerotation on a factor change ------------------------------------ */
+
+/* Turn every cached key of `layers` (host array of n_layers descriptors, device
+ * buffers) from table `from` (factor A) to table `to` (factor B), in place:
+ * each rotary pair at position P is turned by P (omega_B - omega_A) and scaled by
+ * mu_B / mu_A, computed from the two tables' entries with R_a R_b = R_{a+b}
+ * ([DYN] "The cached keys follow a change"; [SINK] RoPE section).  The tail dims
+ * are unchanged.  An int8 K row is dequantised (code * scale), turned and
+ * requantised with a new scale = max|x| / 127 and codes rint(x / scale)
+ * (half to even), clamped to [-127, 127].
+ * Positions come from the layer state: global slot s < pos[b] holds position s;
+ * ring sink slot s < min(pos, S) holds s; ring slot j < count holds
+ * pos - 1 - ((head - 1 - j) mod window).  Both tables must share head_dim,
+ * rotary_dim, pairing and theta, and cover every cached position (else
+ * SK_DEVERR_POSITION_RANGE for the row, which stays unchanged).
+ * k_dtype SK_BF16 or SK_I8.  n_layers <= 128. */
+SK_API sk_status sk_kv_rerotate(const sk_kv_layer* layers, int32_t n_layers, const sk_rope_table* from,
+                         const sk_rope_table* to, void* stream);
+
+/* ---- Misc ------------------------------------------------------------------------ */
+
+/* A static, human-readable name for a status code. */
+SK_API const char* sk_status_str(sk_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+SK_API int32_t sk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINKKV_H */

@@ -1,0 +1,323 @@
+"""Python binding of libsinkkv (sink + window KV attention with RoPE/YaRN on GB300).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels, reached through the C ABI declared in ``include/sinkkv.h``.  PyTorch
+tensors supply device memory and the current CUDA stream.  There is no CPU
+fallback: if ``libsinkkv.so`` is missing or fails to load, importing the binding's
+functions raises.
+
+C entry point          Python
+sk_rope_table_*        RopeTable
+sk_rope_apply          rope_apply
+sk_kv_append           kv_append
+sk_decode_attention    decode_attention (+ decode_workspace_bytes)
+sk_prefill_attention   prefill_attention
+sk_kv_rerotate         kv_rerotate
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsinkkv.so")
+
+SK_OK, SK_ERR_ARG, SK_ERR_CAPACITY, SK_ERR_POSITION_RANGE, SK_ERR_UNSUPPORTED, SK_ERR_CUDA = range(6)
+SK_BF16, SK_F32, SK_I8 = 0, 1, 2
+SK_LAYER_RING, SK_LAYER_GLOBAL = 0, 1
+SK_DEVERR_POSITION_RANGE, SK_DEVERR_CAPACITY, SK_DEVERR_TIMEOUT = 1, 2, 4
+
+
+class SinkKVError(RuntimeError):
+    """A non-OK sk_status from the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib().sk_status_str(status).decode()}")
+
+
+class RopeConfig(ctypes.Structure):
+    _fields_ = [("head_dim", ctypes.c_int32), ("rotary_dim", ctypes.c_int32),
+                ("neox", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("theta", ctypes.c_double), ("yarn_factor", ctypes.c_double),
+                ("yarn_orig_ctx", ctypes.c_int64), ("beta_fast", ctypes.c_double),
+                ("beta_slow", ctypes.c_double), ("max_positions", ctypes.c_int64)]
+
+
+class KVLayerStruct(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("k_dtype", ctypes.c_int32), ("v_dtype", ctypes.c_int32),
+                ("batch", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("sinks", ctypes.c_int32), ("window", ctypes.c_int32), ("capacity", ctypes.c_int64),
+                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("head", ctypes.c_void_p), ("count", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("err", ctypes.c_void_p)]
+
+
+_LIB = None
+
+# (name, restype, argtypes) of every entry point in include/sinkkv.h
+_SIGNATURES = [
+    ("sk_rope_table_create", ctypes.c_int, [ctypes.POINTER(RopeConfig), ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
+    ("sk_rope_table_rebuild", ctypes.c_int, [ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p]),
+    ("sk_rope_table_destroy", None, [ctypes.c_void_p]),
+    ("sk_rope_table_info", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(RopeConfig), ctypes.POINTER(ctypes.c_void_p)]),
+    ("sk_rope_apply", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                     ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    ("sk_kv_append", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]),
+    ("sk_decode_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32]),
+    ("sk_decode_attention", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    ("sk_prefill_attention", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                            ctypes.c_void_p]),
+    ("sk_kv_rerotate", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p]),
+    ("sk_status_str", ctypes.c_char_p, [ctypes.c_int]),
+    ("sk_version", ctypes.c_int32, []),
+]
+
+EXPORTED = [name for name, _, _ in _SIGNATURES]
+
+
+def _lib():
+    """Load libsinkkv.so once; raise loudly if it is missing (no fallback)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libsinkkv.so not built at {LIB_PATH}; run "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, res, args in _SIGNATURES:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _check(status: int, what: str):
+    if status != SK_OK:
+        raise SinkKVError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _sk_dtype(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return SK_BF16
+    if dt == torch.float32:
+        return SK_F32
+    if dt == torch.int8:
+        return SK_I8
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _need_contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+# ---------------------------------------------------------------------------
+# RoPE table
+# ---------------------------------------------------------------------------
+
+class RopeTable:
+    """Library-owned cos/sin table (sk_rope_table_create / rebuild / destroy)."""
+
+    def __init__(self, head_dim: int, rotary_dim: int, theta: float, max_positions: int,
+                 neox: bool = True, yarn_factor: float = 1.0, yarn_orig_ctx: int = 4096,
+                 beta_fast: float = 32.0, beta_slow: float = 1.0, stream=None):
+        self.cfg = RopeConfig(head_dim, rotary_dim, 1 if neox else 0, 0, float(theta),
+                              float(yarn_factor), int(yarn_orig_ctx), float(beta_fast),
+                              float(beta_slow), int(max_positions))
+        h = ctypes.c_void_p()
+        _check(_lib().sk_rope_table_create(ctypes.byref(self.cfg), _stream(stream), ctypes.byref(h)),
+               "sk_rope_table_create")
+        self.handle = h
+
+    def rebuild(self, yarn_factor: float, stream=None):
+        _check(_lib().sk_rope_table_rebuild(self.handle, float(yarn_factor), _stream(stream)),
+               "sk_rope_table_rebuild")
+        self.cfg.yarn_factor = float(yarn_factor)
+
+    def device_ptr(self) -> int:
+        out = ctypes.c_void_p()
+        _check(_lib().sk_rope_table_info(self.handle, None, ctypes.byref(out)), "sk_rope_table_info")
+        return out.value
+
+    def config(self) -> RopeConfig:
+        c = RopeConfig()
+        _check(_lib().sk_rope_table_info(self.handle, ctypes.byref(c), None), "sk_rope_table_info")
+        return c
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            _lib().sk_rope_table_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---------------------------------------------------------------------------
+# KV layer (caller-owned device buffers held as torch tensors)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class KVLayer:
+    """One layer's cache for a batch, as described by sk_kv_layer.
+
+    k, v: [batch, n_kv_heads, capacity, head_dim]; k_scale: [batch, n_kv_heads, capacity]
+    float32 (int8 K only); head, count: int32 [batch] (ring); pos: int64 [batch];
+    err: uint32 word as int32 [1].
+    """
+    kind: int
+    k: torch.Tensor
+    v: torch.Tensor
+    pos: torch.Tensor
+    sinks: int = 0
+    window: int = 0
+    head: Optional[torch.Tensor] = None
+    count: Optional[torch.Tensor] = None
+    k_scale: Optional[torch.Tensor] = None
+    err: Optional[torch.Tensor] = None
+
+    @staticmethod
+    def allocate(kind: int, batch: int, n_kv_heads: int, head_dim: int, *, sinks: int = 0,
+                 window: int = 0, capacity: Optional[int] = None, k_dtype=torch.bfloat16,
+                 v_dtype=torch.bfloat16, device="cuda") -> "KVLayer":
+        if kind == SK_LAYER_RING:
+            capacity = sinks + window
+        assert capacity is not None and capacity >= 1
+        k = torch.zeros(batch, n_kv_heads, capacity, head_dim, dtype=k_dtype, device=device)
+        v = torch.zeros(batch, n_kv_heads, capacity, head_dim, dtype=v_dtype, device=device)
+        ks = (torch.ones(batch, n_kv_heads, capacity, dtype=torch.float32, device=device)
+              if k_dtype == torch.int8 else None)
+        z32 = lambda: torch.zeros(batch, dtype=torch.int32, device=device)
+        return KVLayer(kind, k, v, torch.zeros(batch, dtype=torch.int64, device=device), sinks, window,
+                       z32() if kind == SK_LAYER_RING else None, z32() if kind == SK_LAYER_RING else None,
+                       ks, torch.zeros(1, dtype=torch.int32, device=device))
+
+    @property
+    def batch(self):
+        return self.k.shape[0]
+
+    @property
+    def n_kv_heads(self):
+        return self.k.shape[1]
+
+    @property
+    def capacity(self):
+        return self.k.shape[2]
+
+    @property
+    def head_dim(self):
+        return self.k.shape[3]
+
+    def struct(self) -> KVLayerStruct:
+        _need_contig(self.k, self.v, self.k_scale, self.head, self.count, self.pos)
+        return KVLayerStruct(self.kind, _sk_dtype(self.k.dtype), _sk_dtype(self.v.dtype), self.batch,
+                             self.n_kv_heads, self.head_dim, self.sinks, self.window, self.capacity,
+                             self.k.data_ptr(), self.v.data_ptr(),
+                             None if self.k_scale is None else self.k_scale.data_ptr(),
+                             None if self.head is None else self.head.data_ptr(),
+                             None if self.count is None else self.count.data_ptr(),
+                             self.pos.data_ptr(), None if self.err is None else self.err.data_ptr())
+
+    def error_bits(self) -> int:
+        """Read the device error word (synchronises)."""
+        return 0 if self.err is None else int(self.err.item()) & 0xFFFFFFFF
+
+
+# ---------------------------------------------------------------------------
+# Entry points
+# ---------------------------------------------------------------------------
+
+def rope_apply(table: RopeTable, x: torch.Tensor, positions: torch.Tensor,
+               err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Rotate x [n_tok, H, D] in place at positions [n_tok] (sk_rope_apply)."""
+    _need_contig(x, positions)
+    n_tok, H = x.shape[0], x.shape[1]
+    _check(_lib().sk_rope_apply(table.handle, _ptr(x), _sk_dtype(x.dtype), n_tok, H, _ptr(positions),
+                                _ptr(err), _stream(stream)), "sk_rope_apply")
+    return x
+
+
+def kv_append(table: RopeTable, layer: KVLayer, q: Optional[torch.Tensor], k: torch.Tensor,
+              v: torch.Tensor, stream=None):
+    """Fused RoPE + append of T tokens per sequence (sk_kv_append).
+
+    q [B, T, Hq, D] (optional) and k [B, T, Hkv, D] are rotated in place; v [B, T, Hkv, D]."""
+    _need_contig(q, k, v)
+    T = k.shape[1]
+    hq = 0 if q is None else q.shape[2]
+    s = layer.struct()
+    _check(_lib().sk_kv_append(table.handle, ctypes.byref(s), _ptr(q), hq, _ptr(k), _ptr(v),
+                               _sk_dtype(k.dtype), T, _stream(stream)), "sk_kv_append")
+
+
+def decode_workspace_bytes(layer: KVLayer, n_q_heads: int) -> int:
+    s = layer.struct()
+    return int(_lib().sk_decode_workspace_bytes(ctypes.byref(s), n_q_heads))
+
+
+def decode_attention(layer: KVLayer, q_rot: torch.Tensor, out: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Split-K decode attention of q_rot [B, Hq, D] over the layer's visible set."""
+    _need_contig(q_rot)
+    Hq = q_rot.shape[1]
+    if out is None:
+        out = torch.empty_like(q_rot)
+    s = layer.struct()
+    need = int(_lib().sk_decode_workspace_bytes(ctypes.byref(s), Hq))
+    if need == 0:
+        raise SinkKVError(SK_ERR_UNSUPPORTED, "sk_decode_workspace_bytes")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_rot.device)
+    _check(_lib().sk_decode_attention(ctypes.byref(s), _ptr(q_rot), Hq, _sk_dtype(q_rot.dtype), _ptr(out),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream)), "sk_decode_attention")
+    return out
+
+
+def prefill_attention(q_rot: torch.Tensor, k_rot: torch.Tensor, v: torch.Tensor, p0: int, sinks: int,
+                      window: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Masked prefill attention of a chunk over itself: q [B,T,Hq,D], k/v [B,T,Hkv,D]."""
+    _need_contig(q_rot, k_rot, v)
+    B, T, Hq, D = q_rot.shape
+    Hkv = k_rot.shape[2]
+    if out is None:
+        out = torch.empty_like(q_rot)
+    _check(_lib().sk_prefill_attention(_ptr(q_rot), _ptr(k_rot), _ptr(v), B, T, Hq, Hkv, D, int(p0),
+                                       int(sinks), int(window), _ptr(out), _stream(stream)),
+           "sk_prefill_attention")
+    return out
+
+
+def kv_rerotate(layers: Sequence[KVLayer], table_from: RopeTable, table_to: RopeTable, stream=None):
+    """Turn every cached key of `layers` from table_from's factor to table_to's (sk_kv_rerotate)."""
+    arr = (KVLayerStruct * len(layers))(*[l.struct() for l in layers])
+    _check(_lib().sk_kv_rerotate(arr, len(layers), table_from.handle, table_to.handle, _stream(stream)),
+           "sk_kv_rerotate")
+
+
+def version() -> int:
+    return int(_lib().sk_version())

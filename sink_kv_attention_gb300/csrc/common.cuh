@@ -1,0 +1,155 @@
+// Shared device helpers for libsinkkv: bf16 packing, mbarrier / bulk-copy PTX,
+// bounded waits.  sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sinkkv.h"
+
+#define SK_RET_IF(cond, status) \
+    do {                        \
+        if (cond) return (status); \
+    } while (0)
+
+#define SK_CUDA_RET(call)                          \
+    do {                                           \
+        cudaError_t e_ = (call);                   \
+        if (e_ != cudaSuccess) return SK_ERR_CUDA; \
+    } while (0)
+
+namespace sk {
+
+// ---------------------------------------------------------------------------
+// Element types.
+// ---------------------------------------------------------------------------
+
+// Two bf16 in one 32-bit word -> two floats (bf16 is the high half of an fp32).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Two floats -> two bf16 (round to nearest even) in one 32-bit word.
+__device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <typename T> struct ElemIO;
+
+template <> struct ElemIO<float> {
+    static constexpr int kPerVec = 4;  // elements in 16 bytes
+    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float* f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                          __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+};
+
+template <> struct ElemIO<__nv_bfloat16> {
+    static constexpr int kPerVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+        float2 a = bf16x2_to_float2(u.x), b = bf16x2_to_float2(u.y);
+        float2 c = bf16x2_to_float2(u.z), d = bf16x2_to_float2(u.w);
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+        f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+    }
+    __device__ __forceinline__ static uint4 pack(const float* f) {
+        return make_uint4(float2_to_bf16x2(f[0], f[1]), float2_to_bf16x2(f[2], f[3]),
+                          float2_to_bf16x2(f[4], f[5]), float2_to_bf16x2(f[6], f[7]));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Shared-memory barriers and bulk copies (inline PTX).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity.  Gives up after about one
+// second and returns false; callers then record SK_DEVERR_TIMEOUT and carry on, so
+// a kernel can never spin forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > 1000000000ull) return false;
+    }
+}
+
+// L2 policy: data streamed once (evict first).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// One-dimensional bulk copy global -> shared, completion counted in bytes on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
+    if (err != nullptr) atomicOr(err, bits);
+}
+
+}  // namespace sk
+
+// Host helpers shared by the entry points.
+namespace sk {
+int device_sm_count();                                   // api.cu
+const float2* table_device(const sk_rope_table* t);      // rope_table.cu
+const sk_rope_config& table_config(const sk_rope_table* t);
+}

@@ -1,0 +1,351 @@
+// In-place rerotation of cached keys when the RoPE factor changes.
+//
+// "#2961 rope: --rope-scaling dynamic", "What it does": K is stored post-RoPE, so a
+// key written at factor A becomes the key of factor B after one more rotation of each
+// pair by p (w_B - w_A) and the magnitude ratio mscale_B / mscale_A; int8 keys are
+// dequantized, turned and requantized.  "Attention Sink 与 Streaming KV Cache": R_a R_b
+// = R_{a+b}, so no raw key is needed.  The delta rotation comes from the two tables'
+// entries at P: with (cA, sA) = mu_A (cos a, sin a) and (cB, sB) = mu_B (cos b, sin b),
+//   (cB cA + sB sA) / mu_A^2 = (mu_B / mu_A) cos(b - a),
+//   (sB cA - cB sA) / mu_A^2 = (mu_B / mu_A) sin(b - a).
+//
+// Layout of the work: one block covers a range of slots; each thread group owns one
+// slot and walks every (layer, sequence, kv head) row at that slot, recomputing the
+// delta only when the slot's position changes (never, for global layers).  The bf16
+// path reads and writes only the rotary bytes of each row; the int8 path moves the
+// whole row of codes plus its scale.
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace sk {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxLayers = 128;
+
+struct RerotLayer {
+    void* k;
+    float* scale;
+    const int32_t* head;
+    const int32_t* count;
+    const int64_t* pos;
+    uint32_t* err;
+    int64_t cap;
+    int kind, S, W;
+};
+
+struct RerotParams {
+    RerotLayer layers[kMaxLayers];
+    int n_layers;
+    int B, Hkv, r;
+    const float2* tA;
+    const float2* tB;
+    int64_t maxA, maxB;
+    float inv_muA2;
+};
+
+// Position held by `slot` of (layer, sequence b), or -1 when the slot is empty.
+__device__ __forceinline__ int64_t slot_position(const RerotLayer& L, int b, int64_t slot) {
+    if (slot >= L.cap) return -1;
+    const int64_t pos = L.pos[b];
+    if (L.kind == SK_LAYER_GLOBAL) return slot < pos ? slot : -1;
+    if (slot < L.S) return slot < min(pos, int64_t(L.S)) ? slot : -1;
+    const int64_t j = slot - L.S;
+    const int count = L.count[b];
+    if (j >= count) return -1;
+    const int64_t W = L.W;
+    const int64_t back = ((int64_t(L.head[b]) - 1 - j) % W + W) % W;  // steps behind the newest
+    return pos - 1 - back;
+}
+
+// Delta rotation (dc, ds) of NP consecutive pairs starting at j0, at position P.
+template <int NP>
+__device__ __forceinline__ void delta_pairs(const RerotParams& p, int64_t P, int j0, float* dc,
+                                            float* ds) {
+    const int half = p.r / 2;
+    const float4* a4 = reinterpret_cast<const float4*>(p.tA + P * half + j0);
+    const float4* b4 = reinterpret_cast<const float4*>(p.tB + P * half + j0);
+#pragma unroll
+    for (int i = 0; i < NP / 2; ++i) {
+        const float4 a = __ldg(a4 + i), b = __ldg(b4 + i);
+        dc[2 * i] = (b.x * a.x + b.y * a.y) * p.inv_muA2;
+        ds[2 * i] = (b.y * a.x - b.x * a.y) * p.inv_muA2;
+        dc[2 * i + 1] = (b.z * a.z + b.w * a.w) * p.inv_muA2;
+        ds[2 * i + 1] = (b.w * a.z - b.z * a.w) * p.inv_muA2;
+    }
+}
+
+// ---- bf16 keys: NeoX thread = 8 pairs (16 B of each half); GPT-J thread = 4 pairs ----
+template <int D, bool NEOX>
+__global__ void __launch_bounds__(kThreads) rerotate_bf16_kernel(RerotParams p) {
+    constexpr int NP = NEOX ? 8 : 4;  // pairs per thread
+    const int tpr = p.r / (2 * NP);   // threads per row
+    const int spb = kThreads / tpr;   // slots per block
+    const int t = threadIdx.x % tpr;
+    const int local = threadIdx.x / tpr;
+    if (local >= spb) return;
+    const int64_t slot = int64_t(blockIdx.x) * spb + local;
+    const int half = p.r / 2;
+    const int j0 = t * NP;
+    float dc[NP], ds[NP];
+    int64_t lastP = -1;
+    for (int l = 0; l < p.n_layers; ++l) {
+        const RerotLayer& L = p.layers[l];
+        for (int b = 0; b < p.B; ++b) {
+            const int64_t P = slot_position(L, b, slot);
+            if (P < 0) continue;
+            if (P >= p.maxA || P >= p.maxB) {
+                set_error(L.err, SK_DEVERR_POSITION_RANGE);
+                continue;
+            }
+            if (P != lastP) {
+                delta_pairs<NP>(p, P, j0, dc, ds);
+                lastP = P;
+            }
+            __nv_bfloat16* base = static_cast<__nv_bfloat16*>(L.k);
+            for (int g0 = 0; g0 < p.Hkv; g0 += 4) {
+                const int ng = min(4, p.Hkv - g0);
+                uint4 x1[4], x2[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (u < ng) {
+                        const __nv_bfloat16* row =
+                            base + ((int64_t(b) * p.Hkv + g0 + u) * L.cap + slot) * D;
+                        if (NEOX) {
+                            x1[u] = *reinterpret_cast<const uint4*>(row + j0);
+                            x2[u] = *reinterpret_cast<const uint4*>(row + half + j0);
+                        } else {
+                            x1[u] = *reinterpret_cast<const uint4*>(row + 2 * j0);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (u >= ng) continue;
+                    __nv_bfloat16* row = base + ((int64_t(b) * p.Hkv + g0 + u) * L.cap + slot) * D;
+                    if (NEOX) {
+                        float a[8], c[8];
+                        ElemIO<__nv_bfloat16>::unpack(x1[u], a);
+                        ElemIO<__nv_bfloat16>::unpack(x2[u], c);
+                        float o1[8], o2[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            o1[i] = fmaf(-c[i], ds[i], a[i] * dc[i]);
+                            o2[i] = fmaf(a[i], ds[i], c[i] * dc[i]);
+                        }
+                        *reinterpret_cast<uint4*>(row + j0) = ElemIO<__nv_bfloat16>::pack(o1);
+                        *reinterpret_cast<uint4*>(row + half + j0) = ElemIO<__nv_bfloat16>::pack(o2);
+                    } else {
+                        float a[8], o[8];
+                        ElemIO<__nv_bfloat16>::unpack(x1[u], a);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            o[2 * i] = fmaf(-a[2 * i + 1], ds[i], a[2 * i] * dc[i]);
+                            o[2 * i + 1] = fmaf(a[2 * i], ds[i], a[2 * i + 1] * dc[i]);
+                        }
+                        *reinterpret_cast<uint4*>(row + 2 * j0) = ElemIO<__nv_bfloat16>::pack(o);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---- int8 keys + per-row fp32 scale: D/32 threads per row, 32 codes each ----
+__device__ __forceinline__ void unpack16_i8(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[4 * i + e] = float(int8_t((w[i] >> (8 * e)) & 0xffu));
+}
+
+__device__ __forceinline__ uint4 pack16_i8(const float* x, float scale) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float q = rintf(__fdiv_rn(x[4 * i + e], scale));
+            q = fminf(127.0f, fmaxf(-127.0f, q));
+            packed |= (uint32_t(int32_t(q)) & 0xffu) << (8 * e);
+        }
+        w[i] = packed;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int D, bool NEOX>
+__global__ void __launch_bounds__(kThreads) rerotate_i8_kernel(RerotParams p) {
+    constexpr int TPR = D / 32;  // threads per row (aligned group of 2 or 4 lanes)
+    constexpr int SPB = kThreads / TPR;
+    const int t = threadIdx.x % TPR;
+    const int64_t slot = int64_t(blockIdx.x) * SPB + threadIdx.x / TPR;
+    const int half = p.r / 2;
+    const bool rot = t < p.r / 32;
+    // NeoX rotary thread t: codes [16t, 16t+16) and [half+16t, ...), pairs j0 = 16t.
+    // GPT-J rotary thread t: codes [32t, 32t+32), pairs j0 = 16t.
+    // Tail thread: codes [r + 32 (t - r/32), +32).
+    const int j0 = 16 * t;
+    const int off1 = rot ? (NEOX ? 16 * t : 32 * t) : p.r + 32 * (t - p.r / 32);
+    const int off2 = rot ? (NEOX ? half + 16 * t : 32 * t + 16) : off1 + 16;
+    float dc[16], ds[16];
+    int64_t lastP = -1;
+    for (int l = 0; l < p.n_layers; ++l) {
+        const RerotLayer& L = p.layers[l];
+        for (int b = 0; b < p.B; ++b) {
+            // Lanes of one warp hold different slots, so validity differs between row
+            // groups: every lane runs the loop and the shuffles, only valid rows touch memory.
+            int64_t P = slot_position(L, b, slot);
+            bool valid = P >= 0;
+            if (valid && (P >= p.maxA || P >= p.maxB)) {
+                set_error(L.err, SK_DEVERR_POSITION_RANGE);
+                valid = false;
+            }
+            if (valid && rot && P != lastP) {
+                delta_pairs<16>(p, P, j0, dc, ds);
+                lastP = P;
+            }
+            for (int g = 0; g < p.Hkv; ++g) {
+                const int64_t crow = (int64_t(b) * p.Hkv + g) * L.cap + slot;
+                int8_t* row = static_cast<int8_t*>(L.k) + crow * D;
+                float s_old = 0.0f;
+                uint4 u1 = make_uint4(0, 0, 0, 0), u2 = make_uint4(0, 0, 0, 0);
+                if (valid) {
+                    s_old = L.scale[crow];
+                    u1 = *reinterpret_cast<const uint4*>(row + off1);
+                    u2 = *reinterpret_cast<const uint4*>(row + off2);
+                }
+                float a[16], c[16];
+                unpack16_i8(u1, a);
+                unpack16_i8(u2, c);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    a[i] *= s_old;
+                    c[i] *= s_old;
+                }
+                if (valid && rot) {
+                    if (NEOX) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float x1 = a[i], x2 = c[i];
+                            a[i] = fmaf(-x2, ds[i], x1 * dc[i]);
+                            c[i] = fmaf(x1, ds[i], x2 * dc[i]);
+                        }
+                    } else {
+                        float f[32];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            f[i] = a[i];
+                            f[16 + i] = c[i];
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float x1 = f[2 * i], x2 = f[2 * i + 1];
+                            f[2 * i] = fmaf(-x2, ds[i], x1 * dc[i]);
+                            f[2 * i + 1] = fmaf(x1, ds[i], x2 * dc[i]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            a[i] = f[i];
+                            c[i] = f[16 + i];
+                        }
+                    }
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(a[i]), fabsf(c[i])));
+#pragma unroll
+                for (int o = TPR / 2; o > 0; o >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                const float s_new = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 127.0f);
+                if (valid) {
+                    *reinterpret_cast<uint4*>(row + off1) = pack16_i8(a, s_new);
+                    *reinterpret_cast<uint4*>(row + off2) = pack16_i8(c, s_new);
+                    if (t == 0) L.scale[crow] = s_new;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+}  // namespace sk
+
+using namespace sk;
+
+extern "C" sk_status sk_kv_rerotate(const sk_kv_layer* layers, int32_t n_layers,
+                                    const sk_rope_table* from, const sk_rope_table* to,
+                                    void* stream) {
+    SK_RET_IF(layers == nullptr || from == nullptr || to == nullptr, SK_ERR_ARG);
+    SK_RET_IF(n_layers < 1 || n_layers > kMaxLayers, SK_ERR_ARG);
+    const sk_rope_config& ca = table_config(from);
+    const sk_rope_config& cb = table_config(to);
+    SK_RET_IF(ca.head_dim != cb.head_dim || ca.rotary_dim != cb.rotary_dim || ca.neox != cb.neox ||
+                  ca.theta != cb.theta,
+              SK_ERR_ARG);
+    const sk_kv_layer& L0 = layers[0];
+    const int D = L0.head_dim;
+    SK_RET_IF(D != ca.head_dim, SK_ERR_ARG);
+    SK_RET_IF(L0.k_dtype != SK_BF16 && L0.k_dtype != SK_I8, SK_ERR_UNSUPPORTED);
+    SK_RET_IF(L0.k_dtype == SK_I8 && ca.rotary_dim % 32 != 0, SK_ERR_UNSUPPORTED);
+    // the bf16 path needs a whole number of thread groups per block
+    RerotParams p{};
+    p.n_layers = n_layers;
+    p.B = L0.batch;
+    p.Hkv = L0.n_kv_heads;
+    p.r = ca.rotary_dim;
+    p.tA = table_device(from);
+    p.tB = table_device(to);
+    p.maxA = ca.max_positions;
+    p.maxB = cb.max_positions;
+    const double mu_a = ca.yarn_factor <= 1.0 ? 1.0 : 0.1 * std::log(ca.yarn_factor) + 1.0;
+    p.inv_muA2 = float(1.0 / (mu_a * mu_a));
+    int64_t max_cap = 0;
+    for (int l = 0; l < n_layers; ++l) {
+        const sk_kv_layer& L = layers[l];
+        SK_RET_IF(L.k == nullptr || L.pos == nullptr, SK_ERR_ARG);
+        SK_RET_IF(L.batch != p.B || L.n_kv_heads != p.Hkv || L.head_dim != D ||
+                      L.k_dtype != L0.k_dtype,
+                  SK_ERR_ARG);
+        SK_RET_IF(L.k_dtype == SK_I8 && L.k_scale == nullptr, SK_ERR_ARG);
+        SK_RET_IF(reinterpret_cast<uintptr_t>(L.k) & 15u, SK_ERR_ARG);
+        if (L.kind == SK_LAYER_RING) {
+            SK_RET_IF(L.head == nullptr || L.count == nullptr || L.window < 1 || L.sinks < 0 ||
+                          L.capacity != int64_t(L.sinks) + L.window,
+                      SK_ERR_ARG);
+        } else {
+            SK_RET_IF(L.kind != SK_LAYER_GLOBAL || L.capacity < 1, SK_ERR_ARG);
+        }
+        p.layers[l] = RerotLayer{L.k, L.k_scale, L.head, L.count, L.pos, L.err,
+                                 L.capacity, L.kind, L.sinks, L.window};
+        max_cap = std::max(max_cap, L.capacity);
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool neox = ca.neox != 0;
+    int64_t blocks;
+    if (L0.k_dtype == SK_BF16) {
+        const int tpr = p.r / (neox ? 16 : 8);
+        const int spb = kThreads / tpr;
+        blocks = (max_cap + spb - 1) / spb;
+        if (D == 64)
+            neox ? rerotate_bf16_kernel<64, true><<<unsigned(blocks), kThreads, 0, st>>>(p)
+                 : rerotate_bf16_kernel<64, false><<<unsigned(blocks), kThreads, 0, st>>>(p);
+        else
+            neox ? rerotate_bf16_kernel<128, true><<<unsigned(blocks), kThreads, 0, st>>>(p)
+                 : rerotate_bf16_kernel<128, false><<<unsigned(blocks), kThreads, 0, st>>>(p);
+    } else {
+        const int spb = kThreads / (D / 32);
+        blocks = (max_cap + spb - 1) / spb;
+        if (D == 64)
+            neox ? rerotate_i8_kernel<64, true><<<unsigned(blocks), kThreads, 0, st>>>(p)
+                 : rerotate_i8_kernel<64, false><<<unsigned(blocks), kThreads, 0, st>>>(p);
+        else
+            neox ? rerotate_i8_kernel<128, true><<<unsigned(blocks), kThreads, 0, st>>>(p)
+                 : rerotate_i8_kernel<128, false><<<unsigned(blocks), kThreads, 0, st>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}

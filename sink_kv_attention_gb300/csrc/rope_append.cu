@@ -1,0 +1,441 @@
+// RoPE apply and fused RoPE + KV append (ring with pinned sinks, or global prefix).
+//
+// "RoPE, scaling, sliding window, attention sinks": the rotation listing
+// (o1 = x1 cos - x2 sin, o2 = x2 cos + x1 sin), NeoX vs GPT-J pairing, partial rotary,
+// table gather with no trigonometry at runtime, and one counter for angle and slot.
+// "Inference & 128K Long Context", MixedKVCache: the ring's head/count rules and the
+// global prefix; "Attention Sink 与 Streaming KV Cache": S pinned sink slots.
+//
+// Work layout: a row (one head of one token, head_dim elements) is handled by
+// LPR = head_dim / (16 bytes / element size) lanes, each holding one 16-byte vector,
+// so every load and store is a coalesced 16-byte access.  A NeoX pair (j, j + r/2)
+// lives in two lanes of the same row; the partner's vector arrives by shuffle.
+#include "common.cuh"
+
+namespace sk {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+template <typename T, int D> struct RowLayout {
+    static constexpr int VEC = ElemIO<T>::kPerVec;  // elements per lane
+    static constexpr int LPR = D / VEC;             // lanes per row: 8, 16 or 32
+    static constexpr int RPW = 32 / LPR;            // rows per warp
+};
+
+// Rotate the VEC elements of this lane (c = lane index within its row).  Every lane of
+// the warp must call this (it shuffles); `active` lanes update f.
+template <typename T, int D, bool NEOX>
+__device__ __forceinline__ void rotate_lane(float* f, const uint4& raw, const float2* trow,
+                                            int rotary_dim, int c, int lane, bool active) {
+    constexpr int VEC = RowLayout<T, D>::VEC;
+    if constexpr (NEOX) {
+        const int hc = (rotary_dim / 2) / VEC;  // vectors per half of the rotary part
+        const bool rot = c < 2 * hc;
+        const int partner_c = c < hc ? c + hc : c - hc;
+        const int src = lane - c + (rot ? partner_c : c);
+        uint4 pr;
+        pr.x = __shfl_sync(kFull, raw.x, src);
+        pr.y = __shfl_sync(kFull, raw.y, src);
+        pr.z = __shfl_sync(kFull, raw.z, src);
+        pr.w = __shfl_sync(kFull, raw.w, src);
+        if (active && rot) {
+            float p[VEC];
+            ElemIO<T>::unpack(pr, p);
+            const int j0 = (c < hc ? c : c - hc) * VEC;
+            const float4* t4 = reinterpret_cast<const float4*>(trow + j0);
+            const float sign = c < hc ? -1.0f : 1.0f;  // first: x1 c - x2 s; second: x2 c + x1 s
+#pragma unroll
+            for (int i = 0; i < VEC / 2; ++i) {
+                const float4 cs = __ldg(t4 + i);  // (cos, sin) of pairs j0+2i, j0+2i+1
+                f[2 * i] = fmaf(sign * p[2 * i], cs.y, f[2 * i] * cs.x);
+                f[2 * i + 1] = fmaf(sign * p[2 * i + 1], cs.w, f[2 * i + 1] * cs.z);
+            }
+        }
+    } else {
+        if (active && c * VEC < rotary_dim) {
+            const int j0 = c * VEC / 2;
+            const float4* t4 = reinterpret_cast<const float4*>(trow + j0);
+#pragma unroll
+            for (int i = 0; i < VEC / 4; ++i) {
+                const float4 cs = __ldg(t4 + i);
+                float x1 = f[4 * i], x2 = f[4 * i + 1];
+                f[4 * i] = fmaf(-x2, cs.y, x1 * cs.x);
+                f[4 * i + 1] = fmaf(x1, cs.y, x2 * cs.x);
+                x1 = f[4 * i + 2]; x2 = f[4 * i + 3];
+                f[4 * i + 2] = fmaf(-x2, cs.w, x1 * cs.z);
+                f[4 * i + 3] = fmaf(x1, cs.w, x2 * cs.z);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// rope_apply: in-place rotation of x [n_tok][H][D].
+// ---------------------------------------------------------------------------
+
+struct ApplyParams {
+    const float2* table;
+    int64_t max_pos;
+    int rotary_dim;
+    void* x;
+    int64_t n_tok;
+    int H;
+    const int64_t* positions;
+    uint32_t* err;
+};
+
+template <typename T, int D, bool NEOX>
+__global__ void __launch_bounds__(kThreads) rope_apply_kernel(ApplyParams p) {
+    using L = RowLayout<T, D>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c = lane % L::LPR, rw = lane / L::LPR;
+    const int half = p.rotary_dim / 2;
+    const int64_t n_rows = p.n_tok * p.H;
+    const int64_t stride = int64_t(gridDim.x) * kWarps * L::RPW;
+    T* x = static_cast<T*>(p.x);
+    for (int64_t base = (int64_t(blockIdx.x) * kWarps + warp) * L::RPW; base < n_rows;
+         base += stride) {
+        const int64_t row = base + rw;
+        bool active = row < n_rows;
+        int64_t P = 0;
+        if (active) {
+            P = p.positions[row / p.H];
+            if (P < 0 || P >= p.max_pos) {
+                if (c == 0) set_error(p.err, SK_DEVERR_POSITION_RANGE);
+                active = false;
+            }
+        }
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        uint4* ptr = reinterpret_cast<uint4*>(x + row * D) + c;
+        if (active) raw = *ptr;
+        float f[L::VEC];
+        ElemIO<T>::unpack(raw, f);
+        rotate_lane<T, D, NEOX>(f, raw, p.table + (active ? P : 0) * half, p.rotary_dim, c, lane,
+                                active);
+        if (active) *ptr = ElemIO<T>::pack(f);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// kv_append: rotate q (in place) and k (in place), write k and v into the cache.
+// ---------------------------------------------------------------------------
+
+struct AppendParams {
+    const float2* table;
+    int64_t max_pos;
+    int rotary_dim;
+    void* q;
+    void* k;
+    const void* v;
+    int Hq, Hkv, T, B;
+    void* kc;
+    void* vc;
+    float* kscale;
+    int64_t cap;
+    int S, W, kind;
+    int32_t* head;
+    int32_t* count;
+    int64_t* pos;
+    uint32_t* err;
+    int fused_state;
+};
+
+struct SeqState {
+    int64_t pos;
+    int head, count;
+    bool ok;
+    uint32_t err_bits;
+};
+
+__device__ __forceinline__ SeqState load_state(const AppendParams& p, int b) {
+    SeqState s;
+    s.pos = p.pos[b];
+    s.head = p.kind == SK_LAYER_RING ? p.head[b] : 0;
+    s.count = p.kind == SK_LAYER_RING ? p.count[b] : 0;
+    s.err_bits = 0;
+    if (s.pos < 0 || s.pos + p.T > p.max_pos) s.err_bits |= SK_DEVERR_POSITION_RANGE;
+    if (p.kind == SK_LAYER_GLOBAL && s.pos + p.T > p.cap) s.err_bits |= SK_DEVERR_CAPACITY;
+    s.ok = s.err_bits == 0;
+    return s;
+}
+
+// Slot of chunk token t, or -1 when a long chunk drops it (ring rules in the header).
+__device__ __forceinline__ int64_t token_slot(const AppendParams& p, const SeqState& s, int t) {
+    const int64_t P = s.pos + t;
+    if (p.kind == SK_LAYER_GLOBAL) return P;
+    if (P < p.S) return P;
+    const int64_t t0 = max(int64_t(0), min(int64_t(p.T), int64_t(p.S) - s.pos));
+    const int64_t n = p.T - t0;
+    const int64_t u = t - t0;
+    if (n >= p.W) {
+        if (u < n - p.W) return -1;
+        return p.S + (u - (n - p.W));
+    }
+    return p.S + (s.head + u) % p.W;
+}
+
+__device__ __forceinline__ void advance_state(const AppendParams& p, const SeqState& s, int b) {
+    if (!s.ok) {
+        set_error(p.err, s.err_bits);
+        return;
+    }
+    if (p.kind == SK_LAYER_RING) {
+        const int64_t t0 = max(int64_t(0), min(int64_t(p.T), int64_t(p.S) - s.pos));
+        const int64_t n = p.T - t0;
+        if (n >= p.W) {
+            p.head[b] = 0;
+            p.count[b] = p.W;
+        } else {
+            p.head[b] = int((s.head + n) % p.W);
+            p.count[b] = int(min(int64_t(p.W), s.count + n));
+        }
+    }
+    p.pos[b] = s.pos + p.T;
+}
+
+template <typename KC> struct CacheStore;
+
+template <> struct CacheStore<float> {
+    template <int VEC>
+    __device__ __forceinline__ static void store(void* base, int64_t elem, const float* f) {
+        static_assert(VEC == 4, "f32 cache takes f32 rows");
+        *reinterpret_cast<uint4*>(static_cast<float*>(base) + elem) = ElemIO<float>::pack(f);
+    }
+};
+
+template <> struct CacheStore<__nv_bfloat16> {
+    template <int VEC>
+    __device__ __forceinline__ static void store(void* base, int64_t elem, const float* f) {
+        static_assert(VEC == 8, "bf16 cache takes bf16 rows");
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + elem) =
+            ElemIO<__nv_bfloat16>::pack(f);
+    }
+};
+
+template <typename IO, typename KC, typename VC, int D, bool NEOX>
+__global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendParams p) {
+    using L = RowLayout<IO, D>;
+    constexpr int VEC = L::VEC;
+    const int b = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c = lane % L::LPR, rw = lane / L::LPR;
+    const int half = p.rotary_dim / 2;
+    const SeqState s = load_state(p, b);
+    const int hq = p.q != nullptr ? p.Hq : 0;
+    const int rows_per_tok = hq + 2 * p.Hkv;
+    const int64_t n_rows = int64_t(p.T) * rows_per_tok;
+    const int64_t stride = int64_t(gridDim.x) * kWarps * L::RPW;
+
+    IO* q = static_cast<IO*>(p.q);
+    IO* k = static_cast<IO*>(p.k);
+    const IO* v = static_cast<const IO*>(p.v);
+
+    for (int64_t base = (int64_t(blockIdx.x) * kWarps + warp) * L::RPW; base < n_rows;
+         base += stride) {
+        const int64_t row = base + rw;
+        const bool in_range = s.ok && row < n_rows;
+        const int t = in_range ? int(row / rows_per_tok) : 0;
+        const int r = in_range ? int(row % rows_per_tok) : 0;
+        // which tensor: 0 = q, 1 = k, 2 = v
+        const int which = r < hq ? 0 : (r < hq + p.Hkv ? 1 : 2);
+        const int h = which == 0 ? r : (which == 1 ? r - hq : r - hq - p.Hkv);
+        const int64_t tok = int64_t(b) * p.T + t;
+        IO* src = which == 0 ? q + (tok * p.Hq + h) * D
+                             : (which == 1 ? k + (tok * p.Hkv + h) * D
+                                           : const_cast<IO*>(v) + (tok * p.Hkv + h) * D);
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (in_range) raw = reinterpret_cast<const uint4*>(src)[c];
+        float f[VEC];
+        ElemIO<IO>::unpack(raw, f);
+        const int64_t P = s.pos + t;
+        rotate_lane<IO, D, NEOX>(f, raw, p.table + (in_range ? P : 0) * half, p.rotary_dim, c,
+                                 lane, in_range && which != 2);
+        if (in_range && which != 2) reinterpret_cast<uint4*>(src)[c] = ElemIO<IO>::pack(f);
+
+        const int64_t slot = in_range && which != 0 ? token_slot(p, s, t) : -1;
+        const int64_t crow = (int64_t(b) * p.Hkv + h) * p.cap + slot;  // cache row index
+        if constexpr (sizeof(KC) == 1) {
+            // int8 K: symmetric absmax over the row, rint half to even, IEEE division.
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+            for (int o = L::LPR / 2; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            if (which == 1 && slot >= 0) {
+                const float scale = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 127.0f);
+                uint32_t w[VEC / 4];
+#pragma unroll
+                for (int i = 0; i < VEC / 4; ++i) {
+                    uint32_t packed = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float qv = rintf(__fdiv_rn(f[4 * i + e], scale));
+                        qv = fminf(127.0f, fmaxf(-127.0f, qv));
+                        packed |= (uint32_t(int32_t(qv)) & 0xffu) << (8 * e);
+                    }
+                    w[i] = packed;
+                }
+                int8_t* dst = static_cast<int8_t*>(p.kc) + crow * D + c * VEC;
+                if constexpr (VEC == 8)
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                else
+                    *reinterpret_cast<uint32_t*>(dst) = w[0];
+                if (c == 0) p.kscale[crow] = scale;
+            }
+        } else {
+            if (which == 1 && slot >= 0) CacheStore<KC>::template store<VEC>(p.kc, crow * D + c * VEC, f);
+        }
+        if (which == 2 && slot >= 0) CacheStore<VC>::template store<VEC>(p.vc, crow * D + c * VEC, f);
+    }
+    if (p.fused_state) {
+        __syncthreads();  // every thread has read the state before it changes
+        if (threadIdx.x == 0) advance_state(p, s, b);
+    }
+}
+
+__global__ void kv_append_state_kernel(AppendParams p) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= p.B) return;
+    const SeqState s = load_state(p, b);
+    advance_state(p, s, b);
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+template <typename T, int D, bool NEOX>
+cudaError_t launch_apply(const ApplyParams& p, cudaStream_t st) {
+    using L = RowLayout<T, D>;
+    const int64_t n_rows = p.n_tok * p.H;
+    int64_t blocks = (n_rows + kWarps * L::RPW - 1) / (kWarps * L::RPW);
+    blocks = std::min<int64_t>(blocks, int64_t(device_sm_count()) * 8);
+    if (blocks < 1) blocks = 1;
+    rope_apply_kernel<T, D, NEOX><<<unsigned(blocks), kThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename IO, typename KC, typename VC, int D, bool NEOX>
+cudaError_t launch_append(AppendParams p, cudaStream_t st) {
+    using L = RowLayout<IO, D>;
+    const int hq = p.q != nullptr ? p.Hq : 0;
+    const int64_t n_rows = int64_t(p.T) * (hq + 2 * p.Hkv);
+    const int64_t per_block = kWarps * L::RPW;
+    int64_t gx = (n_rows + per_block - 1) / per_block;
+    p.fused_state = gx <= 4 ? 1 : 0;
+    if (p.fused_state) {
+        gx = 1;
+    } else {
+        const int64_t cap = std::max<int64_t>(1, int64_t(device_sm_count()) * 8 / p.B);
+        gx = std::min(gx, cap);
+    }
+    dim3 grid(unsigned(gx), unsigned(p.B));
+    kv_append_kernel<IO, KC, VC, D, NEOX><<<grid, kThreads, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.fused_state) return e;
+    kv_append_state_kernel<<<(p.B + 127) / 128, 128, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename IO, typename KC, typename VC>
+cudaError_t dispatch_append(const AppendParams& p, int D, bool neox, cudaStream_t st) {
+    if (D == 64)
+        return neox ? launch_append<IO, KC, VC, 64, true>(p, st)
+                    : launch_append<IO, KC, VC, 64, false>(p, st);
+    return neox ? launch_append<IO, KC, VC, 128, true>(p, st)
+                : launch_append<IO, KC, VC, 128, false>(p, st);
+}
+
+}  // namespace
+}  // namespace sk
+
+using namespace sk;
+
+extern "C" sk_status sk_rope_apply(const sk_rope_table* table, void* x, int32_t dtype, int64_t n_tok,
+                                   int32_t n_heads, const int64_t* positions, uint32_t* err,
+                                   void* stream) {
+    SK_RET_IF(table == nullptr || x == nullptr || positions == nullptr, SK_ERR_ARG);
+    SK_RET_IF(n_tok < 0 || n_heads < 1, SK_ERR_ARG);
+    SK_RET_IF(dtype != SK_BF16 && dtype != SK_F32, SK_ERR_UNSUPPORTED);
+    SK_RET_IF(!aligned16(x), SK_ERR_ARG);
+    if (n_tok == 0) return SK_OK;
+    const sk_rope_config& c = table_config(table);
+    ApplyParams p{table_device(table), c.max_positions, c.rotary_dim, x, n_tok, n_heads, positions, err};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    const bool neox = c.neox != 0;
+    if (dtype == SK_BF16) {
+        if (c.head_dim == 64)
+            e = neox ? launch_apply<__nv_bfloat16, 64, true>(p, st) : launch_apply<__nv_bfloat16, 64, false>(p, st);
+        else
+            e = neox ? launch_apply<__nv_bfloat16, 128, true>(p, st) : launch_apply<__nv_bfloat16, 128, false>(p, st);
+    } else {
+        if (c.head_dim == 64)
+            e = neox ? launch_apply<float, 64, true>(p, st) : launch_apply<float, 64, false>(p, st);
+        else
+            e = neox ? launch_apply<float, 128, true>(p, st) : launch_apply<float, 128, false>(p, st);
+    }
+    return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}
+
+extern "C" sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer* layer, void* q,
+                                  int32_t n_q_heads, void* k, const void* v, int32_t io_dtype,
+                                  int32_t T, void* stream) {
+    SK_RET_IF(table == nullptr || layer == nullptr || k == nullptr || v == nullptr, SK_ERR_ARG);
+    const sk_kv_layer& L = *layer;
+    const sk_rope_config& c = table_config(table);
+    SK_RET_IF(L.k == nullptr || L.v == nullptr || L.pos == nullptr, SK_ERR_ARG);
+    SK_RET_IF(L.batch < 1 || L.n_kv_heads < 1 || T < 0, SK_ERR_ARG);
+    SK_RET_IF(L.head_dim != c.head_dim, SK_ERR_ARG);
+    if (L.kind == SK_LAYER_RING) {
+        SK_RET_IF(L.head == nullptr || L.count == nullptr, SK_ERR_ARG);
+        SK_RET_IF(L.sinks < 0 || L.window < 1, SK_ERR_ARG);
+        SK_RET_IF(L.capacity != int64_t(L.sinks) + L.window, SK_ERR_ARG);
+    } else if (L.kind == SK_LAYER_GLOBAL) {
+        SK_RET_IF(L.capacity < 1, SK_ERR_ARG);
+    } else {
+        return SK_ERR_ARG;
+    }
+    if (q != nullptr) SK_RET_IF(n_q_heads < 1 || n_q_heads % L.n_kv_heads != 0, SK_ERR_ARG);
+    SK_RET_IF(!aligned16(k) || !aligned16(v) || !aligned16(L.k) || !aligned16(L.v), SK_ERR_ARG);
+    SK_RET_IF(q != nullptr && !aligned16(q), SK_ERR_ARG);
+    if (L.k_dtype == SK_I8) SK_RET_IF(L.k_scale == nullptr, SK_ERR_ARG);
+    if (T == 0) return SK_OK;
+
+    AppendParams p{};
+    p.table = table_device(table);
+    p.max_pos = c.max_positions;
+    p.rotary_dim = c.rotary_dim;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.Hq = n_q_heads;
+    p.Hkv = L.n_kv_heads;
+    p.T = T;
+    p.B = L.batch;
+    p.kc = L.k;
+    p.vc = L.v;
+    p.kscale = L.k_scale;
+    p.cap = L.capacity;
+    p.S = L.sinks;
+    p.W = L.window;
+    p.kind = L.kind;
+    p.head = L.head;
+    p.count = L.count;
+    p.pos = L.pos;
+    p.err = L.err;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool neox = c.neox != 0;
+    cudaError_t e;
+    if (io_dtype == SK_F32 && L.k_dtype == SK_F32 && L.v_dtype == SK_F32)
+        e = dispatch_append<float, float, float>(p, L.head_dim, neox, st);
+    else if (io_dtype == SK_BF16 && L.k_dtype == SK_BF16 && L.v_dtype == SK_BF16)
+        e = dispatch_append<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(p, L.head_dim, neox, st);
+    else if (io_dtype == SK_BF16 && L.k_dtype == SK_I8 && L.v_dtype == SK_BF16)
+        e = dispatch_append<__nv_bfloat16, int8_t, __nv_bfloat16>(p, L.head_dim, neox, st);
+    else
+        return SK_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}

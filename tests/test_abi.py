@@ -1,0 +1,91 @@
+"""The C-ABI library loads and exports every symbol include/sinkkv.h declares, and its
+host-side argument checks reject bad calls before touching the GPU (no compute calls)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "sinkkv.h")
+
+
+def _declared():
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^SK_API\s+[\w\s\*]+?\b(sk_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import sink_kv_attention_gb300 as sk
+    if not os.path.exists(sk.LIB_PATH):
+        from sink_kv_attention_gb300 import build
+        build.build()
+    return sk._lib()
+
+
+def test_header_declares_the_five_operations():
+    names = _declared()
+    for op in ["sk_rope_apply", "sk_kv_append", "sk_decode_attention", "sk_prefill_attention",
+               "sk_kv_rerotate", "sk_rope_table_create", "sk_rope_table_rebuild"]:
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import sink_kv_attention_gb300 as sk
+    declared = _declared()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(sk.EXPORTED) == declared
+    out = subprocess.run(["nm", "-D", "--defined-only", sk.LIB_PATH], capture_output=True, text=True).stdout
+    exported = sorted(l.split()[-1] for l in out.splitlines() if " T " in l)
+    assert exported == declared  # nothing else leaks out of the library
+
+
+def test_status_strings_and_version(lib):
+    assert lib.sk_status_str(0) == b"SK_OK"
+    assert b"capacity" in lib.sk_status_str(2)
+    assert lib.sk_version() >= 100
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """ctypes mirrors of sk_rope_config / sk_kv_layer match the C compiler's layout."""
+    import sink_kv_attention_gb300 as sk
+    src = tmp_path / "layout.c"
+    fields = {"sk_rope_config": [f for f, _ in sk.RopeConfig._fields_],
+              "sk_kv_layer": [f for f, _ in sk.KVLayerStruct._fields_]}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "sinkkv.h"', "int main(void) {"]
+    for st, fs in fields.items():
+        lines.append(f'printf("{st} %zu\\n", sizeof({st}));')
+        for f in fs:
+            lines.append(f'printf("{st}.{f} %zu\\n", offsetof({st}, {f}));')
+    lines.append("return 0; }")
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True).stdout.splitlines())
+    for name, cls in [("sk_rope_config", sk.RopeConfig), ("sk_kv_layer", sk.KVLayerStruct)]:
+        assert int(got[name]) == ctypes.sizeof(cls)
+        for f, _ in cls._fields_:
+            assert int(got[f"{name}.{f}"]) == getattr(cls, f).offset, f
+
+
+def test_bad_arguments_rejected_on_host(lib):
+    import sink_kv_attention_gb300 as sk
+    out = ctypes.c_void_p()
+    bad = sk.RopeConfig(96, 64, 1, 0, 1e4, 1.0, 4096, 32.0, 1.0, 16)   # head_dim 96 unsupported
+    assert lib.sk_rope_table_create(ctypes.byref(bad), None, ctypes.byref(out)) == sk.SK_ERR_ARG
+    bad = sk.RopeConfig(128, 72, 1, 0, 1e4, 1.0, 4096, 32.0, 1.0, 16)  # r not a multiple of 16
+    assert lib.sk_rope_table_create(ctypes.byref(bad), None, ctypes.byref(out)) == sk.SK_ERR_ARG
+    bad = sk.RopeConfig(128, 128, 1, 0, 1.0, 1.0, 4096, 32.0, 1.0, 16)  # theta must exceed 1
+    assert lib.sk_rope_table_create(ctypes.byref(bad), None, ctypes.byref(out)) == sk.SK_ERR_ARG
+    assert lib.sk_rope_table_create(None, None, ctypes.byref(out)) == sk.SK_ERR_ARG
+    assert lib.sk_kv_append(None, None, None, 0, None, None, 0, 1, None) == sk.SK_ERR_ARG
+    assert lib.sk_decode_attention(None, None, 8, 0, None, None, 0, None) == sk.SK_ERR_ARG
+    assert lib.sk_decode_workspace_bytes(None, 8) == 0
+    assert lib.sk_kv_rerotate(None, 1, None, None, None) == sk.SK_ERR_ARG
+    assert lib.sk_rope_apply(None, None, 0, 1, 1, None, None, None) == sk.SK_ERR_ARG
+    lib.sk_rope_table_destroy(None)  # NULL is ignored
