@@ -201,6 +201,36 @@ SK_API sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q_rot
                               int32_t io_dtype, void* out, void* workspace, size_t ws_bytes,
                               void* stream);
 
+/* ---- Decode attention without any allocation -------------------------------------- */
+
+/* Bytes of the library's built-in decode scratch (see below). */
+#define SK_DECODE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* sk_decode_attention for callers that cannot allocate device memory.
+ * The source pages have no counterpart to this call: it exists for callers that
+ * must not call cudaMalloc or any allocating routine, for example a serving loop
+ * whose device memory is fully carved up by its own pool at start-up, a plug-in that
+ * runs inside a host application that owns all device allocations, or a runtime
+ * with a no-allocation rule on its steady-state path.  It does the same work with
+ * the same arguments, minus the workspace: the scratch comes from one fixed
+ * SK_DECODE_NOALLOC_SCRATCH_BYTES (4 MiB) array in device memory that the library
+ * declares statically, so every GPU that loads the library holds those 4 MiB until
+ * the process exits.
+ *   - Set-up: the first call on each device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream capture.
+ *   - Limit: the scratch needed grows with batch * n_kv_heads (about
+ *     (152 + batch * n_kv_heads) * n_q_heads/n_kv_heads * (head_dim + 2) * 4 bytes);
+ *     when it exceeds the array the call launches nothing and returns
+ *     SK_ERR_CAPACITY.  Use sk_decode_attention with your own workspace then.
+ *   - Sharing: every call uses the same array.  Calls that may overlap on the GPU
+ *     (on different streams without ordering) race on it and give wrong results;
+ *     serialise them on one stream.  Each call writes every scratch word it reads,
+ *     so the contents left by an earlier call never matter.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+SK_API sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const void* q_rot,
+                                             int32_t n_q_heads, int32_t io_dtype, void* out,
+                                             void* stream);
+
 /* ---- Prefill attention (causal + window + sinks) ---------------------------------- */
 
 /* Masked attention of a prompt chunk over itself on the tensor cores.

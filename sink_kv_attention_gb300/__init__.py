@@ -72,6 +72,8 @@ _SIGNATURES = [
     ("sk_decode_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32]),
     ("sk_decode_attention", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    ("sk_decode_attention_noalloc", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32,
+                                                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_prefill_attention", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                             ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
@@ -295,6 +297,18 @@ def decode_attention(layer: KVLayer, q_rot: torch.Tensor, out: Optional[torch.Te
     _check(_lib().sk_decode_attention(ctypes.byref(s), _ptr(q_rot), Hq, _sk_dtype(q_rot.dtype), _ptr(out),
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "sk_decode_attention")
+    return out
+
+
+def decode_attention_noalloc(layer: KVLayer, q_rot: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Decode attention for callers that cannot allocate device memory: the scratch
+    is the library's fixed 4 MiB device array (sk_decode_attention_noalloc); `out`
+    must be given.  Calls that may overlap on the GPU race on that array."""
+    _need_contig(q_rot, out)
+    s = layer.struct()
+    _check(_lib().sk_decode_attention_noalloc(ctypes.byref(s), _ptr(q_rot), q_rot.shape[1],
+                                              _sk_dtype(q_rot.dtype), _ptr(out), _stream(stream)),
+           "sk_decode_attention_noalloc")
     return out
 
 

@@ -25,6 +25,7 @@
 // back from shared memory as (p, p) pairs ready for packed fp32 FMAs.
 // A second kernel combines each unit's partials by log-sum-exp.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -622,4 +623,52 @@ extern "C" sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q
     p.qscale = kLog2e / sqrtf(float(L.head_dim));
     route(io_dtype, L, nrep, false, &p, static_cast<cudaStream_t>(stream), nullptr, &e);
     return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention with the library's own fixed scratch (no allocation).
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// The scratch of sk_decode_attention_noalloc.  In host code this name is only a
+// stand-in: its device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SK_DECODE_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up on first use.
+sk_status noalloc_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    SK_CUDA_RET(cudaGetDevice(&dev));
+    SK_RET_IF(dev < 0 || dev >= 64, SK_ERR_UNSUPPORTED);
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        SK_CUDA_RET(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+        SK_RET_IF(p == nullptr, SK_ERR_CUDA);
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return SK_OK;
+}
+
+}  // namespace
+
+extern "C" sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const void* q_rot,
+                                                 int32_t n_q_heads, int32_t io_dtype, void* out,
+                                                 void* stream) {
+    sk_status s = check_layer(layer, n_q_heads);
+    if (s != SK_OK) return s;
+    SK_RET_IF(q_rot == nullptr || out == nullptr, SK_ERR_ARG);
+    const int nrep = n_q_heads / layer->n_kv_heads;
+    size_t need = 0;
+    cudaError_t e = cudaSuccess;
+    if (!route(io_dtype, *layer, nrep, true, nullptr, nullptr, &need, &e)) return SK_ERR_UNSUPPORTED;
+    SK_RET_IF(need > SK_DECODE_NOALLOC_SCRATCH_BYTES, SK_ERR_CAPACITY);
+    void* scratch = nullptr;
+    s = noalloc_scratch(&scratch);
+    if (s != SK_OK) return s;
+    return sk_decode_attention(layer, q_rot, n_q_heads, io_dtype, out, scratch,
+                               SK_DECODE_NOALLOC_SCRATCH_BYTES, stream);
 }
