@@ -271,6 +271,138 @@ def bench_window(args, rank, world):
 
 
 # ---------------------------------------------------------------------------
+# other rows of the hot path (measured with --workload)
+# ---------------------------------------------------------------------------
+
+def _timed(fn, steps, warm):
+    """Run fn(i) warm times, then time exactly `steps` calls with CUDA events."""
+    import torch
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    e0.record()
+    for i in range(steps):
+        fn(warm + i)
+    e1.record()
+    torch.cuda.synchronize()
+    clocks.mark("end")
+    clocks.stop()
+    return e0.elapsed_time(e1) / steps, clocks.summary()
+
+
+def bench_hybrid(args):
+    """Llama-3-8B-shaped hybrid decode: 32 layers (every 4th global with a 131072-token
+    prefix, the rest S=4 + W=4096 rings), B=16; one step = append + attention on all
+    32 layers."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.HYBRID
+    B, Hq, Hkv, D, S, W, prefix = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"], c["prefix"]
+    steps, warm = args.steps, args.warmup
+    tbl = sk.RopeTable(D, c["r"], c["theta"], prefix + steps + warm + 8)
+    layers = []
+    for i in range(c["layers"]):
+        if synth.hybrid_layer_is_global(i):
+            L = sk.KVLayer.allocate(sk.SK_LAYER_GLOBAL, B, Hkv, D, capacity=prefix + steps + warm + 4)
+        else:
+            L = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W)
+            L.count.fill_(W)
+            L.head.copy_(synth.randint((B,), 900 + i, 0, W).to(torch.int32))
+        synth.fill_normal_(L.k, 1000 + i)
+        synth.fill_normal_(L.v, 2000 + i)
+        L.pos.fill_(prefix)
+        layers.append(L)
+    n = steps + warm
+    nl = c["layers"]
+    # fresh q/k/v per layer and step, resident in HBM before timing
+    qs = synth.normal((n, nl, B, 1, Hq, D), 3, torch.bfloat16, device="cuda")
+    ks = synth.normal((n, nl, B, 1, Hkv, D), 4, torch.bfloat16, device="cuda")
+    vs = synth.normal((n, nl, B, 1, Hkv, D), 5, torch.bfloat16, device="cuda")
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(sk.decode_workspace_bytes(L, Hq) for L in layers), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        for j, L in enumerate(layers):
+            sk.kv_append(tbl, L, qs[i, j], ks[i, j], vs[i, j])
+            sk.decode_attention(L, qs[i, j, :, 0], out=out, workspace=ws)
+
+    ms, clk = _timed(step, steps, warm)
+    n_glob = sum(1 for i in range(c["layers"]) if synth.hybrid_layer_is_global(i))
+    n_slid = c["layers"] - n_glob
+    # visible rows grow by one per step on global layers; use the mean over the timed steps
+    mean_glob = prefix + 1 + warm + (steps - 1) / 2
+    kv_bytes = (n_glob * mean_glob + n_slid * (S + W)) * B * Hkv * D * 2 * 2
+    hbm, _, _, peak_kind = _peaks()
+    value = kv_bytes / (ms * 1e-3) / 1e9
+    assert all(L.error_bits() == 0 for L in layers)
+    return {"metric": "hybrid decode step KV-read GB/s (frac of HBM peak), tokens/s", "value": round(value, 2),
+            "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": warm, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "Llama-3-8B-shaped hybrid decode: 32 layers 3:1 sliding:global, B=16, "
+                                   "H_q=32, H_kv=8, d_h=128, W=4096+4 sinks, global prefix 131072",
+                       "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.1f} GB per step)"},
+            "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+            "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": steps * c["layers"] * 3, "clocks": clk}
+
+
+def bench_rerotate(args, kdt):
+    """Cached-key rerotation: 1 sequence, 48 layers, H_kv=4, d_h=128 with r=64,
+    524288 cached positions, YaRN L0=262144, factor 1 <-> 2 (alternating so the keys
+    stay well scaled); bf16 keys or int8 keys with one fp32 scale per row."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.REROTATE
+    D, r, Hkv, N, nl = c["D"], c["r"], c["Hkv"], c["positions"], c["layers"]
+    t0 = time.perf_counter()
+    tA = sk.RopeTable(D, r, c["theta"], N, yarn_factor=c["factor_a"], yarn_orig_ctx=c["orig_ctx"])
+    table_ms = (time.perf_counter() - t0) * 1e3
+    tB = sk.RopeTable(D, r, c["theta"], N, yarn_factor=c["factor_b"], yarn_orig_ctx=c["orig_ctx"])
+    t0 = time.perf_counter()
+    tB.rebuild(c["factor_b"])
+    rebuild_ms = (time.perf_counter() - t0) * 1e3
+    kdtype = torch.bfloat16 if kdt == "bf16" else torch.int8
+    layers = []
+    for l in range(nl):
+        L = sk.KVLayer.allocate(sk.SK_LAYER_GLOBAL, 1, Hkv, D, capacity=N, k_dtype=kdtype, with_v=False)
+        L.pos.fill_(N)
+        if kdt == "bf16":
+            synth.fill_uniform_(L.k, 500 + l, -1.0, 1.0)
+        else:
+            L.k.copy_(synth.randint(L.k.shape, 600 + l, -127, 128, device="cuda").to(torch.int8))
+            synth.fill_uniform_(L.k_scale, 700 + l, 1.0 / 127, 2.0 / 127)
+        layers.append(L)
+
+    def step(i):
+        if i % 2 == 0:
+            sk.kv_rerotate(layers, tA, tB)
+        else:
+            sk.kv_rerotate(layers, tB, tA)
+
+    ms, clk = _timed(step, args.steps, args.warmup)
+    rows = nl * Hkv * N
+    alg = rows * (r * 2 * 2 if kdt == "bf16" else (D + 4) * 2)
+    hbm, _, _, peak_kind = _peaks()
+    value = alg / (ms * 1e-3) / 1e9
+    assert all(L.error_bits() == 0 for L in layers)
+    return {"metric": f"cached-key rerotation ({kdt}) GB/s (frac of HBM peak), keys/s", "value": round(value, 2),
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "dtype": kdt, "data": "synthetic",
+            "config": {"workload": "48 layers x 4 kv heads x 524288 positions, d_h=128, r=64, YaRN 1<->2",
+                       "algorithmic_bytes": alg, "l2": "inputs larger than L2"},
+            "frac_of_hbm_peak": round(value / hbm, 4), "keys_per_s": round(rows / (ms * 1e-3), 1),
+            "table_build_ms": round(table_ms, 1), "table_rebuild_ms": round(rebuild_ms, 1),
+            "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": args.steps, "clocks": clk}
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle baseline (single thread, in a subprocess)
 # ---------------------------------------------------------------------------
 
@@ -334,7 +466,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="window", choices=["window"])
+    ap.add_argument("--workload", default="window",
+                    choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8"])
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -375,6 +508,13 @@ def main():
         return
 
     _, world_, _ = _dist_init(args.gpus)
+    if args.workload != "window":
+        if rank == 0:
+            if args.workload == "hybrid":
+                print(json.dumps(bench_hybrid(args)))
+            else:
+                print(json.dumps(bench_rerotate(args, args.workload.split("_")[1])))
+        return
     result = bench_window(args, rank, world_)
     if rank == 0:
         if not args.no_cpu_baseline and world_ == 1:

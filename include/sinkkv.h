@@ -253,7 +253,7 @@ SK_API sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, cons
  * mu_B / mu_A, computed from the two tables' entries with R_a R_b = R_{a+b}
  * ([DYN] "The cached keys follow a change"; [SINK] RoPE section).  The tail dims
  * are unchanged.  An int8 K row is dequantised (code * scale), turned and
- * requantised with a new scale = max|x| / 127 and codes rint(x / scale)
+ * requantised with a new scale = max|x| / 127 and codes rint(x * (127 / max|x|))
  * (half to even), clamped to [-127, 127].
  * Positions come from the layer state: global slot s < pos[b] holds position s;
  * ring sink slot s < min(pos, S) holds s; ring slot j < count holds

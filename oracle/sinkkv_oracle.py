@@ -202,17 +202,21 @@ def quantize_int8_rows(x: np.ndarray):
     """Symmetric absmax int8 codes with one scale per row (last axis).
 
     scale = max_k |x_k| / 127 (a zero row gets scale 1 and codes 0);
-    code = clamp(rint(x / scale), -127, 127), rint rounding half to even.
+    code = clamp(rint(x * (127 / max_k |x_k|)), -127, 127), rint rounding half to even.
     The pages fix neither the rounding nor its precision ("#2961", "What it does":
-    dequantize, turn, requantize), so the decision is taken in float32, the
-    precision of the CUDA kernel: x is rounded to float32 first and the division
-    is an IEEE float32 division.
+    dequantize, turn, requantize), so the decision is taken the way the CUDA kernel
+    takes it, in float32: x is rounded to float32 first, the row's reciprocal
+    127 / max|x| is one IEEE float32 division, and each code is rint of the float32
+    product.
     """
     x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
     amax = np.max(np.abs(x32), axis=-1, keepdims=True)
-    scale = (amax / np.float32(127.0)).astype(np.float32)
-    scale = np.where(amax == 0, np.float32(1.0), scale).astype(np.float32)
-    q = np.rint((x32 / scale).astype(np.float32))
+    zero = amax == 0
+    safe = np.where(zero, np.float32(1.0), amax).astype(np.float32)
+    scale = np.where(zero, np.float32(1.0), (safe / np.float32(127.0)).astype(np.float32)).astype(np.float32)
+    inv = (np.float32(127.0) / safe).astype(np.float32)
+    q = np.rint((x32 * inv).astype(np.float32))
+    q = np.where(zero, np.float32(0.0), q)
     codes = np.clip(q, -127, 127).astype(np.int8)
     return codes, scale[..., 0]
 

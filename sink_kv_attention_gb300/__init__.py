@@ -205,12 +205,15 @@ class KVLayer:
     @staticmethod
     def allocate(kind: int, batch: int, n_kv_heads: int, head_dim: int, *, sinks: int = 0,
                  window: int = 0, capacity: Optional[int] = None, k_dtype=torch.bfloat16,
-                 v_dtype=torch.bfloat16, device="cuda") -> "KVLayer":
+                 v_dtype=torch.bfloat16, device="cuda", with_v: bool = True) -> "KVLayer":
+        """with_v=False leaves V as a one-row placeholder, for callers (such as a
+        key rerotation) that never touch V."""
         if kind == SK_LAYER_RING:
             capacity = sinks + window
         assert capacity is not None and capacity >= 1
         k = torch.zeros(batch, n_kv_heads, capacity, head_dim, dtype=k_dtype, device=device)
-        v = torch.zeros(batch, n_kv_heads, capacity, head_dim, dtype=v_dtype, device=device)
+        v = (torch.zeros(batch, n_kv_heads, capacity, head_dim, dtype=v_dtype, device=device) if with_v
+             else torch.zeros(1, 1, 1, head_dim, dtype=v_dtype, device=device))
         ks = (torch.ones(batch, n_kv_heads, capacity, dtype=torch.float32, device=device)
               if k_dtype == torch.int8 else None)
         z32 = lambda: torch.zeros(batch, dtype=torch.int32, device=device)

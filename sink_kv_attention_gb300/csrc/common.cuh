@@ -65,6 +65,47 @@ template <> struct ElemIO<__nv_bfloat16> {
 };
 
 // ---------------------------------------------------------------------------
+// int8 codes (symmetric, one fp32 scale per row).
+// ---------------------------------------------------------------------------
+
+// Four int8 codes of a word -> four exact floats: bias each byte to unsigned, place it
+// under the exponent of 2^23 with one byte permute, subtract 2^23 + 128.
+__device__ __forceinline__ void codes4_to_float(uint32_t w, float* f) {
+    const uint32_t u = w ^ 0x80808080u;
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.0f;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.0f;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.0f;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.0f;
+}
+
+// Codes of four values: clamp(rint(x * inv), -127, 127), rint half to even.  Adding
+// 1.5 * 2^23 to a value of magnitude <= 127 rounds it to the nearest integer (ties to
+// even) and leaves that integer, two's complement, in the low byte.
+__device__ __forceinline__ uint32_t float4_to_codes(const float* x, float inv) {
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float t = fminf(127.0f, fmaxf(-127.0f, x[e] * inv));
+        r[e] = __float_as_uint(t + 12582912.0f);
+    }
+    const uint32_t lo = __byte_perm(r[0], r[1], 0x0040);
+    const uint32_t hi = __byte_perm(r[2], r[3], 0x0040);
+    return __byte_perm(lo, hi, 0x5410);
+}
+
+// Row scale max|x| / 127 and its quantisation multiplier 127 / max|x| (IEEE fp32
+// divisions, once per row); a zero row gets scale 1 and multiplier 0.
+__device__ __forceinline__ void int8_row_scale(float amax, float* scale, float* inv) {
+    if (amax == 0.0f) {
+        *scale = 1.0f;
+        *inv = 0.0f;
+    } else {
+        *scale = __fdiv_rn(amax, 127.0f);
+        *inv = __fdiv_rn(127.0f, amax);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Shared-memory barriers and bulk copies (inline PTX).
 // ---------------------------------------------------------------------------
 

@@ -155,27 +155,15 @@ __global__ void __launch_bounds__(kThreads) rerotate_bf16_kernel(RerotParams p) 
 
 // ---- int8 keys + per-row fp32 scale: D/32 threads per row, 32 codes each ----
 __device__ __forceinline__ void unpack16_i8(const uint4& u, float* f) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) f[4 * i + e] = float(int8_t((w[i] >> (8 * e)) & 0xffu));
+    codes4_to_float(u.x, f);
+    codes4_to_float(u.y, f + 4);
+    codes4_to_float(u.z, f + 8);
+    codes4_to_float(u.w, f + 12);
 }
 
-__device__ __forceinline__ uint4 pack16_i8(const float* x, float scale) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t packed = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float q = rintf(__fdiv_rn(x[4 * i + e], scale));
-            q = fminf(127.0f, fmaxf(-127.0f, q));
-            packed |= (uint32_t(int32_t(q)) & 0xffu) << (8 * e);
-        }
-        w[i] = packed;
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+__device__ __forceinline__ uint4 pack16_i8(const float* x, float inv) {
+    return make_uint4(float4_to_codes(x, inv), float4_to_codes(x + 4, inv), float4_to_codes(x + 8, inv),
+                      float4_to_codes(x + 12, inv));
 }
 
 template <int D, bool NEOX>
@@ -261,10 +249,11 @@ __global__ void __launch_bounds__(kThreads) rerotate_i8_kernel(RerotParams p) {
 #pragma unroll
                 for (int o = TPR / 2; o > 0; o >>= 1)
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                const float s_new = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 127.0f);
+                float s_new, inv;
+                int8_row_scale(amax, &s_new, &inv);
                 if (valid) {
-                    *reinterpret_cast<uint4*>(row + off1) = pack16_i8(a, s_new);
-                    *reinterpret_cast<uint4*>(row + off2) = pack16_i8(c, s_new);
+                    *reinterpret_cast<uint4*>(row + off1) = pack16_i8(a, inv);
+                    *reinterpret_cast<uint4*>(row + off2) = pack16_i8(c, inv);
                     if (t == 0) L.scale[crow] = s_new;
                 }
             }

@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendParams p) {
         const int64_t slot = in_range && which != 0 ? token_slot(p, s, t) : -1;
         const int64_t crow = (int64_t(b) * p.Hkv + h) * p.cap + slot;  // cache row index
         if constexpr (sizeof(KC) == 1) {
-            // int8 K: symmetric absmax over the row, rint half to even, IEEE division.
+            // int8 K: symmetric absmax over the row, codes rint(x * 127 / max|x|), ties to even.
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(f[i]));
@@ -266,19 +266,11 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendParams p) {
             for (int o = L::LPR / 2; o > 0; o >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
             if (which == 1 && slot >= 0) {
-                const float scale = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 127.0f);
+                float scale, inv;
+                int8_row_scale(amax, &scale, &inv);
                 uint32_t w[VEC / 4];
 #pragma unroll
-                for (int i = 0; i < VEC / 4; ++i) {
-                    uint32_t packed = 0;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float qv = rintf(__fdiv_rn(f[4 * i + e], scale));
-                        qv = fminf(127.0f, fmaxf(-127.0f, qv));
-                        packed |= (uint32_t(int32_t(qv)) & 0xffu) << (8 * e);
-                    }
-                    w[i] = packed;
-                }
+                for (int i = 0; i < VEC / 4; ++i) w[i] = float4_to_codes(f + 4 * i, inv);
                 int8_t* dst = static_cast<int8_t*>(p.kc) + crow * D + c * VEC;
                 if constexpr (VEC == 8)
                     *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
