@@ -78,16 +78,15 @@ __device__ __forceinline__ void codes4_to_float(uint32_t w, float* f) {
     f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.0f;
 }
 
-// Codes of four values: clamp(rint(x * inv), -127, 127), rint half to even.  Adding
-// 1.5 * 2^23 to a value of magnitude <= 127 rounds it to the nearest integer (ties to
-// even) and leaves that integer, two's complement, in the low byte.
+// Codes of four values: rint(x * inv), rint half to even, for |x| <= max|x| of the row
+// and inv = 127 / max|x| (so |x * inv| < 127.5 and the code lies in [-127, 127]).
+// Adding 1.5 * 2^23 to a value of magnitude below 2^22 rounds it to the nearest
+// integer (ties to even) and leaves that integer, two's complement, in the low byte.
 __device__ __forceinline__ uint32_t float4_to_codes(const float* x, float inv) {
     uint32_t r[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float t = fminf(127.0f, fmaxf(-127.0f, x[e] * inv));
-        r[e] = __float_as_uint(t + 12582912.0f);
-    }
+    for (int e = 0; e < 4; ++e)  // the product is rounded first: no fused multiply-add here
+        r[e] = __float_as_uint(__fadd_rn(__fmul_rn(x[e], inv), 12582912.0f));
     const uint32_t lo = __byte_perm(r[0], r[1], 0x0040);
     const uint32_t hi = __byte_perm(r[2], r[3], 0x0040);
     return __byte_perm(lo, hi, 0x5410);

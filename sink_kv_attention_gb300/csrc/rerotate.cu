@@ -197,64 +197,77 @@ __global__ void __launch_bounds__(kThreads) rerotate_i8_kernel(RerotParams p) {
                 delta_pairs<16>(p, P, j0, dc, ds);
                 lastP = P;
             }
-            for (int g = 0; g < p.Hkv; ++g) {
-                const int64_t crow = (int64_t(b) * p.Hkv + g) * L.cap + slot;
-                int8_t* row = static_cast<int8_t*>(L.k) + crow * D;
-                float s_old = 0.0f;
-                uint4 u1 = make_uint4(0, 0, 0, 0), u2 = make_uint4(0, 0, 0, 0);
-                if (valid) {
-                    s_old = L.scale[crow];
-                    u1 = *reinterpret_cast<const uint4*>(row + off1);
-                    u2 = *reinterpret_cast<const uint4*>(row + off2);
-                }
-                float a[16], c[16];
-                unpack16_i8(u1, a);
-                unpack16_i8(u2, c);
+            for (int g0 = 0; g0 < p.Hkv; g0 += 4) {
+                const int ng = min(4, p.Hkv - g0);
+                uint4 u1[4], u2[4];
+                float s_old[4];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    a[i] *= s_old;
-                    c[i] *= s_old;
-                }
-                if (valid && rot) {
-                    if (NEOX) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float x1 = a[i], x2 = c[i];
-                            a[i] = fmaf(-x2, ds[i], x1 * dc[i]);
-                            c[i] = fmaf(x1, ds[i], x2 * dc[i]);
-                        }
-                    } else {
-                        float f[32];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            f[i] = a[i];
-                            f[16 + i] = c[i];
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float x1 = f[2 * i], x2 = f[2 * i + 1];
-                            f[2 * i] = fmaf(-x2, ds[i], x1 * dc[i]);
-                            f[2 * i + 1] = fmaf(x1, ds[i], x2 * dc[i]);
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            a[i] = f[i];
-                            c[i] = f[16 + i];
-                        }
+                for (int u = 0; u < 4; ++u) {  // issue the loads of up to four rows first
+                    u1[u] = make_uint4(0, 0, 0, 0);
+                    u2[u] = make_uint4(0, 0, 0, 0);
+                    s_old[u] = 0.0f;
+                    if (valid && u < ng) {
+                        const int64_t crow = (int64_t(b) * p.Hkv + g0 + u) * L.cap + slot;
+                        const int8_t* row = static_cast<const int8_t*>(L.k) + crow * D;
+                        s_old[u] = L.scale[crow];
+                        u1[u] = *reinterpret_cast<const uint4*>(row + off1);
+                        u2[u] = *reinterpret_cast<const uint4*>(row + off2);
                     }
                 }
-                float amax = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(a[i]), fabsf(c[i])));
+                for (int u = 0; u < 4; ++u) {
+                    if (u >= ng) break;  // uniform across the warp
+                    const int64_t crow = (int64_t(b) * p.Hkv + g0 + u) * L.cap + slot;
+                    int8_t* row = static_cast<int8_t*>(L.k) + crow * D;
+                    float a[16], c[16];
+                    unpack16_i8(u1[u], a);
+                    unpack16_i8(u2[u], c);
 #pragma unroll
-                for (int o = TPR / 2; o > 0; o >>= 1)
-                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                float s_new, inv;
-                int8_row_scale(amax, &s_new, &inv);
-                if (valid) {
-                    *reinterpret_cast<uint4*>(row + off1) = pack16_i8(a, inv);
-                    *reinterpret_cast<uint4*>(row + off2) = pack16_i8(c, inv);
-                    if (t == 0) L.scale[crow] = s_new;
+                    for (int i = 0; i < 16; ++i) {
+                        a[i] *= s_old[u];
+                        c[i] *= s_old[u];
+                    }
+                    if (valid && rot) {
+                        if (NEOX) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float x1 = a[i], x2 = c[i];
+                                a[i] = fmaf(-x2, ds[i], x1 * dc[i]);
+                                c[i] = fmaf(x1, ds[i], x2 * dc[i]);
+                            }
+                        } else {
+                            float f[32];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                f[i] = a[i];
+                                f[16 + i] = c[i];
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float x1 = f[2 * i], x2 = f[2 * i + 1];
+                                f[2 * i] = fmaf(-x2, ds[i], x1 * dc[i]);
+                                f[2 * i + 1] = fmaf(x1, ds[i], x2 * dc[i]);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                a[i] = f[i];
+                                c[i] = f[16 + i];
+                            }
+                        }
+                    }
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(a[i]), fabsf(c[i])));
+#pragma unroll
+                    for (int o = TPR / 2; o > 0; o >>= 1)
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                    float s_new, inv;
+                    int8_row_scale(amax, &s_new, &inv);
+                    if (valid) {
+                        *reinterpret_cast<uint4*>(row + off1) = pack16_i8(a, inv);
+                        *reinterpret_cast<uint4*>(row + off2) = pack16_i8(c, inv);
+                        if (t == 0) L.scale[crow] = s_new;
+                    }
                 }
             }
         }
