@@ -402,6 +402,71 @@ def bench_rerotate(args, kdt):
             "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": args.steps, "clocks": clk}
 
 
+def _prefill_tiles(T, S, W, p0=0, BM=128, BN=64):
+    """Key tiles the prefill kernel visits per (sequence, head): the same plan as the
+    kernel (sink tiles below the window, then the window's tiles)."""
+    n_total = 0
+    for q0 in range(0, T, BM):
+        q_last = min(q0 + BM, T) - 1
+        win_lo = max(0, q0 - W + 1) if W > 0 else 0
+        first, last = win_lo // BN, q_last // BN
+        sink_keys = min(T, S - p0) if (W > 0 and p0 < S) else 0
+        n_sink = min(first, (sink_keys + BN - 1) // BN)
+        n_total += n_sink + (last - first + 1)
+    return n_total
+
+
+def bench_prefill(args):
+    """Prefill chunk: B=1, T=32768, H_q=32, H_kv=8, d_h=r=128, bf16, S=4, W=4092: RoPE +
+    ring append of the chunk, then masked attention of the chunk over itself."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.PREFILL
+    B, T, Hq, Hkv, D, S, W = c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    tbl = sk.RopeTable(D, c["r"], c["theta"], T + 8)
+    # a fresh ring per append step, so every step appends the chunk at positions 0..T-1
+    layers = [sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W)
+              for _ in range(args.steps + args.warmup)]
+    q0 = synth.normal((B, T, Hq, D), 63, torch.bfloat16, device="cuda")
+    k0 = synth.normal((B, T, Hkv, D), 64, torch.bfloat16, device="cuda")
+    v = synth.normal((B, T, Hkv, D), 65, torch.bfloat16, device="cuda")
+    q, k = q0.clone(), k0.clone()
+    out = torch.empty_like(q)
+    ws = torch.empty(sk.prefill_workspace_bytes(B, T, Hkv, D), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def append(i):
+        sk.kv_append(tbl, layers[i], q, k, v)
+
+    def attend(i):
+        sk.prefill_attention(q, k, v, 0, S, W, out=out, workspace=ws, err=err)
+
+    ms_append, clk_a = _timed(append, args.steps, args.warmup)
+    ms_attn, clk = _timed(attend, args.steps, args.warmup)
+    assert int(err.item()) == 0
+    _, bf16_peak, bf16_sust, peak_kind = _peaks()
+    hbm = _peaks()[0]
+    vis_pairs = sum(min(t + 1, S + W) for t in range(T))      # (query, key) pairs per head
+    alg_flops = vis_pairs * Hq * B * 4 * D
+    tiles = _prefill_tiles(T, S, W)
+    tile_flops = tiles * Hq * B * 4 * 128 * 64 * D
+    append_bytes = B * T * (Hq + 2 * Hkv) * D * 2 + B * T * (Hq + Hkv) * D * 2 + B * Hkv * (S + W) * D * 2 * 2
+    tf = tile_flops / (ms_attn * 1e-3) / 1e12
+    return {"metric": "prefill attention TFLOP/s on visited tiles (frac of dense bf16 peak); append GB/s",
+            "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_attn, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "prefill chunk: B=1, T=32768, H_q=32, H_kv=8, d_h=128, S=4, W=4092",
+                       "visited_tiles_per_head": tiles, "tile": "128 queries x 64 keys"},
+            "frac_of_bf16_peak": round(tf / bf16_peak, 4),
+            "algorithmic_tflops": round(alg_flops / (ms_attn * 1e-3) / 1e12, 1),
+            "algorithmic_flops": alg_flops, "tile_flops": tile_flops,
+            "append_ms": round(ms_append, 4), "append_gbs": round(append_bytes / (ms_append * 1e-3) / 1e9, 1),
+            "append_frac_of_hbm_peak": round(append_bytes / (ms_append * 1e-3) / 1e9 / hbm, 4),
+            "peak_source": f"{peak_kind} bf16_tflops {bf16_peak} / hbm_gbs {hbm}",
+            "gpu_launches": args.steps * 2, "clocks": clk}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (single thread, in a subprocess)
 # ---------------------------------------------------------------------------
@@ -467,7 +532,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="window",
-                    choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8"])
+                    choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill"])
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -512,6 +577,8 @@ def main():
         if rank == 0:
             if args.workload == "hybrid":
                 print(json.dumps(bench_hybrid(args)))
+            elif args.workload == "prefill":
+                print(json.dumps(bench_prefill(args)))
             else:
                 print(json.dumps(bench_rerotate(args, args.workload.split("_")[1])))
         return

@@ -233,17 +233,26 @@ SK_API sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const voi
 
 /* ---- Prefill attention (causal + window + sinks) ---------------------------------- */
 
+/* Workspace bytes sk_prefill_attention needs (a transposed copy of V); 0 for an
+ * unsupported shape. */
+SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim);
+
 /* Masked attention of a prompt chunk over itself on the tensor cores.
  *   q_rot: [batch][T][n_q_heads][head_dim], k_rot, v: [batch][T][n_kv_heads][head_dim],
- *   out: [batch][T][n_q_heads][head_dim]; all SK_BF16, device.
+ *   out: [batch][T][n_q_heads][head_dim]; all SK_BF16, device, 16-byte aligned.
  * Chunk index t has absolute position p0 + t.  Query t sees key k iff k <= t and
  * (p0 + k < sinks or t - k < window) ([MIXED] 5.5: idx_q >= idx_k and
  * idx_q - idx_k < window; [SINK] sink + recent).  window <= 0 means a global layer
- * (causal only).  Tiles the mask rules out entirely are skipped.
+ * (causal only).  Only key tiles the mask leaves at least partly visible are visited.
+ * q head h reads kv head h / (n_q_heads / n_kv_heads).
+ *   workspace: device, >= sk_prefill_workspace_bytes(...) bytes, 16-byte aligned, no
+ *   initialisation needed.  err: device error word (SK_DEVERR_TIMEOUT if a bounded
+ *   in-kernel wait gave up), may be NULL.
  * Supported: head_dim 128, SK_BF16. */
 SK_API sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
-                               int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                               int64_t p0, int32_t sinks, int32_t window, void* out, void* stream);
+                                      int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                      int64_t p0, int32_t sinks, int32_t window, void* out, void* workspace,
+                                      size_t ws_bytes, uint32_t* err, void* stream);
 
 /* ---- Cached-key rerotation on a factor change ------------------------------------ */
 

@@ -74,10 +74,11 @@ _SIGNATURES = [
                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     ("sk_decode_attention_noalloc", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32,
                                                    ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
+    ("sk_prefill_workspace_bytes", ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     ("sk_prefill_attention", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                             ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
-                                            ctypes.c_void_p]),
+                                            ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_kv_rerotate", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_status_str", ctypes.c_char_p, [ctypes.c_int]),
@@ -315,16 +316,28 @@ def decode_attention_noalloc(layer: KVLayer, q_rot: torch.Tensor, out: torch.Ten
     return out
 
 
+def prefill_workspace_bytes(batch: int, T: int, n_kv_heads: int, head_dim: int) -> int:
+    return int(_lib().sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim))
+
+
 def prefill_attention(q_rot: torch.Tensor, k_rot: torch.Tensor, v: torch.Tensor, p0: int, sinks: int,
-                      window: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Masked prefill attention of a chunk over itself: q [B,T,Hq,D], k/v [B,T,Hkv,D]."""
+                      window: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                      err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Masked prefill attention of a chunk over itself: q [B,T,Hq,D], k/v [B,T,Hkv,D]
+    (sk_prefill_attention); window <= 0 is a global layer."""
     _need_contig(q_rot, k_rot, v)
     B, T, Hq, D = q_rot.shape
     Hkv = k_rot.shape[2]
     if out is None:
         out = torch.empty_like(q_rot)
-    _check(_lib().sk_prefill_attention(_ptr(q_rot), _ptr(k_rot), _ptr(v), B, T, Hq, Hkv, D, int(p0),
-                                       int(sinks), int(window), _ptr(out), _stream(stream)),
+    need = prefill_workspace_bytes(B, T, Hkv, D)
+    if need == 0:
+        raise SinkKVError(SK_ERR_UNSUPPORTED, "sk_prefill_workspace_bytes")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_rot.device)
+    _check(_lib().sk_prefill_attention(_ptr(q_rot), _ptr(k_rot), _ptr(v), B, T, Hq, Hkv, D, int(p0), int(sinks),
+                                       int(window), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)),
            "sk_prefill_attention")
     return out
 

@@ -181,6 +181,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_s
         : "memory");
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz.f32): -inf -> +0.
+__device__ __forceinline__ float fast_exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
     if (err != nullptr) atomicOr(err, bits);
 }

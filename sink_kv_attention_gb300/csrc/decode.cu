@@ -141,12 +141,6 @@ template <typename T, int D, int NREP> struct DecodeCfg {
     static_assert(OFF_PS % 16 == 0 && OFF_PRE % 16 == 0, "alignment");
 };
 
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // This lane's PV slice of a row (DPV dims starting at lane * DPV) as DPV/2 pairs.
 template <typename T, int DPV>
 __device__ __forceinline__ void load_pv_slice(const T* row, int lane, float2* v) {
@@ -339,8 +333,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
             for (int o = NREP; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
             const float m_new = fmaxf(m_run, tmax);
             const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-            const float alpha = fast_exp2(m_run - m_use);
-            const float pr = fast_exp2(s - m_use);
+            const float alpha = fast_exp2_approx(m_run - m_use);
+            const float pr = fast_exp2_approx(s - m_use);
             m_run = m_new;
             l_run = fmaf(l_run, alpha, pr);
             ps[my_row * NREP + my_h] = make_float2(pr, pr);
@@ -410,7 +404,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
 #pragma unroll
             for (int ww = 0; ww < NWARPS; ++ww) {
                 const float* mm = merge + ww * NREP * (D + 2);
-                const float f = fast_exp2(mm[h] - Mu);
+                const float f = fast_exp2_approx(mm[h] - Mu);
                 a = fmaf(f, mm[2 * NREP + h * D + d], a);
                 lsum = fmaf(f, mm[NREP + h], lsum);
             }
@@ -471,7 +465,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
     for (int i = 0; i < n; ++i) {
         if (!owns_rows(i)) continue;
         const float* pp = base + i * PF;
-        const float f = fast_exp2(pp[h] - Mu);
+        const float f = fast_exp2_approx(pp[h] - Mu);
         lsum = fmaf(f, pp[NREP + h], lsum);
 #pragma unroll
         for (int d = 0; d < DPV; ++d) acc[d] = fmaf(f, pp[2 * NREP + h * D + lane * DPV + d], acc[d]);

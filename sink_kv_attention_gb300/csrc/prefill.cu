@@ -1,11 +1,467 @@
-// Prefill attention (causal + window + sinks) on the tensor cores.
-#include "common.cuh"
+// Prefill attention of a prompt chunk over itself, causal + sliding window + sinks,
+// on the tcgen05 tensor cores.
+//
+// Mask ("KV-Cache Engineering", 5.5, and "Attention Sink 与 Streaming KV Cache"):
+// query t sees key k iff k <= t and (p0 + k < S or t - k < W); W <= 0 is a global
+// layer (causal only).  "Inference & 128K Long Context", prefill vs decode: masking a
+// dense score matrix does not cut FLOPs, so here only key tiles the mask leaves (at
+// least partly) visible are visited: the sink tile(s) and the tiles of the window.
+//
+// One CTA = one (sequence, query head, block of BM = 128 query rows):
+//   warps 0-3  softmax: thread r owns query row r = TMEM lane r
+//   warp 4     MMA issue (one lane)
+//   warp 5     TMA loads (one lane)
+// Per key tile i (BN = 64 keys):
+//   S_i = Q K_i^T      tcgen05.mma M=128 N=64, into one of two TMEM S buffers
+//   softmax_i          tcgen05.ld S_i, mask, online max/sum in base 2 with a lazy
+//                      rescale of O (only when the row max grows by more than 2^8),
+//                      P_i (bf16) into 128-byte swizzled shared memory
+//   O += P_i V_i       tcgen05.mma M=128 N=128, V taken transposed so that both
+//                      operands are K-major
+// QK of tile i+1 runs on the tensor cores while softmax of tile i runs; two CTAs per
+// SM overlap one CTA's softmax with the other's MMAs.
+// V is transposed once per call into the workspace ([B][Hkv][D][T_pad]).
+#include <cudaTypedefs.h>
 
-extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v,
-                                          int32_t batch, int32_t T, int32_t n_q_heads,
-                                          int32_t n_kv_heads, int32_t head_dim, int64_t p0,
-                                          int32_t sinks, int32_t window, void* out, void* stream) {
-    (void)q_rot; (void)k_rot; (void)v; (void)batch; (void)T; (void)n_q_heads; (void)n_kv_heads;
-    (void)head_dim; (void)p0; (void)sinks; (void)window; (void)out; (void)stream;
-    return SK_ERR_UNSUPPORTED;
+#include <algorithm>
+#include <mutex>
+
+#include "tcgen05.cuh"
+
+namespace sk {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 64;
+constexpr int HD = 128;
+constexpr int kThreads = 6 * 32;
+constexpr uint32_t kTmemCols = 256;  // S0 [0, 64), S1 [64, 128), O [128, 256)
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// shared-memory layout (bytes from a 1024-aligned base)
+constexpr int SM_Q = 0;                       // Q dims 0-63 then 64-127: 2 x 16 KB
+constexpr int SM_KV = 32768;                  // 2 stages x (K lo 8 KB, K hi 8 KB, V^T 16 KB)
+constexpr int KV_STAGE = 32768;
+constexpr int SM_P = SM_KV + 2 * KV_STAGE;    // P: 128 rows x 128 B
+constexpr int SM_BAR = SM_P + 16384;
+constexpr int N_BARS = 12;
+constexpr int SM_TMEM = SM_BAR + N_BARS * 8;
+constexpr int SM_BYTES = SM_TMEM + 16;
+// Two CTAs per SM: 2 x (SM_ALLOC + 1 KB reserved) = 228 KB.  The slack left for
+// aligning the base to 1024 bytes (912 bytes) covers any base aligned to 128 bytes;
+// the kernel checks and reports rather than overflow.
+constexpr int SM_ALLOC = 115712;
+static_assert(SM_ALLOC >= SM_BYTES + 896, "no room to align the shared-memory base");
+
+struct PrefillParams {
+    void* out;
+    uint32_t* err;
+    int64_t p0;
+    int T, Hq, Hkv, B;
+    int S, W;
+    int nqb;
+    float scale_log2;  // log2(e) / sqrt(head_dim)
+};
+
+struct TilePlan {
+    int n;          // tiles to visit
+    int n_sink;     // leading sink tiles (below the window)
+    int first_win;  // first window tile
+};
+
+__device__ __forceinline__ TilePlan plan_tiles(const PrefillParams& p, int q0) {
+    TilePlan tp;
+    const int q_last = min(q0 + BM, p.T) - 1;
+    const int win_lo = p.W > 0 ? max(0, q0 - p.W + 1) : 0;
+    tp.first_win = win_lo / BN;
+    const int last = q_last / BN;
+    int sink_keys = 0;
+    if (p.W > 0 && p.p0 < p.S) sink_keys = int(min(int64_t(p.T), int64_t(p.S) - p.p0));
+    tp.n_sink = min(tp.first_win, (sink_keys + BN - 1) / BN);
+    tp.n = tp.n_sink + (last - tp.first_win + 1);
+    return tp;
+}
+
+__device__ __forceinline__ int key_tile(const TilePlan& tp, int i) {
+    return i < tp.n_sink ? i : tp.first_win + (i - tp.n_sink);
+}
+
+__device__ __forceinline__ bool visible(const PrefillParams& p, int t, int k) {
+    if (k > t || k >= p.T) return false;
+    if (p.W <= 0) return true;
+    return p.p0 + k < int64_t(p.S) || t - k < p.W;
+}
+
+// Every (row, key) of the tile visible to every row of the block?
+__device__ __forceinline__ bool tile_full(const PrefillParams& p, int q0, int k0) {
+    const int q_last = min(q0 + BM, p.T) - 1;
+    if (q0 + BM > p.T) return false;
+    if (k0 + BN - 1 > q0 || k0 + BN > p.T) return false;
+    if (p.W <= 0) return true;
+    return q_last - k0 < p.W || p.p0 + k0 + BN - 1 < int64_t(p.S);
+}
+
+__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, bool& bad) {
+    if (mbar_wait_bounded(bar, parity)) return true;
+    bad = true;
+    return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    prefill_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmVT, PrefillParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
+    if (pad + SM_BYTES > uint32_t(SM_ALLOC)) {  // uniform for the whole block
+        if (threadIdx.x == 0) set_error(p.err, SK_DEVERR_TIMEOUT);
+        return;
+    }
+    uint8_t* smem = smem_raw + pad;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_BAR);
+    uint64_t* q_full = bars + 0;
+    uint64_t* kv_full = bars + 1;   // [2]
+    uint64_t* kv_empty = bars + 3;  // [2]
+    uint64_t* s_full = bars + 5;    // [2]
+    uint64_t* s_free = bars + 7;    // [2]
+    uint64_t* p_full = bars + 9;
+    uint64_t* pv_done = bars + 10;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_TMEM);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // block -> (query block, descending so the long blocks start first; head; sequence)
+    const int b = blockIdx.x % p.B;
+    const int h = (blockIdx.x / p.B) % p.Hq;
+    const int qb = p.nqb - 1 - blockIdx.x / (p.B * p.Hq);
+    const int q0 = qb * BM;
+    const int g = h / (p.Hq / p.Hkv);
+    const TilePlan tp = plan_tiles(p, q0);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_free[s], 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    bool bad = false;
+
+    if (warp == 5) {
+        // ------------------------------- TMA loads -------------------------------
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, 2 * BM * 128);
+            tma_load_4d(smem + SM_Q, &tmQ, 0, h, q0, b, q_full);
+            tma_load_4d(smem + SM_Q + BM * 128, &tmQ, 64, h, q0, b, q_full);
+            for (int i = 0; i < tp.n; ++i) {
+                const int s = i & 1;
+                if (i >= 2) wait_or_flag(&kv_empty[s], ((i >> 1) - 1) & 1, bad);
+                const int k0 = key_tile(tp, i) * BN;
+                uint8_t* st = smem + SM_KV + s * KV_STAGE;
+                mbar_arrive_expect_tx(&kv_full[s], KV_STAGE);
+                tma_load_4d(st, &tmK, 0, g, k0, b, &kv_full[s]);
+                tma_load_4d(st + BN * 128, &tmK, 64, g, k0, b, &kv_full[s]);
+                tma_load_3d(st + 2 * BN * 128, &tmVT, k0, 0, b * p.Hkv + g, &kv_full[s]);
+            }
+        }
+    } else if (warp == 4) {
+        // ------------------------------- MMA issue -------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, HD);
+            const uint32_t sq = smem_u32(smem + SM_Q);
+            const uint32_t sp = smem_u32(smem + SM_P);
+            wait_or_flag(q_full, 0, bad);
+            tc_fence_after_sync();
+            for (int i = 0; i <= tp.n; ++i) {
+                if (i < tp.n) {
+                    const int s = i & 1;
+                    wait_or_flag(&kv_full[s], (i >> 1) & 1, bad);
+                    if (i >= 2) wait_or_flag(&s_free[s], ((i >> 1) - 1) & 1, bad);
+                    tc_fence_after_sync();
+                    const uint32_t sk = smem_u32(smem + SM_KV + s * KV_STAGE);
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint32_t half = (kk >> 2);           // dims 0-63 or 64-127
+                        const uint32_t off = (kk & 3) * 32;        // 16 dims = 32 bytes
+                        const uint64_t da = desc_kmajor_sw128(sq + half * (BM * 128) + off);
+                        const uint64_t db = desc_kmajor_sw128(sk + half * (BN * 128) + off);
+                        umma_bf16(tmem + s * BN, da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&s_full[s]);
+                }
+                if (i >= 1) {
+                    const int j = i - 1;
+                    const int s = j & 1;
+                    wait_or_flag(p_full, j & 1, bad);
+                    tc_fence_after_sync();
+                    const uint32_t svt = smem_u32(smem + SM_KV + s * KV_STAGE + 2 * BN * 128);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t da = desc_kmajor_sw128(sp + kk * 32);
+                        const uint64_t db = desc_kmajor_sw128(svt + kk * 32);
+                        umma_bf16(tmem + 2 * BN, da, db, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(pv_done);
+                    umma_commit(&kv_empty[s]);
+                }
+            }
+        }
+    } else {
+        // ------------------------------- softmax ---------------------------------
+        const int r = threadIdx.x;           // 0..127: query row and TMEM lane
+        const int t = q0 + r;
+        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        float m_run = -INFINITY, l_run = 0.0f;
+        uint8_t* prow = smem + SM_P + r * 128;
+        for (int i = 0; i < tp.n; ++i) {
+            const int s = i & 1;
+            wait_or_flag(&s_full[s], (i >> 1) & 1, bad);
+            tc_fence_after_sync();
+            uint32_t raw[64];
+            tmem_ld_32x32(tmem + lane_base + s * BN, raw);
+            tmem_ld_32x32(tmem + lane_base + s * BN + 32, raw + 32);
+            tmem_ld_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[s]);
+
+            const int k0 = key_tile(tp, i) * BN;
+            const bool full = tile_full(p, q0, k0);
+            float sc[64];
+            float m_tile = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                float v = __uint_as_float(raw[j]) * p.scale_log2;
+                if (!full && !visible(p, t, k0 + j)) v = -INFINITY;
+                sc[j] = v;
+                m_tile = fmaxf(m_tile, v);
+            }
+            if (i > 0) {
+                // PV of the previous tile done: O is stable and the P buffer is free
+                wait_or_flag(pv_done, (i - 1) & 1, bad);
+                tc_fence_after_sync();
+            }
+            bool grow = m_tile > m_run + kRescaleThreshold || (m_run == -INFINITY && m_tile != -INFINITY);
+            if (i == 0) {
+                m_run = m_tile;  // O is overwritten by the first PV
+                grow = false;
+            }
+            if (__any_sync(0xffffffffu, grow)) {
+                const float alpha = grow ? fast_exp2_approx(m_run - m_tile) : 1.0f;
+                // m_run == -inf gives alpha = 0: that row of O holds only zeros so far
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_32x32(tmem + lane_base + 2 * BN + c * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st_32x32(tmem + lane_base + 2 * BN + c * 32, o);
+                }
+                tmem_st_wait();
+                if (grow) {
+                    l_run *= alpha;
+                    m_run = m_tile;
+                }
+            }
+            const float m_ref = m_run == -INFINITY ? 0.0f : m_run;
+            float lsum = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 8 chunks of 8 keys = 16 bytes of bf16
+                float pv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    pv[e] = fast_exp2_approx(sc[c * 8 + e] - m_ref);
+                    lsum += pv[e];
+                }
+                const uint4 w = make_uint4(float2_to_bf16x2(pv[0], pv[1]), float2_to_bf16x2(pv[2], pv[3]),
+                                           float2_to_bf16x2(pv[4], pv[5]), float2_to_bf16x2(pv[6], pv[7]));
+                *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = w;
+            }
+            l_run += lsum;
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        // ---- epilogue: O / l -> bf16 rows ----
+        wait_or_flag(pv_done, (tp.n - 1) & 1, bad);
+        tc_fence_after_sync();
+        const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                              ((int64_t(b) * p.T + t) * p.Hq + h) * HD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld_32x32(tmem + lane_base + 2 * BN + c * 32, o);
+            tmem_ld_wait();
+            if (t < p.T) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    const uint4 w = make_uint4(
+                        float2_to_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                        float2_to_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                        float2_to_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                        float2_to_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+                    *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
+                }
+            }
+        }
+    }
+    if (bad) set_error(p.err, SK_DEVERR_TIMEOUT);
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// v [B][T][Hkv][D] -> vt [B*Hkv][D][T_pad], 64 x 64 tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_v_kernel(const __nv_bfloat16* __restrict__ v,
+                                                          __nv_bfloat16* __restrict__ vt, int T, int T_pad,
+                                                          int Hkv) {
+    __shared__ __nv_bfloat16 tile[64][66];
+    const int t0 = blockIdx.x * 64, d0 = blockIdx.y * 64, bg = blockIdx.z;
+    const int b = bg / Hkv, g = bg % Hkv;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int i = ty; i < 64; i += 8) {
+        const int t = t0 + i;
+        if (t < T) {
+            const __nv_bfloat162 x =
+                *reinterpret_cast<const __nv_bfloat162*>(v + ((int64_t(b) * T + t) * Hkv + g) * HD + d0 + 2 * tx);
+            tile[i][2 * tx] = x.x;
+            tile[i][2 * tx + 1] = x.y;
+        }
+    }
+    __syncthreads();
+    for (int i = ty; i < 64; i += 8) {
+        const int d = d0 + i;
+        const int t = t0 + 2 * tx;
+        if (t < T) {
+            __nv_bfloat162 y;
+            y.x = tile[2 * tx][i];
+            y.y = t + 1 < T ? tile[2 * tx + 1][i] : __float2bfloat16(0.0f);
+            *reinterpret_cast<__nv_bfloat162*>(vt + (int64_t(bg) * HD + d) * T_pad + t) = y;
+        }
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int64_t t_pad_of(int T) { return (int64_t(T) + 63) / 64 * 64; }
+
+}  // namespace
+}  // namespace sk
+
+using namespace sk;
+
+extern "C" size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim) {
+    if (batch < 1 || T < 1 || n_kv_heads < 1 || head_dim != HD) return 0;
+    return size_t(batch) * n_kv_heads * HD * t_pad_of(T) * sizeof(__nv_bfloat16);
+}
+
+extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
+                                          int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                          int64_t p0, int32_t sinks, int32_t window, void* out, void* workspace,
+                                          size_t ws_bytes, uint32_t* err, void* stream) {
+    SK_RET_IF(q_rot == nullptr || k_rot == nullptr || v == nullptr || out == nullptr || workspace == nullptr,
+              SK_ERR_ARG);
+    SK_RET_IF(batch < 1 || T < 0 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads != 0, SK_ERR_ARG);
+    SK_RET_IF(p0 < 0 || sinks < 0, SK_ERR_ARG);
+    SK_RET_IF(head_dim != HD, SK_ERR_UNSUPPORTED);
+    const uintptr_t al = reinterpret_cast<uintptr_t>(q_rot) | reinterpret_cast<uintptr_t>(k_rot) |
+                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
+                         reinterpret_cast<uintptr_t>(workspace);
+    SK_RET_IF(al & 15u, SK_ERR_ARG);
+    if (T == 0) return SK_OK;
+    SK_RET_IF(ws_bytes < sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim), SK_ERR_ARG);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t T_pad = t_pad_of(T);
+    __nv_bfloat16* vt = static_cast<__nv_bfloat16*>(workspace);
+
+    CUtensorMap mq, mk, mvt;
+    {
+        const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_q_heads), cuuint64_t(T), cuuint64_t(batch)};
+        const cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(n_q_heads) * HD * 2,
+                                       cuuint64_t(T) * n_q_heads * HD * 2};
+        const cuuint32_t box[4] = {64, 1, BM, 1};
+        SK_RET_IF(!make_map(&mq, q_rot, 4, dims, strides, box), SK_ERR_CUDA);
+    }
+    {
+        const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_kv_heads), cuuint64_t(T), cuuint64_t(batch)};
+        const cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(n_kv_heads) * HD * 2,
+                                       cuuint64_t(T) * n_kv_heads * HD * 2};
+        const cuuint32_t box[4] = {64, 1, BN, 1};
+        SK_RET_IF(!make_map(&mk, k_rot, 4, dims, strides, box), SK_ERR_CUDA);
+    }
+    {
+        const cuuint64_t dims[3] = {cuuint64_t(T), cuuint64_t(HD), cuuint64_t(batch) * n_kv_heads};
+        const cuuint64_t strides[2] = {cuuint64_t(T_pad) * 2, cuuint64_t(HD) * T_pad * 2};
+        const cuuint32_t box[3] = {BN, HD, 1};
+        SK_RET_IF(!make_map(&mvt, vt, 3, dims, strides, box), SK_ERR_CUDA);
+    }
+
+    dim3 tgrid(unsigned((T + 63) / 64), HD / 64, unsigned(batch * n_kv_heads));
+    transpose_v_kernel<<<tgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(v), vt, T, int(T_pad), n_kv_heads);
+    SK_CUDA_RET(cudaGetLastError());
+
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SM_ALLOC);
+    });
+    SK_CUDA_RET(attr_err);
+
+    PrefillParams p{};
+    p.out = out;
+    p.err = err;
+    p.p0 = p0;
+    p.T = T;
+    p.Hq = n_q_heads;
+    p.Hkv = n_kv_heads;
+    p.B = batch;
+    p.S = sinks;
+    p.W = window;
+    p.nqb = (T + BM - 1) / BM;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
+    const int64_t grid = int64_t(p.nqb) * n_q_heads * batch;
+    prefill_attn_kernel<<<unsigned(grid), kThreads, SM_ALLOC, st>>>(mq, mk, mvt, p);
+    SK_CUDA_RET(cudaGetLastError());
+    return SK_OK;
 }
