@@ -86,12 +86,6 @@ __device__ __forceinline__ int key_tile(const TilePlan& tp, int i) {
     return i < tp.n_sink ? i : tp.first_win + (i - tp.n_sink);
 }
 
-__device__ __forceinline__ bool visible(const PrefillParams& p, int t, int k) {
-    if (k > t || k >= p.T) return false;
-    if (p.W <= 0) return true;
-    return p.p0 + k < int64_t(p.S) || t - k < p.W;
-}
-
 // Every (row, key) of the tile visible to every row of the block?
 __device__ __forceinline__ bool tile_full(const PrefillParams& p, int q0, int k0) {
     const int q_last = min(q0 + BM, p.T) - 1;
@@ -241,14 +235,28 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int k0 = key_tile(tp, i) * BN;
             const bool full = tile_full(p, q0, k0);
             float sc[64];
-            float m_tile = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                float v = __uint_as_float(raw[j]) * p.scale_log2;
-                if (!full && !visible(p, t, k0 + j)) v = -INFINITY;
-                sc[j] = v;
-                m_tile = fmaxf(m_tile, v);
+            for (int j = 0; j < 64; ++j) sc[j] = __uint_as_float(raw[j]);
+            if (!full) {
+                // key k0 + j visible iff j <= jmax and (j >= jwin or j < jsink): branch-free
+                const int jmax = min(t, p.T - 1) - k0;
+                const int jwin = p.W > 0 ? t - p.W + 1 - k0 : -(1 << 30);
+                const int jsink = p.W > 0 ? int(max(int64_t(-(1 << 30)), int64_t(p.S) - p.p0 - k0)) : -(1 << 30);
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const bool vis = (j <= jmax) && (j >= jwin || j < jsink);
+                    sc[j] = vis ? sc[j] : -INFINITY;
+                }
             }
+            // row max of the raw scores: 8 independent chains, then a tree
+            float mx[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx[e] = sc[e];
+#pragma unroll
+            for (int j = 8; j < 64; ++j) mx[j & 7] = fmaxf(mx[j & 7], sc[j]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], mx[e + 4]);
+            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
             if (i > 0) {
                 // PV of the previous tile done: O is stable and the P buffer is free
                 wait_or_flag(pv_done, (i - 1) & 1, bad);
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (__any_sync(0xffffffffu, grow)) {
                 const float alpha = grow ? fast_exp2_approx(m_run - m_tile) : 1.0f;
                 // m_run == -inf gives alpha = 0: that row of O holds only zeros so far
-#pragma unroll
+#pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
                     tmem_ld_32x32(tmem + lane_base + 2 * BN + c * 32, o);
@@ -277,20 +285,29 @@ __global__ void __launch_bounds__(kThreads, 2)
                     m_run = m_tile;
                 }
             }
+            // p = 2^(s * scale - m): one packed FMA per pair, then the hardware exp2
             const float m_ref = m_run == -INFINITY ? 0.0f : m_run;
-            float lsum = 0.0f;
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < 8; ++c) {  // 8 chunks of 8 keys = 16 bytes of bf16
                 float pv[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    pv[e] = fast_exp2_approx(sc[c * 8 + e] - m_ref);
-                    lsum += pv[e];
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 x = __ffma2_rn(make_float2(sc[c * 8 + e], sc[c * 8 + e + 1]), sc2, nm2);
+                    pv[e] = fast_exp2_approx(x.x);
+                    pv[e + 1] = fast_exp2_approx(x.y);
+                    ls[(e >> 1)] = __fadd2_rn(ls[(e >> 1)], make_float2(pv[e], pv[e + 1]));
                 }
                 const uint4 w = make_uint4(float2_to_bf16x2(pv[0], pv[1]), float2_to_bf16x2(pv[2], pv[3]),
                                            float2_to_bf16x2(pv[4], pv[5]), float2_to_bf16x2(pv[6], pv[7]));
                 *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = w;
             }
+            const float2 l01 = __fadd2_rn(ls[0], ls[1]), l23 = __fadd2_rn(ls[2], ls[3]);
+            const float2 l4 = __fadd2_rn(l01, l23);
+            const float lsum = l4.x + l4.y;
             l_run += lsum;
             fence_proxy_async_smem();
             tc_fence_before_sync();

@@ -219,6 +219,7 @@ template <typename IO, typename KC, typename VC, int D, bool NEOX>
 __global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendParams p) {
     using L = RowLayout<IO, D>;
     constexpr int VEC = L::VEC;
+    constexpr int U = 4;  // row pairs (RPW rows each) a warp keeps in flight
     const int b = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = lane % L::LPR, rw = lane / L::LPR;
@@ -226,62 +227,67 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendParams p) {
     const SeqState s = load_state(p, b);
     const int hq = p.q != nullptr ? p.Hq : 0;
     const int rows_per_tok = hq + 2 * p.Hkv;
-    const int64_t n_rows = int64_t(p.T) * rows_per_tok;
-    const int64_t stride = int64_t(gridDim.x) * kWarps * L::RPW;
+    // work item = (token, group of RPW * U rows of that token)
+    const int groups = (rows_per_tok + L::RPW * U - 1) / (L::RPW * U);
+    const int n_items = s.ok ? p.T * groups : 0;
 
     IO* q = static_cast<IO*>(p.q);
     IO* k = static_cast<IO*>(p.k);
     const IO* v = static_cast<const IO*>(p.v);
 
-    for (int64_t base = (int64_t(blockIdx.x) * kWarps + warp) * L::RPW; base < n_rows;
-         base += stride) {
-        const int64_t row = base + rw;
-        const bool in_range = s.ok && row < n_rows;
-        const int t = in_range ? int(row / rows_per_tok) : 0;
-        const int r = in_range ? int(row % rows_per_tok) : 0;
-        // which tensor: 0 = q, 1 = k, 2 = v
-        const int which = r < hq ? 0 : (r < hq + p.Hkv ? 1 : 2);
-        const int h = which == 0 ? r : (which == 1 ? r - hq : r - hq - p.Hkv);
-        const int64_t tok = int64_t(b) * p.T + t;
-        IO* src = which == 0 ? q + (tok * p.Hq + h) * D
-                             : (which == 1 ? k + (tok * p.Hkv + h) * D
-                                           : const_cast<IO*>(v) + (tok * p.Hkv + h) * D);
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (in_range) raw = reinterpret_cast<const uint4*>(src)[c];
-        float f[VEC];
-        ElemIO<IO>::unpack(raw, f);
+    for (int item = blockIdx.x * kWarps + warp; item < n_items; item += gridDim.x * kWarps) {
+        const int t = item / groups;
+        const int r0 = (item - t * groups) * L::RPW * U;
         const int64_t P = s.pos + t;
-        rotate_lane<IO, D, NEOX>(f, raw, p.table + (in_range ? P : 0) * half, p.rotary_dim, c,
-                                 lane, in_range && which != 2);
-        if (in_range && which != 2) reinterpret_cast<uint4*>(src)[c] = ElemIO<IO>::pack(f);
-
-        const int64_t slot = in_range && which != 0 ? token_slot(p, s, t) : -1;
-        const int64_t crow = (int64_t(b) * p.Hkv + h) * p.cap + slot;  // cache row index
-        if constexpr (sizeof(KC) == 1) {
-            // int8 K: symmetric absmax over the row, codes rint(x * 127 / max|x|), ties to even.
-            float amax = 0.0f;
+        const int64_t slot = token_slot(p, s, t);  // of this token's K and V rows
+        const int64_t tok = int64_t(b) * p.T + t;
+        IO* ptr[U];
+        uint4 raws[U];
+        int which[U], h[U];
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-            for (int o = L::LPR / 2; o > 0; o >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-            if (which == 1 && slot >= 0) {
-                float scale, inv;
-                int8_row_scale(amax, &scale, &inv);
-                uint32_t w[VEC / 4];
-#pragma unroll
-                for (int i = 0; i < VEC / 4; ++i) w[i] = float4_to_codes(f + 4 * i, inv);
-                int8_t* dst = static_cast<int8_t*>(p.kc) + crow * D + c * VEC;
-                if constexpr (VEC == 8)
-                    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-                else
-                    *reinterpret_cast<uint32_t*>(dst) = w[0];
-                if (c == 0) p.kscale[crow] = scale;
-            }
-        } else {
-            if (which == 1 && slot >= 0) CacheStore<KC>::template store<VEC>(p.kc, crow * D + c * VEC, f);
+        for (int u = 0; u < U; ++u) {
+            const int r = r0 + u * L::RPW + rw;
+            which[u] = r < hq ? 0 : (r < hq + p.Hkv ? 1 : (r < rows_per_tok ? 2 : 3));  // 3: past the token
+            h[u] = which[u] == 0 ? r : (which[u] == 1 ? r - hq : r - hq - p.Hkv);
+            ptr[u] = which[u] == 0 ? q + (tok * p.Hq + h[u]) * D
+                   : (which[u] == 1 ? k + (tok * p.Hkv + h[u]) * D : const_cast<IO*>(v) + (tok * p.Hkv + h[u]) * D);
+            raws[u] = which[u] < 3 ? reinterpret_cast<const uint4*>(ptr[u])[c] : make_uint4(0, 0, 0, 0);
         }
-        if (which == 2 && slot >= 0) CacheStore<VC>::template store<VEC>(p.vc, crow * D + c * VEC, f);
+        const float2* trow = p.table + P * half;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool live = which[u] < 3;
+            float f[VEC];
+            ElemIO<IO>::unpack(raws[u], f);
+            rotate_lane<IO, D, NEOX>(f, raws[u], trow, p.rotary_dim, c, lane, live && which[u] < 2);
+            if (live && which[u] < 2) reinterpret_cast<uint4*>(ptr[u])[c] = ElemIO<IO>::pack(f);
+            const int64_t crow = (int64_t(b) * p.Hkv + h[u]) * p.cap + slot;  // cache row index
+            const bool store_kv = live && which[u] != 0 && slot >= 0;
+            if constexpr (sizeof(KC) == 1) {
+                // int8 K: symmetric absmax over the row, codes rint(x * 127 / max|x|), ties to even.
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+                for (int o = L::LPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+                if (store_kv && which[u] == 1) {
+                    float scale, inv;
+                    int8_row_scale(amax, &scale, &inv);
+                    uint32_t w[VEC / 4];
+#pragma unroll
+                    for (int i = 0; i < VEC / 4; ++i) w[i] = float4_to_codes(f + 4 * i, inv);
+                    int8_t* dst = static_cast<int8_t*>(p.kc) + crow * D + c * VEC;
+                    if constexpr (VEC == 8)
+                        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                    else
+                        *reinterpret_cast<uint32_t*>(dst) = w[0];
+                    if (c == 0) p.kscale[crow] = scale;
+                }
+            } else {
+                if (store_kv && which[u] == 1) CacheStore<KC>::template store<VEC>(p.kc, crow * D + c * VEC, f);
+            }
+            if (store_kv && which[u] == 2) CacheStore<VC>::template store<VEC>(p.vc, crow * D + c * VEC, f);
+        }
     }
     if (p.fused_state) {
         __syncthreads();  // every thread has read the state before it changes
@@ -313,10 +319,10 @@ template <typename IO, typename KC, typename VC, int D, bool NEOX>
 cudaError_t launch_append(AppendParams p, cudaStream_t st) {
     using L = RowLayout<IO, D>;
     const int hq = p.q != nullptr ? p.Hq : 0;
-    const int64_t n_rows = int64_t(p.T) * (hq + 2 * p.Hkv);
-    const int64_t per_block = kWarps * L::RPW;
-    int64_t gx = (n_rows + per_block - 1) / per_block;
-    p.fused_state = gx <= 4 ? 1 : 0;
+    const int groups = (hq + 2 * p.Hkv + L::RPW * 4 - 1) / (L::RPW * 4);
+    const int64_t items = int64_t(p.T) * groups;   // one warp per item
+    int64_t gx = (items + kWarps - 1) / kWarps;
+    p.fused_state = gx <= 1 ? 1 : 0;  // one block per sequence: it also advances the state
     if (p.fused_state) {
         gx = 1;
     } else {
