@@ -30,6 +30,27 @@ if ROOT not in sys.path:
 METRIC = "sink+window decode attn KV-read GB/s (frac of HBM peak), tokens/s, keys/s"
 
 
+def _profiled_traffic():
+    """DRAM bytes per launch of the split-K decode kernel from the committed ncu summary,
+    or None when the kernel sources changed since that capture."""
+    import hashlib
+    import re
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_split_window_b32.md")) as f:
+            text = f.read()
+        m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+        pairs = re.findall(r"(\w+\.cuh?) sha256 ([0-9a-f]{64})", text)
+        if not m or not pairs:
+            return None
+        for name, digest in pairs:
+            with open(os.path.join(ROOT, "sink_kv_attention_gb300", "csrc", name), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        return int(m.group(1))
+    except OSError:
+        return None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -258,7 +279,7 @@ def bench_window(args, rank, world):
         "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
         "keys_per_s": round(world * B * L / (ms_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4), "traffic": _profiled_traffic(),
                      "kernel": "decode attention (split-K + combine), per launch",
                      "algorithmic_bytes_per_launch": alg_bytes_decode,
                      "launch_ms": round(dec_ms, 5), "peak_source": f"{peak_kind} hbm_gbs"},
@@ -360,7 +381,8 @@ def bench_rerotate(args, kdt):
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
     c = synth.REROTATE
-    D, r, Hkv, N, nl = c["D"], c["r"], c["Hkv"], c["positions"], c["layers"]
+    D, r, Hkv, N = c["D"], c["r"], c["Hkv"], c["positions"]
+    nl = args.layers or c["layers"]   # fewer layers only for small profiling captures
     t0 = time.perf_counter()
     tA = sk.RopeTable(D, r, c["theta"], N, yarn_factor=c["factor_a"], yarn_orig_ctx=c["orig_ctx"])
     table_ms = (time.perf_counter() - t0) * 1e3
@@ -395,7 +417,7 @@ def bench_rerotate(args, kdt):
     return {"metric": f"cached-key rerotation ({kdt}) GB/s (frac of HBM peak), keys/s", "value": round(value, 2),
             "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "dtype": kdt, "data": "synthetic",
-            "config": {"workload": "48 layers x 4 kv heads x 524288 positions, d_h=128, r=64, YaRN 1<->2",
+            "config": {"workload": f"{nl} layers x 4 kv heads x 524288 positions, d_h=128, r=64, YaRN 1<->2",
                        "algorithmic_bytes": alg, "l2": "inputs larger than L2"},
             "frac_of_hbm_peak": round(value / hbm, 4), "keys_per_s": round(rows / (ms * 1e-3), 1),
             "table_build_ms": round(table_ms, 1), "table_rebuild_ms": round(rebuild_ms, 1),
@@ -534,6 +556,7 @@ def main():
     ap.add_argument("--workload", default="window",
                     choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill"])
     ap.add_argument("--cpu-worker", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
