@@ -146,14 +146,25 @@ def _barrier(world):
         dist.barrier()
 
 
-def _max_over_ranks(x, world):
+def _max_over_ranks(x, world, device="cuda"):
+    """Slowest rank's time: the whole job is as fast as its slowest replica."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_seed_base(rank):
+    """Each replica draws its own synthetic inputs (independent sequences per GPU)."""
+    return 100 * rank
+
+
+def weak_scaling_value(bytes_per_rank, ms_per_step_max, world):
+    """Whole-job GB/s: every rank moved bytes_per_rank per step; time is the slowest rank's."""
+    return world * bytes_per_rank / (ms_per_step_max * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -182,7 +193,7 @@ def bench_window(args, rank, world):
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
     steps, warm = args.steps, args.warmup
-    tbl, layer, c = window_setup(seed_base=100 * rank, steps=steps + warm + 2)
+    tbl, layer, c = window_setup(seed_base=replica_seed_base(rank), steps=steps + warm + 2)
     B, Hq, Hkv, D, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["W"]
     n = steps + warm
     # one fresh token per sequence per step, resident in HBM before timing
@@ -231,7 +242,7 @@ def bench_window(args, rank, world):
     kv_bytes = B * Hkv * L * D * 2 * 2
     alg_bytes_decode = kv_bytes + 2 * (B * Hq * D * 2)          # + q read, out write
     ms_step = ms / steps
-    value = world * kv_bytes / (ms_step * 1e-3) / 1e9
+    value = weak_scaling_value(kv_bytes, ms_step, world)
 
     # end to end through the public API with host buffers: pinned inputs copied in,
     # the output copied out, every step
