@@ -15,10 +15,11 @@
 //   S_i = Q K_i^T      tcgen05.mma M=128 N=64, into one of two TMEM S buffers
 //   softmax_i          tcgen05.ld S_i, mask, online max/sum in base 2 with a lazy
 //                      rescale of O (only when the row max grows by more than 2^8),
-//                      P_i (bf16) into 128-byte swizzled shared memory
-//   O += P_i V_i       tcgen05.mma M=128 N=128, V taken transposed so that both
-//                      operands are K-major
-// QK of tile i+1 runs on the tensor cores while softmax of tile i runs; two CTAs per
+//                      P_i as bf16 pairs written back over S_i with tcgen05.st
+//   O += P_i V_i       tcgen05.mma M=128 N=128 with A = P_i read from tensor memory
+//                      and B = V_i^T (V taken transposed so B is K-major)
+// QK of tile i+1 runs on the tensor cores while softmax of tile i runs, and softmax no
+// longer waits for P.V of the previous tile (only a rare O rescale does); two CTAs per
 // SM overlap one CTA's softmax with the other's MMAs.
 // V is transposed once per call into the workspace ([B][Hkv][D][T_pad]).
 #include <cudaTypedefs.h>
@@ -42,15 +43,14 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int SM_Q = 0;                       // Q dims 0-63 then 64-127: 2 x 16 KB
 constexpr int SM_KV = 32768;                  // 2 stages x (K lo 8 KB, K hi 8 KB, V^T 16 KB)
 constexpr int KV_STAGE = 32768;
-constexpr int SM_P = SM_KV + 2 * KV_STAGE;    // P: 128 rows x 128 B
-constexpr int SM_BAR = SM_P + 16384;
+constexpr int SM_BAR = SM_KV + 2 * KV_STAGE;
 constexpr int N_BARS = 12;
 constexpr int SM_TMEM = SM_BAR + N_BARS * 8;
 constexpr int SM_BYTES = SM_TMEM + 16;
-// Two CTAs per SM: 2 x (SM_ALLOC + 1 KB reserved) = 228 KB.  The slack left for
-// aligning the base to 1024 bytes (912 bytes) covers any base aligned to 128 bytes;
-// the kernel checks and reports rather than overflow.
-constexpr int SM_ALLOC = 115712;
+// Two CTAs per SM fit comfortably (2 x (SM_ALLOC + 1 KB reserved) < 228 KB), with
+// room to align the base to 1024 bytes; the kernel checks and reports rather than
+// overflow.
+constexpr int SM_ALLOC = SM_BYTES + 1024;
 static_assert(SM_ALLOC >= SM_BYTES + 896, "no room to align the shared-memory base");
 
 struct PrefillParams {
@@ -112,14 +112,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         return;
     }
     uint8_t* smem = smem_raw + pad;
+    // Barriers come in pairs indexed by tile parity, so that no wait can see a phase
+    // two tiles old (each wait below is at most one phase behind on its barrier).
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_BAR);
     uint64_t* q_full = bars + 0;
-    uint64_t* kv_full = bars + 1;   // [2]
-    uint64_t* kv_empty = bars + 3;  // [2]
-    uint64_t* s_full = bars + 5;    // [2]
-    uint64_t* s_free = bars + 7;    // [2]
-    uint64_t* p_full = bars + 9;
-    uint64_t* pv_done = bars + 10;
+    uint64_t* kv_full = bars + 1;   // [2] K_i, V_i^T landed in stage i & 1
+    uint64_t* kv_empty = bars + 3;  // [2] P.V of tile i done: stage i & 1 free
+    uint64_t* s_full = bars + 5;    // [2] S_i = Q K_i^T in TMEM buffer i & 1
+    uint64_t* p_full = bars + 7;    // [2] P_i (bf16) written over S_i
+    uint64_t* pv_done = bars + 9;   // [2] O += P_i V_i done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_TMEM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -137,10 +138,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
             mbar_init(&s_full[s], 1);
-            mbar_init(&s_free[s], 4);
+            mbar_init(&p_full[s], 4);
+            mbar_init(&pv_done[s], 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -176,14 +176,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, HD);
             const uint32_t sq = smem_u32(smem + SM_Q);
-            const uint32_t sp = smem_u32(smem + SM_P);
             wait_or_flag(q_full, 0, bad);
             tc_fence_after_sync();
             for (int i = 0; i <= tp.n; ++i) {
                 if (i < tp.n) {
                     const int s = i & 1;
                     wait_or_flag(&kv_full[s], (i >> 1) & 1, bad);
-                    if (i >= 2) wait_or_flag(&s_free[s], ((i >> 1) - 1) & 1, bad);
+                    // S buffer s last held P_{i-2}: its P.V must be done before QK_i overwrites it
+                    if (i >= 2) wait_or_flag(&pv_done[s], ((i >> 1) - 1) & 1, bad);
                     tc_fence_after_sync();
                     const uint32_t sk = smem_u32(smem + SM_KV + s * KV_STAGE);
 #pragma unroll
@@ -199,16 +199,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (i >= 1) {
                     const int j = i - 1;
                     const int s = j & 1;
-                    wait_or_flag(p_full, j & 1, bad);
+                    wait_or_flag(&p_full[s], (j >> 1) & 1, bad);
                     tc_fence_after_sync();
                     const uint32_t svt = smem_u32(smem + SM_KV + s * KV_STAGE + 2 * BN * 128);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t da = desc_kmajor_sw128(sp + kk * 32);
+                        // A = P_j in TMEM: 16 keys = 8 columns of packed bf16 pairs
                         const uint64_t db = desc_kmajor_sw128(svt + kk * 32);
-                        umma_bf16(tmem + 2 * BN, da, db, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_tmem_a(tmem + 2 * BN, tmem + s * BN + kk * 8, db, idesc_pv,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(pv_done);
+                    umma_commit(&pv_done[s]);
                     umma_commit(&kv_empty[s]);
                 }
             }
@@ -219,7 +220,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int t = q0 + r;
         const uint32_t lane_base = uint32_t(warp * 32) << 16;
         float m_run = -INFINITY, l_run = 0.0f;
-        uint8_t* prow = smem + SM_P + r * 128;
         for (int i = 0; i < tp.n; ++i) {
             const int s = i & 1;
             wait_or_flag(&s_full[s], (i >> 1) & 1, bad);
@@ -228,9 +228,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_ld_32x32(tmem + lane_base + s * BN, raw);
             tmem_ld_32x32(tmem + lane_base + s * BN + 32, raw + 32);
             tmem_ld_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[s]);
 
             const int k0 = key_tile(tp, i) * BN;
             const bool full = tile_full(p, q0, k0);
@@ -257,19 +254,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], mx[e + 4]);
             const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
-            if (i > 0) {
-                // PV of the previous tile done: O is stable and the P buffer is free
-                wait_or_flag(pv_done, (i - 1) & 1, bad);
-                tc_fence_after_sync();
-            }
-            bool grow = m_tile > m_run + kRescaleThreshold || (m_run == -INFINITY && m_tile != -INFINITY);
-            if (i == 0) {
-                m_run = m_tile;  // O is overwritten by the first PV
-                grow = false;
-            }
+            // Lazy rescale: keep the running max unless the row max grows by more than
+            // 2^8.  A row that has seen only masked keys (m_run = -inf) has O = 0 and
+            // l = 0, so it adopts the new max without touching O.
+            bool grow = i > 0 && m_tile > m_run + kRescaleThreshold && m_run != -INFINITY;
+            if (m_run == -INFINITY) m_run = m_tile;
             if (__any_sync(0xffffffffu, grow)) {
+                // O += P_{i-1} V_{i-1} must be done before O is rescaled
+                wait_or_flag(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, bad);
+                tc_fence_after_sync();
                 const float alpha = grow ? fast_exp2_approx(m_run - m_tile) : 1.0f;
-                // m_run == -inf gives alpha = 0: that row of O holds only zeros so far
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
@@ -279,43 +273,37 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                     tmem_st_32x32(tmem + lane_base + 2 * BN + c * 32, o);
                 }
-                tmem_st_wait();
                 if (grow) {
                     l_run *= alpha;
                     m_run = m_tile;
                 }
             }
-            // p = 2^(s * scale - m): one packed FMA per pair, then the hardware exp2
+            // p = 2^(s * scale - m): one packed FMA per pair, then the hardware exp2;
+            // P (bf16 pairs) overwrites the first 32 columns of this tile's S buffer.
             const float m_ref = m_run == -INFINITY ? 0.0f : m_run;
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm2 = make_float2(-m_ref, -m_ref);
             float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 8 chunks of 8 keys = 16 bytes of bf16
-                float pv[8];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float2 x = __ffma2_rn(make_float2(sc[c * 8 + e], sc[c * 8 + e + 1]), sc2, nm2);
-                    pv[e] = fast_exp2_approx(x.x);
-                    pv[e + 1] = fast_exp2_approx(x.y);
-                    ls[(e >> 1)] = __fadd2_rn(ls[(e >> 1)], make_float2(pv[e], pv[e + 1]));
-                }
-                const uint4 w = make_uint4(float2_to_bf16x2(pv[0], pv[1]), float2_to_bf16x2(pv[2], pv[3]),
-                                           float2_to_bf16x2(pv[4], pv[5]), float2_to_bf16x2(pv[6], pv[7]));
-                *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = w;
+            for (int e = 0; e < 64; e += 2) {
+                const float2 x = __ffma2_rn(make_float2(sc[e], sc[e + 1]), sc2, nm2);
+                const float p0 = fast_exp2_approx(x.x), p1 = fast_exp2_approx(x.y);
+                ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], make_float2(p0, p1));
+                pk[e >> 1] = float2_to_bf16x2(p0, p1);
             }
+            tmem_st_32x32(tmem + lane_base + s * BN, pk);
             const float2 l01 = __fadd2_rn(ls[0], ls[1]), l23 = __fadd2_rn(ls[2], ls[3]);
             const float2 l4 = __fadd2_rn(l01, l23);
-            const float lsum = l4.x + l4.y;
-            l_run += lsum;
-            fence_proxy_async_smem();
+            l_run += l4.x + l4.y;
+            tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[s]);
         }
         // ---- epilogue: O / l -> bf16 rows ----
-        wait_or_flag(pv_done, (tp.n - 1) & 1, bad);
+        wait_or_flag(&pv_done[(tp.n - 1) & 1], ((tp.n - 1) >> 1) & 1, bad);
         tc_fence_after_sync();
         const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
