@@ -193,9 +193,9 @@ def bench_window(args, rank, world):
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
     steps, warm = args.steps, args.warmup
-    tbl, layer, c = window_setup(seed_base=replica_seed_base(rank), steps=steps + warm + 2)
+    tbl, layer, c = window_setup(seed_base=replica_seed_base(rank), steps=2 * steps + warm + 2)
     B, Hq, Hkv, D, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["W"]
-    n = steps + warm
+    n = 2 * steps + warm
     # one fresh token per sequence per step, resident in HBM before timing
     qs = synth.normal((n, B, 1, Hq, D), 14, torch.bfloat16, device="cuda")
     ks = synth.normal((n, B, 1, Hkv, D), 15, torch.bfloat16, device="cuda")
@@ -205,17 +205,29 @@ def bench_window(args, rank, world):
     stream = torch.cuda.current_stream()
 
     def step(i, ev=None):
+        st = torch.cuda.current_stream()  # the capture stream while a graph is captured
         sk.kv_append(tbl, layer, qs[i], ks[i], vs[i])
         if ev is not None:
-            ev[0].record(stream)
+            ev[0].record(st)
         sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws)
         if ev is not None:
-            ev[1].record(stream)
+            ev[1].record(st)
 
     for i in range(warm):
         step(i)
     torch.cuda.synchronize()
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    # The timed steps run as one captured CUDA graph, the way a serving loop runs decode
+    # (the library's calls keep all state on the device, so they capture).  That graph
+    # holds no timing events between the kernels: an event node would serialise the
+    # programmatic-dependent launches.  The decode launches are timed with events in a
+    # second captured pass of as many steps right after.
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(steps):
+                step(warm + i)
+        torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     if rank == 0:
@@ -225,14 +237,35 @@ def bench_window(args, rank, world):
     torch.cuda.synchronize()
     clocks.mark("start")
     t_start.record(stream)
-    for i in range(steps):
-        step(warm + i, dec_ev[i])
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(steps):
+            step(warm + i)
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks.mark("end")
     _barrier(world)
     if rank == 0:
         clocks.stop()
+    # per-launch timing of the decode attention call
+    dec_ev = None
+    if graph is not None:
+        try:
+            dec_ev = [(torch.cuda.Event(enable_timing=True, external=True),
+                       torch.cuda.Event(enable_timing=True, external=True)) for _ in range(steps)]
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2):
+                for i in range(steps):
+                    step(warm + steps + i, dec_ev[i])
+            g2.replay()
+        except TypeError:
+            dec_ev = None
+    if dec_ev is None:
+        dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            step(warm + steps + i, dec_ev[i])
+    torch.cuda.synchronize()
     ms = t_start.elapsed_time(t_end)
     ms = _max_over_ranks(ms, world)
     dec_ms = sum(a.elapsed_time(b) for a, b in dec_ev) / steps
@@ -256,16 +289,29 @@ def bench_window(args, rank, world):
         dq = torch.empty_like(qs[0]); dk = torch.empty_like(ks[0]); dv = torch.empty_like(vs[0])
         tbl2, layer2, _ = window_setup(seed_base=100 * rank + 7, steps=steps + 2)
         torch.cuda.synchronize()
+
+        def e2e_steps():
+            for i in range(steps):
+                dq.copy_(hq[i], non_blocking=True)
+                dk.copy_(hk[i], non_blocking=True)
+                dv.copy_(hv[i], non_blocking=True)
+                sk.kv_append(tbl2, layer2, dq, dk, dv)
+                sk.decode_attention(layer2, dq[:, 0], out=out, workspace=ws)
+                hout[i].copy_(out, non_blocking=True)
+
+        g_e2e = None
+        if not args.eager:  # the same calls, host copies included, as one captured graph
+            g_e2e = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_e2e):
+                e2e_steps()
+            torch.cuda.synchronize()
         _barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(steps):
-            dq.copy_(hq[i], non_blocking=True)
-            dk.copy_(hk[i], non_blocking=True)
-            dv.copy_(hv[i], non_blocking=True)
-            sk.kv_append(tbl2, layer2, dq, dk, dv)
-            sk.decode_attention(layer2, dq[:, 0], out=out, workspace=ws)
-            hout[i].copy_(out, non_blocking=True)
+        if g_e2e is not None:
+            g_e2e.replay()
+        else:
+            e2e_steps()
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world) / steps
@@ -291,11 +337,12 @@ def bench_window(args, rank, world):
         "keys_per_s": round(world * B * L / (ms_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": _profiled_traffic(),
-                     "kernel": "decode attention (split-K + combine), per launch",
+                     "kernel": "decode attention (split-K + combine), per launch, events in a second captured pass of the same steps",
                      "algorithmic_bytes_per_launch": alg_bytes_decode,
                      "launch_ms": round(dec_ms, 5), "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": e2e,
         "gpu_launches": steps * 3,
+        "launch": "eager" if graph is None else "cuda graph of the timed steps",
     }
     if rank == 0:
         result["clocks"] = clocks.summary()
@@ -569,6 +616,7 @@ def main():
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch each step from Python instead of a CUDA graph")
     args = ap.parse_args()
 
     if args.cpu_worker:
@@ -579,9 +627,12 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
 
     if args.impl == "reference":
-        # The reference arm is the float64 CPU oracle, on rank 0 only.
+        # The reference arm is the float64 CPU oracle, on rank 0 only, one thread (set
+        # before numpy loads its BLAS).
         if rank != 0:
             return
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
         steps, warm = args.steps, args.warmup
         per_step = 2  # sequences of the 32 per step: a bounded sample
         n = min(steps, 20)

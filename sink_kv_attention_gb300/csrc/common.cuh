@@ -188,11 +188,36 @@ __device__ __forceinline__ float fast_exp2_approx(float x) {
     return y;
 }
 
+// Programmatic dependent launch: a kernel launched with launch_pdl may start while the
+// previous kernel on the stream is still running.  pdl_wait() blocks until that kernel
+// has completed and its writes are visible: call it before the first access to
+// anything an earlier kernel writes.  pdl_trigger() lets the next kernel launch early.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
     if (err != nullptr) atomicOr(err, bits);
 }
 
 }  // namespace sk
+
+// Launch `kernel` with programmatic stream serialization allowed (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 // Host helpers shared by the entry points.
 namespace sk {

@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
     uint64_t* empty_bar = full_bar + STAGES;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();  // the combine kernel may launch now; it waits for this grid to finish
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
@@ -185,6 +186,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
         }
         fence_barrier_init();
     }
+    pdl_wait();  // the append before this kernel has written the state, q and the new rows
     if (warp == 0) unit_prefix(p, pre, lane);
     __syncthreads();
 
@@ -426,6 +428,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
     constexpr int PF = NREP * (D + 2);
     __shared__ int64_t pre[kMaxBatch + 1];
     const int lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();  // the split kernel's partials are complete
     if (threadIdx.x < 32) unit_prefix(p, pre, lane);
     __syncthreads();
     const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -508,12 +512,10 @@ struct DecodeLaunch {
     static cudaError_t run(DecodeParams p, const sk_kv_layer& L, cudaStream_t st) {
         if (blocks_per_sm() < 1) return cudaErrorInvalidConfiguration;
         p.n_blocks = grid();
-        decode_split_kernel<T, D, NREP><<<p.n_blocks, C::THREADS, C::SMEM, st>>>(p);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(decode_split_kernel<T, D, NREP>, dim3(p.n_blocks), dim3(C::THREADS), C::SMEM, st, p);
         if (e != cudaSuccess) return e;
         const int warps = L.batch * L.n_kv_heads * NREP;
-        decode_combine_kernel<T, D, NREP><<<(warps + 7) / 8, 256, 0, st>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(decode_combine_kernel<T, D, NREP>, dim3((warps + 7) / 8), dim3(256), 0, st, p);
     }
 };
 

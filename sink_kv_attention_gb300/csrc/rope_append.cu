@@ -224,6 +224,8 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = lane % L::LPR, rw = lane / L::LPR;
     const int half = p.rotary_dim / 2;
+    pdl_trigger();  // the attention after this kernel may launch and run its prologue
+    pdl_wait();     // earlier kernels (the previous step's attention) are done
     const SeqState s = load_state(p, b);
     const int hq = p.q != nullptr ? p.Hq : 0;
     const int rows_per_tok = hq + 2 * p.Hkv;
@@ -330,8 +332,7 @@ cudaError_t launch_append(AppendParams p, cudaStream_t st) {
         gx = std::min(gx, cap);
     }
     dim3 grid(unsigned(gx), unsigned(p.B));
-    kv_append_kernel<IO, KC, VC, D, NEOX><<<grid, kThreads, 0, st>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kv_append_kernel<IO, KC, VC, D, NEOX>, grid, dim3(kThreads), 0, st, p);
     if (e != cudaSuccess || p.fused_state) return e;
     kv_append_state_kernel<<<(p.B + 127) / 128, 128, 0, st>>>(p);
     return cudaGetLastError();
