@@ -163,6 +163,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// Per-thread asynchronous 16-byte copy global -> shared (cp.async).  The issuing thread
+// sees the data after cp_async_wait<N>() has retired its group.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // L2 policy: data streamed once (evict first).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
@@ -195,6 +205,16 @@ __device__ __forceinline__ float fast_exp2_approx(float x) {
 // Both are no-ops for a kernel launched without the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// The same copy without a cache hint (for small data that is read again, like table rows).
+__device__ __forceinline__ void bulk_copy_g2s_nohint(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                                     uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
     if (err != nullptr) atomicOr(err, bits);

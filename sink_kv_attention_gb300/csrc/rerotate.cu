@@ -154,17 +154,46 @@ __global__ void __launch_bounds__(kThreads) rerotate_bf16_kernel(RerotParams p) 
 }
 
 // ---- int8 keys + per-row fp32 scale: D/32 threads per row, 32 codes each ----
-__device__ __forceinline__ void unpack16_i8(const uint4& u, float* f) {
-    codes4_to_float(u.x, f);
-    codes4_to_float(u.y, f + 4);
-    codes4_to_float(u.z, f + 8);
-    codes4_to_float(u.w, f + 12);
+//
+// The row is turned in code units: with x = code * s_old, the new codes are
+// rint(x * 127 / max|x|) = rint(t * 127 / max|t|) for t = the turned codes, and the new
+// scale is max|t| * s_old / 127.  Pairs of values go through packed fp32 arithmetic.
+
+// 16 codes -> 8 exact float pairs (byte permute under 2^23, subtract 2^23 + 128).
+__device__ __forceinline__ void codes16_to_pairs(const uint4& u, float2* f) {
+    const uint32_t w[4] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u, u.z ^ 0x80808080u, u.w ^ 0x80808080u};
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7540)),
+                                          __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7541))), bias);
+        f[2 * i + 1] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7542)),
+                                              __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7543))), bias);
+    }
 }
 
-__device__ __forceinline__ uint4 pack16_i8(const float* x, float inv) {
-    return make_uint4(float4_to_codes(x, inv), float4_to_codes(x + 4, inv), float4_to_codes(x + 8, inv),
-                      float4_to_codes(x + 12, inv));
+// 8 float pairs -> 16 codes rint(t * inv), ties to even (|t * inv| < 127.5 by construction).
+__device__ __forceinline__ uint4 pairs_to_codes16(const float2* t, float inv) {
+    const float2 inv2 = make_float2(inv, inv), magic = make_float2(12582912.0f, 12582912.0f);
+    uint32_t r[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        // the product is rounded before the rounding add: no fused multiply-add
+        const float2 y = __fadd2_rn(__fmul2_rn(t[i], inv2), magic);
+        r[2 * i] = __float_as_uint(y.x);
+        r[2 * i + 1] = __float_as_uint(y.y);
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = __byte_perm(r[4 * i], r[4 * i + 1], 0x0040);
+        const uint32_t hi = __byte_perm(r[4 * i + 2], r[4 * i + 3], 0x0040);
+        w[i] = __byte_perm(lo, hi, 0x5410);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
+
+constexpr int kRowsInFlight = 2;  // kv-head rows each thread loads before computing
 
 template <int D, bool NEOX>
 __global__ void __launch_bounds__(kThreads) rerotate_i8_kernel(RerotParams p) {
@@ -180,29 +209,35 @@ __global__ void __launch_bounds__(kThreads) rerotate_i8_kernel(RerotParams p) {
     const int j0 = 16 * t;
     const int off1 = rot ? (NEOX ? 16 * t : 32 * t) : p.r + 32 * (t - p.r / 32);
     const int off2 = rot ? (NEOX ? half + 16 * t : 32 * t + 16) : off1 + 16;
-    float dc[16], ds[16];
+    float2 dc2[8], ds2[8];  // delta rotation of pairs j0 .. j0+15, as pairs
     int64_t lastP = -1;
     for (int l = 0; l < p.n_layers; ++l) {
         const RerotLayer& L = p.layers[l];
         for (int b = 0; b < p.B; ++b) {
             // Lanes of one warp hold different slots, so validity differs between row
             // groups: every lane runs the loop and the shuffles, only valid rows touch memory.
-            int64_t P = slot_position(L, b, slot);
+            const int64_t P = slot_position(L, b, slot);
             bool valid = P >= 0;
             if (valid && (P >= p.maxA || P >= p.maxB)) {
                 set_error(L.err, SK_DEVERR_POSITION_RANGE);
                 valid = false;
             }
             if (valid && rot && P != lastP) {
+                float dc[16], ds[16];
                 delta_pairs<16>(p, P, j0, dc, ds);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    dc2[i] = make_float2(dc[2 * i], dc[2 * i + 1]);
+                    ds2[i] = make_float2(ds[2 * i], ds[2 * i + 1]);
+                }
                 lastP = P;
             }
-            for (int g0 = 0; g0 < p.Hkv; g0 += 4) {
-                const int ng = min(4, p.Hkv - g0);
-                uint4 u1[4], u2[4];
-                float s_old[4];
+            for (int g0 = 0; g0 < p.Hkv; g0 += kRowsInFlight) {
+                const int ng = min(kRowsInFlight, p.Hkv - g0);
+                uint4 u1[kRowsInFlight], u2[kRowsInFlight];
+                float s_old[kRowsInFlight];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {  // issue the loads of up to four rows first
+                for (int u = 0; u < kRowsInFlight; ++u) {  // issue the loads of the rows first
                     u1[u] = make_uint4(0, 0, 0, 0);
                     u2[u] = make_uint4(0, 0, 0, 0);
                     s_old[u] = 0.0f;
@@ -215,57 +250,65 @@ __global__ void __launch_bounds__(kThreads) rerotate_i8_kernel(RerotParams p) {
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kRowsInFlight; ++u) {
                     if (u >= ng) break;  // uniform across the warp
                     const int64_t crow = (int64_t(b) * p.Hkv + g0 + u) * L.cap + slot;
                     int8_t* row = static_cast<int8_t*>(L.k) + crow * D;
-                    float a[16], c[16];
-                    unpack16_i8(u1[u], a);
-                    unpack16_i8(u2[u], c);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        a[i] *= s_old[u];
-                        c[i] *= s_old[u];
-                    }
+                    float2 a[8], c[8];  // codes off1 .. +15 and off2 .. +15 as pairs
+                    codes16_to_pairs(u1[u], a);
+                    codes16_to_pairs(u2[u], c);
                     if (valid && rot) {
                         if (NEOX) {
+                            // pair j: x1 = a, x2 = c -> (x1 dc - x2 ds, x2 dc + x1 ds)
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float x1 = a[i], x2 = c[i];
-                                a[i] = fmaf(-x2, ds[i], x1 * dc[i]);
-                                c[i] = fmaf(x1, ds[i], x2 * dc[i]);
+                            for (int i = 0; i < 8; ++i) {
+                                const float2 x1 = a[i], x2 = c[i];
+                                a[i] = __ffma2_rn(x1, dc2[i], __fmul2_rn(make_float2(-x2.x, -x2.y), ds2[i]));
+                                c[i] = __ffma2_rn(x2, dc2[i], __fmul2_rn(x1, ds2[i]));
                             }
                         } else {
-                            float f[32];
+                            // interleaved pairs (2j, 2j+1) of codes [32t, 32t+32): regroup
+                            float2 x1[8], x2[8];
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                f[i] = a[i];
-                                f[16 + i] = c[i];
+                            for (int i = 0; i < 4; ++i) {
+                                x1[i] = make_float2(a[2 * i].x, a[2 * i + 1].x);
+                                x2[i] = make_float2(a[2 * i].y, a[2 * i + 1].y);
+                                x1[4 + i] = make_float2(c[2 * i].x, c[2 * i + 1].x);
+                                x2[4 + i] = make_float2(c[2 * i].y, c[2 * i + 1].y);
                             }
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float x1 = f[2 * i], x2 = f[2 * i + 1];
-                                f[2 * i] = fmaf(-x2, ds[i], x1 * dc[i]);
-                                f[2 * i + 1] = fmaf(x1, ds[i], x2 * dc[i]);
+                            for (int i = 0; i < 8; ++i) {
+                                const float2 y1 =
+                                    __ffma2_rn(x1[i], dc2[i], __fmul2_rn(make_float2(-x2[i].x, -x2[i].y), ds2[i]));
+                                const float2 y2 = __ffma2_rn(x2[i], dc2[i], __fmul2_rn(x1[i], ds2[i]));
+                                x1[i] = y1;
+                                x2[i] = y2;
                             }
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                a[i] = f[i];
-                                c[i] = f[16 + i];
+                            for (int i = 0; i < 4; ++i) {
+                                a[2 * i] = make_float2(x1[i].x, x2[i].x);
+                                a[2 * i + 1] = make_float2(x1[i].y, x2[i].y);
+                                c[2 * i] = make_float2(x1[4 + i].x, x2[4 + i].x);
+                                c[2 * i + 1] = make_float2(x1[4 + i].y, x2[4 + i].y);
                             }
                         }
                     }
-                    float amax = 0.0f;
+                    float m0 = 0.0f, m1 = 0.0f;  // max |t| in code units, two chains
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(a[i]), fabsf(c[i])));
+                    for (int i = 0; i < 8; ++i) {
+                        m0 = fmaxf(m0, fmaxf(fabsf(a[i].x), fabsf(a[i].y)));
+                        m1 = fmaxf(m1, fmaxf(fabsf(c[i].x), fabsf(c[i].y)));
+                    }
+                    float amax_c = fmaxf(m0, m1);
 #pragma unroll
                     for (int o = TPR / 2; o > 0; o >>= 1)
-                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                        amax_c = fmaxf(amax_c, __shfl_xor_sync(0xffffffffu, amax_c, o));
                     float s_new, inv;
-                    int8_row_scale(amax, &s_new, &inv);
+                    int8_row_scale(amax_c * s_old[u], &s_new, &inv);
+                    inv = amax_c * s_old[u] == 0.0f ? 0.0f : __fdiv_rn(127.0f, amax_c);  // in code units
                     if (valid) {
-                        *reinterpret_cast<uint4*>(row + off1) = pack16_i8(a, inv);
-                        *reinterpret_cast<uint4*>(row + off2) = pack16_i8(c, inv);
+                        *reinterpret_cast<uint4*>(row + off1) = pairs_to_codes16(a, inv);
+                        *reinterpret_cast<uint4*>(row + off2) = pairs_to_codes16(c, inv);
                         if (t == 0) L.scale[crow] = s_new;
                     }
                 }

@@ -25,11 +25,32 @@ template <typename T, int D> struct RowLayout {
     static constexpr int RPW = 32 / LPR;            // rows per warp
 };
 
-// Rotate the VEC elements of this lane (c = lane index within its row).  Every lane of
-// the warp must call this (it shuffles); `active` lanes update f.
+// 16-byte chunks of (cos, sin) pairs a lane needs: NeoX lanes hold VEC pairs (one per
+// element), GPT-J lanes VEC/2 pairs.
+template <typename T, bool NEOX> constexpr int table_chunks() {
+    return NEOX ? ElemIO<T>::kPerVec / 2 : ElemIO<T>::kPerVec / 4;
+}
+
+// First (cos, sin) pair index of lane c's elements, and whether the lane rotates.
 template <typename T, int D, bool NEOX>
-__device__ __forceinline__ void rotate_lane(float* f, const uint4& raw, const float2* trow,
-                                            int rotary_dim, int c, int lane, bool active) {
+__device__ __forceinline__ bool lane_pairs(int rotary_dim, int c, int* j0) {
+    constexpr int VEC = RowLayout<T, D>::VEC;
+    if constexpr (NEOX) {
+        const int hc = (rotary_dim / 2) / VEC;
+        *j0 = (c < hc ? c : c - hc) * VEC;
+        return c < 2 * hc;
+    } else {
+        *j0 = c * VEC / 2;
+        return c * VEC < rotary_dim;
+    }
+}
+
+// Rotate the VEC elements of this lane (c = lane index within its row), with the lane's
+// (cos, sin) pairs at cs (global or shared memory).  Every lane of the warp must call
+// this (it shuffles); `active` lanes update f.
+template <typename T, int D, bool NEOX>
+__device__ __forceinline__ void rotate_lane(float* f, const uint4& raw, const float4* cs, int rotary_dim, int c,
+                                            int lane, bool active) {
     constexpr int VEC = RowLayout<T, D>::VEC;
     if constexpr (NEOX) {
         const int hc = (rotary_dim / 2) / VEC;  // vectors per half of the rotary part
@@ -44,29 +65,29 @@ __device__ __forceinline__ void rotate_lane(float* f, const uint4& raw, const fl
         if (active && rot) {
             float p[VEC];
             ElemIO<T>::unpack(pr, p);
-            const int j0 = (c < hc ? c : c - hc) * VEC;
-            const float4* t4 = reinterpret_cast<const float4*>(trow + j0);
-            const float sign = c < hc ? -1.0f : 1.0f;  // first: x1 c - x2 s; second: x2 c + x1 s
+            // first half: x1 c - x2 s; second half: x2 c + x1 s
+            const float2 sg = c < hc ? make_float2(-1.0f, -1.0f) : make_float2(1.0f, 1.0f);
 #pragma unroll
             for (int i = 0; i < VEC / 2; ++i) {
-                const float4 cs = __ldg(t4 + i);  // (cos, sin) of pairs j0+2i, j0+2i+1
-                f[2 * i] = fmaf(sign * p[2 * i], cs.y, f[2 * i] * cs.x);
-                f[2 * i + 1] = fmaf(sign * p[2 * i + 1], cs.w, f[2 * i + 1] * cs.z);
+                const float4 t = cs[i];  // (cos, sin) of the lane's pairs 2i, 2i+1
+                const float2 fc = __fmul2_rn(make_float2(f[2 * i], f[2 * i + 1]), make_float2(t.x, t.z));
+                const float2 ps = __fmul2_rn(make_float2(p[2 * i], p[2 * i + 1]), sg);
+                const float2 o = __ffma2_rn(ps, make_float2(t.y, t.w), fc);
+                f[2 * i] = o.x;
+                f[2 * i + 1] = o.y;
             }
         }
     } else {
         if (active && c * VEC < rotary_dim) {
-            const int j0 = c * VEC / 2;
-            const float4* t4 = reinterpret_cast<const float4*>(trow + j0);
 #pragma unroll
             for (int i = 0; i < VEC / 4; ++i) {
-                const float4 cs = __ldg(t4 + i);
+                const float4 t = cs[i];
                 float x1 = f[4 * i], x2 = f[4 * i + 1];
-                f[4 * i] = fmaf(-x2, cs.y, x1 * cs.x);
-                f[4 * i + 1] = fmaf(x1, cs.y, x2 * cs.x);
+                f[4 * i] = fmaf(-x2, t.y, x1 * t.x);
+                f[4 * i + 1] = fmaf(x1, t.y, x2 * t.x);
                 x1 = f[4 * i + 2]; x2 = f[4 * i + 3];
-                f[4 * i + 2] = fmaf(-x2, cs.w, x1 * cs.z);
-                f[4 * i + 3] = fmaf(x1, cs.w, x2 * cs.z);
+                f[4 * i + 2] = fmaf(-x2, t.w, x1 * t.z);
+                f[4 * i + 3] = fmaf(x1, t.w, x2 * t.z);
             }
         }
     }
@@ -113,8 +134,10 @@ __global__ void __launch_bounds__(kThreads) rope_apply_kernel(ApplyParams p) {
         if (active) raw = *ptr;
         float f[L::VEC];
         ElemIO<T>::unpack(raw, f);
-        rotate_lane<T, D, NEOX>(f, raw, p.table + (active ? P : 0) * half, p.rotary_dim, c, lane,
-                                active);
+        int j0 = 0;
+        lane_pairs<T, D, NEOX>(p.rotary_dim, c, &j0);
+        rotate_lane<T, D, NEOX>(f, raw, reinterpret_cast<const float4*>(p.table + (active ? P : 0) * half + j0),
+                                p.rotary_dim, c, lane, active);
         if (active) *ptr = ElemIO<T>::pack(f);
     }
 }
@@ -215,82 +238,146 @@ template <> struct CacheStore<__nv_bfloat16> {
     }
 };
 
+constexpr int kAppendStages = 4;  // tokens in flight per block
+
+// Shared memory of the append kernel: kAppendStages stages of one token's q, k and v
+// rows (q first, then k, then v), plus the stage barriers.
+template <typename IO> constexpr size_t append_stage_bytes(int hq, int hkv, int D) {
+    return size_t(hq + 2 * hkv) * D * sizeof(IO);
+}
+
+// One block per (sequence, share of its tokens).  Lane 0 of the last warp streams each
+// token's q, k and v rows (contiguous per tensor) into a kAppendStages-deep ring of
+// shared-memory stages with 1-D bulk copies; the other warps rotate the rows out of
+// shared memory (LPR lanes per row, 16-byte vectors, the NeoX partner vector by
+// shuffle), write q and k back in place and k, v into the cache.
 template <typename IO, typename KC, typename VC, int D, bool NEOX>
-__global__ void __launch_bounds__(kThreads) kv_append_kernel(AppendParams p) {
+__global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p) {
     using L = RowLayout<IO, D>;
     constexpr int VEC = L::VEC;
-    constexpr int U = 4;  // row pairs (RPW rows each) a warp keeps in flight
+    constexpr int TCH = table_chunks<IO, NEOX>();
+    extern __shared__ __align__(128) uint8_t smem_raw[];
     const int b = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = lane % L::LPR, rw = lane / L::LPR;
     const int half = p.rotary_dim / 2;
-    pdl_trigger();  // the attention after this kernel may launch and run its prologue
-    pdl_wait();     // earlier kernels (the previous step's attention) are done
-    const SeqState s = load_state(p, b);
     const int hq = p.q != nullptr ? p.Hq : 0;
     const int rows_per_tok = hq + 2 * p.Hkv;
-    // work item = (token, group of RPW * U rows of that token)
-    const int groups = (rows_per_tok + L::RPW * U - 1) / (L::RPW * U);
-    const int n_items = s.ok ? p.T * groups : 0;
+    const size_t rows_bytes = size_t(rows_per_tok) * D * sizeof(IO);
+    const size_t stage_bytes = rows_bytes + size_t(half) * sizeof(float2);  // rows, then the cos/sin row
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_raw + kAppendStages * stage_bytes);
+    uint64_t* empty_bar = full_bar + kAppendStages;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kAppendStages; ++st) {
+            mbar_init(&full_bar[st], 1);
+            mbar_init(&empty_bar[st], kWarps);
+        }
+        fence_barrier_init();
+    }
+    pdl_trigger();  // the attention after this kernel may launch and run its prologue
+    pdl_wait();     // earlier kernels (the previous step's attention) are done
+    __syncthreads();
+    const SeqState s = load_state(p, b);
+    const int n_tok = s.ok ? p.T : 0;
+    bool timed_out = false;
 
     IO* q = static_cast<IO*>(p.q);
     IO* k = static_cast<IO*>(p.k);
     const IO* v = static_cast<const IO*>(p.v);
 
-    for (int item = blockIdx.x * kWarps + warp; item < n_items; item += gridDim.x * kWarps) {
-        const int t = item / groups;
-        const int r0 = (item - t * groups) * L::RPW * U;
-        const int64_t P = s.pos + t;
-        const int64_t slot = token_slot(p, s, t);  // of this token's K and V rows
-        const int64_t tok = int64_t(b) * p.T + t;
-        IO* ptr[U];
-        uint4 raws[U];
-        int which[U], h[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int r = r0 + u * L::RPW + rw;
-            which[u] = r < hq ? 0 : (r < hq + p.Hkv ? 1 : (r < rows_per_tok ? 2 : 3));  // 3: past the token
-            h[u] = which[u] == 0 ? r : (which[u] == 1 ? r - hq : r - hq - p.Hkv);
-            ptr[u] = which[u] == 0 ? q + (tok * p.Hq + h[u]) * D
-                   : (which[u] == 1 ? k + (tok * p.Hkv + h[u]) * D : const_cast<IO*>(v) + (tok * p.Hkv + h[u]) * D);
-            raws[u] = which[u] < 3 ? reinterpret_cast<const uint4*>(ptr[u])[c] : make_uint4(0, 0, 0, 0);
-        }
-        const float2* trow = p.table + P * half;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const bool live = which[u] < 3;
-            float f[VEC];
-            ElemIO<IO>::unpack(raws[u], f);
-            rotate_lane<IO, D, NEOX>(f, raws[u], trow, p.rotary_dim, c, lane, live && which[u] < 2);
-            if (live && which[u] < 2) reinterpret_cast<uint4*>(ptr[u])[c] = ElemIO<IO>::pack(f);
-            const int64_t crow = (int64_t(b) * p.Hkv + h[u]) * p.cap + slot;  // cache row index
-            const bool store_kv = live && which[u] != 0 && slot >= 0;
-            if constexpr (sizeof(KC) == 1) {
-                // int8 K: symmetric absmax over the row, codes rint(x * 127 / max|x|), ties to even.
-                float amax = 0.0f;
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-                for (int o = L::LPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-                if (store_kv && which[u] == 1) {
-                    float scale, inv;
-                    int8_row_scale(amax, &scale, &inv);
-                    uint32_t w[VEC / 4];
-#pragma unroll
-                    for (int i = 0; i < VEC / 4; ++i) w[i] = float4_to_codes(f + 4 * i, inv);
-                    int8_t* dst = static_cast<int8_t*>(p.kc) + crow * D + c * VEC;
-                    if constexpr (VEC == 8)
-                        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-                    else
-                        *reinterpret_cast<uint32_t*>(dst) = w[0];
-                    if (c == 0) p.kscale[crow] = scale;
-                }
-            } else {
-                if (store_kv && which[u] == 1) CacheStore<KC>::template store<VEC>(p.kc, crow * D + c * VEC, f);
+    if (warp == kWarps) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            int st = 0;
+            uint32_t phase = 0;
+            for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+                if (!mbar_wait_bounded(&empty_bar[st], phase ^ 1)) timed_out = true;
+                uint8_t* dst = smem_raw + st * stage_bytes;
+                const int64_t tok = int64_t(b) * p.T + t;
+                mbar_arrive_expect_tx(&full_bar[st], uint32_t(stage_bytes));
+                if (hq > 0)
+                    bulk_copy_g2s(dst, q + tok * p.Hq * D, uint32_t(hq * D * sizeof(IO)), &full_bar[st], policy);
+                bulk_copy_g2s(dst + size_t(hq) * D * sizeof(IO), k + tok * p.Hkv * D,
+                              uint32_t(p.Hkv * D * sizeof(IO)), &full_bar[st], policy);
+                bulk_copy_g2s(dst + size_t(hq + p.Hkv) * D * sizeof(IO), v + tok * p.Hkv * D,
+                              uint32_t(p.Hkv * D * sizeof(IO)), &full_bar[st], policy);
+                bulk_copy_g2s_nohint(dst + rows_bytes, p.table + (s.pos + t) * half, uint32_t(half * sizeof(float2)),
+                                     &full_bar[st]);
+                if (++st == kAppendStages) { st = 0; phase ^= 1; }
             }
-            if (store_kv && which[u] == 2) CacheStore<VC>::template store<VEC>(p.vc, crow * D + c * VEC, f);
+            for (int i = 0; i < kAppendStages; ++i) {  // drain: no copy in flight at exit
+                if (!mbar_wait_bounded(&empty_bar[st], phase ^ 1)) timed_out = true;
+                if (++st == kAppendStages) { st = 0; phase ^= 1; }
+            }
+        }
+    } else {
+        // ------------------------------ consumers -----------------------------
+        int j0 = 0;
+        const bool rot_lane = lane_pairs<IO, D, NEOX>(p.rotary_dim, c, &j0);
+        int st = 0;
+        uint32_t phase = 0;
+        for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+            const int64_t slot_kv = token_slot(p, s, t);
+            const int64_t tok = int64_t(b) * p.T + t;
+            // per-token bases; rows below add small per-row offsets only
+            IO* qtok = q + tok * p.Hq * D;
+            IO* ktok = k + tok * p.Hkv * D;
+            const int64_t cbase = int64_t(b) * p.Hkv * p.cap + slot_kv;  // cache row of kv head 0
+            if (!mbar_wait_bounded(&full_bar[st], phase)) timed_out = true;
+            const uint8_t* stage = smem_raw + st * stage_bytes;
+            // this lane's (cos, sin) pairs of position pos + t, copied in with the rows
+            float4 cs[TCH];
+            const float4* trow = reinterpret_cast<const float4*>(stage + rows_bytes) + j0 / 2;
+#pragma unroll
+            for (int i = 0; i < TCH; ++i) cs[i] = rot_lane ? trow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r0 = warp * L::RPW; r0 < rows_per_tok; r0 += kWarps * L::RPW) {
+                const int r = r0 + rw;  // uniform trip count per warp; lanes past the token idle
+                const bool live = r < rows_per_tok;
+                const int which = r < hq ? 0 : (r < hq + p.Hkv ? 1 : 2);
+                const int h = which == 0 ? r : (which == 1 ? r - hq : r - hq - p.Hkv);
+                const uint4 raw = live ? reinterpret_cast<const uint4*>(stage + size_t(r) * D * sizeof(IO))[c]
+                                       : make_uint4(0, 0, 0, 0);
+                float f[VEC];
+                ElemIO<IO>::unpack(raw, f);
+                rotate_lane<IO, D, NEOX>(f, raw, cs, p.rotary_dim, c, lane, live && which < 2);
+                const uint4 out = ElemIO<IO>::pack(f);
+                if (live && which == 0) reinterpret_cast<uint4*>(qtok + h * D)[c] = out;
+                if (live && which == 1) reinterpret_cast<uint4*>(ktok + h * D)[c] = out;
+                const int64_t crow = cbase + int64_t(h) * p.cap;  // cache row index
+                const bool store_kv = live && which != 0 && slot_kv >= 0;
+                if constexpr (sizeof(KC) == 1) {
+                    // int8 K: symmetric absmax over the row, codes rint(x * 127 / max|x|), ties to even.
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+                    for (int o = L::LPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+                    if (store_kv && which == 1) {
+                        float scale, inv;
+                        int8_row_scale(amax, &scale, &inv);
+                        uint32_t w[VEC / 4];
+#pragma unroll
+                        for (int i = 0; i < VEC / 4; ++i) w[i] = float4_to_codes(f + 4 * i, inv);
+                        int8_t* dst = static_cast<int8_t*>(p.kc) + crow * D + c * VEC;
+                        if constexpr (VEC == 8)
+                            *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                        else
+                            *reinterpret_cast<uint32_t*>(dst) = w[0];
+                        if (c == 0) p.kscale[crow] = scale;
+                    }
+                } else {
+                    if (store_kv && which == 1)
+                        reinterpret_cast<uint4*>(static_cast<KC*>(p.kc) + crow * D)[c] = out;
+                }
+                if (store_kv && which == 2) reinterpret_cast<uint4*>(static_cast<VC*>(p.vc) + crow * D)[c] = raw;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[st]);
+            if (++st == kAppendStages) { st = 0; phase ^= 1; }
         }
     }
+    if (timed_out) set_error(p.err, SK_DEVERR_TIMEOUT);
     if (p.fused_state) {
         __syncthreads();  // every thread has read the state before it changes
         if (threadIdx.x == 0) advance_state(p, s, b);
@@ -319,20 +406,19 @@ cudaError_t launch_apply(const ApplyParams& p, cudaStream_t st) {
 
 template <typename IO, typename KC, typename VC, int D, bool NEOX>
 cudaError_t launch_append(AppendParams p, cudaStream_t st) {
-    using L = RowLayout<IO, D>;
     const int hq = p.q != nullptr ? p.Hq : 0;
-    const int groups = (hq + 2 * p.Hkv + L::RPW * 4 - 1) / (L::RPW * 4);
-    const int64_t items = int64_t(p.T) * groups;   // one warp per item
-    int64_t gx = (items + kWarps - 1) / kWarps;
-    p.fused_state = gx <= 1 ? 1 : 0;  // one block per sequence: it also advances the state
-    if (p.fused_state) {
-        gx = 1;
-    } else {
-        const int64_t cap = std::max<int64_t>(1, int64_t(device_sm_count()) * 8 / p.B);
-        gx = std::min(gx, cap);
-    }
+    const size_t smem = kAppendStages * (append_stage_bytes<IO>(hq, p.Hkv, D) + size_t(p.rotary_dim / 2) * 8) +
+                        2 * kAppendStages * 8;
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;  // more heads than the stages can hold
+    static cudaError_t attr = cudaFuncSetAttribute(kv_append_kernel<IO, KC, VC, D, NEOX>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (attr != cudaSuccess) return attr;
+    // blocks per sequence: one when a single block covers the tokens (it then also
+    // advances the state), else enough blocks to fill the GPU
+    int64_t gx = p.T <= kAppendStages ? 1 : std::min<int64_t>(p.T, std::max<int64_t>(1, 2 * device_sm_count() / p.B));
+    p.fused_state = gx == 1 ? 1 : 0;
     dim3 grid(unsigned(gx), unsigned(p.B));
-    cudaError_t e = launch_pdl(kv_append_kernel<IO, KC, VC, D, NEOX>, grid, dim3(kThreads), 0, st, p);
+    cudaError_t e = launch_pdl(kv_append_kernel<IO, KC, VC, D, NEOX>, grid, dim3(kThreads + 32), smem, st, p);
     if (e != cudaSuccess || p.fused_state) return e;
     kv_append_state_kernel<<<(p.B + 127) / 128, 128, 0, st>>>(p);
     return cudaGetLastError();
