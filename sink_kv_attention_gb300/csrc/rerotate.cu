@@ -196,7 +196,7 @@ __device__ __forceinline__ uint4 pairs_to_codes16(const float2* t, float inv) {
 constexpr int kRowsInFlight = 2;  // kv-head rows each thread loads before computing
 
 template <int D, bool NEOX>
-__global__ void __launch_bounds__(kThreads) rerotate_i8_kernel(RerotParams p) {
+__global__ void __launch_bounds__(kThreads, 3) rerotate_i8_kernel(RerotParams p) {
     constexpr int TPR = D / 32;  // threads per row (aligned group of 2 or 4 lanes)
     constexpr int SPB = kThreads / TPR;
     const int t = threadIdx.x % TPR;
