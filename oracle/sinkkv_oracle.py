@@ -380,13 +380,35 @@ def mask_allows(P: int, k: int, sinks: int, window: Optional[int]) -> bool:
 # O6. Attention.
 # ---------------------------------------------------------------------------
 
-def attend(q: np.ndarray, keys: np.ndarray, values: np.ndarray) -> np.ndarray:
+# Bounds of a learned sink logit ("Inference & 128K Long Context", "Sink clamp cache":
+# the forward pass clamps the trained per-head sink bias to [-10, 15]).
+SINK_LOGIT_MIN = -10.0
+SINK_LOGIT_MAX = 15.0
+
+
+def clamp_sink_logits(sink_logits) -> np.ndarray:
+    """The per-head learned sink logits as the forward pass uses them: clamped to
+    [SINK_LOGIT_MIN, SINK_LOGIT_MAX] ("Inference & 128K Long Context", "Sink clamp
+    cache")."""
+    return np.clip(np.asarray(sink_logits, dtype=np.float64), SINK_LOGIT_MIN, SINK_LOGIT_MAX)
+
+
+def attend(q: np.ndarray, keys: np.ndarray, values: np.ndarray,
+           sink_logits: Optional[Sequence[float]] = None) -> np.ndarray:
     """Softmax attention of one query row over a key/value set, with GQA.
 
     q [H_q, D], keys and values [n, H_kv, D]; q head h reads kv head h // n_rep
     ("KV-Cache Engineering", 5.5, ``repeat_kv``).  scores = q . k / sqrt(D), a
     max-subtracted softmax in float64, out = sum_j p_j v_j ("Attention Sink 与
     Streaming KV Cache", the experiment's ``incremental_sink``).
+
+    ``sink_logits`` ([H_q], optional): learned sinks, a trained per-head scalar whose
+    exponential joins the softmax denominator and that carries no value
+    ("RoPE, scaling, sliding window, attention sinks", "Hybrid models break the
+    uniform-spec assumption", the second kind of sink; clamped as
+    ``clamp_sink_logits``).  Reading: the scalar is a logit in
+    the units of the scaled scores, so head h's weights are
+    exp(s_j) / (sum_i exp(s_i) + exp(z_h)).
     """
     q = np.asarray(q, dtype=np.float64)
     keys = np.asarray(keys, dtype=np.float64)
@@ -394,38 +416,48 @@ def attend(q: np.ndarray, keys: np.ndarray, values: np.ndarray) -> np.ndarray:
     Hq, D = q.shape
     Hkv = keys.shape[1]
     n_rep = Hq // Hkv
+    z = None if sink_logits is None else clamp_sink_logits(sink_logits)
     out = np.zeros((Hq, D), dtype=np.float64)
     for h in range(Hq):
         g = h // n_rep
         s = keys[:, g, :] @ q[h] / math.sqrt(D)
-        s = s - s.max()
-        p = np.exp(s)
-        p = p / p.sum()
+        if z is None:
+            s = s - s.max()
+            p = np.exp(s)
+            p = p / p.sum()
+        else:
+            m = max(s.max(), z[h])
+            e = np.exp(s - m)
+            p = e / (e.sum() + math.exp(z[h] - m))
         out[h] = p @ values[:, g, :]
     return out
 
 
-def decode_attention(cache, q_rot: np.ndarray) -> np.ndarray:
+def decode_attention(cache, q_rot: np.ndarray,
+                     sink_logits: Optional[Sequence[float]] = None) -> np.ndarray:
     """Decode attention of one new query over a cache after its own append:
     the cache's chronological rows are exactly the visible set V(P).
 
     Rows of the cache are (k_rot, v) pairs of shape [H_kv, D] each.
     "Inference & 128K Long Context", "_attn_forward_layer" (append, get, attend).
+    ``sink_logits``: optional learned per-head sinks, as in ``attend``.
     """
     rows = cache.chronological_rows()
     keys = np.stack([r[0] for r in rows])
     values = np.stack([r[1] for r in rows])
-    return attend(q_rot, keys, values)
+    return attend(q_rot, keys, values, sink_logits)
 
 
 def prefill_attention(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray, p0: int,
                       sinks: int, window: Optional[int],
-                      rows: Optional[Sequence[int]] = None) -> np.ndarray:
+                      rows: Optional[Sequence[int]] = None,
+                      sink_logits: Optional[Sequence[float]] = None) -> np.ndarray:
     """Masked attention of a prompt chunk over itself.
 
     q_rot [T, H_q, D], k_rot and v [T, H_kv, D]; chunk index t has absolute
     position p0 + t.  Query t sees key k iff ``mask_allows(p0+t, p0+k, S, W)``.
     ``rows`` picks the query indices to evaluate (all by default).
+    ``sink_logits``: optional learned per-head sinks, as in ``attend``.
     Returns [len(rows), H_q, D].
     """
     T = q_rot.shape[0]
@@ -435,7 +467,7 @@ def prefill_attention(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray, p0: i
     for t in rows:
         P = p0 + t
         ks = [k for k in range(T) if mask_allows(P, p0 + k, sinks, window)]
-        out.append(attend(q_rot[t], k_rot[ks], v[ks]))
+        out.append(attend(q_rot[t], k_rot[ks], v[ks], sink_logits))
     return np.stack(out)
 
 

@@ -174,3 +174,81 @@ def test_global_decode_equals_causal():
     for t in range(T):
         g.append([(k[t], v[t])])
         np.testing.assert_allclose(decode_attention(g, q[t]), dense[t], atol=1e-12)
+
+
+# ---- learned sink logits ---------------------------------------------------------------
+
+def _sdpa_with_sink_column(q, k, v, z):
+    """torch's float64 SDPA over the keys plus one extra key column whose logit is
+    forced to z[h] by an additive mask (a zero key scores 0, the mask adds z[h]) and
+    whose value row is zero: a per-head term exp(z_h) in the denominator only.
+    q [Hq,D], k/v [n,Hkv,D]."""
+    n_rep = q.shape[0] // k.shape[1]
+    n, D = k.shape[0], k.shape[2]
+    kt = torch.from_numpy(np.concatenate([k, np.zeros((1,) + k.shape[1:])])).permute(1, 0, 2)
+    vt = torch.from_numpy(np.concatenate([v, np.zeros((1,) + v.shape[1:])])).permute(1, 0, 2)
+    kt, vt = kt.repeat_interleave(n_rep, 0), vt.repeat_interleave(n_rep, 0)
+    mask = torch.zeros(q.shape[0], 1, n + 1, dtype=torch.float64)
+    mask[:, 0, n] = torch.from_numpy(np.asarray(z, dtype=np.float64))
+    qt = torch.from_numpy(q)[:, None, :]
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask)[:, 0].numpy()
+
+
+def test_learned_sink_equals_extra_zero_value_column_in_library_sdpa():
+    """A learned sink is a per-head logit in the softmax denominator with no value
+    ("RoPE, scaling, sliding window, attention sinks", "Hybrid models break the
+    uniform-spec assumption"): the same as one more key column of logit z_h and value 0."""
+    rng = np.random.default_rng(11)
+    q, k, v = rng.standard_normal((8, 64)) * 2, rng.standard_normal((37, 4, 64)), rng.standard_normal((37, 4, 64))
+    z = np.array([-9.5, -3.0, 0.0, 0.7, 2.5, 4.0, 9.0, 14.9])
+    np.testing.assert_allclose(attend(q, k, v, z), _sdpa_with_sink_column(q, k, v, z), atol=1e-12)
+
+
+def test_learned_sink_single_key_is_a_sigmoid_gate():
+    """One visible key of logit s and value v: out = v * sigmoid(s - z)."""
+    q = np.array([[2.0, 0.0, 0.0, 0.0]])
+    k = np.array([[[1.5, 0.0, 0.0, 0.0]]])      # s = 2 * 1.5 / sqrt(4) = 1.5
+    v = np.array([[[1.0, -2.0, 0.5, 3.0]]])
+    out = attend(q, k, v, [0.5])
+    np.testing.assert_allclose(out[0], v[0, 0] * 0.7310585786300049, rtol=1e-15)  # sigmoid(1)
+    # equal logits: half the weight goes to the sink
+    np.testing.assert_allclose(attend(q, k, v, [1.5])[0], v[0, 0] * 0.5, rtol=1e-15)
+
+
+def test_learned_sink_logits_are_clamped_to_page_bounds():
+    """The forward pass clamps the sink bias to [-10, 15] ("Inference & 128K Long
+    Context", "Sink clamp cache")."""
+    rng = np.random.default_rng(12)
+    q, k, v = rng.standard_normal((4, 16)), rng.standard_normal((9, 2, 16)), rng.standard_normal((9, 2, 16))
+    np.testing.assert_array_equal(attend(q, k, v, [100.0, -1e9, 15.0, -10.0]),
+                                  attend(q, k, v, [15.0, -10.0, 15.0, -10.0]))
+    # inside the bounds nothing is clamped: z = 14.99 differs from 15
+    assert np.abs(attend(q, k, v, [14.99] * 4) - attend(q, k, v, [15.0] * 4)).max() > 1e-12
+
+
+def test_learned_sink_shrinks_plain_attention_by_its_weight():
+    """out_sink = (1 - p_sink) * out_plain with p_sink = e^z / (e^z + sum_j e^{s_j});
+    the sum of exponentials is taken with an explicit loop."""
+    rng = np.random.default_rng(13)
+    q, k, v = rng.standard_normal((2, 8)), rng.standard_normal((5, 1, 8)), rng.standard_normal((5, 1, 8))
+    z = [1.25, -4.0]
+    got = attend(q, k, v, z)
+    plain = attend(q, k, v)
+    for h in range(2):
+        tot = 0.0
+        for j in range(5):
+            tot += float(np.exp(sum(q[h, d] * k[j, 0, d] for d in range(8)) / np.sqrt(8)))
+        p_sink = np.exp(z[h]) / (np.exp(z[h]) + tot)
+        np.testing.assert_allclose(got[h], (1 - p_sink) * plain[h], rtol=1e-12, atol=1e-15)
+
+
+def test_learned_sink_in_decode_and_prefill_agree():
+    """A decode step at P equals row P of the prefill with the same mask and sinks."""
+    T, Hq, Hkv, D, S, W = 13, 4, 2, 16, 2, 4
+    q, k, v = _qkv(T, Hq, Hkv, D, 14)
+    z = [-1.0, 0.5, 3.0, 20.0]
+    dense = prefill_attention(q, k, v, 0, S, W, sink_logits=z)
+    c = RingCache(S, W)
+    for t in range(T):
+        c.append([(k[t], v[t])])
+        np.testing.assert_allclose(decode_attention(c, q[t], sink_logits=z), dense[t], atol=1e-12)
