@@ -188,6 +188,15 @@ def window_setup(seed_base=0, steps=1):
     return tbl, layer, c
 
 
+def _learned_sinks(args, n_q_heads):
+    """Per-head learned sink logits for --learned-sink runs (float32 on the device),
+    spread over the clamp range; None otherwise."""
+    import torch
+    if not args.learned_sink:
+        return None
+    return torch.linspace(-12.0, 17.0, n_q_heads, device="cuda").contiguous()
+
+
 def bench_window(args, rank, world):
     import torch
     import sink_kv_attention_gb300 as sk
@@ -203,13 +212,14 @@ def bench_window(args, rank, world):
     out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(sk.decode_workspace_bytes(layer, Hq), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
+    zl = _learned_sinks(args, Hq)
 
     def step(i, ev=None):
         st = torch.cuda.current_stream()  # the capture stream while a graph is captured
         sk.kv_append(tbl, layer, qs[i], ks[i], vs[i])
         if ev is not None:
             ev[0].record(st)
-        sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws)
+        sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws, sink_logits=zl)
         if ev is not None:
             ev[1].record(st)
 
@@ -296,7 +306,7 @@ def bench_window(args, rank, world):
                 dk.copy_(hk[i], non_blocking=True)
                 dv.copy_(hv[i], non_blocking=True)
                 sk.kv_append(tbl2, layer2, dq, dk, dv)
-                sk.decode_attention(layer2, dq[:, 0], out=out, workspace=ws)
+                sk.decode_attention(layer2, dq[:, 0], out=out, workspace=ws, sink_logits=zl)
                 hout[i].copy_(out, non_blocking=True)
 
         g_e2e = None
@@ -330,6 +340,7 @@ def bench_window(args, rank, world):
                    "batch_per_gpu": B, "H_q": Hq, "H_kv": Hkv, "d_h": D, "rotary_dim": c["r"],
                    "theta": c["theta"], "sinks": c["S"], "window": W, "visible_keys": L,
                    "positions": "U[4096, 32768], ring wrapped at random head",
+                   "learned_sink_logits": bool(args.learned_sink),
                    "l2": f"inputs larger than L2 (KV {kv_bytes / 1e6:.0f} MB per step > 129 MB)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_hbm_peak": round(value / world / hbm, 4),
@@ -406,11 +417,12 @@ def bench_hybrid(args):
     vs = synth.normal((n, nl, B, 1, Hkv, D), 5, torch.bfloat16, device="cuda")
     out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(max(sk.decode_workspace_bytes(L, Hq) for L in layers), dtype=torch.uint8, device="cuda")
+    zl = _learned_sinks(args, Hq)
 
     def step(i):
         for j, L in enumerate(layers):
             sk.kv_append(tbl, L, qs[i, j], ks[i, j], vs[i, j])
-            sk.decode_attention(L, qs[i, j, :, 0], out=out, workspace=ws)
+            sk.decode_attention(L, qs[i, j, :, 0], out=out, workspace=ws, sink_logits=zl)
 
     ms, clk = _timed(step, steps, warm)
     n_glob = sum(1 for i in range(c["layers"]) if synth.hybrid_layer_is_global(i))
@@ -426,7 +438,8 @@ def bench_hybrid(args):
             "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "Llama-3-8B-shaped hybrid decode: 32 layers 3:1 sliding:global, B=16, "
                                    "H_q=32, H_kv=8, d_h=128, W=4096+4 sinks, global prefix 131072",
-                       "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.1f} GB per step)"},
+                       "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.1f} GB per step)",
+                       "learned_sink_logits": bool(args.learned_sink)},
             "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
             "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": steps * c["layers"] * 3, "clocks": clk}
 
@@ -515,12 +528,13 @@ def bench_prefill(args):
     out = torch.empty_like(q)
     ws = torch.empty(sk.prefill_workspace_bytes(B, T, Hkv, D), dtype=torch.uint8, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    zl = _learned_sinks(args, Hq)
 
     def append(i):
         sk.kv_append(tbl, layers[i], q, k, v)
 
     def attend(i):
-        sk.prefill_attention(q, k, v, 0, S, W, out=out, workspace=ws, err=err)
+        sk.prefill_attention(q, k, v, 0, S, W, out=out, workspace=ws, err=err, sink_logits=zl)
 
     ms_append, clk_a = _timed(append, args.steps, args.warmup)
     ms_attn, clk = _timed(attend, args.steps, args.warmup)
@@ -537,7 +551,8 @@ def bench_prefill(args):
             "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_attn, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "prefill chunk: B=1, T=32768, H_q=32, H_kv=8, d_h=128, S=4, W=4092",
-                       "visited_tiles_per_head": tiles, "tile": "128 queries x 64 keys"},
+                       "visited_tiles_per_head": tiles, "tile": "128 queries x 64 keys",
+                       "learned_sink_logits": bool(args.learned_sink)},
             "frac_of_bf16_peak": round(tf / bf16_peak, 4),
             "algorithmic_tflops": round(alg_flops / (ms_attn * 1e-3) / 1e12, 1),
             "algorithmic_flops": alg_flops, "tile_flops": tile_flops,
@@ -616,6 +631,8 @@ def main():
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--learned-sink", action="store_true",
+                    help="window/hybrid/prefill: add per-head learned sink logits to the attention")
     ap.add_argument("--eager", action="store_true", help="launch each step from Python instead of a CUDA graph")
     args = ap.parse_args()
 

@@ -83,8 +83,9 @@ typedef struct {
 
 /* Opaque, library-owned cos/sin table.  Its device buffer is
  * float2[max_positions][rotary_dim/2] = (mu cos(P omega_j), mu sin(P omega_j)),
- * computed in float64 on the host and rounded to float32 ([RoPE]: "a table of
- * shape [max_position_embeddings, r] built once ... No trigonometry at runtime"). */
+ * computed in float64 on the host and rounded to float32 ([RoPE] "Hybrid models
+ * break the uniform-spec assumption", the walk of one decode token: the rotation
+ * gathers table rows and does no trigonometry). */
 typedef struct sk_rope_table sk_rope_table;
 
 /*
@@ -193,13 +194,19 @@ SK_API size_t sk_decode_workspace_bytes(const sk_kv_layer* layer, int32_t n_q_he
  * in-register broadcast).  scores = q.k / sqrt(d_h), softmax, out = sum p v
  * ([SINK] the experiment's incremental_sink).
  *   q_rot: [batch][n_q_heads][head_dim] of io_dtype (device); out: same shape and dtype.
+ *   sink_logits: NULL, or device float32 [n_q_heads], 4-byte aligned: learned sinks
+ *   ([RoPE] "Hybrid models break the uniform-spec assumption": a trained per-head
+ *   scalar in the softmax denominator that holds no cache rows).  Head h's weights
+ *   become exp(s_j) / (sum_i exp(s_i) + exp(z_h)) with s the scaled scores and
+ *   z_h = sink_logits[h] clamped to [-10, 15] in the kernel ([MIXED] "Sink clamp
+ *   cache").  The same value serves every sequence.
  *   workspace: device, >= sk_decode_workspace_bytes(layer, n_q_heads) bytes, 16-byte
  *   aligned; its contents need no initialisation.
  * Supported: io SK_F32 with an F32/F32 cache, io SK_BF16 with a BF16/BF16 cache;
  * n_q_heads / n_kv_heads in {1, 2, 4} for head_dim 128 and {1, 2, 4, 8} for 64. */
 SK_API sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q_rot, int32_t n_q_heads,
-                              int32_t io_dtype, void* out, void* workspace, size_t ws_bytes,
-                              void* stream);
+                                     int32_t io_dtype, const float* sink_logits, void* out,
+                                     void* workspace, size_t ws_bytes, void* stream);
 
 /* ---- Decode attention without any allocation -------------------------------------- */
 
@@ -228,8 +235,8 @@ SK_API sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q_rot
  *     so the contents left by an earlier call never matter.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
 SK_API sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const void* q_rot,
-                                             int32_t n_q_heads, int32_t io_dtype, void* out,
-                                             void* stream);
+                                             int32_t n_q_heads, int32_t io_dtype,
+                                             const float* sink_logits, void* out, void* stream);
 
 /* ---- Prefill attention (causal + window + sinks) ---------------------------------- */
 
@@ -240,6 +247,8 @@ SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_
 /* Masked attention of a prompt chunk over itself on the tensor cores.
  *   q_rot: [batch][T][n_q_heads][head_dim], k_rot, v: [batch][T][n_kv_heads][head_dim],
  *   out: [batch][T][n_q_heads][head_dim]; all SK_BF16, device, 16-byte aligned.
+ *   sink_logits: NULL, or device float32 [n_q_heads] learned sinks, as for
+ *   sk_decode_attention (clamped to [-10, 15], denominator only).
  * Chunk index t has absolute position p0 + t.  Query t sees key k iff k <= t and
  * (p0 + k < sinks or t - k < window) ([MIXED] 5.5: idx_q >= idx_k and
  * idx_q - idx_k < window; [SINK] sink + recent).  window <= 0 means a global layer
@@ -251,8 +260,9 @@ SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_
  * Supported: head_dim 128, SK_BF16. */
 SK_API sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
                                       int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                      int64_t p0, int32_t sinks, int32_t window, void* out, void* workspace,
-                                      size_t ws_bytes, uint32_t* err, void* stream);
+                                      int64_t p0, int32_t sinks, int32_t window, const float* sink_logits,
+                                      void* out, void* workspace, size_t ws_bytes, uint32_t* err,
+                                      void* stream);
 
 /* ---- Cached-key rerotation on a factor change ------------------------------------ */
 

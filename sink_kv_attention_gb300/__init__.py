@@ -71,14 +71,16 @@ _SIGNATURES = [
                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]),
     ("sk_decode_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32]),
     ("sk_decode_attention", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
-                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                           ctypes.c_void_p]),
     ("sk_decode_attention_noalloc", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32,
-                                                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
+                                                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_prefill_workspace_bytes", ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     ("sk_prefill_attention", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                             ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
-                                            ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                            ctypes.c_void_p]),
     ("sk_kv_rerotate", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_status_str", ctypes.c_char_p, [ctypes.c_int]),
@@ -285,9 +287,20 @@ def decode_workspace_bytes(layer: KVLayer, n_q_heads: int) -> int:
     return int(_lib().sk_decode_workspace_bytes(ctypes.byref(s), n_q_heads))
 
 
+def _sink_logits(sink_logits: Optional[torch.Tensor], n_q_heads: int):
+    """Checks learned sink logits (float32 [n_q_heads] on the device, or None)."""
+    if sink_logits is None:
+        return None
+    if sink_logits.dtype != torch.float32 or sink_logits.numel() != n_q_heads or not sink_logits.is_contiguous():
+        raise ValueError("sink_logits must be a contiguous float32 tensor of n_q_heads values")
+    return _ptr(sink_logits)
+
+
 def decode_attention(layer: KVLayer, q_rot: torch.Tensor, out: Optional[torch.Tensor] = None,
-                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Split-K decode attention of q_rot [B, Hq, D] over the layer's visible set."""
+                     workspace: Optional[torch.Tensor] = None, stream=None,
+                     sink_logits: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Split-K decode attention of q_rot [B, Hq, D] over the layer's visible set;
+    optional learned per-head sink logits (float32 [Hq], clamped to [-10, 15])."""
     _need_contig(q_rot)
     Hq = q_rot.shape[1]
     if out is None:
@@ -298,20 +311,23 @@ def decode_attention(layer: KVLayer, q_rot: torch.Tensor, out: Optional[torch.Te
         raise SinkKVError(SK_ERR_UNSUPPORTED, "sk_decode_workspace_bytes")
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q_rot.device)
-    _check(_lib().sk_decode_attention(ctypes.byref(s), _ptr(q_rot), Hq, _sk_dtype(q_rot.dtype), _ptr(out),
-                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                      _stream(stream)), "sk_decode_attention")
+    _check(_lib().sk_decode_attention(ctypes.byref(s), _ptr(q_rot), Hq, _sk_dtype(q_rot.dtype),
+                                      _sink_logits(sink_logits, Hq), _ptr(out), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+           "sk_decode_attention")
     return out
 
 
-def decode_attention_noalloc(layer: KVLayer, q_rot: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+def decode_attention_noalloc(layer: KVLayer, q_rot: torch.Tensor, out: torch.Tensor, stream=None,
+                             sink_logits: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Decode attention for callers that cannot allocate device memory: the scratch
     is the library's fixed 4 MiB device array (sk_decode_attention_noalloc); `out`
     must be given.  Calls that may overlap on the GPU race on that array."""
     _need_contig(q_rot, out)
     s = layer.struct()
     _check(_lib().sk_decode_attention_noalloc(ctypes.byref(s), _ptr(q_rot), q_rot.shape[1],
-                                              _sk_dtype(q_rot.dtype), _ptr(out), _stream(stream)),
+                                              _sk_dtype(q_rot.dtype), _sink_logits(sink_logits, q_rot.shape[1]),
+                                              _ptr(out), _stream(stream)),
            "sk_decode_attention_noalloc")
     return out
 
@@ -322,9 +338,11 @@ def prefill_workspace_bytes(batch: int, T: int, n_kv_heads: int, head_dim: int) 
 
 def prefill_attention(q_rot: torch.Tensor, k_rot: torch.Tensor, v: torch.Tensor, p0: int, sinks: int,
                       window: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                      err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                      err: Optional[torch.Tensor] = None, stream=None,
+                      sink_logits: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Masked prefill attention of a chunk over itself: q [B,T,Hq,D], k/v [B,T,Hkv,D]
-    (sk_prefill_attention); window <= 0 is a global layer."""
+    (sk_prefill_attention); window <= 0 is a global layer; optional learned per-head
+    sink logits (float32 [Hq])."""
     _need_contig(q_rot, k_rot, v)
     B, T, Hq, D = q_rot.shape
     Hkv = k_rot.shape[2]
@@ -336,7 +354,7 @@ def prefill_attention(q_rot: torch.Tensor, k_rot: torch.Tensor, v: torch.Tensor,
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q_rot.device)
     _check(_lib().sk_prefill_attention(_ptr(q_rot), _ptr(k_rot), _ptr(v), B, T, Hq, Hkv, D, int(p0), int(sinks),
-                                       int(window), _ptr(out), _ptr(workspace),
+                                       int(window), _sink_logits(sink_logits, Hq), _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)),
            "sk_prefill_attention")
     return out

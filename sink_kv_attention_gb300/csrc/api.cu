@@ -31,4 +31,4 @@ extern "C" const char* sk_status_str(sk_status status) {
     }
 }
 
-extern "C" int32_t sk_version(void) { return 100; }
+extern "C" int32_t sk_version(void) { return 200; }

@@ -23,7 +23,8 @@
 // round adds the same register slots, with no selects; online softmax in base 2;
 // then P.V with each lane owning D/32 dims of all NREP heads, the probabilities read
 // back from shared memory as (p, p) pairs ready for packed fp32 FMAs.
-// A second kernel combines each unit's partials by log-sum-exp.
+// A second kernel combines each unit's partials by log-sum-exp; a learned sink logit
+// (a per-head term in the softmax denominator) enters there.
 #include <algorithm>
 #include <mutex>
 
@@ -35,11 +36,15 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxBatch = 1024;
+// Bounds of a learned sink logit ("Inference & 128K Long Context", "Sink clamp cache").
+constexpr float kSinkLogitMin = -10.0f;
+constexpr float kSinkLogitMax = 15.0f;
 
 struct DecodeParams {
     const void* kc;
     const void* vc;
     const void* q;
+    const float* sink_logits;  // [Hq] learned sinks or null
     void* out;
     float* ws;
     const int32_t* count;
@@ -458,14 +463,21 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
         const int64_t c = fb + i;
         return (c * R + P - 1) / P < ((c + 1) * R + P - 1) / P;
     };
-    float M = -INFINITY;
+    // A learned sink is one more logit z (scaled-score units, clamped) in the
+    // denominator with no value row ("RoPE, scaling, sliding window, attention sinks",
+    // "Hybrid models break the uniform-spec assumption"); in base 2 it is z log2(e).
+    const bool has_sink = p.sink_logits != nullptr;
+    const float z2 = has_sink
+                         ? fminf(fmaxf(p.sink_logits[hq], kSinkLogitMin), kSinkLogitMax) * kLog2e
+                         : -INFINITY;
+    float M = z2;
     for (int i = 0; i < n; ++i)
         if (owns_rows(i)) M = fmaxf(M, base[i * PF + h]);
     const float Mu = M == -INFINITY ? 0.0f : M;
     float acc[DPV];
 #pragma unroll
     for (int d = 0; d < DPV; ++d) acc[d] = 0.0f;
-    float lsum = 0.0f;
+    float lsum = has_sink ? fast_exp2_approx(z2 - Mu) : 0.0f;
     for (int i = 0; i < n; ++i) {
         if (!owns_rows(i)) continue;
         const float* pp = base + i * PF;
@@ -590,12 +602,13 @@ extern "C" size_t sk_decode_workspace_bytes(const sk_kv_layer* layer, int32_t n_
 }
 
 extern "C" sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q_rot, int32_t n_q_heads,
-                                         int32_t io_dtype, void* out, void* workspace, size_t ws_bytes,
-                                         void* stream) {
+                                         int32_t io_dtype, const float* sink_logits, void* out,
+                                         void* workspace, size_t ws_bytes, void* stream) {
     sk_status s = check_layer(layer, n_q_heads);
     if (s != SK_OK) return s;
     SK_RET_IF(q_rot == nullptr || out == nullptr || workspace == nullptr, SK_ERR_ARG);
     SK_RET_IF((reinterpret_cast<uintptr_t>(q_rot) | reinterpret_cast<uintptr_t>(workspace)) & 15u, SK_ERR_ARG);
+    SK_RET_IF(reinterpret_cast<uintptr_t>(sink_logits) & 3u, SK_ERR_ARG);
     const sk_kv_layer& L = *layer;
     const int nrep = n_q_heads / L.n_kv_heads;
     size_t need = 0;
@@ -606,6 +619,7 @@ extern "C" sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q
     p.kc = L.k;
     p.vc = L.v;
     p.q = q_rot;
+    p.sink_logits = sink_logits;
     p.out = out;
     p.ws = static_cast<float*>(workspace);
     p.count = L.count;
@@ -652,8 +666,8 @@ sk_status noalloc_scratch(void** out) {
 }  // namespace
 
 extern "C" sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const void* q_rot,
-                                                 int32_t n_q_heads, int32_t io_dtype, void* out,
-                                                 void* stream) {
+                                                 int32_t n_q_heads, int32_t io_dtype,
+                                                 const float* sink_logits, void* out, void* stream) {
     sk_status s = check_layer(layer, n_q_heads);
     if (s != SK_OK) return s;
     SK_RET_IF(q_rot == nullptr || out == nullptr, SK_ERR_ARG);
@@ -665,6 +679,6 @@ extern "C" sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const
     void* scratch = nullptr;
     s = noalloc_scratch(&scratch);
     if (s != SK_OK) return s;
-    return sk_decode_attention(layer, q_rot, n_q_heads, io_dtype, out, scratch,
+    return sk_decode_attention(layer, q_rot, n_q_heads, io_dtype, sink_logits, out, scratch,
                                SK_DECODE_NOALLOC_SCRATCH_BYTES, stream);
 }

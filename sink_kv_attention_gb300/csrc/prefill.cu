@@ -22,6 +22,8 @@
 // longer waits for P.V of the previous tile (only a rare O rescale does); two CTAs per
 // SM overlap one CTA's softmax with the other's MMAs.
 // V is transposed once per call into the workspace ([B][Hkv][D][T_pad]).
+// An optional learned sink logit per query head (a denominator-only term) enters at
+// the epilogue.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -38,6 +40,9 @@ constexpr int HD = 128;
 constexpr int kThreads = 6 * 32;
 constexpr uint32_t kTmemCols = 256;  // S0 [0, 64), S1 [64, 128), O [128, 256)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Bounds of a learned sink logit ("Inference & 128K Long Context", "Sink clamp cache").
+constexpr float kSinkLogitMin = -10.0f;
+constexpr float kSinkLogitMax = 15.0f;
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr int SM_Q = 0;                       // Q dims 0-63 then 64-127: 2 x 16 KB
@@ -55,6 +60,7 @@ static_assert(SM_ALLOC >= SM_BYTES + 896, "no room to align the shared-memory ba
 
 struct PrefillParams {
     void* out;
+    const float* sink_logits;  // [Hq] learned sinks or null
     uint32_t* err;
     int64_t p0;
     int T, Hq, Hkv, B;
@@ -305,7 +311,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- epilogue: O / l -> bf16 rows ----
         wait_or_flag(&pv_done[(tp.n - 1) & 1], ((tp.n - 1) >> 1) & 1, bad);
         tc_fence_after_sync();
-        const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+        float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+        if (p.sink_logits != nullptr) {
+            // Learned sink: one more logit z in the denominator, no value row ("RoPE,
+            // scaling, sliding window, attention sinks", "Hybrid models break the
+            // uniform-spec assumption").  O and l are relative to m_run; bring both to
+            // max(m_run, z) before adding 2^(z - max).
+            const float z2 =
+                fminf(fmaxf(p.sink_logits[h], kSinkLogitMin), kSinkLogitMax) * 1.4426950408889634f;
+            const float m_ref = m_run == -INFINITY ? z2 : m_run;
+            const float m_new = fmaxf(m_ref, z2);
+            const float a = fast_exp2_approx(m_ref - m_new);
+            inv = a / fmaf(l_run, a, fast_exp2_approx(z2 - m_new));
+        }
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
                               ((int64_t(b) * p.T + t) * p.Hq + h) * HD;
 #pragma unroll
@@ -403,8 +421,9 @@ extern "C" size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n
 
 extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
                                           int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                          int64_t p0, int32_t sinks, int32_t window, void* out, void* workspace,
-                                          size_t ws_bytes, uint32_t* err, void* stream) {
+                                          int64_t p0, int32_t sinks, int32_t window, const float* sink_logits,
+                                          void* out, void* workspace, size_t ws_bytes, uint32_t* err,
+                                          void* stream) {
     SK_RET_IF(q_rot == nullptr || k_rot == nullptr || v == nullptr || out == nullptr || workspace == nullptr,
               SK_ERR_ARG);
     SK_RET_IF(batch < 1 || T < 0 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads != 0, SK_ERR_ARG);
@@ -414,6 +433,7 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
                          reinterpret_cast<uintptr_t>(workspace);
     SK_RET_IF(al & 15u, SK_ERR_ARG);
+    SK_RET_IF(reinterpret_cast<uintptr_t>(sink_logits) & 3u, SK_ERR_ARG);
     if (T == 0) return SK_OK;
     SK_RET_IF(ws_bytes < sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim), SK_ERR_ARG);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -455,6 +475,7 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
 
     PrefillParams p{};
     p.out = out;
+    p.sink_logits = sink_logits;
     p.err = err;
     p.p0 = p0;
     p.T = T;

@@ -84,7 +84,10 @@ def test_bad_arguments_rejected_on_host(lib):
     assert lib.sk_rope_table_create(ctypes.byref(bad), None, ctypes.byref(out)) == sk.SK_ERR_ARG
     assert lib.sk_rope_table_create(None, None, ctypes.byref(out)) == sk.SK_ERR_ARG
     assert lib.sk_kv_append(None, None, None, 0, None, None, 0, 1, None) == sk.SK_ERR_ARG
-    assert lib.sk_decode_attention(None, None, 8, 0, None, None, 0, None) == sk.SK_ERR_ARG
+    assert lib.sk_decode_attention(None, None, 8, 0, None, None, None, 0, None) == sk.SK_ERR_ARG
+    assert lib.sk_decode_attention_noalloc(None, None, 8, 0, None, None, None) == sk.SK_ERR_ARG
+    assert lib.sk_prefill_attention(None, None, None, 1, 1, 1, 1, 128, 0, 0, 0, None, None, None, 0, None,
+                                    None) == sk.SK_ERR_ARG
     assert lib.sk_decode_workspace_bytes(None, 8) == 0
     assert lib.sk_kv_rerotate(None, 1, None, None, None) == sk.SK_ERR_ARG
     assert lib.sk_rope_apply(None, None, 0, 1, 1, None, None, None) == sk.SK_ERR_ARG

@@ -36,7 +36,7 @@ def test_noalloc_decode_matches_workspace_decode_twice():
         want = sk.decode_attention(layer, q)
         out = torch.full_like(q, float("nan"))
         status = lib.sk_decode_attention_noalloc(ctypes.byref(st), ctypes.c_void_p(q.data_ptr()), Hq, sk.SK_BF16,
-                                                 ctypes.c_void_p(out.data_ptr()), stream)
+                                                 None, ctypes.c_void_p(out.data_ptr()), stream)
         assert status == sk.SK_OK, lib.sk_status_str(status)
         torch.cuda.synchronize()
         assert torch.isfinite(out.float()).all()
@@ -55,5 +55,5 @@ def test_noalloc_decode_rejects_batches_past_its_scratch():
     out = torch.zeros_like(q)
     st = layer.struct()
     status = lib.sk_decode_attention_noalloc(ctypes.byref(st), ctypes.c_void_p(q.data_ptr()), 32, sk.SK_BF16,
-                                             ctypes.c_void_p(out.data_ptr()), None)
+                                             None, ctypes.c_void_p(out.data_ptr()), None)
     assert status == sk.SK_ERR_CAPACITY
