@@ -132,8 +132,7 @@ typedef struct {
 SK_API sk_status sk_rope_table_create(const sk_rope_config* cfg, void* stream, sk_rope_table** out);
 
 /* Rebuild the table in place for a new YaRN factor: same device pointer, so CUDA
- * graphs captured against it read the new angles ([DYN] "The table. The cos/sin
- * table is rebuilt in place ... so the captured CUDA graphs keep their pointer").
+ * graphs captured against it read the new angles ([DYN] "What it does", the table).
  * The entries are computed independently on host threads, so the result is bitwise
  * that of sk_rope_table_create with the new factor.  Ordered on `stream`
  * (kernels already queued on it finish first) and synchronises it. */

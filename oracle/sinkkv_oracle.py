@@ -184,9 +184,9 @@ def rerotate(k_a: np.ndarray, positions: Sequence[int], spec_a: RopeSpec,
              spec_b: RopeSpec) -> np.ndarray:
     """Turn keys stored rotated under spec A into keys rotated under spec B.
 
-    "#2961 rope: --rope-scaling dynamic", "What it does": one more rotation of each
-    pair by p * (w_B - w_A) and the magnitude ratio mscale_B / mscale_A; this is
-    R_a R_b = R_{a+b} ("Attention Sink 与 Streaming KV Cache", RoPE section).
+    "#2961 rope: --rope-scaling dynamic", "What it does": since keys are cached after
+    RoPE, each pair is turned by a further angle p * (w_B - w_A) and scaled by
+    mscale_B / mscale_A; this is R_a R_b = R_{a+b} ("Attention Sink 与 Streaming KV Cache", RoPE section).
     No raw key is needed.
     """
     delta = spec_b.omega() - spec_a.omega()

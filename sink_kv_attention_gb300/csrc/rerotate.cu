@@ -1,8 +1,8 @@
 // In-place rerotation of cached keys when the RoPE factor changes.
 //
-// "#2961 rope: --rope-scaling dynamic", "What it does": K is stored post-RoPE, so a
-// key written at factor A becomes the key of factor B after one more rotation of each
-// pair by p (w_B - w_A) and the magnitude ratio mscale_B / mscale_A; int8 keys are
+// "#2961 rope: --rope-scaling dynamic", "What it does": keys are cached after RoPE, so
+// turning each pair of a key cached at factor A by a further angle p (w_B - w_A) and
+// scaling it by mscale_B / mscale_A gives the key at factor B; int8 keys are
 // dequantized, turned and requantized.  "Attention Sink 与 Streaming KV Cache": R_a R_b
 // = R_{a+b}, so no raw key is needed.  The delta rotation comes from the two tables'
 // entries at P: with (cA, sA) = mu_A (cos a, sin a) and (cB, sB) = mu_B (cos b, sin b),
