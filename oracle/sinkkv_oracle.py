@@ -180,6 +180,20 @@ def rope_rotate(x: np.ndarray, positions: Sequence[int], omega: np.ndarray,
     return out
 
 
+def rope_table(spec: RopeSpec, n_positions: int) -> np.ndarray:
+    """The cos/sin table for positions 0 .. n_positions-1: [n_positions, r/2, 2] with
+    entry (P, j) = mscale (cos(P omega_j), sin(P omega_j)), in float64.
+
+    "RoPE, scaling, sliding window, attention sinks": the rotation gathers rows of a
+    table built once per configuration ("Hybrid models break the uniform-spec
+    assumption", the walk of one decode token), and YaRN's mscale rides on both cos
+    and sin ("YaRN, precisely").
+    """
+    angle = np.arange(n_positions, dtype=np.float64)[:, None] * spec.omega()[None, :]
+    mu = spec.mscale()
+    return np.stack([mu * np.cos(angle), mu * np.sin(angle)], axis=-1)
+
+
 def rerotate(k_a: np.ndarray, positions: Sequence[int], spec_a: RopeSpec,
              spec_b: RopeSpec) -> np.ndarray:
     """Turn keys stored rotated under spec A into keys rotated under spec B.

@@ -152,3 +152,45 @@ def test_kv_bytes_context_numbers(golden):
     uniform = 32 * 131072 * per_layer_token
     assert hybrid / 2 ** 30 == float(g["hybrid_gib_128k"])
     assert uniform / 2 ** 30 == float(g["uniform_gib_128k"])
+
+
+# ---- the cos/sin table -----------------------------------------------------------------
+
+def test_table_worked_number_row(golden):
+    """Row P=2, pair 16 (theta 1e4, r 128, omega 0.1) holds (cos 0.2, sin 0.2): the
+    page's worked score cos(0.2) for a relative offset of 2."""
+    from oracle.sinkkv_oracle import rope_table
+    g = golden("rope_yarn_worked_values.txt")
+    t = rope_table(RopeSpec(128, 128, 1e4), 3)
+    assert t[2, 16, 0] == pytest.approx(float(g["score_q5_k3"]), abs=5e-8)
+    assert t[2, 16, 1] == pytest.approx(math.sqrt(1 - float(g["score_q5_k3"]) ** 2), abs=5e-7)
+    np.testing.assert_array_equal(t[0, :, 0], np.ones(64))
+    np.testing.assert_array_equal(t[0, :, 1], np.zeros(64))
+
+
+@pytest.mark.parametrize("neox", [True, False])
+def test_table_rows_are_the_rotation_of_a_unit_pair(neox):
+    """Rotating the unit vector of a pair's first element at P gives the table entry:
+    (cos, sin) land in the pair's (first, second) slots."""
+    from oracle.sinkkv_oracle import rope_table, rotary_pairs
+    spec = RopeSpec(128, 64, 5e5, neox, 2.0, 4096)
+    t = rope_table(spec, 40)
+    first, second = rotary_pairs(64, neox)
+    for j in [0, 7, 31]:
+        x = np.zeros((40, 1, 128))
+        x[:, 0, first[j]] = 1.0
+        y = rope_rotate(x, range(40), spec.omega(), spec.mscale(), 64, neox)
+        np.testing.assert_allclose(y[:, 0, first[j]], t[:, j, 0], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(y[:, 0, second[j]], t[:, j, 1], rtol=0, atol=1e-15)
+
+
+def test_table_rows_compose_and_carry_mscale(golden):
+    """|row| = mu (0.1 ln s + 1; 1.2079 at s = 8) and row(a) row(b) = mu row(a + b) as
+    complex numbers (R_a R_b = R_{a+b})."""
+    from oracle.sinkkv_oracle import rope_table
+    g = golden("rope_yarn_worked_values.txt")
+    t = rope_table(RopeSpec(128, 128, 1e4, True, 8.0, 4096), 300)
+    z = t[..., 0] + 1j * t[..., 1]
+    np.testing.assert_allclose(np.abs(z), float(g["yarn_mscale_s8"]), atol=5e-5)
+    for a, b in [(3, 5), (100, 199), (17, 0)]:
+        np.testing.assert_allclose(z[a] * z[b], np.abs(z[0, 0]) * z[a + b], atol=1e-12)
