@@ -495,6 +495,77 @@ def bench_rerotate(args, kdt):
             "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": args.steps, "clocks": clk}
 
 
+DYNAMIC_CHAIN = (1.125, 1.25, 1.5, 1.625, 1.75, 1.875, 2.0)
+
+
+def bench_dynamic(args, kdt):
+    """Dynamic YaRN switches on the rerotation workload (48 layers x 4 kv heads x
+    524288 cached positions, L0 = 262144): one step drives a growing dialog through the
+    seven switches 1 -> 1.125 -> 1.25 -> 1.5 -> 1.625 -> 1.75 -> 1.875 -> 2 and back
+    to 1; each switch = host build of the new table + turning every cached key + the
+    in-place table copy, timed on the host clock around the public call (which
+    synchronises its stream)."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.REROTATE
+    D, r, Hkv, N, L0 = c["D"], c["r"], c["Hkv"], c["positions"], c["orig_ctx"]
+    nl = args.layers or c["layers"]
+    dyn = sk.DynamicRope(D, r, c["theta"], N, L0, cap=2.0)
+    kdtype = torch.bfloat16 if kdt == "bf16" else torch.int8
+    layers = []
+    for l in range(nl):
+        L = sk.KVLayer.allocate(sk.SK_LAYER_GLOBAL, 1, Hkv, D, capacity=N, k_dtype=kdtype, with_v=False)
+        L.pos.fill_(N)
+        if kdt == "bf16":
+            synth.fill_uniform_(L.k, 500 + l, -1.0, 1.0)
+        else:
+            L.k.copy_(synth.randint(L.k.shape, 600 + l, -127, 128, device="cuda").to(torch.int8))
+            synth.fill_uniform_(L.k_scale, 700 + l, 1.0 / 127, 2.0 / 127)
+        layers.append(L)
+    lengths = [int(L0 * (f - 0.125)) + 1 for f in DYNAMIC_CHAIN]
+    lengths[2] = int(L0 * 1.375) + 1            # the page's chain steps over 1.375
+    targets = lengths + [L0]                    # ... and a dialog below L0 again
+
+    def one_chain(times):
+        for n in targets:
+            t0 = time.perf_counter()
+            f, switched = dyn.update(n, layers)
+            times.append((time.perf_counter() - t0) * 1e3)
+            assert switched
+
+    for _ in range(max(1, args.warmup)):
+        one_chain([])
+    torch.cuda.synchronize()
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    clocks.mark("start")
+    times = []
+    for _ in range(args.steps):
+        one_chain(times)
+    clocks.mark("end")
+    clocks.stop()
+    # the host table build alone, at the same size and thread count
+    t0 = time.perf_counter()
+    sk.rope_table_fill_host(D, r, c["theta"], N, yarn_factor=2.0, yarn_orig_ctx=L0)
+    build_ms = (time.perf_counter() - t0) * 1e3
+    assert all(L.error_bits() == 0 for L in layers)
+    rows = nl * Hkv * N
+    alg = rows * (r * 2 * 2 if kdt == "bf16" else (D + 4) * 2)
+    ms = statistics.mean(times)
+    return {"metric": f"dynamic YaRN switch ({kdt} keys): ms per switch (table build + key rotation)",
+            "value": round(ms, 3), "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms * len(targets), 3), "higher_is_better": False, "dtype": kdt,
+            "data": "synthetic",
+            "config": {"workload": f"{nl} layers x 4 kv heads x 524288 positions, d_h=128, r=64, L0=262144; "
+                                   "chain 1->1.125->1.25->1.5->1.625->1.75->1.875->2->1",
+                       "switches_per_step": len(targets), "rotated_bytes_per_switch": alg},
+            "switch_ms_min": round(min(times), 3), "switch_ms_max": round(max(times), 3),
+            "table_build_ms": round(build_ms, 2), "keys_per_switch": rows,
+            "gpu_launches": args.steps * len(targets), "clocks": clocks.summary()}
+
+
 def _prefill_tiles(T, S, W, p0=0, BM=128, BN=64):
     """Key tiles the prefill kernel visits per (sequence, head): the same plan as the
     kernel (sink tiles below the window, then the window's tiles)."""
@@ -627,7 +698,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="window",
-                    choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill"])
+                    choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill", "dynamic_bf16",
+                             "dynamic_i8"])
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -681,6 +753,8 @@ def main():
                 print(json.dumps(bench_hybrid(args)))
             elif args.workload == "prefill":
                 print(json.dumps(bench_prefill(args)))
+            elif args.workload.startswith("dynamic"):
+                print(json.dumps(bench_dynamic(args, args.workload.split("_")[1])))
             else:
                 print(json.dumps(bench_rerotate(args, args.workload.split("_")[1])))
         return

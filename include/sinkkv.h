@@ -147,6 +147,67 @@ SK_API void sk_rope_table_destroy(sk_rope_table* table);
 SK_API sk_status sk_rope_table_info(const sk_rope_table* table, sk_rope_config* cfg_out,
                              const void** device_cos_sin);
 
+/* Fill a host buffer with the table for `cfg` without any device: out is float
+ * [max_positions][rotary_dim/2][2] (cos, sin pairs, the layout of the device table),
+ * 8-byte aligned, owned by the caller.  n_threads host threads (0 = automatic); every entry is
+ * computed on its own, so the bits do not depend on n_threads ([DYN] "Measured on
+ * this branch": the threaded build equals the single-thread one bit for bit).
+ * Each entry is computed in float64 as cos/sin of its block's anchor P0 w (P0 a
+ * multiple of 64) combined with cos/sin of the offset (P - P0) w by angle addition,
+ * then scaled by mu and rounded to float32.
+ * Errors: SK_ERR_ARG for a bad config, NULL or misaligned out, or n_threads outside
+ * [0, 256]. */
+SK_API sk_status sk_rope_table_fill_host(const sk_rope_config* cfg, int32_t n_threads, float* out);
+
+/* ---- Dynamic YaRN factor ------------------------------------------------------------ */
+
+/* [DYN] "What it does", the factor: 1 while total_positions <= orig_ctx (the trained
+ * context L0); beyond it (total_positions / orig_ctx) rounded up to a multiple of
+ * `step`, then capped at `cap`.  Host only.  Errors: SK_ERR_ARG for
+ * total_positions < 0, orig_ctx < 1, step <= 0, cap < 1 or NULL factor_out. */
+SK_API sk_status sk_rope_dynamic_factor(int64_t total_positions, int64_t orig_ctx, double step, double cap,
+                                        double* factor_out);
+
+/* A table whose YaRN factor follows the dialog's length, and which turns the cached
+ * keys when the factor changes ([DYN] "What it does": the factor, the cached keys,
+ * the table).  Opaque, library-owned: a live table (the one to pass to
+ * sk_kv_append / sk_rope_apply; its device pointer never changes) and a spare of
+ * the same size. */
+typedef struct sk_rope_dynamic sk_rope_dynamic;
+
+/* cfg->yarn_factor is the starting factor (<= 1: plain RoPE), cfg->yarn_orig_ctx is
+ * L0 and cfg's beta_fast / beta_slow shape every later factor; `step` > 0 is the
+ * rounding step; cap <= 0 means max_positions / L0 (the most positions the table
+ * holds, over the trained ones).  Allocates two device tables of max_positions x
+ * rotary_dim/2 float2 each and synchronises `stream`.  Errors: SK_ERR_ARG for a bad
+ * config (checked at the starting factor and at factor max(2, cap)), SK_ERR_CUDA. */
+SK_API sk_status sk_rope_dynamic_create(const sk_rope_config* cfg, double step, double cap, void* stream,
+                                        sk_rope_dynamic** out);
+
+/* The live table (stable for the object's lifetime); NULL for a NULL handle. */
+SK_API const sk_rope_table* sk_rope_dynamic_table(const sk_rope_dynamic* dyn);
+
+/* The factor the live table and the turned keys hold (1 = plain RoPE). */
+SK_API double sk_rope_dynamic_current_factor(const sk_rope_dynamic* dyn);
+
+/* Pick the factor for a dialog that now spans total_positions positions (the
+ * prompt's length at prefill, the grown length in decode).  If it differs from the
+ * current one: build the new factor's table on host threads into the spare, turn
+ * every cached key of `layers` (host array of n_layers descriptors; as
+ * sk_kv_rerotate) from the live factor to the new one, copy the spare over the live
+ * table's device buffer, and synchronise `stream`; the live table then equals, bit
+ * for bit, sk_rope_table_create at the new factor.  If the factor is unchanged
+ * nothing is launched.  *factor_out (may be NULL) gets the factor now in force,
+ * *switched_out (may be NULL) 1 if it changed.  Errors: SK_ERR_POSITION_RANGE if
+ * total_positions exceeds max_positions (nothing changes), SK_ERR_ARG, the errors of
+ * sk_kv_rerotate, SK_ERR_CUDA. */
+SK_API sk_status sk_rope_dynamic_update(sk_rope_dynamic* dyn, int64_t total_positions,
+                                        const sk_kv_layer* layers, int32_t n_layers, void* stream,
+                                        double* factor_out, int32_t* switched_out);
+
+/* Free both tables.  NULL is ignored.  No queued kernel may still read them. */
+SK_API void sk_rope_dynamic_destroy(sk_rope_dynamic* dyn);
+
 /* ---- RoPE apply ------------------------------------------------------------------ */
 
 /* Rotate x in place: x [n_tok][n_heads][head_dim] (dtype SK_BF16 or SK_F32, device),

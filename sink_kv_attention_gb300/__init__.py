@@ -7,10 +7,11 @@ fallback: if ``libsinkkv.so`` is missing or fails to load, importing the binding
 functions raises.
 
 C entry point          Python
-sk_rope_table_*        RopeTable
+sk_rope_table_*        RopeTable (+ rope_table_fill_host)
+sk_rope_dynamic_*      DynamicRope (+ dynamic_factor)
 sk_rope_apply          rope_apply
 sk_kv_append           kv_append
-sk_decode_attention    decode_attention (+ decode_workspace_bytes)
+sk_decode_attention    decode_attention (+ decode_workspace_bytes, decode_attention_noalloc)
 sk_prefill_attention   prefill_attention
 sk_kv_rerotate         kv_rerotate
 """
@@ -65,6 +66,17 @@ _SIGNATURES = [
     ("sk_rope_table_rebuild", ctypes.c_int, [ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p]),
     ("sk_rope_table_destroy", None, [ctypes.c_void_p]),
     ("sk_rope_table_info", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(RopeConfig), ctypes.POINTER(ctypes.c_void_p)]),
+    ("sk_rope_table_fill_host", ctypes.c_int, [ctypes.POINTER(RopeConfig), ctypes.c_int32, ctypes.c_void_p]),
+    ("sk_rope_dynamic_factor", ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_double, ctypes.c_double,
+                                              ctypes.POINTER(ctypes.c_double)]),
+    ("sk_rope_dynamic_create", ctypes.c_int, [ctypes.POINTER(RopeConfig), ctypes.c_double, ctypes.c_double,
+                                              ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
+    ("sk_rope_dynamic_table", ctypes.c_void_p, [ctypes.c_void_p]),
+    ("sk_rope_dynamic_current_factor", ctypes.c_double, [ctypes.c_void_p]),
+    ("sk_rope_dynamic_update", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(KVLayerStruct),
+                                              ctypes.c_int32, ctypes.c_void_p, ctypes.POINTER(ctypes.c_double),
+                                              ctypes.POINTER(ctypes.c_int32)]),
+    ("sk_rope_dynamic_destroy", None, [ctypes.c_void_p]),
     ("sk_rope_apply", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_kv_append", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32,
@@ -173,6 +185,85 @@ class RopeTable:
     def close(self):
         if getattr(self, "handle", None) is not None and self.handle.value:
             _lib().sk_rope_table_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def rope_table_fill_host(head_dim: int, rotary_dim: int, theta: float, max_positions: int, neox: bool = True,
+                         yarn_factor: float = 1.0, yarn_orig_ctx: int = 4096, beta_fast: float = 32.0,
+                         beta_slow: float = 1.0, n_threads: int = 0):
+    """The table as sk_rope_table_fill_host builds it on the host (no device):
+    numpy float32 [max_positions, rotary_dim/2, 2] of (cos, sin) pairs."""
+    import numpy as np
+    cfg = RopeConfig(head_dim, rotary_dim, 1 if neox else 0, 0, float(theta), float(yarn_factor),
+                     int(yarn_orig_ctx), float(beta_fast), float(beta_slow), int(max_positions))
+    out = np.empty((max_positions, rotary_dim // 2, 2), dtype=np.float32)
+    _check(_lib().sk_rope_table_fill_host(ctypes.byref(cfg), int(n_threads), out.ctypes.data_as(ctypes.c_void_p)),
+           "sk_rope_table_fill_host")
+    return out
+
+
+def dynamic_factor(total_positions: int, orig_ctx: int, step: float = 0.125, cap: float = 2.0) -> float:
+    """The YaRN factor for a dialog of total_positions (sk_rope_dynamic_factor)."""
+    f = ctypes.c_double()
+    _check(_lib().sk_rope_dynamic_factor(int(total_positions), int(orig_ctx), float(step), float(cap),
+                                         ctypes.byref(f)), "sk_rope_dynamic_factor")
+    return f.value
+
+
+class _TableView(RopeTable):
+    """A table owned by another library object (not freed here)."""
+
+    def __init__(self, handle: int, owner):
+        self.handle = ctypes.c_void_p(handle)
+        self._owner = owner
+        self.cfg = self.config()
+
+    def rebuild(self, yarn_factor: float, stream=None):
+        raise RuntimeError("the table of a DynamicRope changes only through DynamicRope.update")
+
+    def close(self):
+        self.handle = ctypes.c_void_p()
+
+
+class DynamicRope:
+    """A RoPE table whose YaRN factor follows the dialog's length (sk_rope_dynamic_*).
+    ``table`` is the live table to pass to kv_append / rope_apply; ``update`` picks the
+    factor for a length and, on a change, turns the given layers' cached keys."""
+
+    def __init__(self, head_dim: int, rotary_dim: int, theta: float, max_positions: int, orig_ctx: int,
+                 neox: bool = True, yarn_factor: float = 1.0, beta_fast: float = 32.0, beta_slow: float = 1.0,
+                 step: float = 0.125, cap: float = 0.0, stream=None):
+        cfg = RopeConfig(head_dim, rotary_dim, 1 if neox else 0, 0, float(theta), float(yarn_factor),
+                         int(orig_ctx), float(beta_fast), float(beta_slow), int(max_positions))
+        h = ctypes.c_void_p()
+        _check(_lib().sk_rope_dynamic_create(ctypes.byref(cfg), float(step), float(cap), _stream(stream),
+                                             ctypes.byref(h)), "sk_rope_dynamic_create")
+        self.handle = h
+        self.table = _TableView(_lib().sk_rope_dynamic_table(h), self)
+
+    @property
+    def factor(self) -> float:
+        return float(_lib().sk_rope_dynamic_current_factor(self.handle))
+
+    def update(self, total_positions: int, layers: Sequence["KVLayer"] = (), stream=None):
+        """Returns (factor now in force, whether it changed)."""
+        arr = (KVLayerStruct * max(1, len(layers)))(*[L.struct() for L in layers])
+        f = ctypes.c_double()
+        sw = ctypes.c_int32()
+        _check(_lib().sk_rope_dynamic_update(self.handle, int(total_positions), arr, len(layers), _stream(stream),
+                                             ctypes.byref(f), ctypes.byref(sw)), "sk_rope_dynamic_update")
+        return f.value, bool(sw.value)
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            self.table.close()
+            _lib().sk_rope_dynamic_destroy(self.handle)
             self.handle = ctypes.c_void_p()
 
     def __del__(self):
