@@ -356,6 +356,25 @@ class GlobalCache:
         return list(self.rows)
 
 
+def shift_recent_keys(cache: "RingCache", delta: int, omega: np.ndarray, rotary_dim: int,
+                      neox: bool = True) -> None:
+    """Turn every occupied recent (ring) key of ``cache`` by ``delta`` positions, in
+    place; sink keys and all values stay as they are.
+
+    "Attention Sink 与 Streaming KV Cache", "RoPE：absolute positions 与 local
+    rerotation 是两种实现": a cache that feeds attention local positions in [0, C-1]
+    moves each recent key from local position p to p - 1 when the window slides; a
+    key cached as R_p k becomes R_{p+delta} k by one more turn of delta positions
+    (R_a R_b = R_{a+b}, no raw key needed), with no mscale change, and the sink keys
+    keep their local positions.  Rows are (k_rot [H_kv, D], v) pairs.
+    """
+    for j in range(cache.count):
+        s = cache.S + j
+        k, v = cache.slots[s]
+        turned = rope_rotate(np.asarray(k)[None], [delta], omega, 1.0, rotary_dim, neox)[0]
+        cache.slots[s] = (turned, v)
+
+
 # ---------------------------------------------------------------------------
 # O5. The visible set of a query.
 # ---------------------------------------------------------------------------

@@ -126,3 +126,61 @@ def test_dynamic_factor_policy():
     # the switch chain of the page's growing dialog is a subset of the policy's values
     seen = {dynamic_factor(p, 262144, 0.125, 2.0) for p in range(262144, 524289, 4096)}
     assert {1.125, 1.25, 1.5, 1.625, 1.75, 1.875, 2.0} <= seen
+
+
+def _local_ring(S, W, T, seed, neox=True, r=64, D=128):
+    """A ring whose keys are rotated at their local positions: sinks at 0..S-1, the
+    recent keys at S.. in chronological order (the local-position scheme of page 4),
+    plus the raw keys by absolute position."""
+    from oracle.sinkkv_oracle import RingCache
+    rng = np.random.default_rng(seed)
+    raw = rng.standard_normal((T, 2, D))
+    v = rng.standard_normal((T, 2, D))
+    ring = RingCache(S, W)
+    ring.append([(raw[t], v[t]) for t in range(T)])
+    om = rope_inv_freq(r, 1e4)
+    local = {}
+    for i, s in enumerate(ring.chronological_slots()):
+        P = ring.slot_pos[s]
+        local[s] = i
+        k, vv = ring.slots[s]
+        ring.slots[s] = (rope_rotate(k[None], [i], om, 1.0, r, neox)[0], vv)
+    return ring, raw, v, om, local
+
+
+@pytest.mark.parametrize("neox", [True, False])
+def test_shift_recent_equals_recompute_at_local_minus_one(neox):
+    """Page 4's C=6, S=2 cache after 10 tokens: recent keys (absolute 6..9) sit at
+    local positions 2..5; shifting them by -1 equals rotating their raw keys at local
+    1..4 (1e-12); sink keys and every value stay bit for bit."""
+    from oracle.sinkkv_oracle import shift_recent_keys
+    ring, raw, v, om, local = _local_ring(2, 4, 10, 7, neox)
+    assert [ring.slot_pos[s] for s in ring.chronological_slots()] == [0, 1, 6, 7, 8, 9]
+    before = {s: (ring.slots[s][0].copy(), ring.slots[s][1]) for s in range(ring.C)}
+    shift_recent_keys(ring, -1, om, 64, neox)
+    for s in range(ring.C):
+        k, vv = ring.slots[s]
+        assert vv is before[s][1]
+        P = ring.slot_pos[s]
+        if s < ring.S:
+            np.testing.assert_array_equal(k, before[s][0])
+        else:
+            want = rope_rotate(raw[P][None], [local[s] - 1], om, 1.0, 64, neox)[0]
+            np.testing.assert_allclose(k, want, atol=1e-12)
+
+
+def test_shift_recent_there_and_back_and_partial_ring():
+    """+3 then -3 is the identity; a ring that has not wrapped turns only its
+    occupied slots (count < W)."""
+    from oracle.sinkkv_oracle import shift_recent_keys
+    ring, raw, v, om, local = _local_ring(3, 8, 7, 8)
+    assert ring.count == 4
+    before = [None if x is None else x[0].copy() for x in ring.slots]
+    shift_recent_keys(ring, 3, om, 64)
+    for s in range(ring.S, ring.S + ring.count):
+        assert np.abs(ring.slots[s][0] - before[s]).max() > 1e-3
+    for s in range(ring.S + ring.count, ring.C):
+        assert ring.slots[s] is None
+    shift_recent_keys(ring, -3, om, 64)
+    for s in range(ring.S + ring.count):
+        np.testing.assert_allclose(ring.slots[s][0], before[s], atol=1e-12)
