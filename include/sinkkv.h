@@ -343,6 +343,24 @@ SK_API sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, cons
 SK_API sk_status sk_kv_rerotate(const sk_kv_layer* layers, int32_t n_layers, const sk_rope_table* from,
                          const sk_rope_table* to, void* stream);
 
+/* ---- Local-position caches: turn the recent keys on a window slide ---------------- */
+
+/* Turn every occupied recent (ring) key of the ring layers `layers` (host array of
+ * n_layers descriptors, device buffers) by `delta` positions, in place: each rotary
+ * pair is multiplied by R(delta w_j) of `table`'s frequencies, with no mscale change;
+ * sink slots [0, sinks), empty ring slots, the tail dims and all values are left
+ * untouched.  This is the rerotation a cache needs when it feeds attention local
+ * positions in [0, C-1] and its window slides: recent keys move from local p to
+ * p - 1, i.e. delta = -(keys evicted), while the sink keys keep their local
+ * positions ([SINK] "RoPE：absolute positions 与 local rerotation 是两种实现",
+ * R_a R_b = R_{a+b}: no raw key needed).  A cache holding absolute positions (the
+ * rest of this library) never needs it.  int8 rows are requantised as in
+ * sk_kv_rerotate.  Errors: SK_ERR_ARG for a global layer or bad descriptors,
+ * SK_ERR_POSITION_RANGE if |delta| >= table max_positions; delta = 0 launches
+ * nothing.  k_dtype SK_BF16 or SK_I8, n_layers <= 128. */
+SK_API sk_status sk_kv_shift_recent(const sk_kv_layer* layers, int32_t n_layers, const sk_rope_table* table,
+                                    int32_t delta, void* stream);
+
 /* ---- Misc ------------------------------------------------------------------------ */
 
 /* A static, human-readable name for a status code. */

@@ -14,6 +14,7 @@ sk_kv_append           kv_append
 sk_decode_attention    decode_attention (+ decode_workspace_bytes, decode_attention_noalloc)
 sk_prefill_attention   prefill_attention
 sk_kv_rerotate         kv_rerotate
+sk_kv_shift_recent     kv_shift_recent
 """
 from __future__ import annotations
 
@@ -95,6 +96,8 @@ _SIGNATURES = [
                                             ctypes.c_void_p]),
     ("sk_kv_rerotate", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p]),
+    ("sk_kv_shift_recent", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32, ctypes.c_void_p,
+                                          ctypes.c_int32, ctypes.c_void_p]),
     ("sk_status_str", ctypes.c_char_p, [ctypes.c_int]),
     ("sk_version", ctypes.c_int32, []),
 ]
@@ -456,6 +459,14 @@ def kv_rerotate(layers: Sequence[KVLayer], table_from: RopeTable, table_to: Rope
     arr = (KVLayerStruct * len(layers))(*[l.struct() for l in layers])
     _check(_lib().sk_kv_rerotate(arr, len(layers), table_from.handle, table_to.handle, _stream(stream)),
            "sk_kv_rerotate")
+
+
+def kv_shift_recent(layers: Sequence[KVLayer], table: RopeTable, delta: int, stream=None):
+    """Turn the recent keys of ring layers by `delta` positions in place; sinks and
+    values stay (sk_kv_shift_recent)."""
+    arr = (KVLayerStruct * max(1, len(layers)))(*[L.struct() for L in layers])
+    _check(_lib().sk_kv_shift_recent(arr, len(layers), table.handle, int(delta), _stream(stream)),
+           "sk_kv_shift_recent")
 
 
 def version() -> int:

@@ -9,8 +9,17 @@
 //   (cB cA + sB sA) / mu_A^2 = (mu_B / mu_A) cos(b - a),
 //   (sB cA - cB sA) / mu_A^2 = (mu_B / mu_A) sin(b - a).
 //
-// Layout of the work: one block covers a range of slots; each thread group owns one
-// slot and walks every (layer, sequence, kv head) row at that slot, recomputing the
+// The same kernels turn the recent keys of ring layers by a uniform number of positions
+// delta ("Attention Sink 与 Streaming KV Cache", "RoPE：absolute positions 与 local
+// rerotation 是两种实现": a cache fed local positions moves its recent keys from p to
+// p - 1 when the window slides; sink keys keep their positions).  The rotation is then
+// the same for every row, R(delta w) with no mscale change, taken from one table: rows
+// A = max(0, -delta) and B = max(0, delta) give exactly (cos, sin)(delta w) in the
+// formulas above with mu_A = mu_B = mu.
+//
+// Layout of the work: one block covers a range of slots (and, when the slots alone
+// give too few blocks, a stride of the sequences: blockIdx.y); each thread group owns
+// one slot and walks every (layer, sequence, kv head) row at that slot, recomputing the
 // delta only when the slot's position changes (never, for global layers).  The bf16
 // path reads and writes only the rotary bytes of each row; the int8 path moves the
 // whole row of codes plus its scale.
@@ -44,6 +53,8 @@ struct RerotParams {
     const float2* tB;
     int64_t maxA, maxB;
     float inv_muA2;
+    int shift;            // 1: uniform turn of the recent keys (sinks skipped)
+    int64_t rowA, rowB;   // shift mode: the table rows whose entries give the turn
 };
 
 // Position held by `slot` of (layer, sequence b), or -1 when the slot is empty.
@@ -60,13 +71,24 @@ __device__ __forceinline__ int64_t slot_position(const RerotLayer& L, int b, int
     return pos - 1 - back;
 }
 
-// Delta rotation (dc, ds) of NP consecutive pairs starting at j0, at position P.
+// The slot's position for a factor change, or -1 to skip the slot.  In shift mode
+// the sink slots are skipped and every other occupied slot gets key 0 (the turn does
+// not depend on the position).
+__device__ __forceinline__ int64_t rerot_key(const RerotParams& p, const RerotLayer& L, int b, int64_t slot) {
+    const int64_t P = slot_position(L, b, slot);
+    if (!p.shift) return P;
+    return (P < 0 || slot < L.S) ? -1 : 0;
+}
+
+// Delta rotation (dc, ds) of NP consecutive pairs starting at j0, at position P (a
+// factor change) or of the uniform turn (shift mode).
 template <int NP>
 __device__ __forceinline__ void delta_pairs(const RerotParams& p, int64_t P, int j0, float* dc,
                                             float* ds) {
     const int half = p.r / 2;
-    const float4* a4 = reinterpret_cast<const float4*>(p.tA + P * half + j0);
-    const float4* b4 = reinterpret_cast<const float4*>(p.tB + P * half + j0);
+    const int64_t PA = p.shift ? p.rowA : P, PB = p.shift ? p.rowB : P;
+    const float4* a4 = reinterpret_cast<const float4*>(p.tA + PA * half + j0);
+    const float4* b4 = reinterpret_cast<const float4*>(p.tB + PB * half + j0);
 #pragma unroll
     for (int i = 0; i < NP / 2; ++i) {
         const float4 a = __ldg(a4 + i), b = __ldg(b4 + i);
@@ -93,8 +115,8 @@ __global__ void __launch_bounds__(kThreads) rerotate_bf16_kernel(RerotParams p) 
     int64_t lastP = -1;
     for (int l = 0; l < p.n_layers; ++l) {
         const RerotLayer& L = p.layers[l];
-        for (int b = 0; b < p.B; ++b) {
-            const int64_t P = slot_position(L, b, slot);
+        for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
+            const int64_t P = rerot_key(p, L, b, slot);
             if (P < 0) continue;
             if (P >= p.maxA || P >= p.maxB) {
                 set_error(L.err, SK_DEVERR_POSITION_RANGE);
@@ -213,10 +235,10 @@ __global__ void __launch_bounds__(kThreads, 3) rerotate_i8_kernel(RerotParams p)
     int64_t lastP = -1;
     for (int l = 0; l < p.n_layers; ++l) {
         const RerotLayer& L = p.layers[l];
-        for (int b = 0; b < p.B; ++b) {
+        for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
             // Lanes of one warp hold different slots, so validity differs between row
             // groups: every lane runs the loop and the shuffles, only valid rows touch memory.
-            const int64_t P = slot_position(L, b, slot);
+            const int64_t P = rerot_key(p, L, b, slot);
             bool valid = P >= 0;
             if (valid && (P >= p.maxA || P >= p.maxB)) {
                 set_error(L.err, SK_DEVERR_POSITION_RANGE);
@@ -322,33 +344,22 @@ __global__ void __launch_bounds__(kThreads, 3) rerotate_i8_kernel(RerotParams p)
 
 using namespace sk;
 
-extern "C" sk_status sk_kv_rerotate(const sk_kv_layer* layers, int32_t n_layers,
-                                    const sk_rope_table* from, const sk_rope_table* to,
-                                    void* stream) {
-    SK_RET_IF(layers == nullptr || from == nullptr || to == nullptr, SK_ERR_ARG);
-    SK_RET_IF(n_layers < 1 || n_layers > kMaxLayers, SK_ERR_ARG);
-    const sk_rope_config& ca = table_config(from);
-    const sk_rope_config& cb = table_config(to);
-    SK_RET_IF(ca.head_dim != cb.head_dim || ca.rotary_dim != cb.rotary_dim || ca.neox != cb.neox ||
-                  ca.theta != cb.theta,
-              SK_ERR_ARG);
+namespace {
+
+// Checks the layers, fills p.layers / n_layers / B / Hkv / r and launches the kernel
+// for the table config `c` (both tables share d_h, r, pairing and theta).
+sk_status launch_rerotation(const sk_kv_layer* layers, int32_t n_layers, const sk_rope_config& c, bool rings_only,
+                            RerotParams& p, cudaStream_t st) {
+    SK_RET_IF(layers == nullptr || n_layers < 1 || n_layers > kMaxLayers, SK_ERR_ARG);
     const sk_kv_layer& L0 = layers[0];
     const int D = L0.head_dim;
-    SK_RET_IF(D != ca.head_dim, SK_ERR_ARG);
+    SK_RET_IF(D != c.head_dim, SK_ERR_ARG);
     SK_RET_IF(L0.k_dtype != SK_BF16 && L0.k_dtype != SK_I8, SK_ERR_UNSUPPORTED);
-    SK_RET_IF(L0.k_dtype == SK_I8 && ca.rotary_dim % 32 != 0, SK_ERR_UNSUPPORTED);
-    // the bf16 path needs a whole number of thread groups per block
-    RerotParams p{};
+    SK_RET_IF(L0.k_dtype == SK_I8 && c.rotary_dim % 32 != 0, SK_ERR_UNSUPPORTED);
     p.n_layers = n_layers;
     p.B = L0.batch;
     p.Hkv = L0.n_kv_heads;
-    p.r = ca.rotary_dim;
-    p.tA = table_device(from);
-    p.tB = table_device(to);
-    p.maxA = ca.max_positions;
-    p.maxB = cb.max_positions;
-    const double mu_a = ca.yarn_factor <= 1.0 ? 1.0 : 0.1 * std::log(ca.yarn_factor) + 1.0;
-    p.inv_muA2 = float(1.0 / (mu_a * mu_a));
+    p.r = c.rotary_dim;
     int64_t max_cap = 0;
     for (int l = 0; l < n_layers; ++l) {
         const sk_kv_layer& L = layers[l];
@@ -363,34 +374,83 @@ extern "C" sk_status sk_kv_rerotate(const sk_kv_layer* layers, int32_t n_layers,
                           L.capacity != int64_t(L.sinks) + L.window,
                       SK_ERR_ARG);
         } else {
-            SK_RET_IF(L.kind != SK_LAYER_GLOBAL || L.capacity < 1, SK_ERR_ARG);
+            SK_RET_IF(rings_only || L.kind != SK_LAYER_GLOBAL || L.capacity < 1, SK_ERR_ARG);
         }
         p.layers[l] = RerotLayer{L.k, L.k_scale, L.head, L.count, L.pos, L.err,
                                  L.capacity, L.kind, L.sinks, L.window};
         max_cap = std::max(max_cap, L.capacity);
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool neox = ca.neox != 0;
-    int64_t blocks;
+    const bool neox = c.neox != 0;
+    const int spb = L0.k_dtype == SK_BF16 ? kThreads / (p.r / (neox ? 16 : 8)) : kThreads / (D / 32);
+    const int64_t bx = (max_cap + spb - 1) / spb;
+    // sequences split over blockIdx.y until there are about 16 blocks per SM
+    const int64_t want = 16 * int64_t(device_sm_count());
+    const int64_t by0 = std::min<int64_t>(p.B, std::max<int64_t>(1, (want + bx - 1) / bx));
+    const int64_t per_block = (p.B + by0 - 1) / by0;  // sequences per block, the same for all
+    const int by = int((p.B + per_block - 1) / per_block);
+    const dim3 grid{unsigned(bx), unsigned(by), 1u};
     if (L0.k_dtype == SK_BF16) {
-        const int tpr = p.r / (neox ? 16 : 8);
-        const int spb = kThreads / tpr;
-        blocks = (max_cap + spb - 1) / spb;
         if (D == 64)
-            neox ? rerotate_bf16_kernel<64, true><<<unsigned(blocks), kThreads, 0, st>>>(p)
-                 : rerotate_bf16_kernel<64, false><<<unsigned(blocks), kThreads, 0, st>>>(p);
+            neox ? rerotate_bf16_kernel<64, true><<<grid, kThreads, 0, st>>>(p)
+                 : rerotate_bf16_kernel<64, false><<<grid, kThreads, 0, st>>>(p);
         else
-            neox ? rerotate_bf16_kernel<128, true><<<unsigned(blocks), kThreads, 0, st>>>(p)
-                 : rerotate_bf16_kernel<128, false><<<unsigned(blocks), kThreads, 0, st>>>(p);
+            neox ? rerotate_bf16_kernel<128, true><<<grid, kThreads, 0, st>>>(p)
+                 : rerotate_bf16_kernel<128, false><<<grid, kThreads, 0, st>>>(p);
     } else {
-        const int spb = kThreads / (D / 32);
-        blocks = (max_cap + spb - 1) / spb;
         if (D == 64)
-            neox ? rerotate_i8_kernel<64, true><<<unsigned(blocks), kThreads, 0, st>>>(p)
-                 : rerotate_i8_kernel<64, false><<<unsigned(blocks), kThreads, 0, st>>>(p);
+            neox ? rerotate_i8_kernel<64, true><<<grid, kThreads, 0, st>>>(p)
+                 : rerotate_i8_kernel<64, false><<<grid, kThreads, 0, st>>>(p);
         else
-            neox ? rerotate_i8_kernel<128, true><<<unsigned(blocks), kThreads, 0, st>>>(p)
-                 : rerotate_i8_kernel<128, false><<<unsigned(blocks), kThreads, 0, st>>>(p);
+            neox ? rerotate_i8_kernel<128, true><<<grid, kThreads, 0, st>>>(p)
+                 : rerotate_i8_kernel<128, false><<<grid, kThreads, 0, st>>>(p);
     }
     return cudaGetLastError() == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}
+
+double mscale_of(const sk_rope_config& c) {
+    return c.yarn_factor <= 1.0 ? 1.0 : 0.1 * std::log(c.yarn_factor) + 1.0;
+}
+
+}  // namespace
+
+extern "C" sk_status sk_kv_rerotate(const sk_kv_layer* layers, int32_t n_layers,
+                                    const sk_rope_table* from, const sk_rope_table* to,
+                                    void* stream) {
+    SK_RET_IF(layers == nullptr || from == nullptr || to == nullptr, SK_ERR_ARG);
+    const sk_rope_config& ca = table_config(from);
+    const sk_rope_config& cb = table_config(to);
+    SK_RET_IF(ca.head_dim != cb.head_dim || ca.rotary_dim != cb.rotary_dim || ca.neox != cb.neox ||
+                  ca.theta != cb.theta,
+              SK_ERR_ARG);
+    RerotParams p{};
+    p.tA = table_device(from);
+    p.tB = table_device(to);
+    p.maxA = ca.max_positions;
+    p.maxB = cb.max_positions;
+    const double mu_a = mscale_of(ca);
+    p.inv_muA2 = float(1.0 / (mu_a * mu_a));
+    return launch_rerotation(layers, n_layers, ca, false, p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" sk_status sk_kv_shift_recent(const sk_kv_layer* layers, int32_t n_layers, const sk_rope_table* table,
+                                        int32_t delta, void* stream) {
+    SK_RET_IF(layers == nullptr || table == nullptr, SK_ERR_ARG);
+    const sk_rope_config& c = table_config(table);
+    const int64_t mag = delta < 0 ? -int64_t(delta) : int64_t(delta);
+    SK_RET_IF(mag >= c.max_positions, SK_ERR_POSITION_RANGE);
+    RerotParams p{};
+    p.tA = p.tB = table_device(table);
+    p.maxA = p.maxB = c.max_positions;
+    const double mu = mscale_of(c);
+    p.inv_muA2 = float(1.0 / (mu * mu));
+    p.shift = 1;
+    p.rowA = delta < 0 ? mag : 0;
+    p.rowB = delta > 0 ? mag : 0;
+    if (delta == 0) {  // nothing to turn; the arguments are still checked
+        p.n_layers = 0;
+        SK_RET_IF(n_layers < 1 || n_layers > kMaxLayers, SK_ERR_ARG);
+        for (int l = 0; l < n_layers; ++l) SK_RET_IF(layers[l].kind != SK_LAYER_RING, SK_ERR_ARG);
+        return SK_OK;
+    }
+    return launch_rerotation(layers, n_layers, c, true, p, static_cast<cudaStream_t>(stream));
 }
