@@ -505,6 +505,89 @@ def prefill_attention(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray, p0: i
 
 
 # ---------------------------------------------------------------------------
+# O6b. Paged caches: block tables with static sink blocks.
+# ---------------------------------------------------------------------------
+
+def blocks_for_tokens(n_tokens: int, block_size: int) -> int:
+    """Blocks holding n tokens: cdiv(n, block_size) ("RoPE, scaling, sliding window,
+    attention sinks", the sliding-window section: full attention at 128k and 16-token
+    blocks needs cdiv(131072, 16) = 8192 blocks)."""
+    return -(-n_tokens // block_size)
+
+
+def window_blocks(window: int, block_size: int, extra_retained: int = 0, in_flight: int = 0,
+                  max_len: Optional[int] = None) -> int:
+    """Blocks a sliding-window layer may hold per request: the window's tokens (W - 1
+    behind the query, plus retained and in-flight tokens, at most max_len) in whole
+    blocks, plus one because the window need not start on a block boundary (same
+    section: 257 blocks for W = 4096 and 16-token blocks)."""
+    n = window - 1 + extra_retained + in_flight
+    if max_len is not None:
+        n = min(n, max_len)
+    return blocks_for_tokens(n, block_size) + 1
+
+
+def first_window_token(n_computed: int, window: int, extra_retained: int = 0) -> int:
+    """The oldest token a sliding-window query still needs; every block wholly before
+    it may be freed (replaced by the null block) (same section, the window edge)."""
+    return max(0, n_computed - window + 1 - extra_retained)
+
+
+def prepend_static_sinks(block_table: np.ndarray, seq_lens: Sequence[int], sink_blocks: Sequence[int],
+                         sink_len: int):
+    """The attention metadata with static sink blocks ("RoPE, scaling, sliding window,
+    attention sinks", "Hybrid models break the uniform-spec assumption", the static
+    sink excerpt): the sink blocks go in front of every request's block table and each
+    nonzero sequence length grows by sink_len; a length of zero stays zero."""
+    n_sink = len(sink_blocks)
+    B, nb = block_table.shape
+    table = np.zeros((B, n_sink + nb), dtype=np.int64)
+    table[:, :n_sink] = np.asarray(sink_blocks)[None, :]
+    table[:, n_sink:] = block_table
+    lens = np.asarray(seq_lens, dtype=np.int64) + sink_len
+    lens[lens == sink_len] = 0
+    return table, lens
+
+
+def paged_logical_rows(k_pool: np.ndarray, v_pool: np.ndarray, table_row: Sequence[int], length: int,
+                       block_size: int):
+    """The first ``length`` logical (k, v) rows of one request: logical key i lives in
+    physical block table_row[i // block_size] at offset i % block_size ("vLLM, from
+    the inside out", PagedAttention: blocks, logical blocks, block table).  Pools are
+    [n_blocks][H_kv][block_size][D]; returns k and v as [length][H_kv][D]."""
+    ks, vs = [], []
+    for i in range(length):
+        blk = int(table_row[i // block_size])
+        ks.append(k_pool[blk, :, i % block_size, :])
+        vs.append(v_pool[blk, :, i % block_size, :])
+    return np.stack(ks), np.stack(vs)
+
+
+def paged_decode_attention(q_rot: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray,
+                           table_row: Sequence[int], length: int, block_size: int, sinks: int,
+                           window: Optional[int],
+                           sink_logits: Optional[Sequence[float]] = None) -> np.ndarray:
+    """Decode attention of a request's newest query (logical position length - 1) over
+    its paged keys: the same visible set as a contiguous cache with capacity
+    sinks + window ("Attention Sink 与 Streaming KV Cache", V(P)), every key of a
+    full-attention layer (window None) -- only the visible blocks are ever read, so
+    freed blocks may hold anything."""
+    if length == 0:
+        return np.zeros_like(np.asarray(q_rot, dtype=np.float64))
+    P = length - 1
+    if window is None:
+        vis = list(range(length))
+    else:
+        vis = visible_positions(P, sinks + window, sinks)
+    ks, vs = [], []
+    for i in vis:
+        blk = int(table_row[i // block_size])
+        ks.append(k_pool[blk, :, i % block_size, :])
+        vs.append(v_pool[blk, :, i % block_size, :])
+    return attend(q_rot, np.stack(ks), np.stack(vs), sink_logits)
+
+
+# ---------------------------------------------------------------------------
 # O7. Dynamic factor policy.
 # ---------------------------------------------------------------------------
 
