@@ -57,6 +57,7 @@ typedef enum { SK_LAYER_RING = 0, SK_LAYER_GLOBAL = 1 } sk_layer_kind;
 #define SK_DEVERR_POSITION_RANGE 0x1u  /* a position >= max_positions was skipped   */
 #define SK_DEVERR_CAPACITY       0x2u  /* a global-layer append past capacity was skipped */
 #define SK_DEVERR_TIMEOUT        0x4u  /* a bounded in-kernel wait gave up (never expected) */
+#define SK_DEVERR_BLOCK_TABLE    0x8u  /* a paged block id outside [0, n_blocks) was met  */
 
 /*
  * Rotary configuration.  [RoPE] "Let d_h be the head dimension, r <= d_h the rotary
@@ -123,6 +124,51 @@ typedef struct {
     int64_t* pos;
     uint32_t* err;
 } sk_kv_layer;
+
+/*
+ * One layer's paged KV cache for a batch of requests ("vLLM, from the inside out",
+ * PagedAttention: a shared pool of fixed-size blocks and a per-request block table
+ * from logical block to physical block; [RoPE] "Hybrid models break the uniform-spec
+ * assumption": static sink blocks put in front of every block table).  All pointers
+ * are device pointers owned by the caller; the caller allocates and frees blocks.
+ *   k_pool, v_pool: [n_blocks][n_kv_heads][block_size][head_dim] of k_dtype / v_dtype
+ *   block_table: int32 [batch][max_blocks]; request block j holds the request's tokens
+ *     [j*block_size, (j+1)*block_size).  Entries of blocks that hold no visible key may
+ *     be anything (freed blocks, e.g. -1): they are never read.
+ *   sink_block_ids: int32 [n_sink_blocks] static sink blocks, the same for every
+ *     request, or NULL when n_sink_blocks = 0.
+ *   seq_lens: int64 [batch], the request's own tokens so far (static sink tokens not
+ *     counted) = the RoPE position of its next token.
+ *   err: uint32 device error word, may be NULL.
+ * Attention of a request sees the logical key sequence "static sink tokens
+ * (n_sink_blocks * block_size of them), then the request's tokens", of length
+ * L = sink_len + seq_len (0 when seq_len = 0), and within it the first `sinks` keys
+ * and the last `window` keys (every key when window <= 0): the visible set V(L - 1)
+ * of a cache with capacity sinks + window ([SINK] "可见集合与容量定义").  With static
+ * sink blocks, sinks = their token count gives them the role of the pinned sinks;
+ * without, sinks = S keeps the request's own first S tokens (StreamingLLM on paged
+ * memory).
+ * k_dtype, v_dtype: SK_BF16 or SK_F32 (the same for both).  block_size in [4, 1024].
+ */
+typedef struct {
+    int32_t k_dtype;
+    int32_t v_dtype;
+    int32_t batch;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t max_blocks;
+    int32_t n_sink_blocks;
+    int32_t sinks;
+    int32_t window;
+    int64_t n_blocks;
+    void* k_pool;
+    void* v_pool;
+    const int32_t* block_table;
+    const int32_t* sink_block_ids;
+    int64_t* seq_lens;
+    uint32_t* err;
+} sk_paged_layer;
 
 /* ---- RoPE table (host float64 build, device float32 copy) ---------------------- */
 
@@ -342,6 +388,33 @@ SK_API sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, cons
  * k_dtype SK_BF16 or SK_I8.  n_layers <= 128. */
 SK_API sk_status sk_kv_rerotate(const sk_kv_layer* layers, int32_t n_layers, const sk_rope_table* from,
                          const sk_rope_table* to, void* stream);
+
+/* ---- Paged caches ------------------------------------------------------------------ */
+
+/* sk_kv_append for a paged layer: rotate q (optional, in place) and k (in place) at
+ * positions seq_lens[b] + t and write k, v into the pool slots the block table gives
+ * (block block_table[b][P / block_size], row P % block_size of each kv head);
+ * seq_lens[b] += T.  The blocks for the new tokens must be in the table.  A request
+ * whose seq_lens[b] + T exceeds max_blocks * block_size, or whose positions pass the
+ * table, is skipped with SK_DEVERR_CAPACITY / SK_DEVERR_POSITION_RANGE; a token whose
+ * block id is outside [0, n_blocks) is not stored and sets SK_DEVERR_BLOCK_TABLE.
+ * Layouts and dtypes as sk_kv_append. */
+SK_API sk_status sk_paged_append(const sk_rope_table* table, const sk_paged_layer* layer, void* q,
+                                 int32_t n_q_heads, const void* k, const void* v, int32_t io_dtype, int32_t T,
+                                 void* stream);
+
+/* Workspace bytes sk_paged_decode_attention needs. */
+SK_API size_t sk_paged_decode_workspace_bytes(const sk_paged_layer* layer, int32_t n_q_heads);
+
+/* sk_decode_attention over a paged layer: one query per request (after its own
+ * append) against the visible keys of its logical key sequence (see sk_paged_layer),
+ * gathered block by block.  Only blocks holding visible keys are read; a visible key
+ * whose block id is outside [0, n_blocks) reads block 0 instead and sets
+ * SK_DEVERR_BLOCK_TABLE.  A request with seq_lens[b] = 0 gets zeros.  Arguments,
+ * dtypes, learned sink logits and workspace rules as sk_decode_attention. */
+SK_API sk_status sk_paged_decode_attention(const sk_paged_layer* layer, const void* q_rot, int32_t n_q_heads,
+                                           int32_t io_dtype, const float* sink_logits, void* out,
+                                           void* workspace, size_t ws_bytes, void* stream);
 
 /* ---- Local-position caches: turn the recent keys on a window slide ---------------- */
 

@@ -15,6 +15,7 @@ sk_decode_attention    decode_attention (+ decode_workspace_bytes, decode_attent
 sk_prefill_attention   prefill_attention
 sk_kv_rerotate         kv_rerotate
 sk_kv_shift_recent     kv_shift_recent
+sk_paged_*             PagedLayer, paged_append, paged_decode_attention
 """
 from __future__ import annotations
 
@@ -31,7 +32,7 @@ LIB_PATH = os.path.join(_HERE, "libsinkkv.so")
 SK_OK, SK_ERR_ARG, SK_ERR_CAPACITY, SK_ERR_POSITION_RANGE, SK_ERR_UNSUPPORTED, SK_ERR_CUDA = range(6)
 SK_BF16, SK_F32, SK_I8 = 0, 1, 2
 SK_LAYER_RING, SK_LAYER_GLOBAL = 0, 1
-SK_DEVERR_POSITION_RANGE, SK_DEVERR_CAPACITY, SK_DEVERR_TIMEOUT = 1, 2, 4
+SK_DEVERR_POSITION_RANGE, SK_DEVERR_CAPACITY, SK_DEVERR_TIMEOUT, SK_DEVERR_BLOCK_TABLE = 1, 2, 4, 8
 
 
 class SinkKVError(RuntimeError):
@@ -57,6 +58,15 @@ class KVLayerStruct(ctypes.Structure):
                 ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("head", ctypes.c_void_p), ("count", ctypes.c_void_p), ("pos", ctypes.c_void_p),
                 ("err", ctypes.c_void_p)]
+
+
+class PagedLayerStruct(ctypes.Structure):
+    _fields_ = [("k_dtype", ctypes.c_int32), ("v_dtype", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("max_blocks", ctypes.c_int32), ("n_sink_blocks", ctypes.c_int32), ("sinks", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("n_blocks", ctypes.c_int64), ("k_pool", ctypes.c_void_p),
+                ("v_pool", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("sink_block_ids", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("err", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -96,6 +106,13 @@ _SIGNATURES = [
                                             ctypes.c_void_p]),
     ("sk_kv_rerotate", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p]),
+    ("sk_paged_append", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(PagedLayerStruct), ctypes.c_void_p,
+                                       ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_void_p]),
+    ("sk_paged_decode_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(PagedLayerStruct), ctypes.c_int32]),
+    ("sk_paged_decode_attention", ctypes.c_int, [ctypes.POINTER(PagedLayerStruct), ctypes.c_void_p, ctypes.c_int32,
+                                                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_size_t, ctypes.c_void_p]),
     ("sk_kv_shift_recent", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32, ctypes.c_void_p,
                                           ctypes.c_int32, ctypes.c_void_p]),
     ("sk_status_str", ctypes.c_char_p, [ctypes.c_int]),
@@ -459,6 +476,92 @@ def kv_rerotate(layers: Sequence[KVLayer], table_from: RopeTable, table_to: Rope
     arr = (KVLayerStruct * len(layers))(*[l.struct() for l in layers])
     _check(_lib().sk_kv_rerotate(arr, len(layers), table_from.handle, table_to.handle, _stream(stream)),
            "sk_kv_rerotate")
+
+
+@dataclass
+class PagedLayer:
+    """A paged layer's caller-owned device buffers (sk_paged_layer): pools
+    [n_blocks, H_kv, block_size, D], block_table int32 [B, max_blocks] (-1 = no block),
+    sink_block_ids int32 [n_sink_blocks], seq_lens int64 [B]."""
+    k_pool: torch.Tensor
+    v_pool: torch.Tensor
+    block_table: torch.Tensor
+    sink_block_ids: Optional[torch.Tensor]
+    seq_lens: torch.Tensor
+    err: torch.Tensor
+    sinks: int
+    window: int
+
+    @staticmethod
+    def allocate(batch: int, n_kv_heads: int, head_dim: int, *, block_size: int, n_blocks: int, max_blocks: int,
+                 sinks: int = 0, window: int = 0, n_sink_blocks: int = 0, dtype=torch.bfloat16,
+                 device="cuda") -> "PagedLayer":
+        z = dict(dtype=dtype, device=device)
+        return PagedLayer(
+            k_pool=torch.zeros(n_blocks, n_kv_heads, block_size, head_dim, **z),
+            v_pool=torch.zeros(n_blocks, n_kv_heads, block_size, head_dim, **z),
+            block_table=torch.full((batch, max_blocks), -1, dtype=torch.int32, device=device),
+            sink_block_ids=(torch.arange(n_sink_blocks, dtype=torch.int32, device=device)
+                            if n_sink_blocks > 0 else None),
+            seq_lens=torch.zeros(batch, dtype=torch.int64, device=device),
+            err=torch.zeros(1, dtype=torch.int32, device=device), sinks=sinks, window=window)
+
+    @property
+    def batch(self):
+        return self.block_table.shape[0]
+
+    @property
+    def n_kv_heads(self):
+        return self.k_pool.shape[1]
+
+    @property
+    def block_size(self):
+        return self.k_pool.shape[2]
+
+    def struct(self) -> PagedLayerStruct:
+        n_sink = 0 if self.sink_block_ids is None else self.sink_block_ids.numel()
+        return PagedLayerStruct(_sk_dtype(self.k_pool.dtype), _sk_dtype(self.v_pool.dtype), self.batch,
+                                self.n_kv_heads, self.k_pool.shape[3], self.block_size, self.block_table.shape[1],
+                                n_sink, self.sinks, self.window, self.k_pool.shape[0], self.k_pool.data_ptr(),
+                                self.v_pool.data_ptr(), self.block_table.data_ptr(),
+                                None if self.sink_block_ids is None else self.sink_block_ids.data_ptr(),
+                                self.seq_lens.data_ptr(), self.err.data_ptr())
+
+    def error_bits(self) -> int:
+        return int(self.err.item())
+
+
+def paged_append(table: RopeTable, layer: PagedLayer, q: Optional[torch.Tensor], k: torch.Tensor, v: torch.Tensor,
+                 stream=None):
+    """RoPE on q (optional) and k in place, then k, v into the pool slots of the block
+    table (sk_paged_append); q [B, T, Hq, D], k/v [B, T, Hkv, D]."""
+    _need_contig(k, v)
+    if q is not None:
+        _need_contig(q)
+    s = layer.struct()
+    _check(_lib().sk_paged_append(table.handle, ctypes.byref(s), _ptr(q), 0 if q is None else q.shape[2], _ptr(k),
+                                  _ptr(v), _sk_dtype(k.dtype), k.shape[1], _stream(stream)), "sk_paged_append")
+
+
+def paged_decode_attention(layer: PagedLayer, q_rot: torch.Tensor, out: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, stream=None,
+                           sink_logits: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode attention of q_rot [B, Hq, D] over a paged layer (sk_paged_decode_attention)."""
+    _need_contig(q_rot)
+    Hq = q_rot.shape[1]
+    if out is None:
+        out = torch.empty_like(q_rot)
+    s = layer.struct()
+    need = int(_lib().sk_paged_decode_workspace_bytes(ctypes.byref(s), Hq))
+    if need == 0:
+        raise SinkKVError(SK_ERR_UNSUPPORTED, "sk_paged_decode_workspace_bytes")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_rot.device)
+    _check(_lib().sk_paged_decode_attention(ctypes.byref(s), _ptr(q_rot), Hq, _sk_dtype(q_rot.dtype),
+                                            _sink_logits(sink_logits, Hq), _ptr(out), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _stream(stream)),
+           "sk_paged_decode_attention")
+    return out
 
 
 def kv_shift_recent(layers: Sequence[KVLayer], table: RopeTable, delta: int, stream=None):

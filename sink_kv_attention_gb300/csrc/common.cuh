@@ -245,3 +245,22 @@ int device_sm_count();                                   // api.cu
 const float2* table_device(const sk_rope_table* t);      // rope_table.cu
 const sk_rope_config& table_config(const sk_rope_table* t);
 }
+
+namespace sk {
+// Kernel-side layer kind of a paged layer (sk_paged_layer); not an sk_layer_kind.
+constexpr int kKindPaged = 2;
+
+// Host check of a paged layer descriptor shared by the paged entry points.
+inline sk_status paged_layer_check(const sk_paged_layer& L) {
+    if (L.k_pool == nullptr || L.v_pool == nullptr || L.block_table == nullptr || L.seq_lens == nullptr)
+        return SK_ERR_ARG;
+    if (L.batch < 1 || L.n_kv_heads < 1 || L.max_blocks < 1 || L.n_blocks < 1) return SK_ERR_ARG;
+    if (L.head_dim != 64 && L.head_dim != 128) return SK_ERR_ARG;
+    if (L.block_size < 4 || L.block_size > 1024) return SK_ERR_ARG;
+    if (L.n_sink_blocks < 0 || (L.n_sink_blocks > 0 && L.sink_block_ids == nullptr)) return SK_ERR_ARG;
+    if (int64_t(L.n_sink_blocks) * L.block_size > (int64_t(1) << 30)) return SK_ERR_ARG;
+    if (L.sinks < 0 || L.k_dtype != L.v_dtype || (L.k_dtype != SK_BF16 && L.k_dtype != SK_F32)) return SK_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(L.k_pool) | reinterpret_cast<uintptr_t>(L.v_pool)) & 15u) return SK_ERR_ARG;
+    return SK_OK;
+}
+}  // namespace sk

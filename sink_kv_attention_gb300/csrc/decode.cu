@@ -54,10 +54,20 @@ struct DecodeParams {
     int B, Hkv, S, kind;
     int n_blocks;  // P: blocks of the split kernel
     float qscale;  // log2(e) / sqrt(D)
+    // paged layers (kind kKindPaged): pools in kc / vc, request lengths in pos
+    const int32_t* block_table;
+    const int32_t* sink_blocks;
+    int64_t pool_blocks;
+    int bs, max_blocks, sink_len, W;
 };
 
 __device__ __forceinline__ int64_t visible_rows(const DecodeParams& p, int b) {
     const int64_t pos = p.pos[b];
+    if (p.kind == kKindPaged) {
+        // logical keys: the static sink tokens, then the request's own (none if empty)
+        const int64_t L = pos > 0 ? pos + p.sink_len : 0;
+        return (p.W <= 0 || L <= int64_t(p.S) + p.W) ? L : int64_t(p.S) + p.W;
+    }
     if (p.kind == SK_LAYER_GLOBAL) return max(int64_t(0), min(pos, p.cap));
     return max(int64_t(0), min(pos, int64_t(p.S))) + int64_t(p.count[b]);
 }
@@ -168,6 +178,95 @@ __device__ __forceinline__ void load_pv_slice(const T* row, int lane, float2* v)
     }
 }
 
+// Producer of a paged layer: the whole warp.  The visible rows [row, row + n) of a
+// tile map to at most two runs of logical keys (the leading sinks, then the window),
+// each cut at block boundaries (static sink blocks hold whole blocks, so boundaries
+// are multiples of block_size in logical key space); lane j copies run j, from the
+// physical block its table entry names ("vLLM, from the inside out", PagedAttention:
+// the kernel gathers keys and values block by block).  Lane 0 first waits for the
+// stage and sets the expected bytes.
+template <typename C, typename T, int D>
+__device__ __forceinline__ void paged_producer(const DecodeParams& p, const int64_t* pre, int64_t lo, int64_t hi,
+                                               uint8_t* stages, uint64_t* full_bar, uint64_t* empty_bar,
+                                               int lane) {
+    constexpr int STAGES = C::STAGES;
+    const uint64_t policy = l2_policy_evict_first();
+    const int64_t bs = p.bs;
+    const T* kpool = static_cast<const T*>(p.kc);
+    const T* vpool = static_cast<const T*>(p.vc);
+    bool timed_out = false, bad = false;
+    int stage = 0;
+    uint32_t phase = 0;
+    UnitWalk w{pre, p.B, p.Hkv, 0, 0};
+    w.seek(lo);
+    do {
+        const int64_t st = w.start();
+        if (st >= hi) break;
+        const int64_t r0 = max(lo, st) - st, r1 = min(hi, st + w.len()) - st;
+        const int b = w.b, g = w.g;
+        const int64_t n_req = p.pos[b];
+        const int64_t Lk = n_req > 0 ? n_req + p.sink_len : 0;
+        const bool split = p.W > 0 && Lk > int64_t(p.S) + p.W;  // sinks, then the last W keys
+        const int64_t wstart = Lk - p.W;                          // first window key when split
+        const int32_t* trow = p.block_table + int64_t(b) * p.max_blocks;
+        for (int64_t row = r0; row < r1; row += C::TILE) {
+            const int64_t n = min(int64_t(C::TILE), r1 - row);
+            if (lane == 0) {
+                if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1)) timed_out = true;
+                mbar_arrive_expect_tx(&full_bar[stage], 2u * uint32_t(n) * C::ROW_BYTES);
+            }
+            __syncwarp();
+            uint8_t* dst = stages + size_t(stage) * C::STAGE_BYTES;
+            // run piece 1: rows [row, e1), keys = rows; piece 2: rows [a2, row + n),
+            // keys [k2a, k2b) = wstart + (rows - S)
+            const int64_t e1 = split ? min(row + n, int64_t(p.S)) : row + n;
+            const int64_t n1 = row < e1 ? (e1 - 1) / bs - row / bs + 1 : 0;
+            const int64_t a2 = split ? max(row, int64_t(p.S)) : row + n;
+            const int64_t k2a = wstart + (a2 - p.S), k2b = wstart + (row + n - p.S);
+            const int64_t n2 = a2 < row + n ? (k2b - 1) / bs - k2a / bs + 1 : 0;
+            for (int64_t j = lane; j < n1 + n2; j += 32) {
+                int64_t key0, key1, drow;
+                if (j < n1) {
+                    const int64_t blo = (row / bs + j) * bs;
+                    key0 = max(row, blo);
+                    key1 = min(e1, blo + bs);
+                    drow = key0 - row;
+                } else {
+                    const int64_t blo = (k2a / bs + (j - n1)) * bs;
+                    key0 = max(k2a, blo);
+                    key1 = min(k2b, blo + bs);
+                    drow = (a2 - row) + (key0 - k2a);
+                }
+                int64_t blk;
+                if (key0 < p.sink_len) {
+                    blk = p.sink_blocks[key0 / bs];
+                } else {
+                    const int64_t jb = (key0 - p.sink_len) / bs;
+                    blk = jb < p.max_blocks ? trow[jb] : -1;
+                }
+                if (blk < 0 || blk >= p.pool_blocks) {
+                    bad = true;
+                    blk = 0;  // stay inside the pool; the error word reports it
+                }
+                const int64_t src = ((blk * p.Hkv + g) * bs + key0 % bs) * D;
+                const uint32_t bytes = uint32_t(key1 - key0) * C::ROW_BYTES;
+                bulk_copy_g2s(dst + drow * C::ROW_BYTES, kpool + src, bytes, &full_bar[stage], policy);
+                bulk_copy_g2s(dst + (C::TILE + drow) * C::ROW_BYTES, vpool + src, bytes, &full_bar[stage], policy);
+            }
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+    } while (w.next());
+    if (lane == 0) {
+        // drain: every issued stage has been released, so no copy is in flight at exit
+        for (int s = 0; s < STAGES; ++s) {
+            if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1)) timed_out = true;
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (timed_out) set_error(p.err, SK_DEVERR_TIMEOUT);
+    }
+    if (bad) set_error(p.err, SK_DEVERR_BLOCK_TABLE);
+}
+
 template <typename T, int D, int NREP>
 __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
     decode_split_kernel(DecodeParams p) {
@@ -203,6 +302,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
     if (lo >= hi) return;
     bool timed_out = false;
 
+    if (warp == NWARPS && p.kind == kKindPaged) {
+        paged_producer<C, T, D>(p, pre, lo, hi, stages, full_bar, empty_bar, lane);
+        return;
+    }
     if (warp == NWARPS) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
@@ -631,6 +734,83 @@ extern "C" sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q
     p.S = L.sinks;
     p.kind = L.kind;
     p.qscale = kLog2e / sqrtf(float(L.head_dim));
+    route(io_dtype, L, nrep, false, &p, static_cast<cudaStream_t>(stream), nullptr, &e);
+    return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention over a paged layer.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// The fields of a contiguous layer descriptor that route() and the workspace size read.
+sk_kv_layer paged_as_layer(const sk_paged_layer& L) {
+    sk_kv_layer v{};
+    v.kind = kKindPaged;
+    v.k_dtype = L.k_dtype;
+    v.v_dtype = L.v_dtype;
+    v.batch = L.batch;
+    v.n_kv_heads = L.n_kv_heads;
+    v.head_dim = L.head_dim;
+    return v;
+}
+
+sk_status check_paged(const sk_paged_layer* layer, int32_t n_q_heads) {
+    SK_RET_IF(layer == nullptr, SK_ERR_ARG);
+    SK_RET_IF(paged_layer_check(*layer) != SK_OK, SK_ERR_ARG);
+    SK_RET_IF(layer->batch > kMaxBatch, SK_ERR_UNSUPPORTED);
+    SK_RET_IF(n_q_heads < 1 || n_q_heads % layer->n_kv_heads != 0, SK_ERR_ARG);
+    return SK_OK;
+}
+
+}  // namespace
+
+extern "C" size_t sk_paged_decode_workspace_bytes(const sk_paged_layer* layer, int32_t n_q_heads) {
+    if (check_paged(layer, n_q_heads) != SK_OK) return 0;
+    const sk_kv_layer L = paged_as_layer(*layer);
+    size_t ws = 0;
+    cudaError_t e = cudaSuccess;
+    if (!route(L.k_dtype, L, n_q_heads / L.n_kv_heads, true, nullptr, nullptr, &ws, &e)) return 0;
+    return ws;
+}
+
+extern "C" sk_status sk_paged_decode_attention(const sk_paged_layer* layer, const void* q_rot, int32_t n_q_heads,
+                                               int32_t io_dtype, const float* sink_logits, void* out,
+                                               void* workspace, size_t ws_bytes, void* stream) {
+    sk_status s = check_paged(layer, n_q_heads);
+    if (s != SK_OK) return s;
+    SK_RET_IF(q_rot == nullptr || out == nullptr || workspace == nullptr, SK_ERR_ARG);
+    SK_RET_IF((reinterpret_cast<uintptr_t>(q_rot) | reinterpret_cast<uintptr_t>(workspace)) & 15u, SK_ERR_ARG);
+    SK_RET_IF(reinterpret_cast<uintptr_t>(sink_logits) & 3u, SK_ERR_ARG);
+    const sk_paged_layer& PL = *layer;
+    const sk_kv_layer L = paged_as_layer(PL);
+    const int nrep = n_q_heads / L.n_kv_heads;
+    size_t need = 0;
+    cudaError_t e = cudaSuccess;
+    if (!route(io_dtype, L, nrep, true, nullptr, nullptr, &need, &e)) return SK_ERR_UNSUPPORTED;
+    SK_RET_IF(ws_bytes < need, SK_ERR_ARG);
+    DecodeParams p{};
+    p.kc = PL.k_pool;
+    p.vc = PL.v_pool;
+    p.q = q_rot;
+    p.sink_logits = sink_logits;
+    p.out = out;
+    p.ws = static_cast<float*>(workspace);
+    p.pos = PL.seq_lens;
+    p.err = PL.err;
+    p.B = PL.batch;
+    p.Hkv = PL.n_kv_heads;
+    p.S = PL.sinks;
+    p.kind = kKindPaged;
+    p.qscale = kLog2e / sqrtf(float(PL.head_dim));
+    p.block_table = PL.block_table;
+    p.sink_blocks = PL.sink_block_ids;
+    p.pool_blocks = PL.n_blocks;
+    p.bs = PL.block_size;
+    p.max_blocks = PL.max_blocks;
+    p.sink_len = PL.n_sink_blocks * PL.block_size;
+    p.W = PL.window;
     route(io_dtype, L, nrep, false, &p, static_cast<cudaStream_t>(stream), nullptr, &e);
     return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
 }

@@ -164,7 +164,12 @@ struct AppendParams {
     int64_t* pos;
     uint32_t* err;
     int fused_state;
+    // paged layers (kind kKindPaged): pools in kc / vc, lengths in pos
+    const int32_t* block_table;
+    int max_blocks, bs;
+    int64_t n_blocks;
 };
+
 
 struct SeqState {
     int64_t pos;
@@ -181,6 +186,7 @@ __device__ __forceinline__ SeqState load_state(const AppendParams& p, int b) {
     s.err_bits = 0;
     if (s.pos < 0 || s.pos + p.T > p.max_pos) s.err_bits |= SK_DEVERR_POSITION_RANGE;
     if (p.kind == SK_LAYER_GLOBAL && s.pos + p.T > p.cap) s.err_bits |= SK_DEVERR_CAPACITY;
+    if (p.kind == kKindPaged && s.pos + p.T > int64_t(p.max_blocks) * p.bs) s.err_bits |= SK_DEVERR_CAPACITY;
     s.ok = s.err_bits == 0;
     return s;
 }
@@ -198,6 +204,31 @@ __device__ __forceinline__ int64_t token_slot(const AppendParams& p, const SeqSt
         return p.S + (u - (n - p.W));
     }
     return p.S + (s.head + u) % p.W;
+}
+
+// Cache row of kv head 0 for chunk token t and the row stride between kv heads; ok is
+// false when the token is not stored (dropped by a long ring chunk, or a paged block id
+// outside the pool, which also sets *bad_block).
+struct CacheRow {
+    int64_t base, hstride;
+    bool ok;
+};
+
+__device__ __forceinline__ CacheRow cache_row(const AppendParams& p, const SeqState& s, int b, int t,
+                                              bool* bad_block) {
+    if (p.kind == kKindPaged) {
+        // "vLLM, from the inside out", PagedAttention: position P lives in request block
+        // P / block_size at row P % block_size; the pool is [block][kv head][row][dim].
+        const int64_t P = s.pos + t;
+        const int32_t blk = p.block_table[int64_t(b) * p.max_blocks + P / p.bs];
+        if (blk < 0 || blk >= p.n_blocks) {
+            *bad_block = true;
+            return CacheRow{0, 0, false};
+        }
+        return CacheRow{int64_t(blk) * p.Hkv * p.bs + P % p.bs, p.bs, true};
+    }
+    const int64_t slot = token_slot(p, s, t);
+    return CacheRow{int64_t(b) * p.Hkv * p.cap + slot, p.cap, slot >= 0};
 }
 
 __device__ __forceinline__ void advance_state(const AppendParams& p, const SeqState& s, int b) {
@@ -280,6 +311,7 @@ __global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p
     const SeqState s = load_state(p, b);
     const int n_tok = s.ok ? p.T : 0;
     bool timed_out = false;
+    bool bad_block = false;
 
     IO* q = static_cast<IO*>(p.q);
     IO* k = static_cast<IO*>(p.k);
@@ -318,12 +350,11 @@ __global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p
         int st = 0;
         uint32_t phase = 0;
         for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
-            const int64_t slot_kv = token_slot(p, s, t);
+            const CacheRow crw = cache_row(p, s, b, t, &bad_block);
             const int64_t tok = int64_t(b) * p.T + t;
             // per-token bases; rows below add small per-row offsets only
             IO* qtok = q + tok * p.Hq * D;
             IO* ktok = k + tok * p.Hkv * D;
-            const int64_t cbase = int64_t(b) * p.Hkv * p.cap + slot_kv;  // cache row of kv head 0
             if (!mbar_wait_bounded(&full_bar[st], phase)) timed_out = true;
             const uint8_t* stage = smem_raw + st * stage_bytes;
             // this lane's (cos, sin) pairs of position pos + t, copied in with the rows
@@ -344,8 +375,8 @@ __global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p
                 const uint4 out = ElemIO<IO>::pack(f);
                 if (live && which == 0) reinterpret_cast<uint4*>(qtok + h * D)[c] = out;
                 if (live && which == 1) reinterpret_cast<uint4*>(ktok + h * D)[c] = out;
-                const int64_t crow = cbase + int64_t(h) * p.cap;  // cache row index
-                const bool store_kv = live && which != 0 && slot_kv >= 0;
+                const int64_t crow = crw.base + int64_t(h) * crw.hstride;  // cache row index
+                const bool store_kv = live && which != 0 && crw.ok;
                 if constexpr (sizeof(KC) == 1) {
                     // int8 K: symmetric absmax over the row, codes rint(x * 127 / max|x|), ties to even.
                     float amax = 0.0f;
@@ -378,6 +409,7 @@ __global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p
         }
     }
     if (timed_out) set_error(p.err, SK_DEVERR_TIMEOUT);
+    if (bad_block) set_error(p.err, SK_DEVERR_BLOCK_TABLE);
     if (p.fused_state) {
         __syncthreads();  // every thread has read the state before it changes
         if (threadIdx.x == 0) advance_state(p, s, b);
@@ -465,6 +497,25 @@ extern "C" sk_status sk_rope_apply(const sk_rope_table* table, void* x, int32_t 
     return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
 }
 
+namespace {
+
+sk_status run_append(const AppendParams& p, const sk_rope_config& c, int io_dtype, int k_dtype, int v_dtype,
+                     int head_dim, cudaStream_t st) {
+    const bool neox = c.neox != 0;
+    cudaError_t e;
+    if (io_dtype == SK_F32 && k_dtype == SK_F32 && v_dtype == SK_F32)
+        e = dispatch_append<float, float, float>(p, head_dim, neox, st);
+    else if (io_dtype == SK_BF16 && k_dtype == SK_BF16 && v_dtype == SK_BF16)
+        e = dispatch_append<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(p, head_dim, neox, st);
+    else if (io_dtype == SK_BF16 && k_dtype == SK_I8 && v_dtype == SK_BF16 && p.kind != kKindPaged)
+        e = dispatch_append<__nv_bfloat16, int8_t, __nv_bfloat16>(p, head_dim, neox, st);
+    else
+        return SK_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer* layer, void* q,
                                   int32_t n_q_heads, void* k, const void* v, int32_t io_dtype,
                                   int32_t T, void* stream) {
@@ -511,16 +562,39 @@ extern "C" sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer*
     p.count = L.count;
     p.pos = L.pos;
     p.err = L.err;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool neox = c.neox != 0;
-    cudaError_t e;
-    if (io_dtype == SK_F32 && L.k_dtype == SK_F32 && L.v_dtype == SK_F32)
-        e = dispatch_append<float, float, float>(p, L.head_dim, neox, st);
-    else if (io_dtype == SK_BF16 && L.k_dtype == SK_BF16 && L.v_dtype == SK_BF16)
-        e = dispatch_append<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(p, L.head_dim, neox, st);
-    else if (io_dtype == SK_BF16 && L.k_dtype == SK_I8 && L.v_dtype == SK_BF16)
-        e = dispatch_append<__nv_bfloat16, int8_t, __nv_bfloat16>(p, L.head_dim, neox, st);
-    else
-        return SK_ERR_UNSUPPORTED;
-    return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+    return run_append(p, c, io_dtype, L.k_dtype, L.v_dtype, L.head_dim, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" sk_status sk_paged_append(const sk_rope_table* table, const sk_paged_layer* layer, void* q,
+                                     int32_t n_q_heads, const void* k, const void* v, int32_t io_dtype,
+                                     int32_t T, void* stream) {
+    SK_RET_IF(table == nullptr || layer == nullptr || k == nullptr || v == nullptr, SK_ERR_ARG);
+    const sk_paged_layer& L = *layer;
+    const sk_rope_config& c = table_config(table);
+    SK_RET_IF(paged_layer_check(L) != SK_OK, SK_ERR_ARG);
+    SK_RET_IF(L.head_dim != c.head_dim || T < 0, SK_ERR_ARG);
+    if (q != nullptr) SK_RET_IF(n_q_heads < 1 || n_q_heads % L.n_kv_heads != 0 || !aligned16(q), SK_ERR_ARG);
+    SK_RET_IF(!aligned16(k) || !aligned16(v), SK_ERR_ARG);
+    if (T == 0) return SK_OK;
+    AppendParams p{};
+    p.table = table_device(table);
+    p.max_pos = c.max_positions;
+    p.rotary_dim = c.rotary_dim;
+    p.q = q;
+    p.k = const_cast<void*>(k);
+    p.v = v;
+    p.Hq = n_q_heads;
+    p.Hkv = L.n_kv_heads;
+    p.T = T;
+    p.B = L.batch;
+    p.kc = L.k_pool;
+    p.vc = L.v_pool;
+    p.kind = kKindPaged;
+    p.pos = L.seq_lens;
+    p.err = L.err;
+    p.block_table = L.block_table;
+    p.max_blocks = L.max_blocks;
+    p.bs = L.block_size;
+    p.n_blocks = L.n_blocks;
+    return run_append(p, c, io_dtype, L.k_dtype, L.v_dtype, L.head_dim, static_cast<cudaStream_t>(stream));
 }

@@ -52,11 +52,13 @@ def test_status_strings_and_version(lib):
 
 
 def test_struct_layouts_match_header(tmp_path):
-    """ctypes mirrors of sk_rope_config / sk_kv_layer match the C compiler's layout."""
+    """ctypes mirrors of sk_rope_config / sk_kv_layer / sk_paged_layer match the C
+    compiler's layout."""
     import sink_kv_attention_gb300 as sk
     src = tmp_path / "layout.c"
     fields = {"sk_rope_config": [f for f, _ in sk.RopeConfig._fields_],
-              "sk_kv_layer": [f for f, _ in sk.KVLayerStruct._fields_]}
+              "sk_kv_layer": [f for f, _ in sk.KVLayerStruct._fields_],
+              "sk_paged_layer": [f for f, _ in sk.PagedLayerStruct._fields_]}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "sinkkv.h"', "int main(void) {"]
     for st, fs in fields.items():
         lines.append(f'printf("{st} %zu\\n", sizeof({st}));')
@@ -67,7 +69,8 @@ def test_struct_layouts_match_header(tmp_path):
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True).stdout.splitlines())
-    for name, cls in [("sk_rope_config", sk.RopeConfig), ("sk_kv_layer", sk.KVLayerStruct)]:
+    for name, cls in [("sk_rope_config", sk.RopeConfig), ("sk_kv_layer", sk.KVLayerStruct),
+                      ("sk_paged_layer", sk.PagedLayerStruct)]:
         assert int(got[name]) == ctypes.sizeof(cls)
         for f, _ in cls._fields_:
             assert int(got[f"{name}.{f}"]) == getattr(cls, f).offset, f
@@ -91,4 +94,10 @@ def test_bad_arguments_rejected_on_host(lib):
     assert lib.sk_decode_workspace_bytes(None, 8) == 0
     assert lib.sk_kv_rerotate(None, 1, None, None, None) == sk.SK_ERR_ARG
     assert lib.sk_rope_apply(None, None, 0, 1, 1, None, None, None) == sk.SK_ERR_ARG
+    assert lib.sk_paged_append(None, None, None, 0, None, None, 0, 1, None) == sk.SK_ERR_ARG
+    assert lib.sk_paged_decode_attention(None, None, 8, 0, None, None, None, 0, None) == sk.SK_ERR_ARG
+    assert lib.sk_paged_decode_workspace_bytes(None, 8) == 0
+    bad = sk.PagedLayerStruct(0, 0, 1, 1, 128, 2, 4, 0, 0, 0, 16, 16, 16, 16, None, 16, None)  # block_size 2
+    assert lib.sk_paged_decode_workspace_bytes(ctypes.byref(bad), 1) == 0
+    assert lib.sk_kv_shift_recent(None, 1, None, -1, None) == sk.SK_ERR_ARG
     lib.sk_rope_table_destroy(None)  # NULL is ignored
