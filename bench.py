@@ -495,6 +495,114 @@ def bench_rerotate(args, kdt):
             "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": args.steps, "clocks": clk}
 
 
+def bench_paged(args):
+    """The windowed-layer decode step on a paged cache: B=32, H_q=32, H_kv=8,
+    d_h=r=128, request sinks S=4, window W=4092, 16-token blocks scattered over a
+    shared pool (only the sink block, the window's blocks and the blocks the timed
+    steps will fill are allocated); one step = RoPE + paged append + paged split-K
+    attention, the timed steps captured as one CUDA graph."""
+    import numpy as np_
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    B, Hq, Hkv, D, S, W, bs = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"], 16
+    steps, warm = args.steps, args.warmup
+    n = 2 * steps + warm
+    pos = synth.window_state(13, B, W, c["pos_lo"], c["pos_hi"])[0]
+    end = pos + n + 1                                  # lengths after the last step
+    max_blocks = int((int(end.max()) + bs - 1) // bs)
+    needed = []
+    for b in range(B):
+        first = max(0, int(pos[b]) + 1 - W) // bs      # oldest block the first step's window reads
+        last = (int(end[b]) - 1) // bs
+        needed.append(sorted({0} | set(range(first, last + 1))))
+    n_blocks = sum(len(x) for x in needed)
+    layer = sk.PagedLayer.allocate(B, Hkv, D, block_size=bs, n_blocks=n_blocks, max_blocks=max_blocks,
+                                   sinks=S, window=W)
+    synth.fill_normal_(layer.k_pool, 11)
+    synth.fill_normal_(layer.v_pool, 12)
+    perm = np_.random.default_rng(17).permutation(n_blocks)
+    table = np_.full((B, max_blocks), -1, dtype=np_.int32)
+    k_ = 0
+    for b in range(B):
+        for j in needed[b]:
+            table[b, j] = perm[k_]
+            k_ += 1
+    layer.block_table.copy_(torch.from_numpy(table))
+    layer.seq_lens.copy_(pos)
+    tbl = sk.RopeTable(D, c["r"], c["theta"], int(end.max()) + 64)
+    qs = synth.normal((n, B, 1, Hq, D), 14, torch.bfloat16, device="cuda")
+    ks = synth.normal((n, B, 1, Hkv, D), 15, torch.bfloat16, device="cuda")
+    vs = synth.normal((n, B, 1, Hkv, D), 16, torch.bfloat16, device="cuda")
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(sk.paged_decode_workspace_bytes(layer, Hq), dtype=torch.uint8, device="cuda")
+    zl = _learned_sinks(args, Hq)
+
+    def step(i, ev=None):
+        st = torch.cuda.current_stream()
+        sk.paged_append(tbl, layer, qs[i], ks[i], vs[i])
+        if ev is not None:
+            ev[0].record(st)
+        sk.paged_decode_attention(layer, qs[i, :, 0], out=out, workspace=ws, sink_logits=zl)
+        if ev is not None:
+            ev[1].record(st)
+
+    for i in range(warm):
+        step(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(steps):
+            step(warm + i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("end")
+    clocks.stop()
+    ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+          for _ in range(steps)]
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        for i in range(steps):
+            step(warm + steps + i, ev[i])
+    g2.replay()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    dec_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    assert layer.error_bits() == 0
+    L = S + W
+    kv_bytes = B * Hkv * L * D * 2 * 2
+    alg_decode = kv_bytes + 2 * (B * Hq * D * 2)
+    hbm, _, _, peak_kind = _peaks()
+    value = kv_bytes / (ms * 1e-3) / 1e9
+    achieved = alg_decode / (dec_ms * 1e-3) / 1e9
+    return {"metric": METRIC + " (paged cache)", "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": steps, "warmup": warm, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "windowed-layer decode step on a paged cache (RoPE + paged append + paged "
+                                   "split-K attention)", "batch": B, "H_q": Hq, "H_kv": Hkv, "d_h": D, "sinks": S,
+                       "window": W, "block_size": bs, "pool_blocks": n_blocks,
+                       "learned_sink_logits": bool(args.learned_sink),
+                       "l2": f"inputs larger than L2 (KV {kv_bytes / 1e6:.0f} MB per step)"},
+            "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "traffic": None,
+                         "kernel": "paged decode attention (split-K + combine), per launch",
+                         "algorithmic_bytes_per_launch": alg_decode, "launch_ms": round(dec_ms, 5),
+                         "peak_source": f"{peak_kind} hbm_gbs"},
+            "gpu_launches": steps * 3, "launch": "cuda graph of the timed steps", "clocks": clocks.summary()}
+
+
 def bench_shift(args, kdt):
     """Local-position window slide: the recent keys of the windowed decode workload's
     cache (B=32, H_kv=8, d_h=r=128, S=4, W=4092, every ring full) turned by one
@@ -740,7 +848,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="window",
                     choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill", "dynamic_bf16",
-                             "dynamic_i8", "shift_bf16", "shift_i8"])
+                             "dynamic_i8", "shift_bf16", "shift_i8", "paged"])
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -796,6 +904,8 @@ def main():
                 print(json.dumps(bench_prefill(args)))
             elif args.workload.startswith("dynamic"):
                 print(json.dumps(bench_dynamic(args, args.workload.split("_")[1])))
+            elif args.workload == "paged":
+                print(json.dumps(bench_paged(args)))
             elif args.workload.startswith("shift"):
                 print(json.dumps(bench_shift(args, args.workload.split("_")[1])))
             else:

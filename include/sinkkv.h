@@ -148,7 +148,8 @@ typedef struct {
  * sink blocks, sinks = their token count gives them the role of the pinned sinks;
  * without, sinks = S keeps the request's own first S tokens (StreamingLLM on paged
  * memory).
- * k_dtype, v_dtype: SK_BF16 or SK_F32 (the same for both).  block_size in [4, 1024].
+ * k_dtype, v_dtype: SK_BF16 or SK_F32 (the same for both).  block_size a power of two
+ * in [4, 1024].
  */
 typedef struct {
     int32_t k_dtype;

@@ -543,6 +543,11 @@ def paged_append(table: RopeTable, layer: PagedLayer, q: Optional[torch.Tensor],
                                   _ptr(v), _sk_dtype(k.dtype), k.shape[1], _stream(stream)), "sk_paged_append")
 
 
+def paged_decode_workspace_bytes(layer: PagedLayer, n_q_heads: int) -> int:
+    s = layer.struct()
+    return int(_lib().sk_paged_decode_workspace_bytes(ctypes.byref(s), n_q_heads))
+
+
 def paged_decode_attention(layer: PagedLayer, q_rot: torch.Tensor, out: Optional[torch.Tensor] = None,
                            workspace: Optional[torch.Tensor] = None, stream=None,
                            sink_logits: Optional[torch.Tensor] = None) -> torch.Tensor:

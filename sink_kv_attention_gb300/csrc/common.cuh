@@ -256,7 +256,7 @@ inline sk_status paged_layer_check(const sk_paged_layer& L) {
         return SK_ERR_ARG;
     if (L.batch < 1 || L.n_kv_heads < 1 || L.max_blocks < 1 || L.n_blocks < 1) return SK_ERR_ARG;
     if (L.head_dim != 64 && L.head_dim != 128) return SK_ERR_ARG;
-    if (L.block_size < 4 || L.block_size > 1024) return SK_ERR_ARG;
+    if (L.block_size < 4 || L.block_size > 1024 || (L.block_size & (L.block_size - 1)) != 0) return SK_ERR_ARG;
     if (L.n_sink_blocks < 0 || (L.n_sink_blocks > 0 && L.sink_block_ids == nullptr)) return SK_ERR_ARG;
     if (int64_t(L.n_sink_blocks) * L.block_size > (int64_t(1) << 30)) return SK_ERR_ARG;
     if (L.sinks < 0 || L.k_dtype != L.v_dtype || (L.k_dtype != SK_BF16 && L.k_dtype != SK_F32)) return SK_ERR_ARG;

@@ -58,7 +58,7 @@ struct DecodeParams {
     const int32_t* block_table;
     const int32_t* sink_blocks;
     int64_t pool_blocks;
-    int bs, max_blocks, sink_len, W;
+    int bs, bs_log2, max_blocks, sink_len, W;  // block_size = 1 << bs_log2
 };
 
 __device__ __forceinline__ int64_t visible_rows(const DecodeParams& p, int b) {
@@ -192,6 +192,7 @@ __device__ __forceinline__ void paged_producer(const DecodeParams& p, const int6
     constexpr int STAGES = C::STAGES;
     const uint64_t policy = l2_policy_evict_first();
     const int64_t bs = p.bs;
+    const int lg = p.bs_log2;  // block_size is a power of two: no divisions below
     const T* kpool = static_cast<const T*>(p.kc);
     const T* vpool = static_cast<const T*>(p.vc);
     bool timed_out = false, bad = false;
@@ -209,6 +210,11 @@ __device__ __forceinline__ void paged_producer(const DecodeParams& p, const int6
         const bool split = p.W > 0 && Lk > int64_t(p.S) + p.W;  // sinks, then the last W keys
         const int64_t wstart = Lk - p.W;                          // first window key when split
         const int32_t* trow = p.block_table + int64_t(b) * p.max_blocks;
+        // Lane l caches table entry cbase + l: the window's block ids are consecutive
+        // entries, so one load serves several tiles and the copies are not held up by
+        // a table read per tile.
+        int64_t cbase = -64;
+        int32_t cval = -1;
         for (int64_t row = r0; row < r1; row += C::TILE) {
             const int64_t n = min(int64_t(C::TILE), r1 - row);
             if (lane == 0) {
@@ -220,35 +226,46 @@ __device__ __forceinline__ void paged_producer(const DecodeParams& p, const int6
             // run piece 1: rows [row, e1), keys = rows; piece 2: rows [a2, row + n),
             // keys [k2a, k2b) = wstart + (rows - S)
             const int64_t e1 = split ? min(row + n, int64_t(p.S)) : row + n;
-            const int64_t n1 = row < e1 ? (e1 - 1) / bs - row / bs + 1 : 0;
+            const int64_t n1 = row < e1 ? ((e1 - 1) >> lg) - (row >> lg) + 1 : 0;
             const int64_t a2 = split ? max(row, int64_t(p.S)) : row + n;
             const int64_t k2a = wstart + (a2 - p.S), k2b = wstart + (row + n - p.S);
-            const int64_t n2 = a2 < row + n ? (k2b - 1) / bs - k2a / bs + 1 : 0;
-            for (int64_t j = lane; j < n1 + n2; j += 32) {
-                int64_t key0, key1, drow;
-                if (j < n1) {
-                    const int64_t blo = (row / bs + j) * bs;
+            const int64_t n2 = a2 < row + n ? ((k2b - 1) >> lg) - (k2a >> lg) + 1 : 0;
+            for (int64_t j0 = 0; j0 < n1 + n2; j0 += 32) {  // uniform trip count
+                const int64_t j = j0 + lane;
+                const bool active = j < n1 + n2;
+                int64_t key0 = 0, key1 = 0, drow = 0;
+                if (active && j < n1) {
+                    const int64_t blo = ((row >> lg) + j) << lg;
                     key0 = max(row, blo);
                     key1 = min(e1, blo + bs);
                     drow = key0 - row;
-                } else {
-                    const int64_t blo = (k2a / bs + (j - n1)) * bs;
+                } else if (active) {
+                    const int64_t blo = ((k2a >> lg) + (j - n1)) << lg;
                     key0 = max(k2a, blo);
                     key1 = min(k2b, blo + bs);
                     drow = (a2 - row) + (key0 - k2a);
                 }
-                int64_t blk;
-                if (key0 < p.sink_len) {
-                    blk = p.sink_blocks[key0 / bs];
-                } else {
-                    const int64_t jb = (key0 - p.sink_len) / bs;
-                    blk = jb < p.max_blocks ? trow[jb] : -1;
+                const bool in_table = active && key0 >= p.sink_len;
+                const int64_t jb = in_table ? (key0 - p.sink_len) >> lg : 0;
+                // refill the cache from this round's first table entry when its last one
+                // is not cached (block ids past 2^32 are not cached, only read directly)
+                const int64_t jmax = __reduce_max_sync(kFull, in_table ? uint32_t(jb) : 0u);
+                if (__any_sync(kFull, in_table) && (jmax >= cbase + 32 || jmax < cbase)) {
+                    cbase = __reduce_min_sync(kFull, in_table ? uint32_t(jb) : 0xffffffffu);
+                    cval = cbase + lane < p.max_blocks ? trow[cbase + lane] : -1;
                 }
+                const int64_t ci = jb - cbase;
+                const int32_t cached = __shfl_sync(kFull, cval, int(ci) & 31);
+                if (!active) continue;
+                int64_t blk;
+                if (key0 < p.sink_len) blk = p.sink_blocks[key0 >> lg];
+                else if (ci >= 0 && ci < 32) blk = cached;
+                else blk = jb < p.max_blocks ? trow[jb] : -1;
                 if (blk < 0 || blk >= p.pool_blocks) {
                     bad = true;
                     blk = 0;  // stay inside the pool; the error word reports it
                 }
-                const int64_t src = ((blk * p.Hkv + g) * bs + key0 % bs) * D;
+                const int64_t src = ((blk * p.Hkv + g) * bs + (key0 & (bs - 1))) * D;
                 const uint32_t bytes = uint32_t(key1 - key0) * C::ROW_BYTES;
                 bulk_copy_g2s(dst + drow * C::ROW_BYTES, kpool + src, bytes, &full_bar[stage], policy);
                 bulk_copy_g2s(dst + (C::TILE + drow) * C::ROW_BYTES, vpool + src, bytes, &full_bar[stage], policy);
@@ -808,6 +825,7 @@ extern "C" sk_status sk_paged_decode_attention(const sk_paged_layer* layer, cons
     p.sink_blocks = PL.sink_block_ids;
     p.pool_blocks = PL.n_blocks;
     p.bs = PL.block_size;
+    p.bs_log2 = __builtin_ctz(unsigned(PL.block_size));
     p.max_blocks = PL.max_blocks;
     p.sink_len = PL.n_sink_blocks * PL.block_size;
     p.W = PL.window;

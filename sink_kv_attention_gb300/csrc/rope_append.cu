@@ -166,7 +166,7 @@ struct AppendParams {
     int fused_state;
     // paged layers (kind kKindPaged): pools in kc / vc, lengths in pos
     const int32_t* block_table;
-    int max_blocks, bs;
+    int max_blocks, bs, bs_log2;  // block_size = 1 << bs_log2
     int64_t n_blocks;
 };
 
@@ -220,12 +220,12 @@ __device__ __forceinline__ CacheRow cache_row(const AppendParams& p, const SeqSt
         // "vLLM, from the inside out", PagedAttention: position P lives in request block
         // P / block_size at row P % block_size; the pool is [block][kv head][row][dim].
         const int64_t P = s.pos + t;
-        const int32_t blk = p.block_table[int64_t(b) * p.max_blocks + P / p.bs];
+        const int32_t blk = p.block_table[int64_t(b) * p.max_blocks + (P >> p.bs_log2)];
         if (blk < 0 || blk >= p.n_blocks) {
             *bad_block = true;
             return CacheRow{0, 0, false};
         }
-        return CacheRow{int64_t(blk) * p.Hkv * p.bs + P % p.bs, p.bs, true};
+        return CacheRow{int64_t(blk) * p.Hkv * p.bs + (P & (p.bs - 1)), p.bs, true};
     }
     const int64_t slot = token_slot(p, s, t);
     return CacheRow{int64_t(b) * p.Hkv * p.cap + slot, p.cap, slot >= 0};
@@ -595,6 +595,7 @@ extern "C" sk_status sk_paged_append(const sk_rope_table* table, const sk_paged_
     p.block_table = L.block_table;
     p.max_blocks = L.max_blocks;
     p.bs = L.block_size;
+    p.bs_log2 = __builtin_ctz(unsigned(L.block_size));
     p.n_blocks = L.n_blocks;
     return run_append(p, c, io_dtype, L.k_dtype, L.v_dtype, L.head_dim, static_cast<cudaStream_t>(stream));
 }
