@@ -99,6 +99,22 @@ __device__ __forceinline__ void delta_pairs(const RerotParams& p, int64_t P, int
     }
 }
 
+// The same delta rotation as (cos, sin) pairs of consecutive rotary pairs: dc2[i] holds
+// the cosines of pairs j0 + 2i and j0 + 2i + 1, ds2[i] their sines.
+template <int N2>
+__device__ __forceinline__ void delta_pairs2(const RerotParams& p, int64_t P, int j0, float2* dc2, float2* ds2) {
+    const int half = p.r / 2;
+    const int64_t PA = p.shift ? p.rowA : P, PB = p.shift ? p.rowB : P;
+    const float4* a4 = reinterpret_cast<const float4*>(p.tA + PA * half + j0);
+    const float4* b4 = reinterpret_cast<const float4*>(p.tB + PB * half + j0);
+#pragma unroll
+    for (int i = 0; i < N2; ++i) {
+        const float4 a = __ldg(a4 + i), b = __ldg(b4 + i);
+        dc2[i] = make_float2((b.x * a.x + b.y * a.y) * p.inv_muA2, (b.z * a.z + b.w * a.w) * p.inv_muA2);
+        ds2[i] = make_float2((b.y * a.x - b.x * a.y) * p.inv_muA2, (b.w * a.z - b.z * a.w) * p.inv_muA2);
+    }
+}
+
 // ---- bf16 keys: NeoX thread = 8 pairs (16 B of each half); GPT-J thread = 4 pairs ----
 template <int D, bool NEOX>
 __global__ void __launch_bounds__(kThreads) rerotate_bf16_kernel(RerotParams p) {
@@ -215,10 +231,10 @@ __device__ __forceinline__ uint4 pairs_to_codes16(const float2* t, float inv) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-constexpr int kRowsInFlight = 2;  // kv-head rows each thread loads before computing
+constexpr int kRowsInFlight = 1;  // kv-head rows each thread loads before computing
 
 template <int D, bool NEOX>
-__global__ void __launch_bounds__(kThreads, 3) rerotate_i8_kernel(RerotParams p) {
+__global__ void __launch_bounds__(kThreads, 4) rerotate_i8_kernel(RerotParams p) {
     constexpr int TPR = D / 32;  // threads per row (aligned group of 2 or 4 lanes)
     constexpr int SPB = kThreads / TPR;
     const int t = threadIdx.x % TPR;
@@ -231,7 +247,9 @@ __global__ void __launch_bounds__(kThreads, 3) rerotate_i8_kernel(RerotParams p)
     const int j0 = 16 * t;
     const int off1 = rot ? (NEOX ? 16 * t : 32 * t) : p.r + 32 * (t - p.r / 32);
     const int off2 = rot ? (NEOX ? half + 16 * t : 32 * t + 16) : off1 + 16;
-    float2 dc2[8], ds2[8];  // delta rotation of pairs j0 .. j0+15, as pairs
+    // delta rotation of pairs j0 .. j0+15 as (cos, cos, sin, sin) of two consecutive
+    // pairs, thread-minor in shared memory: keeping it in registers made the loop spill
+    __shared__ float4 sdelta[8][kThreads];
     int64_t lastP = -1;
     for (int l = 0; l < p.n_layers; ++l) {
         const RerotLayer& L = p.layers[l];
@@ -245,13 +263,11 @@ __global__ void __launch_bounds__(kThreads, 3) rerotate_i8_kernel(RerotParams p)
                 valid = false;
             }
             if (valid && rot && P != lastP) {
-                float dc[16], ds[16];
-                delta_pairs<16>(p, P, j0, dc, ds);
+                float2 dc2[8], ds2[8];
+                delta_pairs2<8>(p, P, j0, dc2, ds2);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    dc2[i] = make_float2(dc[2 * i], dc[2 * i + 1]);
-                    ds2[i] = make_float2(ds[2 * i], ds[2 * i + 1]);
-                }
+                for (int i = 0; i < 8; ++i)
+                    sdelta[i][threadIdx.x] = make_float4(dc2[i].x, dc2[i].y, ds2[i].x, ds2[i].y);
                 lastP = P;
             }
             for (int g0 = 0; g0 < p.Hkv; g0 += kRowsInFlight) {
@@ -284,9 +300,11 @@ __global__ void __launch_bounds__(kThreads, 3) rerotate_i8_kernel(RerotParams p)
                             // pair j: x1 = a, x2 = c -> (x1 dc - x2 ds, x2 dc + x1 ds)
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
+                                const float4 d = sdelta[i][threadIdx.x];
+                                const float2 dc = make_float2(d.x, d.y), ds = make_float2(d.z, d.w);
                                 const float2 x1 = a[i], x2 = c[i];
-                                a[i] = __ffma2_rn(x1, dc2[i], __fmul2_rn(make_float2(-x2.x, -x2.y), ds2[i]));
-                                c[i] = __ffma2_rn(x2, dc2[i], __fmul2_rn(x1, ds2[i]));
+                                a[i] = __ffma2_rn(x1, dc, __fmul2_rn(make_float2(-x2.x, -x2.y), ds));
+                                c[i] = __ffma2_rn(x2, dc, __fmul2_rn(x1, ds));
                             }
                         } else {
                             // interleaved pairs (2j, 2j+1) of codes [32t, 32t+32): regroup
@@ -300,9 +318,10 @@ __global__ void __launch_bounds__(kThreads, 3) rerotate_i8_kernel(RerotParams p)
                             }
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
-                                const float2 y1 =
-                                    __ffma2_rn(x1[i], dc2[i], __fmul2_rn(make_float2(-x2[i].x, -x2[i].y), ds2[i]));
-                                const float2 y2 = __ffma2_rn(x2[i], dc2[i], __fmul2_rn(x1[i], ds2[i]));
+                                const float4 d = sdelta[i][threadIdx.x];
+                                const float2 dc = make_float2(d.x, d.y), ds = make_float2(d.z, d.w);
+                                const float2 y1 = __ffma2_rn(x1[i], dc, __fmul2_rn(make_float2(-x2[i].x, -x2[i].y), ds));
+                                const float2 y2 = __ffma2_rn(x2[i], dc, __fmul2_rn(x1[i], ds));
                                 x1[i] = y1;
                                 x2[i] = y2;
                             }
@@ -325,9 +344,10 @@ __global__ void __launch_bounds__(kThreads, 3) rerotate_i8_kernel(RerotParams p)
 #pragma unroll
                     for (int o = TPR / 2; o > 0; o >>= 1)
                         amax_c = fmaxf(amax_c, __shfl_xor_sync(0xffffffffu, amax_c, o));
-                    float s_new, inv;
-                    int8_row_scale(amax_c * s_old[u], &s_new, &inv);
-                    inv = amax_c * s_old[u] == 0.0f ? 0.0f : __fdiv_rn(127.0f, amax_c);  // in code units
+                    // new scale max|x| / 127 with x = t * s_old; codes rint(t * 127 / max|t|)
+                    const float amax_x = amax_c * s_old[u];
+                    const float s_new = amax_x == 0.0f ? 1.0f : __fdiv_rn(amax_x, 127.0f);
+                    const float inv = amax_x == 0.0f ? 0.0f : __fdiv_rn(127.0f, amax_c);  // in code units
                     if (valid) {
                         *reinterpret_cast<uint4*>(row + off1) = pairs_to_codes16(a, inv);
                         *reinterpret_cast<uint4*>(row + off2) = pairs_to_codes16(c, inv);
