@@ -214,9 +214,10 @@ struct CacheRow {
     bool ok;
 };
 
+template <bool PAGED>
 __device__ __forceinline__ CacheRow cache_row(const AppendParams& p, const SeqState& s, int b, int t,
                                               bool* bad_block) {
-    if (p.kind == kKindPaged) {
+    if constexpr (PAGED) {
         // "vLLM, from the inside out", PagedAttention: position P lives in request block
         // P / block_size at row P % block_size; the pool is [block][kv head][row][dim].
         const int64_t P = s.pos + t;
@@ -226,9 +227,10 @@ __device__ __forceinline__ CacheRow cache_row(const AppendParams& p, const SeqSt
             return CacheRow{0, 0, false};
         }
         return CacheRow{int64_t(blk) * p.Hkv * p.bs + (P & (p.bs - 1)), p.bs, true};
+    } else {
+        const int64_t slot = token_slot(p, s, t);
+        return CacheRow{int64_t(b) * p.Hkv * p.cap + slot, p.cap, slot >= 0};
     }
-    const int64_t slot = token_slot(p, s, t);
-    return CacheRow{int64_t(b) * p.Hkv * p.cap + slot, p.cap, slot >= 0};
 }
 
 __device__ __forceinline__ void advance_state(const AppendParams& p, const SeqState& s, int b) {
@@ -282,7 +284,7 @@ template <typename IO> constexpr size_t append_stage_bytes(int hq, int hkv, int 
 // shared-memory stages with 1-D bulk copies; the other warps rotate the rows out of
 // shared memory (LPR lanes per row, 16-byte vectors, the NeoX partner vector by
 // shuffle), write q and k back in place and k, v into the cache.
-template <typename IO, typename KC, typename VC, int D, bool NEOX>
+template <typename IO, typename KC, typename VC, int D, bool NEOX, bool PAGED>
 __global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p) {
     using L = RowLayout<IO, D>;
     constexpr int VEC = L::VEC;
@@ -350,7 +352,7 @@ __global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p
         int st = 0;
         uint32_t phase = 0;
         for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
-            const CacheRow crw = cache_row(p, s, b, t, &bad_block);
+            const CacheRow crw = cache_row<PAGED>(p, s, b, t, &bad_block);
             const int64_t tok = int64_t(b) * p.T + t;
             // per-token bases; rows below add small per-row offsets only
             IO* qtok = q + tok * p.Hq * D;
@@ -436,13 +438,13 @@ cudaError_t launch_apply(const ApplyParams& p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <typename IO, typename KC, typename VC, int D, bool NEOX>
+template <typename IO, typename KC, typename VC, int D, bool NEOX, bool PAGED>
 cudaError_t launch_append(AppendParams p, cudaStream_t st) {
     const int hq = p.q != nullptr ? p.Hq : 0;
     const size_t smem = kAppendStages * (append_stage_bytes<IO>(hq, p.Hkv, D) + size_t(p.rotary_dim / 2) * 8) +
                         2 * kAppendStages * 8;
     if (smem > 200 * 1024) return cudaErrorInvalidValue;  // more heads than the stages can hold
-    static cudaError_t attr = cudaFuncSetAttribute(kv_append_kernel<IO, KC, VC, D, NEOX>,
+    static cudaError_t attr = cudaFuncSetAttribute(kv_append_kernel<IO, KC, VC, D, NEOX, PAGED>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (attr != cudaSuccess) return attr;
     // blocks per sequence: one when a single block covers the tokens (it then also
@@ -450,7 +452,7 @@ cudaError_t launch_append(AppendParams p, cudaStream_t st) {
     int64_t gx = p.T <= kAppendStages ? 1 : std::min<int64_t>(p.T, std::max<int64_t>(1, 2 * device_sm_count() / p.B));
     p.fused_state = gx == 1 ? 1 : 0;
     dim3 grid(unsigned(gx), unsigned(p.B));
-    cudaError_t e = launch_pdl(kv_append_kernel<IO, KC, VC, D, NEOX>, grid, dim3(kThreads + 32), smem, st, p);
+    cudaError_t e = launch_pdl(kv_append_kernel<IO, KC, VC, D, NEOX, PAGED>, grid, dim3(kThreads + 32), smem, st, p);
     if (e != cudaSuccess || p.fused_state) return e;
     kv_append_state_kernel<<<(p.B + 127) / 128, 128, 0, st>>>(p);
     return cudaGetLastError();
@@ -458,11 +460,22 @@ cudaError_t launch_append(AppendParams p, cudaStream_t st) {
 
 template <typename IO, typename KC, typename VC>
 cudaError_t dispatch_append(const AppendParams& p, int D, bool neox, cudaStream_t st) {
+    // paged layers get their own instantiation, so the ring/global kernel keeps its
+    // register budget (two blocks per SM)
+    if constexpr (sizeof(KC) != 1) {
+        if (p.kind == kKindPaged) {
+            if (D == 64)
+                return neox ? launch_append<IO, KC, VC, 64, true, true>(p, st)
+                            : launch_append<IO, KC, VC, 64, false, true>(p, st);
+            return neox ? launch_append<IO, KC, VC, 128, true, true>(p, st)
+                        : launch_append<IO, KC, VC, 128, false, true>(p, st);
+        }
+    }
     if (D == 64)
-        return neox ? launch_append<IO, KC, VC, 64, true>(p, st)
-                    : launch_append<IO, KC, VC, 64, false>(p, st);
-    return neox ? launch_append<IO, KC, VC, 128, true>(p, st)
-                : launch_append<IO, KC, VC, 128, false>(p, st);
+        return neox ? launch_append<IO, KC, VC, 64, true, false>(p, st)
+                    : launch_append<IO, KC, VC, 64, false, false>(p, st);
+    return neox ? launch_append<IO, KC, VC, 128, true, false>(p, st)
+                : launch_append<IO, KC, VC, 128, false, false>(p, st);
 }
 
 }  // namespace
