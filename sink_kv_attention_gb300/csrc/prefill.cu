@@ -10,7 +10,8 @@
 // One CTA = one (sequence, query head, block of BM = 128 query rows):
 //   warps 0-3  softmax: thread r owns query row r = TMEM lane r
 //   warp 4     MMA issue (one lane)
-//   warp 5     TMA loads (one lane)
+//   warp 5     TMA loads of Q and K (one lane)
+//   warp 6     TMA loads of V^T (one lane)
 // Per key tile i (BN = 64 keys):
 //   S_i = Q K_i^T      tcgen05.mma M=128 N=64, into one of two TMEM S buffers
 //   softmax_i          tcgen05.ld S_i, mask, online max/sum in base 2 with a lazy
@@ -37,7 +38,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 64;
 constexpr int HD = 128;
-constexpr int kThreads = 6 * 32;
+constexpr int kThreads = 7 * 32;
 constexpr uint32_t kTmemCols = 256;  // S0 [0, 64), S1 [64, 128), O [128, 256)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Bounds of a learned sink logit ("Inference & 128K Long Context", "Sink clamp cache").
@@ -46,10 +47,12 @@ constexpr float kSinkLogitMax = 15.0f;
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr int SM_Q = 0;                       // Q dims 0-63 then 64-127: 2 x 16 KB
-constexpr int SM_KV = 32768;                  // 2 stages x (K lo 8 KB, K hi 8 KB, V^T 16 KB)
-constexpr int KV_STAGE = 32768;
-constexpr int SM_BAR = SM_KV + 2 * KV_STAGE;
-constexpr int N_BARS = 12;
+constexpr int SM_K = 32768;                   // 2 stages x (K lo 8 KB, K hi 8 KB)
+constexpr int K_STAGE = 16384;
+constexpr int SM_V = SM_K + 2 * K_STAGE;      // 2 stages x V^T 16 KB
+constexpr int V_STAGE = 16384;
+constexpr int SM_BAR = SM_V + 2 * V_STAGE;
+constexpr int N_BARS = 16;
 constexpr int SM_TMEM = SM_BAR + N_BARS * 8;
 constexpr int SM_BYTES = SM_TMEM + 16;
 // Two CTAs per SM fit comfortably (2 x (SM_ALLOC + 1 KB reserved) < 228 KB), with
@@ -122,11 +125,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     // two tiles old (each wait below is at most one phase behind on its barrier).
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_BAR);
     uint64_t* q_full = bars + 0;
-    uint64_t* kv_full = bars + 1;   // [2] K_i, V_i^T landed in stage i & 1
-    uint64_t* kv_empty = bars + 3;  // [2] P.V of tile i done: stage i & 1 free
-    uint64_t* s_full = bars + 5;    // [2] S_i = Q K_i^T in TMEM buffer i & 1
-    uint64_t* p_full = bars + 7;    // [2] P_i (bf16) written over S_i
-    uint64_t* pv_done = bars + 9;   // [2] O += P_i V_i done
+    uint64_t* k_full = bars + 1;    // [2] K_i landed in K stage i & 1
+    uint64_t* k_empty = bars + 3;   // [2] Q K_i^T done: K stage i & 1 free
+    uint64_t* v_full = bars + 5;    // [2] V_i^T landed in V stage i & 1
+    uint64_t* v_empty = bars + 7;   // [2] P_i V_i done: V stage i & 1 free
+    uint64_t* s_full = bars + 9;    // [2] S_i = Q K_i^T in TMEM buffer i & 1
+    uint64_t* p_full = bars + 11;   // [2] P_i (bf16) written over S_i
+    uint64_t* pv_done = bars + 13;  // [2] O += P_i V_i done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_TMEM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -141,8 +146,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], 4);
             mbar_init(&pv_done[s], 1);
@@ -160,20 +167,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool bad = false;
 
     if (warp == 5) {
-        // ------------------------------- TMA loads -------------------------------
+        // ---------------------------- TMA loads: Q, K ----------------------------
+        // K stage i & 1 is free once Q K_i^T is done, so K runs a tile ahead of V
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, 2 * BM * 128);
             tma_load_4d(smem + SM_Q, &tmQ, 0, h, q0, b, q_full);
             tma_load_4d(smem + SM_Q + BM * 128, &tmQ, 64, h, q0, b, q_full);
             for (int i = 0; i < tp.n; ++i) {
                 const int s = i & 1;
-                if (i >= 2) wait_or_flag(&kv_empty[s], ((i >> 1) - 1) & 1, bad);
+                if (i >= 2) wait_or_flag(&k_empty[s], ((i >> 1) - 1) & 1, bad);
                 const int k0 = key_tile(tp, i) * BN;
-                uint8_t* st = smem + SM_KV + s * KV_STAGE;
-                mbar_arrive_expect_tx(&kv_full[s], KV_STAGE);
-                tma_load_4d(st, &tmK, 0, g, k0, b, &kv_full[s]);
-                tma_load_4d(st + BN * 128, &tmK, 64, g, k0, b, &kv_full[s]);
-                tma_load_3d(st + 2 * BN * 128, &tmVT, k0, 0, b * p.Hkv + g, &kv_full[s]);
+                uint8_t* st = smem + SM_K + s * K_STAGE;
+                mbar_arrive_expect_tx(&k_full[s], K_STAGE);
+                tma_load_4d(st, &tmK, 0, g, k0, b, &k_full[s]);
+                tma_load_4d(st + BN * 128, &tmK, 64, g, k0, b, &k_full[s]);
+            }
+        }
+    } else if (warp == 6) {
+        // ---------------------------- TMA loads: V^T -----------------------------
+        if (lane == 0) {
+            for (int i = 0; i < tp.n; ++i) {
+                const int s = i & 1;
+                if (i >= 2) wait_or_flag(&v_empty[s], ((i >> 1) - 1) & 1, bad);
+                const int k0 = key_tile(tp, i) * BN;
+                mbar_arrive_expect_tx(&v_full[s], V_STAGE);
+                tma_load_3d(smem + SM_V + s * V_STAGE, &tmVT, k0, 0, b * p.Hkv + g, &v_full[s]);
             }
         }
     } else if (warp == 4) {
@@ -187,11 +205,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int i = 0; i <= tp.n; ++i) {
                 if (i < tp.n) {
                     const int s = i & 1;
-                    wait_or_flag(&kv_full[s], (i >> 1) & 1, bad);
+                    wait_or_flag(&k_full[s], (i >> 1) & 1, bad);
                     // S buffer s last held P_{i-2}: its P.V must be done before QK_i overwrites it
                     if (i >= 2) wait_or_flag(&pv_done[s], ((i >> 1) - 1) & 1, bad);
                     tc_fence_after_sync();
-                    const uint32_t sk = smem_u32(smem + SM_KV + s * KV_STAGE);
+                    const uint32_t sk = smem_u32(smem + SM_K + s * K_STAGE);
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         const uint32_t half = (kk >> 2);           // dims 0-63 or 64-127
@@ -201,13 +219,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                         umma_bf16(tmem + s * BN, da, db, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&s_full[s]);
+                    umma_commit(&k_empty[s]);
                 }
                 if (i >= 1) {
                     const int j = i - 1;
                     const int s = j & 1;
                     wait_or_flag(&p_full[s], (j >> 1) & 1, bad);
+                    wait_or_flag(&v_full[s], (j >> 1) & 1, bad);
                     tc_fence_after_sync();
-                    const uint32_t svt = smem_u32(smem + SM_KV + s * KV_STAGE + 2 * BN * 128);
+                    const uint32_t svt = smem_u32(smem + SM_V + s * V_STAGE);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
                         // A = P_j in TMEM: 16 keys = 8 columns of packed bf16 pairs
@@ -216,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                          (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(&pv_done[s]);
-                    umma_commit(&kv_empty[s]);
+                    umma_commit(&v_empty[s]);
                 }
             }
         }
