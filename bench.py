@@ -715,18 +715,30 @@ def bench_dynamic(args, kdt):
             "gpu_launches": args.steps * len(targets), "clocks": clocks.summary()}
 
 
-def _prefill_tiles(T, S, W, p0=0, BM=128, BN=64):
-    """Key tiles the prefill kernel visits per (sequence, head): the same plan as the
-    kernel (sink tiles below the window, then the window's tiles)."""
+def _prefill_heads_per_cta(n_rep):
+    """q heads of one GQA group packed into a prefill CTA: the largest power of two
+    dividing n_rep, at most 8 (the library's choice)."""
+    nh = 1
+    while nh < 8 and n_rep % (2 * nh) == 0:
+        nh *= 2
+    return nh
+
+
+def _prefill_tiles(T, S, W, n_rep, p0=0, BM=128, BN=64):
+    """(128-row x 64-key) tiles the prefill kernel visits per (sequence, group of nh q
+    heads), and nh: the kernel's plan (blocks of BM / nh queries of nh heads; per block
+    the sink tiles below the window, then the window's tiles)."""
+    nh = _prefill_heads_per_cta(n_rep)
+    qpb = BM // nh
     n_total = 0
-    for q0 in range(0, T, BM):
-        q_last = min(q0 + BM, T) - 1
+    for q0 in range(0, T, qpb):
+        q_last = min(q0 + qpb, T) - 1
         win_lo = max(0, q0 - W + 1) if W > 0 else 0
         first, last = win_lo // BN, q_last // BN
         sink_keys = min(T, S - p0) if (W > 0 and p0 < S) else 0
         n_sink = min(first, (sink_keys + BN - 1) // BN)
         n_total += n_sink + (last - first + 1)
-    return n_total
+    return n_total, nh
 
 
 def bench_prefill(args):
@@ -763,15 +775,16 @@ def bench_prefill(args):
     hbm = _peaks()[0]
     vis_pairs = sum(min(t + 1, S + W) for t in range(T))      # (query, key) pairs per head
     alg_flops = vis_pairs * Hq * B * 4 * D
-    tiles = _prefill_tiles(T, S, W)
-    tile_flops = tiles * Hq * B * 4 * 128 * 64 * D
+    tiles, nh = _prefill_tiles(T, S, W, Hq // Hkv)
+    tile_flops = tiles * (Hq // nh) * B * 4 * 128 * 64 * D
     append_bytes = B * T * (Hq + 2 * Hkv) * D * 2 + B * T * (Hq + Hkv) * D * 2 + B * Hkv * (S + W) * D * 2 * 2
     tf = tile_flops / (ms_attn * 1e-3) / 1e12
     return {"metric": "prefill attention TFLOP/s on visited tiles (frac of dense bf16 peak); append GB/s",
             "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_attn, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "prefill chunk: B=1, T=32768, H_q=32, H_kv=8, d_h=128, S=4, W=4092",
-                       "visited_tiles_per_head": tiles, "tile": "128 queries x 64 keys",
+                       "visited_tiles_per_head_group": tiles, "heads_per_cta": nh,
+                       "tile": f"128 rows ({nh} heads x {128 // nh} queries) x 64 keys",
                        "learned_sink_logits": bool(args.learned_sink)},
             "frac_of_bf16_peak": round(tf / bf16_peak, 4),
             "algorithmic_tflops": round(alg_flops / (ms_attn * 1e-3) / 1e12, 1),

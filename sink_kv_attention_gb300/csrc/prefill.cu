@@ -7,7 +7,8 @@
 // dense score matrix does not cut FLOPs, so here only key tiles the mask leaves (at
 // least partly) visible are visited: the sink tile(s) and the tiles of the window.
 //
-// One CTA = one (sequence, query head, block of BM = 128 query rows):
+// One CTA = one (sequence, group of nh q heads sharing a kv head, block of qpb = 128 / nh
+// queries): BM = 128 tile rows, row r = head r / qpb, query r % qpb.
 //   warps 0-3  softmax: thread r owns query row r = TMEM lane r
 //   warp 4     MMA issue (one lane)
 //   warp 5     TMA loads of Q and K (one lane)
@@ -68,7 +69,8 @@ struct PrefillParams {
     int64_t p0;
     int T, Hq, Hkv, B;
     int S, W;
-    int nqb;
+    int nqb;           // query blocks of qpb queries
+    int nh, qpb;       // q heads packed per CTA (one GQA group's), queries per block: nh * qpb = BM
     float scale_log2;  // log2(e) / sqrt(head_dim)
 };
 
@@ -80,7 +82,7 @@ struct TilePlan {
 
 __device__ __forceinline__ TilePlan plan_tiles(const PrefillParams& p, int q0) {
     TilePlan tp;
-    const int q_last = min(q0 + BM, p.T) - 1;
+    const int q_last = min(q0 + p.qpb, p.T) - 1;
     const int win_lo = p.W > 0 ? max(0, q0 - p.W + 1) : 0;
     tp.first_win = win_lo / BN;
     const int last = q_last / BN;
@@ -95,10 +97,10 @@ __device__ __forceinline__ int key_tile(const TilePlan& tp, int i) {
     return i < tp.n_sink ? i : tp.first_win + (i - tp.n_sink);
 }
 
-// Every (row, key) of the tile visible to every row of the block?
+// Every (query, key) of the tile visible to every query of the block?
 __device__ __forceinline__ bool tile_full(const PrefillParams& p, int q0, int k0) {
-    const int q_last = min(q0 + BM, p.T) - 1;
-    if (q0 + BM > p.T) return false;
+    const int q_last = min(q0 + p.qpb, p.T) - 1;
+    if (q0 + p.qpb > p.T) return false;
     if (k0 + BN - 1 > q0 || k0 + BN > p.T) return false;
     if (p.W <= 0) return true;
     return q_last - k0 < p.W || p.p0 + k0 + BN - 1 < int64_t(p.S);
@@ -135,12 +137,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_TMEM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // block -> (query block, descending so the long blocks start first; head; sequence)
+    // block -> (query block, descending so the long blocks start first; head group;
+    // sequence).  The nh heads of a group share a kv head, so each K / V tile serves
+    // nh * qpb = BM rows: row r is head h0 + r / qpb, query q0 + r % qpb.
+    const int n_hg = p.Hq / p.nh;
     const int b = blockIdx.x % p.B;
-    const int h = (blockIdx.x / p.B) % p.Hq;
-    const int qb = p.nqb - 1 - blockIdx.x / (p.B * p.Hq);
-    const int q0 = qb * BM;
-    const int g = h / (p.Hq / p.Hkv);
+    const int h0 = ((blockIdx.x / p.B) % n_hg) * p.nh;
+    const int qb = p.nqb - 1 - blockIdx.x / (p.B * n_hg);
+    const int q0 = qb * p.qpb;
+    const int g = h0 / (p.Hq / p.Hkv);
     const TilePlan tp = plan_tiles(p, q0);
 
     if (threadIdx.x == 0) {
@@ -171,8 +176,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         // K stage i & 1 is free once Q K_i^T is done, so K runs a tile ahead of V
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, 2 * BM * 128);
-            tma_load_4d(smem + SM_Q, &tmQ, 0, h, q0, b, q_full);
-            tma_load_4d(smem + SM_Q + BM * 128, &tmQ, 64, h, q0, b, q_full);
+            for (int j = 0; j < p.nh; ++j) {
+                tma_load_4d(smem + SM_Q + j * p.qpb * 128, &tmQ, 0, h0 + j, q0, b, q_full);
+                tma_load_4d(smem + SM_Q + BM * 128 + j * p.qpb * 128, &tmQ, 64, h0 + j, q0, b, q_full);
+            }
             for (int i = 0; i < tp.n; ++i) {
                 const int s = i & 1;
                 if (i >= 2) wait_or_flag(&k_empty[s], ((i >> 1) - 1) & 1, bad);
@@ -242,8 +249,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // ------------------------------- softmax ---------------------------------
-        const int r = threadIdx.x;           // 0..127: query row and TMEM lane
-        const int t = q0 + r;
+        const int r = threadIdx.x;           // 0..127: tile row and TMEM lane
+        const int h = h0 + r / p.qpb;        // its q head
+        const int t = q0 + r % p.qpb;        // its query
         const uint32_t lane_base = uint32_t(warp * 32) << 16;
         float m_run = -INFINITY, l_run = 0.0f;
         for (int i = 0; i < tp.n; ++i) {
@@ -460,12 +468,19 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     const int64_t T_pad = t_pad_of(T);
     __nv_bfloat16* vt = static_cast<__nv_bfloat16*>(workspace);
 
+    // pack the q heads of a GQA group into one CTA (a power of two dividing n_rep, at
+    // most 8): the K / V tiles are then loaded once for all of them
+    const int nrep = n_q_heads / n_kv_heads;
+    int nh = 1;
+    while (nh < 8 && nrep % (2 * nh) == 0) nh *= 2;
+    const int qpb = BM / nh;
+
     CUtensorMap mq, mk, mvt;
     {
         const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_q_heads), cuuint64_t(T), cuuint64_t(batch)};
         const cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(n_q_heads) * HD * 2,
                                        cuuint64_t(T) * n_q_heads * HD * 2};
-        const cuuint32_t box[4] = {64, 1, BM, 1};
+        const cuuint32_t box[4] = {64, 1, cuuint32_t(qpb), 1};
         SK_RET_IF(!make_map(&mq, q_rot, 4, dims, strides, box), SK_ERR_CUDA);
     }
     {
@@ -504,9 +519,11 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     p.B = batch;
     p.S = sinks;
     p.W = window;
-    p.nqb = (T + BM - 1) / BM;
+    p.nh = nh;
+    p.qpb = qpb;
+    p.nqb = (T + qpb - 1) / qpb;
     p.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
-    const int64_t grid = int64_t(p.nqb) * n_q_heads * batch;
+    const int64_t grid = int64_t(p.nqb) * (n_q_heads / nh) * batch;
     prefill_attn_kernel<<<unsigned(grid), kThreads, SM_ALLOC, st>>>(mq, mk, mvt, p);
     SK_CUDA_RET(cudaGetLastError());
     return SK_OK;

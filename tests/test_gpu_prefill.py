@@ -29,8 +29,19 @@ def sk():
     (1, 4, 16, 0),        # one token
 ])
 def test_prefill_matches_oracle_all_rows(sk, T, S, W, p0):
+    _prefill_case(sk, T, S, W, p0, 4, 2)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 1), (6, 2), (16, 2)])
+def test_prefill_head_packing(sk, Hq, Hkv):
+    """q heads of a GQA group packed into one CTA: 1 (MHA), 8 (16 queries per block),
+    n_rep = 3 (no packing possible beyond 1), 8 of 8."""
+    _prefill_case(sk, 300, 4, 100, 0, Hq, Hkv)
+
+
+def _prefill_case(sk, T, S, W, p0, Hq, Hkv):
     from sink_kv_attention_gb300 import synth
-    B, Hq, Hkv, D = 2, 4, 2, 128
+    B, D = 2, 128
     q = synth.normal((B, T, Hq, D), 60, torch.bfloat16).cuda()
     k = synth.normal((B, T, Hkv, D), 61, torch.bfloat16).cuda()
     v = synth.normal((B, T, Hkv, D), 62, torch.bfloat16).cuda()
