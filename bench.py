@@ -799,9 +799,9 @@ def bench_prefill(args):
 # CPU oracle baseline (single thread, in a subprocess)
 # ---------------------------------------------------------------------------
 
-def cpu_oracle_window(n_seq: int, seed_base: int = 0):
-    """Time the float64 oracle on n_seq sequences of the windowed decode step
-    (RoPE + append + attention) and return (seconds, kv_bytes)."""
+def cpu_oracle_window(n_seq: int, seed_base: int = 0, first: int = 0):
+    """Time the float64 oracle on sequences first .. first + n_seq - 1 of the windowed
+    decode step (RoPE + append + attention) and return (seconds, kv_bytes)."""
     import numpy as np
     import torch
     from oracle.sinkkv_oracle import RingCache, RopeSpec, decode_attention, rope_rotate
@@ -812,7 +812,7 @@ def cpu_oracle_window(n_seq: int, seed_base: int = 0):
     spec = RopeSpec(D, c["r"], c["theta"])
     omega = spec.omega()
     total = 0.0
-    for b in range(n_seq):
+    for b in range(first, first + n_seq):
         kb = synth.normal((Hkv, S + W, D), 1000 + b, torch.bfloat16).double().numpy()
         vb = synth.normal((Hkv, S + W, D), 2000 + b, torch.bfloat16).double().numpy()
         q = synth.normal((1, Hq, D), 3000 + b, torch.bfloat16).double().numpy()
@@ -837,6 +837,61 @@ def _cpu_worker(n_seq):
     print(json.dumps({"secs": secs, "kv_bytes": kv}))
 
 
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def _cpu_mt_part(args):
+    """One process of the all-cores oracle run: sequences [lo, hi) of the step."""
+    lo, hi = args
+    os.environ.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    secs = 0.0
+    for b in range(lo, hi):
+        secs += cpu_oracle_window_one(b)
+    return secs
+
+
+def cpu_oracle_window_one(b: int) -> float:
+    """Oracle seconds for sequence b of the windowed decode step."""
+    return cpu_oracle_window(1, seed_base=0, first=b)[0]
+
+
+def _cpu_worker_mt(n_seq):
+    import multiprocessing as mp
+    n = os.cpu_count() or 1
+    parts = [(n_seq * i // n, n_seq * (i + 1) // n) for i in range(n)]
+    parts = [x for x in parts if x[1] > x[0]]
+    with mp.get_context("spawn").Pool(len(parts)) as pool:
+        secs = pool.map(_cpu_mt_part, parts)
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    kv = n_seq * c["Hkv"] * (c["S"] + c["W"]) * c["D"] * 2 * 2
+    print(json.dumps({"secs": max(secs), "kv_bytes": kv, "procs": len(parts)}))
+
+
+def cpu_baseline_all_cores(n_seq=32):
+    """The same oracle sample spread over every host core (one process per core): the
+    parallel time is the slowest process's oracle time."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker-mt", str(n_seq)],
+                       capture_output=True, text=True, env=env, timeout=600)
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    gbs = d["kv_bytes"] / d["secs"] / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": d["procs"], "kind": "oracle",
+            "cpu": _cpu_model(),
+            "sample": f"{n_seq} of 32 sequences of one windowed decode step over {d['procs']} processes "
+                      f"(float64 numpy, one thread each, slowest process {d['secs']:.2f} s)"}
+
+
 def cpu_baseline(n_seq=32):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
@@ -844,7 +899,7 @@ def cpu_baseline(n_seq=32):
                        capture_output=True, text=True, env=env, timeout=600)
     d = json.loads(r.stdout.strip().splitlines()[-1])
     gbs = d["kv_bytes"] / d["secs"] / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": _cpu_model(),
             "sample": f"{n_seq} of 32 sequences of one windowed decode step (float64 numpy, "
                       f"single thread, {d['secs']:.2f} s)"}
 
@@ -863,6 +918,7 @@ def main():
                     choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill", "dynamic_bf16",
                              "dynamic_i8", "shift_bf16", "shift_i8", "paged"])
     ap.add_argument("--cpu-worker", type=int, default=0)
+    ap.add_argument("--cpu-worker-mt", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--learned-sink", action="store_true",
@@ -872,6 +928,9 @@ def main():
 
     if args.cpu_worker:
         _cpu_worker(args.cpu_worker)
+        return
+    if args.cpu_worker_mt:
+        _cpu_worker_mt(args.cpu_worker_mt)
         return
 
     rank = int(os.environ.get("RANK", "0"))
@@ -931,6 +990,10 @@ def main():
                 result["cpu_baseline"] = cpu_baseline()
             except Exception as e:  # reported, never fatal
                 result["cpu_baseline"] = {"value": None, "error": str(e)[:200]}
+            try:
+                result["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
+            except Exception as e:  # reported, never fatal
+                result["cpu_baseline_all_cores"] = {"value": None, "error": str(e)[:200]}
         print(json.dumps(result))
     if world_ > 1:
         import torch.distributed as dist
