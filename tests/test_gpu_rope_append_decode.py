@@ -326,3 +326,40 @@ def test_hybrid_layers_full_size_sampled(sk):
             want = o_decode(cache, qr[0])
             assert float(np.abs(out[b] - want).max()) <= BF16_ATTN_ATOL
         assert L.error_bits() == 0
+
+
+def test_decode_maximum_batch(sk):
+    """The largest batch the decode kernels take (1024 sequences; the unit prefix scan
+    runs 32 rounds), ragged lengths incl. empty rings; sampled sequences against the
+    oracle, and 1025 sequences rejected on the host."""
+    from sink_kv_attention_gb300 import synth
+    B, Hq, Hkv, D, S, W = 1024, 4, 1, 64, 2, 30
+    layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W)
+    synth.fill_normal_(layer.k, 91)
+    synth.fill_normal_(layer.v, 92)
+    lens = synth.randint((B,), 93, 0, 60)
+    rings = []
+    for b in range(B):
+        rc = RingCache(S, W)
+        rc.append(list(range(int(lens[b]))))
+        rings.append(rc)
+    layer.pos.copy_(torch.tensor([rc.pos for rc in rings]))
+    layer.head.copy_(torch.tensor([rc.head for rc in rings], dtype=torch.int32))
+    layer.count.copy_(torch.tensor([rc.count for rc in rings], dtype=torch.int32))
+    q = synth.normal((B, Hq, D), 94, torch.bfloat16).cuda()
+    out = f64(sk.decode_attention(layer, q))
+    k_in, v_in = f64(layer.k), f64(layer.v)
+    empty = [b for b in range(B) if int(lens[b]) == 0]
+    assert empty and all(not out[b].any() for b in empty)
+    for b in [0, 1, 31, 32, 33, 511, 512, 777, 1022, 1023] + [b for b in range(B) if int(lens[b]) == 1][:3]:
+        rc = rings[b]
+        if rc.pos == 0:
+            continue
+        keys = np.stack([k_in[b][:, s] for s in rc.chronological_slots()])
+        vals = np.stack([v_in[b][:, s] for s in rc.chronological_slots()])
+        from oracle.sinkkv_oracle import attend
+        np.testing.assert_allclose(out[b], attend(f64(q[b]), keys, vals), rtol=0, atol=BF16_ATTN_ATOL)
+    big = sk.KVLayer.allocate(sk.SK_LAYER_RING, 1025, 1, D, sinks=S, window=W)
+    with pytest.raises(sk.SinkKVError) as e:
+        sk.decode_attention(big, torch.zeros(1025, Hq, D, dtype=torch.bfloat16, device="cuda"))
+    assert e.value.status == sk.SK_ERR_UNSUPPORTED
