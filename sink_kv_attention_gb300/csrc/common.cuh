@@ -68,16 +68,6 @@ template <> struct ElemIO<__nv_bfloat16> {
 // int8 codes (symmetric, one fp32 scale per row).
 // ---------------------------------------------------------------------------
 
-// Four int8 codes of a word -> four exact floats: bias each byte to unsigned, place it
-// under the exponent of 2^23 with one byte permute, subtract 2^23 + 128.
-__device__ __forceinline__ void codes4_to_float(uint32_t w, float* f) {
-    const uint32_t u = w ^ 0x80808080u;
-    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.0f;
-    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.0f;
-    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.0f;
-    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.0f;
-}
-
 // Codes of four values: rint(x * inv), rint half to even, for |x| <= max|x| of the row
 // and inv = 127 / max|x| (so |x * inv| < 127.5 and the code lies in [-127, 127]).
 // Adding 1.5 * 2^23 to a value of magnitude below 2^22 rounds it to the nearest
@@ -161,16 +151,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > 1000000000ull) return false;
     }
-}
-
-// Per-thread asynchronous 16-byte copy global -> shared (cp.async).  The issuing thread
-// sees the data after cp_async_wait<N>() has retired its group.
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // L2 policy: data streamed once (evict first).
