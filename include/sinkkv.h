@@ -437,6 +437,15 @@ SK_API sk_status sk_kv_shift_recent(const sk_kv_layer* layers, int32_t n_layers,
 
 /* ---- Misc ------------------------------------------------------------------------ */
 
+/* Read a device error word after the work queued on `stream` (synchronises it).
+ * *bits_out (may be NULL) gets the SK_DEVERR_* bits; with clear != 0 the word is reset
+ * to zero afterwards.  Returns SK_OK when no bit is set, else the status of the most
+ * specific condition: SK_ERR_CAPACITY, SK_ERR_POSITION_RANGE, SK_ERR_ARG (a paged block
+ * id outside the pool), SK_ERR_CUDA (a bounded in-kernel wait gave up), in that order.
+ * [MIXED] "KV-Cache Engineering", 4.6: a cache overflow fails loudly, never by silent
+ * truncation; this is how a C caller hears it. */
+SK_API sk_status sk_sync_check(uint32_t* err, int32_t clear, void* stream, uint32_t* bits_out);
+
 /* A static, human-readable name for a status code. */
 SK_API const char* sk_status_str(sk_status status);
 

@@ -261,7 +261,7 @@ def rerotate_int8(codes: np.ndarray, scale: np.ndarray, positions: Sequence[int]
 
 class CapacityError(RuntimeError):
     """A global-layer append past its capacity: a loud error, never a truncation
-    ("KV-Cache Engineering", 4.6 and 6: "The 4M cap is a loud cliff")."""
+    ("KV-Cache Engineering", 4.6 and 6: hitting the context cap fails loudly)."""
 
 
 class RingCache:

@@ -115,6 +115,8 @@ _SIGNATURES = [
                                                  ctypes.c_size_t, ctypes.c_void_p]),
     ("sk_kv_shift_recent", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32, ctypes.c_void_p,
                                           ctypes.c_int32, ctypes.c_void_p]),
+    ("sk_sync_check", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                     ctypes.POINTER(ctypes.c_uint32)]),
     ("sk_status_str", ctypes.c_char_p, [ctypes.c_int]),
     ("sk_version", ctypes.c_int32, []),
 ]
@@ -575,6 +577,13 @@ def kv_shift_recent(layers: Sequence[KVLayer], table: RopeTable, delta: int, str
     arr = (KVLayerStruct * max(1, len(layers)))(*[L.struct() for L in layers])
     _check(_lib().sk_kv_shift_recent(arr, len(layers), table.handle, int(delta), _stream(stream)),
            "sk_kv_shift_recent")
+
+
+def sync_check(err: torch.Tensor, clear: bool = False, stream=None):
+    """(status, bits) of a device error word after the queued work (sk_sync_check)."""
+    bits = ctypes.c_uint32()
+    st = _lib().sk_sync_check(_ptr(err), 1 if clear else 0, _stream(stream), ctypes.byref(bits))
+    return int(st), int(bits.value)
 
 
 def version() -> int:

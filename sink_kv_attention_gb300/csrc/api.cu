@@ -31,4 +31,22 @@ extern "C" const char* sk_status_str(sk_status status) {
     }
 }
 
+extern "C" sk_status sk_sync_check(uint32_t* err, int32_t clear, void* stream, uint32_t* bits_out) {
+    SK_RET_IF(err == nullptr, SK_ERR_ARG);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t bits = 0;
+    SK_CUDA_RET(cudaMemcpyAsync(&bits, err, sizeof(bits), cudaMemcpyDeviceToHost, st));
+    SK_CUDA_RET(cudaStreamSynchronize(st));
+    if (clear && bits != 0) {
+        SK_CUDA_RET(cudaMemsetAsync(err, 0, sizeof(uint32_t), st));
+        SK_CUDA_RET(cudaStreamSynchronize(st));
+    }
+    if (bits_out != nullptr) *bits_out = bits;
+    if (bits & SK_DEVERR_CAPACITY) return SK_ERR_CAPACITY;
+    if (bits & SK_DEVERR_POSITION_RANGE) return SK_ERR_POSITION_RANGE;
+    if (bits & SK_DEVERR_BLOCK_TABLE) return SK_ERR_ARG;
+    if (bits & SK_DEVERR_TIMEOUT) return SK_ERR_CUDA;
+    return SK_OK;
+}
+
 extern "C" int32_t sk_version(void) { return 200; }

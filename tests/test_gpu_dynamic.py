@@ -2,7 +2,7 @@
 does"): the factor follows the dialog's length, every cached key is turned on a switch
 and the live table is rebuilt in place.  The page's chain of seven switches
 1 -> 1.125 -> 1.25 -> 1.5 -> 1.625 -> 1.75 -> 1.875 -> 2 is driven by a growing
-dialog and compared with the float64 oracle's keys at factor 2."""
+dialog and checked against the float64 oracle's keys at factor 2."""
 import numpy as np
 import pytest
 import torch

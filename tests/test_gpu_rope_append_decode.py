@@ -221,6 +221,26 @@ def test_global_capacity_overflow_is_flagged(sk):
     assert int(layer.pos[0]) == 6 and torch.equal(layer.k, before)
 
 
+def test_sync_check_reports_and_clears_device_errors(sk):
+    """sk_sync_check: no bits -> SK_OK; a global overflow -> SK_ERR_CAPACITY with the
+    bit, cleared on request; a position past the table -> SK_ERR_POSITION_RANGE."""
+    D = 64
+    tbl = sk.RopeTable(D, D, 1e4, 8)
+    layer = sk.KVLayer.allocate(sk.SK_LAYER_GLOBAL, 1, 1, D, capacity=4, k_dtype=torch.float32,
+                                v_dtype=torch.float32)
+    mk = lambda T: torch.randn(1, T, 1, D, device="cuda")
+    sk.kv_append(tbl, layer, None, mk(3), mk(3))
+    assert sk.sync_check(layer.err) == (sk.SK_OK, 0)
+    sk.kv_append(tbl, layer, None, mk(2), mk(2))           # 3 + 2 > 4
+    assert sk.sync_check(layer.err, clear=True) == (sk.SK_ERR_CAPACITY, sk.SK_DEVERR_CAPACITY)
+    assert sk.sync_check(layer.err) == (sk.SK_OK, 0)
+    ring = sk.KVLayer.allocate(sk.SK_LAYER_RING, 1, 1, D, sinks=1, window=20, k_dtype=torch.float32,
+                               v_dtype=torch.float32)
+    sk.kv_append(tbl, ring, None, mk(9), mk(9))           # positions 0..8, table holds 8
+    st, bits = sk.sync_check(ring.err)
+    assert st == sk.SK_ERR_POSITION_RANGE and bits & sk.SK_DEVERR_POSITION_RANGE
+
+
 def test_append_position_past_table_is_flagged(sk):
     D = 64
     tbl = sk.RopeTable(D, D, 1e4, 4)
