@@ -171,6 +171,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_s
         : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (a hint: no completion, no data returned).
+// Address 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gmem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem_src), "r"(bytes) : "memory");
+}
+
 // 2^x with the hardware approximation (ex2.approx.ftz.f32): -inf -> +0.
 __device__ __forceinline__ float fast_exp2_approx(float x) {
     float y;
