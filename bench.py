@@ -30,13 +30,13 @@ if ROOT not in sys.path:
 METRIC = "sink+window decode attn KV-read GB/s (frac of HBM peak), tokens/s, keys/s"
 
 
-def _profiled_traffic():
-    """DRAM bytes per launch of the split-K decode kernel from the committed ncu summary,
+def _profiled_traffic(summary="decode_split_window_b32.md"):
+    """DRAM bytes per launch of the split-K decode kernel from a committed ncu summary,
     or None when the kernel sources changed since that capture."""
     import hashlib
     import re
     try:
-        with open(os.path.join(ROOT, "profiles", "decode_split_window_b32.md")) as f:
+        with open(os.path.join(ROOT, "profiles", summary)) as f:
             text = f.read()
         m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
         pairs = re.findall(r"(\w+\.cuh?) sha256 ([0-9a-f]{64})", text)
@@ -629,7 +629,8 @@ def bench_paged(args):
                        "l2": f"inputs larger than L2 (KV {kv_bytes / 1e6:.0f} MB per step)"},
             "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
-                         "frac": round(achieved / hbm, 4), "traffic": None,
+                         "frac": round(achieved / hbm, 4),
+                         "traffic": _profiled_traffic("paged_decode_window_b32_bs16.md"),
                          "kernel": "paged decode attention (split-K + combine), per launch",
                          "algorithmic_bytes_per_launch": alg_decode, "launch_ms": round(dec_ms, 5),
                          "peak_source": f"{peak_kind} hbm_gbs"},

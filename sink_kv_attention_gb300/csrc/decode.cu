@@ -120,6 +120,22 @@ struct UnitWalk {
     }
 };
 
+// Tiles of a paged unit start where the key index is a multiple of the tile height (a
+// power of two), so that a tile spans as few blocks as possible: each block piece costs
+// two bulk copies, and small copies, not bytes, limit a gather of 16-token blocks.
+// Returns the row residue (mod tile) at which this request's tiles start.
+__device__ __forceinline__ int64_t tile_phase(const DecodeParams& p, int b, int tile) {
+    const int64_t n_req = p.pos[b];
+    const int64_t Lk = n_req > 0 ? n_req + p.sink_len : 0;
+    if (!(p.W > 0 && Lk > int64_t(p.S) + p.W)) return 0;  // rows are keys
+    return (int64_t(p.S) - (Lk - p.W)) & (tile - 1);       // row S holds key Lk - W
+}
+
+// End of the paged tile that starts at row0.
+__device__ __forceinline__ int64_t tile_end(int64_t row0, int64_t r1, int64_t phase, int tile) {
+    return min(r1, row0 + tile - ((row0 - phase) & (tile - 1)));
+}
+
 // Consumer warps per block: 8 unless two stages of K+V tiles would not fit.
 template <typename T, int D, int NREP> constexpr int decode_warps() {
     constexpr int warp_stage_bytes = 2 * (4 * (8 / NREP)) * D * int(sizeof(T));
@@ -137,6 +153,7 @@ template <typename T, int D, int NREP> struct DecodeCfg {
     static constexpr int RPG = 8 / NREP;              // rows per 8-lane group
     static constexpr int RPW = 4 * RPG;               // rows per warp per stage
     static constexpr int TILE = NWARPS * RPW;         // rows per stage
+    static_assert((TILE & (TILE - 1)) == 0, "tile height must be a power of two");
     static constexpr int DPV = D / 32;                // dims per lane (PV)
     static constexpr int ROW_BYTES = D * int(sizeof(T));
     static constexpr int STAGE_BYTES = 2 * TILE * ROW_BYTES;   // K tile then V tile
@@ -215,8 +232,10 @@ __device__ __forceinline__ void paged_producer(const DecodeParams& p, const int6
         // a table read per tile.
         int64_t cbase = -64;
         int32_t cval = -1;
-        for (int64_t row = r0; row < r1; row += C::TILE) {
-            const int64_t n = min(int64_t(C::TILE), r1 - row);
+        const int64_t tph = tile_phase(p, b, C::TILE);
+        for (int64_t row = r0, row_end; row < r1; row = row_end) {
+            row_end = tile_end(row, r1, tph, C::TILE);
+            const int64_t n = row_end - row;
             if (lane == 0) {
                 if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1)) timed_out = true;
                 mbar_arrive_expect_tx(&full_bar[stage], 2u * uint32_t(n) * C::ROW_BYTES);
@@ -315,7 +334,10 @@ __device__ __forceinline__ void prefetch_share(const DecodeParams& p, const int6
     } while (w.next());
 }
 
-template <typename T, int D, int NREP>
+// PAGED selects the block-table producer and key-aligned tiles.  The two layouts are
+// separate instantiations: the contiguous kernel then carries none of the paged code
+// (compiled into one kernel, the contiguous path measured 3-5% slower).
+template <typename T, int D, int NREP, bool PAGED>
 __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
     decode_split_kernel(DecodeParams p) {
     using C = DecodeCfg<T, D, NREP>;
@@ -338,7 +360,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
         }
         fence_barrier_init();
     }
-    if (warp == NWARPS && p.kind != kKindPaged && kPrefetchRows > 0) {
+    if (!PAGED && warp == NWARPS && kPrefetchRows > 0) {
         // While the append before this kernel runs, the memory system is idle: warm L2
         // with the first rows of this block's share, split by the state as it reads now.
         // The append changes at most one row per unit and, on a full ring, no length, so
@@ -362,9 +384,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
     if (lo >= hi) return;
     bool timed_out = false;
 
-    if (warp == NWARPS && p.kind == kKindPaged) {
-        paged_producer<C, T, D>(p, pre, lo, hi, stages, full_bar, empty_bar, lane);
-        return;
+    if constexpr (PAGED) {
+        if (warp == NWARPS) {
+            paged_producer<C, T, D>(p, pre, lo, hi, stages, full_bar, empty_bar, lane);
+            return;
+        }
     }
     if (warp == NWARPS) {
         // ------------------------------ producer ------------------------------
@@ -448,8 +472,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
 #pragma unroll
             for (int d = 0; d < C::DPV / 2; ++d) acc[h][d] = make_float2(0.f, 0.f);
 
-        for (int64_t row0 = r0; row0 < r1; row0 += C::TILE) {
-            const int n = int(min(int64_t(C::TILE), r1 - row0));
+        const int64_t tph = PAGED ? tile_phase(p, b, C::TILE) : 0;
+        int n = 0;
+        for (int64_t row0 = r0; row0 < r1; row0 += PAGED ? n : C::TILE) {
+            const int skip = PAGED ? int((row0 - tph) & (C::TILE - 1)) : 0;
+            n = int(min(int64_t(C::TILE - skip), r1 - row0));
             if (!mbar_wait_bounded(&full_bar[stage], phase)) timed_out = true;
             const T* ktile = reinterpret_cast<const T*>(stages + size_t(stage) * C::STAGE_BYTES);
             const T* vtile = ktile + C::TILE * D;
@@ -663,17 +690,23 @@ template <typename T, int D, int NREP>
 struct DecodeLaunch {
     using C = DecodeCfg<T, D, NREP>;
 
+    // Both instantiations (contiguous and paged) get the shared-memory limit; the grid is
+    // sized from the smaller occupancy of the two.
     static int blocks_per_sm() {
         static int cached = -1;
         if (cached < 0) {
-            int n = 0;
-            if (cudaFuncSetAttribute(decode_split_kernel<T, D, NREP>,
+            int n0 = 0, n1 = 0;
+            if (cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM)) != cudaSuccess ||
+                cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM)) != cudaSuccess)
                 return 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<T, D, NREP>, C::THREADS,
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, decode_split_kernel<T, D, NREP, false>, C::THREADS,
+                                                              C::SMEM) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, decode_split_kernel<T, D, NREP, true>, C::THREADS,
                                                               C::SMEM) != cudaSuccess)
                 return 0;
-            cached = n;
+            cached = std::min(n0, n1);
         }
         return cached;
     }
@@ -687,7 +720,11 @@ struct DecodeLaunch {
     static cudaError_t run(DecodeParams p, const sk_kv_layer& L, cudaStream_t st) {
         if (blocks_per_sm() < 1) return cudaErrorInvalidConfiguration;
         p.n_blocks = grid();
-        cudaError_t e = launch_pdl(decode_split_kernel<T, D, NREP>, dim3(p.n_blocks), dim3(C::THREADS), C::SMEM, st, p);
+        cudaError_t e = p.kind == kKindPaged
+                            ? launch_pdl(decode_split_kernel<T, D, NREP, true>, dim3(p.n_blocks), dim3(C::THREADS),
+                                         C::SMEM, st, p)
+                            : launch_pdl(decode_split_kernel<T, D, NREP, false>, dim3(p.n_blocks), dim3(C::THREADS),
+                                         C::SMEM, st, p);
         if (e != cudaSuccess) return e;
         const int warps = L.batch * L.n_kv_heads * NREP;
         return launch_pdl(decode_combine_kernel<T, D, NREP>, dim3((warps + 7) / 8), dim3(256), 0, st, p);

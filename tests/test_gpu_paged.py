@@ -129,6 +129,11 @@ CASES = [
     (torch.float32, 64, 64, 4, 2, 8, 2, 37, 0, [3, 90, 301], [3, 87, 211]),
     (torch.bfloat16, 128, 128, 4, 4, 32, 0, 0, 0, [40, 129, 300], [40, 89, 171]),      # full attention
     (torch.bfloat16, 128, 128, 8, 2, 4, 4, 50, 2, [7, 200], [7, 193]),                # 4-token blocks
+    # blocks as tall as the kernel's tile and taller: tiles start at key multiples of the
+    # tile height inside a block, the window starts anywhere
+    (torch.bfloat16, 128, 128, 8, 2, 64, 4, 130, 1, [64, 65, 500], [64, 1, 435]),
+    (torch.bfloat16, 128, 128, 8, 2, 128, 4, 301, 0, [300, 777, 1025], [300, 477, 248]),
+    (torch.bfloat16, 128, 64, 4, 1, 256, 2, 517, 1, [513, 1100], [513, 587]),
 ]
 
 
