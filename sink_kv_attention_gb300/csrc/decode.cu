@@ -232,7 +232,12 @@ __device__ __forceinline__ void paged_producer(const DecodeParams& p, const int6
         // a table read per tile.
         int64_t cbase = -64;
         int32_t cval = -1;
+        int64_t nbase = -64;  // the next 32 entries, loaded ahead (nbase == cbase + 32 when valid)
+        int32_t cnext = -1;
         const int64_t tph = tile_phase(p, b, C::TILE);
+        // blocks in a full aligned tile (0: no fast path, blocks taller than a tile or more
+        // blocks than lanes)
+        const int64_t nb = (bs <= C::TILE && (C::TILE >> lg) <= 32) ? C::TILE >> lg : 0;
         for (int64_t row = r0, row_end; row < r1; row = row_end) {
             row_end = tile_end(row, r1, tph, C::TILE);
             const int64_t n = row_end - row;
@@ -242,6 +247,42 @@ __device__ __forceinline__ void paged_producer(const DecodeParams& p, const int6
             }
             __syncwarp();
             uint8_t* dst = stages + size_t(stage) * C::STAGE_BYTES;
+            // Fast path: a full tile of window (or unsplit) keys starting on a block boundary
+            // is exactly nb whole blocks, block j for lane j.
+            const int64_t kfirst = (split && row >= p.S) ? wstart + (row - p.S) : row;
+            if (nb > 0 && n == C::TILE && (!split || row >= p.S) && kfirst >= p.sink_len &&
+                (kfirst & (bs - 1)) == 0) {
+                const int64_t jb0 = (kfirst - p.sink_len) >> lg;
+                if (jb0 < cbase || jb0 + nb > cbase + 32) {
+                    if (nbase == cbase + 32 && jb0 >= nbase && jb0 + nb <= nbase + 32) {
+                        cbase = nbase;
+                        cval = cnext;
+                    } else {
+                        cbase = jb0;
+                        cval = cbase + lane < p.max_blocks ? trow[cbase + lane] : -1;
+                    }
+                }
+                if (jb0 + nb > cbase + 16 && nbase != cbase + 32) {  // load the next entries ahead
+                    nbase = cbase + 32;
+                    cnext = nbase + lane < p.max_blocks ? trow[nbase + lane] : -1;
+                }
+                const int32_t cached = __shfl_sync(kFull, cval, int(jb0 - cbase + lane) & 31);
+                if (lane < nb) {
+                    int64_t blk = cached;
+                    if (blk < 0 || blk >= p.pool_blocks) {
+                        bad = true;
+                        blk = 0;  // stay inside the pool; the error word reports it
+                    }
+                    const int64_t src = (blk * p.Hkv + g) * bs * D;
+                    const uint32_t bytes = uint32_t(bs) * C::ROW_BYTES;
+                    const int64_t drow = int64_t(lane) << lg;
+                    bulk_copy_g2s(dst + drow * C::ROW_BYTES, kpool + src, bytes, &full_bar[stage], policy);
+                    bulk_copy_g2s(dst + (C::TILE + drow) * C::ROW_BYTES, vpool + src, bytes, &full_bar[stage],
+                                  policy);
+                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                continue;
+            }
             // run piece 1: rows [row, e1), keys = rows; piece 2: rows [a2, row + n),
             // keys [k2a, k2b) = wstart + (rows - S)
             const int64_t e1 = split ? min(row + n, int64_t(p.S)) : row + n;
