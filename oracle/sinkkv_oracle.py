@@ -504,6 +504,45 @@ def prefill_attention(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray, p0: i
     return np.stack(out)
 
 
+def prefill_attention_prior(q_rot: np.ndarray, k_rot: np.ndarray, v: np.ndarray, prior,
+                            sinks: int, window: Optional[int],
+                            rows: Optional[Sequence[int]] = None,
+                            sink_logits: Optional[Sequence[float]] = None) -> np.ndarray:
+    """Masked attention of a prompt chunk that continues a cached sequence.
+
+    ``prior`` is the sequence's RingCache or GlobalCache before the chunk (rows are
+    (k_rot, v) pairs [H_kv, D]); the chunk starts at p0 = prior.pos.  Query t (position
+    P = p0 + t) attends over the keys the cache still holds together with chunk keys
+    0..t, keeping those ``mask_allows(P, position, S, W)`` admits.  "KV-Cache
+    Engineering", 5.5: the chunk's rotated keys are appended to the cache and the
+    queries attend over what the cache returns; the mask places query t at key index
+    t + (T_k - T_q), which covers a multi-token chunk over a cached prefix.
+
+    A key that the mask admits but the cache has dropped is an error: the cache must
+    have been built with the same sinks and window.
+    """
+    T = q_rot.shape[0]
+    p0 = prior.pos
+    cached_pos = list(prior.chronological_positions())
+    cached = list(prior.chronological_rows())
+    pos_all = cached_pos + [p0 + k for k in range(T)]
+    k_all = [np.asarray(r[0], dtype=np.float64) for r in cached] + [k_rot[k] for k in range(T)]
+    v_all = [np.asarray(r[1], dtype=np.float64) for r in cached] + [v[k] for k in range(T)]
+    have = set(cached_pos)
+    if rows is None:
+        rows = range(T)
+    out = []
+    for t in rows:
+        P = p0 + t
+        for k in range(p0):
+            if mask_allows(P, k, sinks, window) and k not in have:
+                raise ValueError(f"position {k}, visible from {P}, is not in the prior cache")
+        ks = [i for i, pk in enumerate(pos_all) if mask_allows(P, pk, sinks, window)]
+        out.append(attend(q_rot[t], np.stack([k_all[i] for i in ks]), np.stack([v_all[i] for i in ks]),
+                          sink_logits))
+    return np.stack(out)
+
+
 # ---------------------------------------------------------------------------
 # O6b. Paged caches: block tables with static sink blocks.
 # ---------------------------------------------------------------------------
