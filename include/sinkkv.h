@@ -58,6 +58,7 @@ typedef enum { SK_LAYER_RING = 0, SK_LAYER_GLOBAL = 1 } sk_layer_kind;
 #define SK_DEVERR_CAPACITY       0x2u  /* a global-layer append past capacity was skipped */
 #define SK_DEVERR_TIMEOUT        0x4u  /* a bounded in-kernel wait gave up (never expected) */
 #define SK_DEVERR_BLOCK_TABLE    0x8u  /* a paged block id outside [0, n_blocks) was met  */
+#define SK_DEVERR_STATE          0x10u /* a prefill's prior cache did not hold its prefix */
 
 /*
  * Rotary configuration.  [RoPE] "Let d_h be the head dimension, r <= d_h the rotary
@@ -347,29 +348,48 @@ SK_API sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const voi
 
 /* ---- Prefill attention (causal + window + sinks) ---------------------------------- */
 
-/* Workspace bytes sk_prefill_attention needs (a transposed copy of V); 0 for an
- * unsupported shape. */
-SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim);
+/* Keys a chunk starting at position p0 takes from a prior cache: with window > 0 the
+ * first s0 = min(sinks, p0) positions and then the last min(window - 1, p0 - s0)
+ * positions before p0 (all its queries can see); with window <= 0 all p0 of them.
+ * -1 for p0 < 0 or sinks < 0. */
+SK_API int64_t sk_prefill_prior_keys(int64_t p0, int32_t sinks, int32_t window);
 
-/* Masked attention of a prompt chunk over itself on the tensor cores.
+/* Workspace bytes sk_prefill_attention needs: a transposed copy of the keys' V, and
+ * with prior_keys > 0 (sk_prefill_prior_keys of a call that passes a prior) a
+ * combined copy of the prior's and the chunk's keys.  0 for an unsupported shape. */
+SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim,
+                                         int64_t prior_keys);
+
+/* Masked attention of a prompt chunk on the tensor cores, over the chunk itself and,
+ * optionally, over the keys a prior cache holds for the same sequences.
  *   q_rot: [batch][T][n_q_heads][head_dim], k_rot, v: [batch][T][n_kv_heads][head_dim],
  *   out: [batch][T][n_q_heads][head_dim]; all SK_BF16, device, 16-byte aligned.
  *   sink_logits: NULL, or device float32 [n_q_heads] learned sinks, as for
  *   sk_decode_attention (clamped to [-10, 15], denominator only).
- * Chunk index t has absolute position p0 + t.  Query t sees key k iff k <= t and
- * (p0 + k < sinks or t - k < window) ([MIXED] 5.5: idx_q >= idx_k and
- * idx_q - idx_k < window; [SINK] sink + recent).  window <= 0 means a global layer
+ * Chunk index t has absolute position p0 + t.  A query at position P sees a key at
+ * position k iff k <= P and (k < sinks or P - k < window) ([MIXED] 5.5: idx_q >= idx_k
+ * and idx_q - idx_k < window; [SINK] sink + recent).  window <= 0 means a global layer
  * (causal only).  Only key tiles the mask leaves at least partly visible are visited.
  * q head h reads kv head h / (n_q_heads / n_kv_heads).
- *   workspace: device, >= sk_prefill_workspace_bytes(...) bytes, 16-byte aligned, no
+ *   prior: NULL, or the layer whose cache holds positions [0, p0) of every sequence
+ *   (pos[b] == p0; the chunk has not been appended yet).  The keys before p0 come
+ *   from it ([MIXED] 5.5: a multi-token chunk over a cached prefix, query index offset
+ *   by T_k - T_q).  Without a prior, keys before p0 are not seen.  A ring prior must
+ *   have the call's sinks and window (window > 0) and a count of
+ *   min(window, p0 - min(sinks, p0)), as appends through this library leave it; a
+ *   global prior needs p0 <= capacity (SK_ERR_CAPACITY otherwise).  K and V bf16, same batch, n_kv_heads and head_dim.
+ *   A device state that does not match p0 sets SK_DEVERR_STATE in *err; the result
+ *   is then undefined, and every read stays inside the cache.
+ *   workspace: device, >= sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim,
+ *   prior ? sk_prefill_prior_keys(p0, sinks, window) : 0) bytes, 16-byte aligned, no
  *   initialisation needed.  err: device error word (SK_DEVERR_TIMEOUT if a bounded
- *   in-kernel wait gave up), may be NULL.
- * Supported: head_dim 128, SK_BF16. */
+ *   in-kernel wait gave up, SK_DEVERR_STATE as above), may be NULL.
+ * Supported: head_dim 128, SK_BF16, T + prior keys <= 2^30. */
 SK_API sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
                                       int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                      int64_t p0, int32_t sinks, int32_t window, const float* sink_logits,
-                                      void* out, void* workspace, size_t ws_bytes, uint32_t* err,
-                                      void* stream);
+                                      int64_t p0, int32_t sinks, int32_t window, const sk_kv_layer* prior,
+                                      const float* sink_logits, void* out, void* workspace, size_t ws_bytes,
+                                      uint32_t* err, void* stream);
 
 /* ---- Cached-key rerotation on a factor change ------------------------------------ */
 
@@ -441,7 +461,8 @@ SK_API sk_status sk_kv_shift_recent(const sk_kv_layer* layers, int32_t n_layers,
  * *bits_out (may be NULL) gets the SK_DEVERR_* bits; with clear != 0 the word is reset
  * to zero afterwards.  Returns SK_OK when no bit is set, else the status of the most
  * specific condition: SK_ERR_CAPACITY, SK_ERR_POSITION_RANGE, SK_ERR_ARG (a paged block
- * id outside the pool), SK_ERR_CUDA (a bounded in-kernel wait gave up), in that order.
+ * id outside the pool, or a prefill's prior cache state that did not match its p0),
+ * SK_ERR_CUDA (a bounded in-kernel wait gave up), in that order.
  * [MIXED] "KV-Cache Engineering", 4.6: a cache overflow fails loudly, never by silent
  * truncation; this is how a C caller hears it. */
 SK_API sk_status sk_sync_check(uint32_t* err, int32_t clear, void* stream, uint32_t* bits_out);

@@ -33,6 +33,7 @@ SK_OK, SK_ERR_ARG, SK_ERR_CAPACITY, SK_ERR_POSITION_RANGE, SK_ERR_UNSUPPORTED, S
 SK_BF16, SK_F32, SK_I8 = 0, 1, 2
 SK_LAYER_RING, SK_LAYER_GLOBAL = 0, 1
 SK_DEVERR_POSITION_RANGE, SK_DEVERR_CAPACITY, SK_DEVERR_TIMEOUT, SK_DEVERR_BLOCK_TABLE = 1, 2, 4, 8
+SK_DEVERR_STATE = 16
 
 
 class SinkKVError(RuntimeError):
@@ -98,10 +99,13 @@ _SIGNATURES = [
                                            ctypes.c_void_p]),
     ("sk_decode_attention_noalloc", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32,
                                                    ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
-    ("sk_prefill_workspace_bytes", ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    ("sk_prefill_prior_keys", ctypes.c_int64, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
+    ("sk_prefill_workspace_bytes", ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                     ctypes.c_int64]),
     ("sk_prefill_attention", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.POINTER(KVLayerStruct), ctypes.c_void_p,
                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                             ctypes.c_void_p]),
     ("sk_kv_rerotate", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32, ctypes.c_void_p,
@@ -445,29 +449,42 @@ def decode_attention_noalloc(layer: KVLayer, q_rot: torch.Tensor, out: torch.Ten
     return out
 
 
-def prefill_workspace_bytes(batch: int, T: int, n_kv_heads: int, head_dim: int) -> int:
-    return int(_lib().sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim))
+def prefill_prior_keys(p0: int, sinks: int, window: int) -> int:
+    """Keys a chunk starting at p0 takes from a prior cache (sk_prefill_prior_keys)."""
+    n = int(_lib().sk_prefill_prior_keys(int(p0), int(sinks), int(window)))
+    if n < 0:
+        raise SinkKVError(SK_ERR_ARG, "sk_prefill_prior_keys")
+    return n
+
+
+def prefill_workspace_bytes(batch: int, T: int, n_kv_heads: int, head_dim: int, prior_keys: int = 0) -> int:
+    return int(_lib().sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim, int(prior_keys)))
 
 
 def prefill_attention(q_rot: torch.Tensor, k_rot: torch.Tensor, v: torch.Tensor, p0: int, sinks: int,
                       window: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                       err: Optional[torch.Tensor] = None, stream=None,
-                      sink_logits: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Masked prefill attention of a chunk over itself: q [B,T,Hq,D], k/v [B,T,Hkv,D]
+                      sink_logits: Optional[torch.Tensor] = None,
+                      prior: Optional["KVLayer"] = None) -> torch.Tensor:
+    """Masked prefill attention of a chunk: q [B,T,Hq,D], k/v [B,T,Hkv,D]
     (sk_prefill_attention); window <= 0 is a global layer; optional learned per-head
-    sink logits (float32 [Hq])."""
+    sink logits (float32 [Hq]); ``prior``: the layer whose cache holds positions
+    [0, p0) of every sequence (the chunk not yet appended), whose keys the chunk then
+    also sees."""
     _need_contig(q_rot, k_rot, v)
     B, T, Hq, D = q_rot.shape
     Hkv = k_rot.shape[2]
     if out is None:
         out = torch.empty_like(q_rot)
-    need = prefill_workspace_bytes(B, T, Hkv, D)
+    prior_keys = prefill_prior_keys(p0, sinks, window) if prior is not None else 0
+    need = prefill_workspace_bytes(B, T, Hkv, D, prior_keys)
     if need == 0:
         raise SinkKVError(SK_ERR_UNSUPPORTED, "sk_prefill_workspace_bytes")
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q_rot.device)
+    ps = ctypes.byref(prior.struct()) if prior is not None else None
     _check(_lib().sk_prefill_attention(_ptr(q_rot), _ptr(k_rot), _ptr(v), B, T, Hq, Hkv, D, int(p0), int(sinks),
-                                       int(window), _sink_logits(sink_logits, Hq), _ptr(out), _ptr(workspace),
+                                       int(window), ps, _sink_logits(sink_logits, Hq), _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)),
            "sk_prefill_attention")
     return out

@@ -44,7 +44,7 @@ extern "C" sk_status sk_sync_check(uint32_t* err, int32_t clear, void* stream, u
     if (bits_out != nullptr) *bits_out = bits;
     if (bits & SK_DEVERR_CAPACITY) return SK_ERR_CAPACITY;
     if (bits & SK_DEVERR_POSITION_RANGE) return SK_ERR_POSITION_RANGE;
-    if (bits & SK_DEVERR_BLOCK_TABLE) return SK_ERR_ARG;
+    if (bits & (SK_DEVERR_BLOCK_TABLE | SK_DEVERR_STATE)) return SK_ERR_ARG;
     if (bits & SK_DEVERR_TIMEOUT) return SK_ERR_CUDA;
     return SK_OK;
 }

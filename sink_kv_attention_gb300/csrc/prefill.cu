@@ -62,13 +62,16 @@ constexpr int SM_BYTES = SM_TMEM + 16;
 constexpr int SM_ALLOC = SM_BYTES + 1024;
 static_assert(SM_ALLOC >= SM_BYTES + 896, "no room to align the shared-memory base");
 
+// Queries and keys live in one index space: query t is key index t + qoff (the
+// chunk's own key), keys [0, qoff) come from a prior cache.  Key j is visible to
+// query t iff j <= t + qoff and (j < nsk or t + qoff - j < W).
 struct PrefillParams {
     void* out;
     const float* sink_logits;  // [Hq] learned sinks or null
     uint32_t* err;
-    int64_t p0;
     int T, Hq, Hkv, B;
-    int S, W;
+    int Tk, qoff;              // keys in the key buffer; key index of query 0
+    int nsk, W;                // leading sink keys; window (<= 0: global)
     int nqb;           // query blocks of qpb queries
     int nh, qpb;       // q heads packed per CTA (one GQA group's), queries per block: nh * qpb = BM
     float scale_log2;  // log2(e) / sqrt(head_dim)
@@ -82,12 +85,11 @@ struct TilePlan {
 
 __device__ __forceinline__ TilePlan plan_tiles(const PrefillParams& p, int q0) {
     TilePlan tp;
-    const int q_last = min(q0 + p.qpb, p.T) - 1;
-    const int win_lo = p.W > 0 ? max(0, q0 - p.W + 1) : 0;
+    const int q_last = min(q0 + p.qpb, p.T) - 1 + p.qoff;  // in key index space
+    const int win_lo = p.W > 0 ? max(0, q0 + p.qoff - p.W + 1) : 0;
     tp.first_win = win_lo / BN;
     const int last = q_last / BN;
-    int sink_keys = 0;
-    if (p.W > 0 && p.p0 < p.S) sink_keys = int(min(int64_t(p.T), int64_t(p.S) - p.p0));
+    const int sink_keys = p.W > 0 ? min(p.Tk, p.nsk) : 0;
     tp.n_sink = min(tp.first_win, (sink_keys + BN - 1) / BN);
     tp.n = tp.n_sink + (last - tp.first_win + 1);
     return tp;
@@ -99,11 +101,11 @@ __device__ __forceinline__ int key_tile(const TilePlan& tp, int i) {
 
 // Every (query, key) of the tile visible to every query of the block?
 __device__ __forceinline__ bool tile_full(const PrefillParams& p, int q0, int k0) {
-    const int q_last = min(q0 + p.qpb, p.T) - 1;
+    const int q_last = min(q0 + p.qpb, p.T) - 1 + p.qoff;
     if (q0 + p.qpb > p.T) return false;
-    if (k0 + BN - 1 > q0 || k0 + BN > p.T) return false;
+    if (k0 + BN - 1 > q0 + p.qoff || k0 + BN > p.Tk) return false;
     if (p.W <= 0) return true;
-    return q_last - k0 < p.W || p.p0 + k0 + BN - 1 < int64_t(p.S);
+    return q_last - k0 < p.W || k0 + BN - 1 < p.nsk;
 }
 
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, bool& bad) {
@@ -270,9 +272,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < 64; ++j) sc[j] = __uint_as_float(raw[j]);
             if (!full) {
                 // key k0 + j visible iff j <= jmax and (j >= jwin or j < jsink): branch-free
-                const int jmax = min(t, p.T - 1) - k0;
-                const int jwin = p.W > 0 ? t - p.W + 1 - k0 : -(1 << 30);
-                const int jsink = p.W > 0 ? int(max(int64_t(-(1 << 30)), int64_t(p.S) - p.p0 - k0)) : -(1 << 30);
+                const int tq = min(t, p.T - 1) + p.qoff;  // the query's own key index
+                const int jmax = tq - k0;
+                const int jwin = p.W > 0 ? tq - p.W + 1 - k0 : -(1 << 30);
+                const int jsink = p.W > 0 ? p.nsk - k0 : -(1 << 30);
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
                     const bool vis = (j <= jmax) && (j >= jwin || j < jsink);
@@ -381,19 +384,82 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-// v [B][T][Hkv][D] -> vt [B*Hkv][D][T_pad], 64 x 64 tiles through shared memory.
+// The keys a chunk takes from a prior cache, in order: the first s0 positions (sink
+// slots, or the prefix of a global layer), then the last cr positions before p0 (the
+// newest cr entries of the ring in chronological order, or the global rows at those
+// positions).  Key index j < s0 + cr of the combined key buffer is prior row j.  A
+// ring at position p0 holds ring_count = min(W, p0 - s0) entries; the chunk needs
+// the newest cr <= ring_count of them.
+struct PriorView {
+    const __nv_bfloat16* k;  // [B][Hkv][cap][HD]
+    const __nv_bfloat16* v;
+    const int32_t* head;
+    const int32_t* count;
+    const int64_t* pos;
+    int64_t cap, p0;
+    int kind, S, W;  // the layer's kind, sinks and window
+    int s0, cr, ring_count;
+};
+
+// Cache slot of prior row j of sequence b; always inside [0, cap), whatever the state.
+__device__ __forceinline__ int64_t prior_slot(const PriorView& pv, int b, int j) {
+    if (j < pv.s0) return j;
+    const int r = j - pv.s0;
+    if (pv.kind == SK_LAYER_GLOBAL) return pv.p0 - pv.cr + r;
+    // ring: chronological entry cnt - cr + r of the cnt the ring holds
+    const int cnt = min(max(pv.count[b], 0), pv.W);
+    const int hd = ((pv.head[b] % pv.W) + pv.W) % pv.W;
+    const int ci = min(max(cnt - pv.cr + r, 0), pv.W - 1);
+    return pv.S + (cnt == pv.W ? (hd + ci) % pv.W : ci);
+}
+
+// Combined keys kc [B][Tk][Hkv][HD]: prior rows, then the chunk's k [B][T][Hkv][HD].
+// One thread per 16 bytes.  The thread of (b, j = 0, g = 0, c = 0) checks that the
+// prior's state matches the chunk's start (pos = p0; a ring holds cr recent entries).
+__global__ void __launch_bounds__(256) gather_keys_kernel(PriorView pv, const __nv_bfloat16* __restrict__ k,
+                                                          __nv_bfloat16* __restrict__ kc, int B, int T, int Tk,
+                                                          int Hkv, uint32_t* err) {
+    constexpr int CH = HD / 8;  // 16-byte chunks per row
+    const int qoff = pv.s0 + pv.cr;
+    const int64_t total = int64_t(B) * Tk * Hkv * CH;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int c = int(i % CH);
+        const int g = int((i / CH) % Hkv);
+        const int64_t bj = i / (int64_t(CH) * Hkv);
+        const int j = int(bj % Tk), b = int(bj / Tk);
+        const __nv_bfloat16* src;
+        if (j < qoff) {
+            src = pv.k + ((int64_t(b) * Hkv + g) * pv.cap + prior_slot(pv, b, j)) * HD;
+            if (j == 0 && g == 0 && c == 0) {
+                const bool ok = pv.pos[b] == pv.p0 && (pv.kind == SK_LAYER_GLOBAL || pv.count[b] == pv.ring_count);
+                if (!ok) set_error(err, SK_DEVERR_STATE);
+            }
+        } else {
+            src = k + ((int64_t(b) * T + (j - qoff)) * Hkv + g) * HD;
+        }
+        reinterpret_cast<uint4*>(kc + (bj * Hkv + g) * HD)[c] = reinterpret_cast<const uint4*>(src)[c];
+    }
+}
+
+// v [B][T][Hkv][D] -> vt [B*Hkv][D][Tk_pad], 64 x 64 tiles through shared memory.  With
+// a prior (PRIOR), key index t < qoff reads prior row t and t >= qoff chunk row t - qoff.
+template <bool PRIOR>
 __global__ void __launch_bounds__(256) transpose_v_kernel(const __nv_bfloat16* __restrict__ v,
-                                                          __nv_bfloat16* __restrict__ vt, int T, int T_pad,
-                                                          int Hkv) {
+                                                          __nv_bfloat16* __restrict__ vt, int T, int Tk,
+                                                          int T_pad, int Hkv, PriorView pv) {
     __shared__ __nv_bfloat16 tile[64][66];
     const int t0 = blockIdx.x * 64, d0 = blockIdx.y * 64, bg = blockIdx.z;
     const int b = bg / Hkv, g = bg % Hkv;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int qoff = PRIOR ? pv.s0 + pv.cr : 0;
     for (int i = ty; i < 64; i += 8) {
         const int t = t0 + i;
-        if (t < T) {
-            const __nv_bfloat162 x =
-                *reinterpret_cast<const __nv_bfloat162*>(v + ((int64_t(b) * T + t) * Hkv + g) * HD + d0 + 2 * tx);
+        if (t < Tk) {
+            const __nv_bfloat16* row =
+                PRIOR && t < qoff ? pv.v + ((int64_t(b) * Hkv + g) * pv.cap + prior_slot(pv, b, t)) * HD
+                                  : v + ((int64_t(b) * T + (t - qoff)) * Hkv + g) * HD;
+            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(row + d0 + 2 * tx);
             tile[i][2 * tx] = x.x;
             tile[i][2 * tx + 1] = x.y;
         }
@@ -402,10 +468,10 @@ __global__ void __launch_bounds__(256) transpose_v_kernel(const __nv_bfloat16* _
     for (int i = ty; i < 64; i += 8) {
         const int d = d0 + i;
         const int t = t0 + 2 * tx;
-        if (t < T) {
+        if (t < Tk) {
             __nv_bfloat162 y;
             y.x = tile[2 * tx][i];
-            y.y = t + 1 < T ? tile[2 * tx + 1][i] : __float2bfloat16(0.0f);
+            y.y = t + 1 < Tk ? tile[2 * tx + 1][i] : __float2bfloat16(0.0f);
             *reinterpret_cast<__nv_bfloat162*>(vt + (int64_t(bg) * HD + d) * T_pad + t) = y;
         }
     }
@@ -442,16 +508,47 @@ int64_t t_pad_of(int T) { return (int64_t(T) + 63) / 64 * 64; }
 
 using namespace sk;
 
-extern "C" size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim) {
-    if (batch < 1 || T < 1 || n_kv_heads < 1 || head_dim != HD) return 0;
-    return size_t(batch) * n_kv_heads * HD * t_pad_of(T) * sizeof(__nv_bfloat16);
+namespace sk {
+namespace {
+
+// (s0, cr) of a chunk starting at p0: the sinks it sees, then the recent keys before
+// p0 its first query still sees (W - 1 of them: a query's window includes itself);
+// all of the prefix for a global attention (window <= 0).
+void prior_split(int64_t p0, int32_t sinks, int32_t window, int64_t* s0, int64_t* cr) {
+    if (window <= 0) {
+        *s0 = 0;
+        *cr = p0;
+    } else {
+        *s0 = std::min<int64_t>(sinks, p0);
+        *cr = std::min<int64_t>(int64_t(window) - 1, p0 - *s0);
+    }
+}
+
+}  // namespace
+}  // namespace sk
+
+extern "C" int64_t sk_prefill_prior_keys(int64_t p0, int32_t sinks, int32_t window) {
+    if (p0 < 0 || sinks < 0) return -1;
+    int64_t s0 = 0, cr = 0;
+    prior_split(p0, sinks, window, &s0, &cr);
+    return s0 + cr;
+}
+
+extern "C" size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim,
+                                             int64_t prior_keys) {
+    if (batch < 1 || T < 1 || n_kv_heads < 1 || head_dim != HD || prior_keys < 0) return 0;
+    const int64_t Tk = int64_t(T) + prior_keys;
+    if (Tk > (int64_t(1) << 30)) return 0;
+    size_t bytes = size_t(batch) * n_kv_heads * HD * t_pad_of(int(Tk)) * sizeof(__nv_bfloat16);  // V^T
+    if (prior_keys > 0) bytes += size_t(batch) * Tk * n_kv_heads * HD * sizeof(__nv_bfloat16);    // keys
+    return bytes;
 }
 
 extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
                                           int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                          int64_t p0, int32_t sinks, int32_t window, const float* sink_logits,
-                                          void* out, void* workspace, size_t ws_bytes, uint32_t* err,
-                                          void* stream) {
+                                          int64_t p0, int32_t sinks, int32_t window, const sk_kv_layer* prior,
+                                          const float* sink_logits, void* out, void* workspace, size_t ws_bytes,
+                                          uint32_t* err, void* stream) {
     SK_RET_IF(q_rot == nullptr || k_rot == nullptr || v == nullptr || out == nullptr || workspace == nullptr,
               SK_ERR_ARG);
     SK_RET_IF(batch < 1 || T < 0 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads != 0, SK_ERR_ARG);
@@ -462,11 +559,45 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
                          reinterpret_cast<uintptr_t>(workspace);
     SK_RET_IF(al & 15u, SK_ERR_ARG);
     SK_RET_IF(reinterpret_cast<uintptr_t>(sink_logits) & 3u, SK_ERR_ARG);
+    PriorView pv{};
+    int64_t qoff = 0;
+    if (prior != nullptr) {
+        const sk_kv_layer& L = *prior;
+        SK_RET_IF(L.k == nullptr || L.v == nullptr || L.pos == nullptr, SK_ERR_ARG);
+        SK_RET_IF(L.k_dtype != SK_BF16 || L.v_dtype != SK_BF16, SK_ERR_UNSUPPORTED);
+        SK_RET_IF(L.batch != batch || L.n_kv_heads != n_kv_heads || L.head_dim != head_dim, SK_ERR_ARG);
+        SK_RET_IF((reinterpret_cast<uintptr_t>(L.k) | reinterpret_cast<uintptr_t>(L.v)) & 15u, SK_ERR_ARG);
+        int64_t s0 = 0, cr = 0;
+        prior_split(p0, sinks, window, &s0, &cr);
+        if (L.kind == SK_LAYER_RING) {
+            // the ring must keep exactly the keys the chunk's mask admits
+            SK_RET_IF(L.head == nullptr || L.count == nullptr, SK_ERR_ARG);
+            SK_RET_IF(window <= 0 || L.sinks != sinks || L.window != window ||
+                          L.capacity != int64_t(L.sinks) + L.window,
+                      SK_ERR_ARG);
+        } else {
+            SK_RET_IF(L.kind != SK_LAYER_GLOBAL || L.capacity < 1, SK_ERR_ARG);
+            SK_RET_IF(p0 > L.capacity, SK_ERR_CAPACITY);
+        }
+        qoff = s0 + cr;
+        const int64_t ring_count = window > 0 ? std::min<int64_t>(window, p0 - s0) : 0;
+        pv = PriorView{static_cast<const __nv_bfloat16*>(L.k), static_cast<const __nv_bfloat16*>(L.v), L.head,
+                       L.count, L.pos, L.capacity, p0, L.kind, L.sinks, L.window, int(s0), int(cr),
+                       int(ring_count)};
+    }
     if (T == 0) return SK_OK;
-    SK_RET_IF(ws_bytes < sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim), SK_ERR_ARG);
+    const int64_t Tk64 = int64_t(T) + qoff;
+    SK_RET_IF(Tk64 > (int64_t(1) << 30), SK_ERR_UNSUPPORTED);
+    const size_t need = sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim, qoff);
+    SK_RET_IF(need == 0 || ws_bytes < need, SK_ERR_ARG);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int64_t T_pad = t_pad_of(T);
+    const int Tk = int(Tk64);
+    const int64_t T_pad = t_pad_of(Tk);
     __nv_bfloat16* vt = static_cast<__nv_bfloat16*>(workspace);
+    // keys: the chunk's own, or (with a prior) the combined buffer after V^T
+    const void* keys = k_rot;
+    __nv_bfloat16* kc = vt + size_t(batch) * n_kv_heads * HD * T_pad;
+    if (qoff > 0) keys = kc;
 
     // pack the q heads of a GQA group into one CTA (a power of two dividing n_rep, at
     // most 8): the K / V tiles are then loaded once for all of them
@@ -484,21 +615,33 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
         SK_RET_IF(!make_map(&mq, q_rot, 4, dims, strides, box), SK_ERR_CUDA);
     }
     {
-        const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_kv_heads), cuuint64_t(T), cuuint64_t(batch)};
+        const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_kv_heads), cuuint64_t(Tk), cuuint64_t(batch)};
         const cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(n_kv_heads) * HD * 2,
-                                       cuuint64_t(T) * n_kv_heads * HD * 2};
+                                       cuuint64_t(Tk) * n_kv_heads * HD * 2};
         const cuuint32_t box[4] = {64, 1, BN, 1};
-        SK_RET_IF(!make_map(&mk, k_rot, 4, dims, strides, box), SK_ERR_CUDA);
+        SK_RET_IF(!make_map(&mk, keys, 4, dims, strides, box), SK_ERR_CUDA);
     }
     {
-        const cuuint64_t dims[3] = {cuuint64_t(T), cuuint64_t(HD), cuuint64_t(batch) * n_kv_heads};
+        const cuuint64_t dims[3] = {cuuint64_t(Tk), cuuint64_t(HD), cuuint64_t(batch) * n_kv_heads};
         const cuuint64_t strides[2] = {cuuint64_t(T_pad) * 2, cuuint64_t(HD) * T_pad * 2};
         const cuuint32_t box[3] = {BN, HD, 1};
         SK_RET_IF(!make_map(&mvt, vt, 3, dims, strides, box), SK_ERR_CUDA);
     }
 
-    dim3 tgrid(unsigned((T + 63) / 64), HD / 64, unsigned(batch * n_kv_heads));
-    transpose_v_kernel<<<tgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(v), vt, T, int(T_pad), n_kv_heads);
+    if (qoff > 0) {
+        const int64_t threads = int64_t(batch) * Tk * n_kv_heads * (HD / 8);
+        const int64_t blocks = std::min<int64_t>((threads + 255) / 256, int64_t(device_sm_count()) * 16);
+        gather_keys_kernel<<<unsigned(blocks), 256, 0, st>>>(pv, static_cast<const __nv_bfloat16*>(k_rot), kc,
+                                                            batch, T, Tk, n_kv_heads, err);
+        SK_CUDA_RET(cudaGetLastError());
+    }
+    dim3 tgrid(unsigned((Tk + 63) / 64), HD / 64, unsigned(batch * n_kv_heads));
+    if (qoff > 0)
+        transpose_v_kernel<true><<<tgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(v), vt, T, Tk,
+                                                        int(T_pad), n_kv_heads, pv);
+    else
+        transpose_v_kernel<false><<<tgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(v), vt, T, Tk,
+                                                         int(T_pad), n_kv_heads, pv);
     SK_CUDA_RET(cudaGetLastError());
 
     static std::once_flag attr_once;
@@ -512,13 +655,18 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     p.out = out;
     p.sink_logits = sink_logits;
     p.err = err;
-    p.p0 = p0;
     p.T = T;
+    p.Tk = Tk;
+    p.qoff = int(qoff);
+    // sinks in key index space: without a prior, chunk key k has position p0 + k; with
+    // one, the combined buffer starts with the positions 0 .. s0-1 (all of the sinks
+    // when the ring has dropped keys, else positions equal indices)
+    p.nsk = window > 0 ? int(std::min<int64_t>(Tk, std::max<int64_t>(0, qoff > 0 ? sinks : int64_t(sinks) - p0)))
+                       : 0;
+    p.W = window;
     p.Hq = n_q_heads;
     p.Hkv = n_kv_heads;
     p.B = batch;
-    p.S = sinks;
-    p.W = window;
     p.nh = nh;
     p.qpb = qpb;
     p.nqb = (T + qpb - 1) / qpb;

@@ -89,7 +89,7 @@ def test_bad_arguments_rejected_on_host(lib):
     assert lib.sk_kv_append(None, None, None, 0, None, None, 0, 1, None) == sk.SK_ERR_ARG
     assert lib.sk_decode_attention(None, None, 8, 0, None, None, None, 0, None) == sk.SK_ERR_ARG
     assert lib.sk_decode_attention_noalloc(None, None, 8, 0, None, None, None) == sk.SK_ERR_ARG
-    assert lib.sk_prefill_attention(None, None, None, 1, 1, 1, 1, 128, 0, 0, 0, None, None, None, 0, None,
+    assert lib.sk_prefill_attention(None, None, None, 1, 1, 1, 1, 128, 0, 0, 0, None, None, None, None, 0, None,
                                     None) == sk.SK_ERR_ARG
     assert lib.sk_decode_workspace_bytes(None, 8) == 0
     assert lib.sk_kv_rerotate(None, 1, None, None, None) == sk.SK_ERR_ARG
@@ -101,3 +101,45 @@ def test_bad_arguments_rejected_on_host(lib):
     assert lib.sk_paged_decode_workspace_bytes(ctypes.byref(bad), 1) == 0
     assert lib.sk_kv_shift_recent(None, 1, None, -1, None) == sk.SK_ERR_ARG
     lib.sk_rope_table_destroy(None)  # NULL is ignored
+
+
+def test_prefill_prior_keys_are_exactly_the_old_keys_a_chunk_sees(lib):
+    """sk_prefill_prior_keys(p0, S, W) is the number of positions before p0 that any
+    query of a chunk starting at p0 may see under the oracle's mask (its first query
+    sees the most); window <= 0 is a global layer (all of them)."""
+    from oracle.sinkkv_oracle import mask_allows
+    for p0 in range(0, 40):
+        for S in (0, 1, 4):
+            for W in (0, 1, 2, 7, 16):
+                want = sum(1 for k in range(p0) if mask_allows(p0, k, S, W if W > 0 else None))
+                assert lib.sk_prefill_prior_keys(p0, S, W) == want, (p0, S, W)
+    assert lib.sk_prefill_prior_keys(-1, 4, 8) == -1
+    assert lib.sk_prefill_prior_keys(5, -1, 8) == -1
+
+
+def test_prefill_workspace_and_prior_arguments_checked_on_host(lib):
+    import sink_kv_attention_gb300 as sk
+    # V^T for T (+ prior keys), padded to 64 keys, plus the combined keys with a prior
+    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 0) == 2 * 8 * 128 * 128 * 2
+    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 30) == 2 * 8 * 128 * 192 * 2 + 2 * 130 * 8 * 128 * 2
+    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, -1) == 0
+    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 64, 0) == 0
+    fake = 1 << 20  # aligned, never dereferenced: every case below fails before a launch
+
+    def prior(kind=sk.SK_LAYER_RING, k_dtype=sk.SK_BF16, sinks=4, window=60, capacity=64):
+        return sk.KVLayerStruct(kind, k_dtype, sk.SK_BF16, 2, 8, 128, sinks, window, capacity, fake, fake, None,
+                                fake, fake, fake, None)
+
+    def call(pr, p0=100, sinks=4, window=60, ws=1 << 30):
+        return lib.sk_prefill_attention(fake, fake, fake, 2, 100, 32, 8, 128, p0, sinks, window,
+                                        ctypes.byref(pr), None, fake, fake, ws, None, None)
+
+    assert call(prior(window=61)) == sk.SK_ERR_ARG                        # ring window differs
+    assert call(prior(sinks=2)) == sk.SK_ERR_ARG                          # ring sinks differ
+    assert call(prior(), window=0) == sk.SK_ERR_ARG                       # ring under a global mask
+    assert call(prior(k_dtype=sk.SK_I8)) == sk.SK_ERR_UNSUPPORTED         # int8 keys
+    assert call(prior(kind=sk.SK_LAYER_GLOBAL, capacity=99), window=0) == sk.SK_ERR_CAPACITY
+    assert call(prior(), ws=1000) == sk.SK_ERR_ARG                        # workspace too small
+    bad = prior()
+    bad.batch = 3
+    assert call(bad) == sk.SK_ERR_ARG                                     # batch differs
