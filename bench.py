@@ -758,18 +758,21 @@ def _prefill_heads_per_cta(n_rep):
     return nh
 
 
-def _prefill_tiles(T, S, W, n_rep, p0=0, BM=128, BN=64):
+def _prefill_tiles(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64):
     """(128-row x 64-key) tiles the prefill kernel visits per (sequence, group of nh q
     heads), and nh: the kernel's plan (blocks of BM / nh queries of nh heads; per block
-    the sink tiles below the window, then the window's tiles)."""
+    the sink tiles below the window, then the window's tiles).  qoff > 0: a chunk over
+    a prior cache, whose qoff keys come first (the leading S of them sinks)."""
     nh = _prefill_heads_per_cta(n_rep)
     qpb = BM // nh
     n_total = 0
+    Tk = T + qoff
+    nsk = S if qoff > 0 else max(0, S - p0)
     for q0 in range(0, T, qpb):
-        q_last = min(q0 + qpb, T) - 1
-        win_lo = max(0, q0 - W + 1) if W > 0 else 0
+        q_last = min(q0 + qpb, T) - 1 + qoff
+        win_lo = max(0, q0 + qoff - W + 1) if W > 0 else 0
         first, last = win_lo // BN, q_last // BN
-        sink_keys = min(T, S - p0) if (W > 0 and p0 < S) else 0
+        sink_keys = min(Tk, nsk) if W > 0 else 0
         n_sink = min(first, (sink_keys + BN - 1) // BN)
         n_total += n_sink + (last - first + 1)
     return n_total, nh
@@ -827,6 +830,56 @@ def bench_prefill(args):
             "append_frac_of_hbm_peak": round(append_bytes / (ms_append * 1e-3) / 1e9 / hbm, 4),
             "peak_source": f"{peak_kind} bf16_tflops {bf16_peak} / hbm_gbs {hbm}",
             "gpu_launches": args.steps * 2, "clocks": clk}
+
+
+def bench_prefill_chunk(args):
+    """A later chunk of a long prompt: B=1, T=8192 new tokens at p0=32768 attending over
+    the full, wrapped ring a first chunk left (S=4, W=4092) and over themselves;
+    H_q=32, H_kv=8, d_h=128, bf16.  One step = the prior-key gather, the V transpose
+    and the attention (sk_prefill_attention with a prior)."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.PREFILL
+    B, Hq, Hkv, D, S, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    T, p0 = 8192, 32768
+    layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W)
+    synth.fill_normal_(layer.k, 66)
+    synth.fill_normal_(layer.v, 67)
+    layer.pos.fill_(p0)
+    layer.count.fill_(W)
+    layer.head.fill_(1234)
+    q = synth.normal((B, T, Hq, D), 68, torch.bfloat16, device="cuda")
+    k = synth.normal((B, T, Hkv, D), 69, torch.bfloat16, device="cuda")
+    v = synth.normal((B, T, Hkv, D), 70, torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    qoff = sk.prefill_prior_keys(p0, S, W)
+    ws = torch.empty(sk.prefill_workspace_bytes(B, T, Hkv, D, qoff), dtype=torch.uint8, device="cuda")
+    zl = _learned_sinks(args, Hq)
+
+    def attend(i):
+        sk.prefill_attention(q, k, v, p0, S, W, out=out, workspace=ws, err=layer.err, sink_logits=zl, prior=layer)
+
+    ms, clk = _timed(attend, args.steps, args.warmup)
+    assert layer.error_bits() == 0
+    _, bf16_peak, _, peak_kind = _peaks()
+    alg_flops = T * (S + W) * Hq * B * 4 * D          # every query sees S + W keys here
+    tiles, nh = _prefill_tiles(T, S, W, Hq // Hkv, qoff=qoff)
+    tile_flops = tiles * (Hq // nh) * B * 4 * 128 * 64 * D
+    tf = tile_flops / (ms * 1e-3) / 1e12
+    return {"metric": "chunked prefill attention over a prior ring, TFLOP/s on visited tiles (frac of dense bf16 "
+                      "peak)",
+            "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "prompt chunk over a prior ring: B=1, T=8192 at p0=32768, H_q=32, H_kv=8, "
+                                   "d_h=128, S=4, W=4092 (ring full, wrapped)",
+                       "prior_keys": qoff, "visited_tiles_per_head_group": tiles, "heads_per_cta": nh,
+                       "learned_sink_logits": bool(args.learned_sink)},
+            "frac_of_bf16_peak": round(tf / bf16_peak, 4),
+            "algorithmic_tflops": round(alg_flops / (ms * 1e-3) / 1e12, 1),
+            "algorithmic_flops": alg_flops, "tile_flops": tile_flops,
+            "peak_source": f"{peak_kind} bf16_tflops {bf16_peak}",
+            "gpu_launches": args.steps * 3, "clocks": clk}
 
 
 # ---------------------------------------------------------------------------
@@ -959,8 +1012,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="window",
-                    choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill", "dynamic_bf16",
-                             "dynamic_i8", "shift_bf16", "shift_i8", "paged"])
+                    choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill", "prefill_chunk",
+                             "dynamic_bf16", "dynamic_i8", "shift_bf16", "shift_i8", "paged"])
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--cpu-worker-mt", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
@@ -1018,6 +1071,8 @@ def main():
                 print(json.dumps(bench_hybrid(args)))
             elif args.workload == "prefill":
                 print(json.dumps(bench_prefill(args)))
+            elif args.workload == "prefill_chunk":
+                print(json.dumps(bench_prefill_chunk(args)))
             elif args.workload.startswith("dynamic"):
                 print(json.dumps(bench_dynamic(args, args.workload.split("_")[1])))
             elif args.workload == "paged":
