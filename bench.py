@@ -640,7 +640,9 @@ def bench_paged(args):
 def bench_shift(args, kdt):
     """Local-position window slide: the recent keys of the windowed decode workload's
     cache (B=32, H_kv=8, d_h=r=128, S=4, W=4092, every ring full) turned by one
-    position per step (alternately -1 and +1 so the keys stay put), sinks untouched."""
+    position per step (alternately -1 and +1 so the keys stay put), sinks untouched.
+    --layers N turns N such layers in one call (a model slides all its windowed layers
+    at once); default 1."""
     import torch
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
@@ -648,31 +650,35 @@ def bench_shift(args, kdt):
     B, Hkv, D, r, S, W = c["B"], c["Hkv"], c["D"], c["r"], c["S"], c["W"]
     table = sk.RopeTable(D, r, c["theta"], 64)
     kdtype = torch.bfloat16 if kdt == "bf16" else torch.int8
-    layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W, k_dtype=kdtype, with_v=False)
-    if kdt == "bf16":
-        synth.fill_normal_(layer.k, 11)
-    else:
-        layer.k.copy_(synth.randint(layer.k.shape, 11, -127, 128, device="cuda").to(torch.int8))
-        synth.fill_uniform_(layer.k_scale, 12, 1.0 / 127, 2.0 / 127)
+    nl = args.layers or 1
     pos, head, count = synth.window_state(13, B, W, c["pos_lo"], c["pos_hi"])
-    layer.pos.copy_(pos)
-    layer.head.copy_(head)
-    layer.count.copy_(count)
+    layers = []
+    for l in range(nl):
+        layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W, k_dtype=kdtype, with_v=False)
+        if kdt == "bf16":
+            synth.fill_normal_(layer.k, 11 + 100 * l)
+        else:
+            layer.k.copy_(synth.randint(layer.k.shape, 11 + 100 * l, -127, 128, device="cuda").to(torch.int8))
+            synth.fill_uniform_(layer.k_scale, 12 + 100 * l, 1.0 / 127, 2.0 / 127)
+        layer.pos.copy_(pos)
+        layer.head.copy_(head)
+        layer.count.copy_(count)
+        layers.append(layer)
 
     def step(i):
-        sk.kv_shift_recent([layer], table, -1 if i % 2 == 0 else 1)
+        sk.kv_shift_recent(layers, table, -1 if i % 2 == 0 else 1)
 
     ms, clk = _timed(step, args.steps, args.warmup)
-    rows = B * Hkv * W
+    rows = nl * B * Hkv * W
     alg = rows * (r * 2 * 2 if kdt == "bf16" else (D + 4) * 2)
     hbm, _, _, peak_kind = _peaks()
     value = alg / (ms * 1e-3) / 1e9
-    assert layer.error_bits() == 0
+    assert all(l.error_bits() == 0 for l in layers)
     return {"metric": f"recent-key shift ({kdt}) GB/s (frac of HBM peak)", "value": round(value, 2),
             "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "dtype": kdt, "data": "synthetic",
-            "config": {"workload": "windowed decode cache: B=32, H_kv=8, d_h=r=128, S=4, W=4092, rings full; "
-                                   "recent keys turned by one position",
+            "config": {"workload": f"windowed decode cache x {nl} layer(s): B=32, H_kv=8, d_h=r=128, S=4, "
+                                   "W=4092, rings full; recent keys turned by one position", "layers": nl,
                        "algorithmic_bytes": alg, "l2": "inputs larger than L2" if alg > 129e6 else "fits L2"},
             "frac_of_hbm_peak": round(value / hbm, 4), "keys_per_s": round(rows / (ms * 1e-3), 1),
             "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": args.steps, "clocks": clk}
