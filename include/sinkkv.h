@@ -269,6 +269,9 @@ SK_API sk_status sk_rope_apply(const sk_rope_table* table, void* x, int32_t dtyp
 /* ---- Fused RoPE + KV append -------------------------------------------------------- */
 
 /* Append T new tokens per sequence to `layer`, rotating Q and K on the way.
+ *   table: the RoPE table; NULL when k is already rotated (a chunk rotated with
+ *      sk_rope_apply for sk_prefill_attention with a prior): k is then written as
+ *      given, q must be NULL, and head_dim must be 64 or 128.
  *   q: [batch][T][n_q_heads][head_dim] of io_dtype, device, may be NULL; rotated in place.
  *   k: [batch][T][n_kv_heads][head_dim] of io_dtype, device; rotated in place, then
  *      written to the cache (quantised per row for an int8 K cache).

@@ -386,16 +386,18 @@ def rope_apply(table: RopeTable, x: torch.Tensor, positions: torch.Tensor,
     return x
 
 
-def kv_append(table: RopeTable, layer: KVLayer, q: Optional[torch.Tensor], k: torch.Tensor,
+def kv_append(table: Optional[RopeTable], layer: KVLayer, q: Optional[torch.Tensor], k: torch.Tensor,
               v: torch.Tensor, stream=None):
     """Fused RoPE + append of T tokens per sequence (sk_kv_append).
 
-    q [B, T, Hq, D] (optional) and k [B, T, Hkv, D] are rotated in place; v [B, T, Hkv, D]."""
+    q [B, T, Hq, D] (optional) and k [B, T, Hkv, D] are rotated in place; v [B, T, Hkv, D].
+    table None: k is already rotated and is appended as given (q must be None)."""
     _need_contig(q, k, v)
     T = k.shape[1]
     hq = 0 if q is None else q.shape[2]
     s = layer.struct()
-    _check(_lib().sk_kv_append(table.handle, ctypes.byref(s), _ptr(q), hq, _ptr(k), _ptr(v),
+    _check(_lib().sk_kv_append(None if table is None else table.handle, ctypes.byref(s), _ptr(q), hq, _ptr(k),
+                               _ptr(v),
                                _sk_dtype(k.dtype), T, _stream(stream)), "sk_kv_append")
 
 

@@ -336,7 +336,8 @@ __global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p
                               uint32_t(p.Hkv * D * sizeof(IO)), &full_bar[st], policy);
                 bulk_copy_g2s(dst + size_t(hq + p.Hkv) * D * sizeof(IO), v + tok * p.Hkv * D,
                               uint32_t(p.Hkv * D * sizeof(IO)), &full_bar[st], policy);
-                bulk_copy_g2s_nohint(dst + rows_bytes, p.table + (s.pos + t) * half, uint32_t(half * sizeof(float2)),
+                if (half > 0)  // no table row when the keys come rotated
+                    bulk_copy_g2s_nohint(dst + rows_bytes, p.table + (s.pos + t) * half, uint32_t(half * sizeof(float2)),
                                      &full_bar[st]);
                 if (++st == kAppendStages) { st = 0; phase ^= 1; }
             }
@@ -532,9 +533,21 @@ sk_status run_append(const AppendParams& p, const sk_rope_config& c, int io_dtyp
 extern "C" sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer* layer, void* q,
                                   int32_t n_q_heads, void* k, const void* v, int32_t io_dtype,
                                   int32_t T, void* stream) {
-    SK_RET_IF(table == nullptr || layer == nullptr || k == nullptr || v == nullptr, SK_ERR_ARG);
+    SK_RET_IF(layer == nullptr || k == nullptr || v == nullptr, SK_ERR_ARG);
+    SK_RET_IF(table == nullptr && q != nullptr, SK_ERR_ARG);  // nothing would rotate q
     const sk_kv_layer& L = *layer;
-    const sk_rope_config& c = table_config(table);
+    // Without a table the keys come rotated: an identity "rotation" (no rotary dims)
+    // and no position limit but the counter's own.
+    sk_rope_config c{};
+    if (table != nullptr) {
+        c = table_config(table);
+    } else {
+        SK_RET_IF(L.head_dim != 64 && L.head_dim != 128, SK_ERR_UNSUPPORTED);
+        c.head_dim = L.head_dim;
+        c.rotary_dim = 0;
+        c.neox = 1;
+        c.max_positions = int64_t(1) << 62;
+    }
     SK_RET_IF(L.k == nullptr || L.v == nullptr || L.pos == nullptr, SK_ERR_ARG);
     SK_RET_IF(L.batch < 1 || L.n_kv_heads < 1 || T < 0, SK_ERR_ARG);
     SK_RET_IF(L.head_dim != c.head_dim, SK_ERR_ARG);
@@ -554,7 +567,7 @@ extern "C" sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer*
     if (T == 0) return SK_OK;
 
     AppendParams p{};
-    p.table = table_device(table);
+    p.table = table != nullptr ? table_device(table) : nullptr;
     p.max_pos = c.max_positions;
     p.rotary_dim = c.rotary_dim;
     p.q = q;

@@ -143,3 +143,16 @@ def test_prefill_workspace_and_prior_arguments_checked_on_host(lib):
     bad = prior()
     bad.batch = 3
     assert call(bad) == sk.SK_ERR_ARG                                     # batch differs
+
+
+def test_append_without_table_takes_no_q(lib):
+    """sk_kv_append with no table appends rotated keys as given; a q would stay
+    unrotated, so it is refused on the host (before any launch)."""
+    import sink_kv_attention_gb300 as sk
+    fake = 1 << 20
+    s = sk.KVLayerStruct(sk.SK_LAYER_RING, sk.SK_BF16, sk.SK_BF16, 1, 8, 128, 4, 60, 64, fake, fake, None,
+                         fake, fake, fake, None)
+    assert lib.sk_kv_append(None, ctypes.byref(s), fake, 32, fake, fake, sk.SK_BF16, 1, None) == sk.SK_ERR_ARG
+    s.head_dim = 96
+    assert lib.sk_kv_append(None, ctypes.byref(s), None, 0, fake, fake, sk.SK_BF16, 1, None) == \
+        sk.SK_ERR_UNSUPPORTED

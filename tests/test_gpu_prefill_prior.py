@@ -122,33 +122,52 @@ def test_prefill_prior_with_learned_sinks(sk):
 
 
 def test_chunked_prefill_through_the_library(sk):
-    """A prompt in two chunks: the first rotated and appended by kv_append, the second
-    rotated by rope_apply, attended over the ring the first left, then appended.  Its
-    rows equal the oracle's chunked prefill of the raw prompt rotated in float64."""
-    B, Hq, Hkv, S, W, L1, T2 = 2, 8, 2, 4, 150, 333, 260
-    L = L1 + T2
+    """A prompt in three chunks.  The first is rotated and appended by kv_append.  Each
+    later chunk is rotated by rope_apply, attends over the ring the earlier chunks left,
+    and is then appended as given (kv_append without a table).  Rows, ring state and
+    cached keys match the oracle's chunked prefill of the raw prompt rotated in
+    float64."""
+    B, Hq, Hkv, S, W = 2, 8, 2, 4, 150
+    chunks = [333, 260, 97]
+    L = sum(chunks)
     spec = RopeSpec(D, D, 1e4)
     tbl = sk.RopeTable(D, D, 1e4, L + 8)
     layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W)
     q, k, v = _chunk(B, L, Hq, Hkv, 60)
-    k1 = k[:, :L1].contiguous().cuda()
-    sk.kv_append(tbl, layer, None, k1, v[:, :L1].contiguous().cuda())
-    q2, k2 = q[:, L1:].contiguous().cuda(), k[:, L1:].contiguous().cuda()
-    posn = torch.arange(L1, L, dtype=torch.int64, device="cuda").repeat(B)
-    sk.rope_apply(tbl, q2.view(B * T2, Hq, D), posn)
-    sk.rope_apply(tbl, k2.view(B * T2, Hkv, D), posn)
-    v2 = v[:, L1:].contiguous().cuda()
-    out = f64(sk.prefill_attention(q2, k2, v2, L1, S, W, prior=layer, err=layer.err))
-    torch.cuda.synchronize()
-    assert layer.error_bits() == 0
-    rows = [0, 1, 2, 63, 64, 127, 128, 200, T2 - 1]
+    kr = [rope_rotate(f64(k[b]), range(L), spec.omega(), 1.0, D) for b in range(B)]
+    rings = [RingCache(S, W) for _ in range(B)]
+    sk.kv_append(tbl, layer, None, k[:, :chunks[0]].contiguous().cuda(), v[:, :chunks[0]].contiguous().cuda())
     for b in range(B):
-        kr = rope_rotate(f64(k[b]), range(L), spec.omega(), 1.0, D)
-        qr = rope_rotate(f64(q[b, L1:]), range(L1, L), spec.omega(), 1.0, D)
-        ring = RingCache(S, W)
-        ring.append([(kr[P], f64(v[b, P])) for P in range(L1)])
-        want = prefill_attention_prior(qr, kr[L1:], f64(v[b, L1:]), ring, S, W, rows=rows)
-        np.testing.assert_allclose(out[b][rows], want, rtol=0, atol=BF16_ATTN_ATOL)
+        rings[b].append([(kr[b][P], f64(v[b, P])) for P in range(chunks[0])])
+    p0 = chunks[0]
+    for T in chunks[1:]:
+        qc, kc = q[:, p0:p0 + T].contiguous().cuda(), k[:, p0:p0 + T].contiguous().cuda()
+        vc = v[:, p0:p0 + T].contiguous().cuda()
+        posn = torch.arange(p0, p0 + T, dtype=torch.int64, device="cuda").repeat(B)
+        sk.rope_apply(tbl, qc.view(B * T, Hq, D), posn)
+        sk.rope_apply(tbl, kc.view(B * T, Hkv, D), posn)
+        out = f64(sk.prefill_attention(qc, kc, vc, p0, S, W, prior=layer, err=layer.err))
+        sk.kv_append(None, layer, None, kc, vc)
+        torch.cuda.synchronize()
+        assert layer.error_bits() == 0
+        rows = sorted({0, 1, 63, 64, T // 2, T - 1})
+        for b in range(B):
+            qr = rope_rotate(f64(q[b, p0:p0 + T]), range(p0, p0 + T), spec.omega(), 1.0, D)
+            want = prefill_attention_prior(qr, kr[b][p0:p0 + T], f64(v[b, p0:p0 + T]), rings[b], S, W, rows=rows)
+            np.testing.assert_allclose(out[b][rows], want, rtol=0, atol=BF16_ATTN_ATOL)
+            rings[b].append([(kr[b][P], f64(v[b, P])) for P in range(p0, p0 + T)])
+        p0 += T
+        # the append of rotated keys moved the state as the oracle's ring and copied the
+        # keys bit for bit
+        assert layer.pos.tolist() == [p0] * B
+        assert layer.head.tolist() == [r.head for r in rings]
+        assert layer.count.tolist() == [r.count for r in rings]
+        kcache = layer.k.cpu()
+        for b in range(B):
+            for s_ in range(S + W):
+                P = rings[b].slot_pos[s_]
+                if P >= p0 - T:  # a key of this chunk
+                    assert torch.equal(kcache[b, :, s_], kc[b, P - (p0 - T)].cpu())
 
 
 def test_prior_state_mismatch_sets_error_bit(sk):
