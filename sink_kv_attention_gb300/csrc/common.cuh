@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/sinkkv.h"
 
 #define SK_RET_IF(cond, status) \
@@ -230,6 +232,35 @@ namespace sk {
 int device_sm_count();                                   // api.cu
 const float2* table_device(const sk_rope_table* t);      // rope_table.cu
 const sk_rope_config& table_config(const sk_rope_table* t);
+
+// A value computed once for each device (the current one) and kept: kernel attributes
+// and occupancy belong to a device, so a process that drives several GPUs sets them on
+// each.  A result `keep` rejects is not kept, and the next call computes it again.
+constexpr int kMaxDevices = 64;
+template <typename V>
+struct PerDevice {
+    std::mutex mu;
+    bool done[kMaxDevices] = {};
+    V val[kMaxDevices] = {};
+    template <typename Make, typename Keep>
+    V get(Make make, Keep keep, V no_device) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return no_device;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            val[dev] = make();
+            done[dev] = keep(val[dev]);
+        }
+        return val[dev];
+    }
+};
+
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) once per device.
+template <typename Kernel>
+cudaError_t set_smem_limit_once(PerDevice<cudaError_t>& cache, Kernel kernel, int bytes) {
+    return cache.get([&] { return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes); },
+                     [](cudaError_t e) { return e == cudaSuccess; }, cudaErrorInvalidDevice);
+}
 }
 
 namespace sk {

@@ -734,22 +734,23 @@ struct DecodeLaunch {
     // Both instantiations (contiguous and paged) get the shared-memory limit; the grid is
     // sized from the smaller occupancy of the two.
     static int blocks_per_sm() {
-        static int cached = -1;
-        if (cached < 0) {
-            int n0 = 0, n1 = 0;
-            if (cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM)) != cudaSuccess ||
-                cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM)) != cudaSuccess)
-                return 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, decode_split_kernel<T, D, NREP, false>, C::THREADS,
-                                                              C::SMEM) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, decode_split_kernel<T, D, NREP, true>, C::THREADS,
-                                                              C::SMEM) != cudaSuccess)
-                return 0;
-            cached = std::min(n0, n1);
-        }
-        return cached;
+        static PerDevice<int> cache;
+        return cache.get(
+            [] {
+                int n0 = 0, n1 = 0;
+                if (cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM)) != cudaSuccess ||
+                    cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM)) != cudaSuccess)
+                    return 0;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, decode_split_kernel<T, D, NREP, false>,
+                                                                  C::THREADS, C::SMEM) != cudaSuccess ||
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, decode_split_kernel<T, D, NREP, true>,
+                                                                  C::THREADS, C::SMEM) != cudaSuccess)
+                    return 0;
+                return std::min(n0, n1);
+            },
+            [](int n) { return n > 0; }, 0);
     }
 
     static int grid() { return std::max(1, blocks_per_sm()) * device_sm_count(); }

@@ -644,12 +644,8 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
                                                          int(T_pad), n_kv_heads, pv);
     SK_CUDA_RET(cudaGetLastError());
 
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SM_ALLOC);
-    });
-    SK_CUDA_RET(attr_err);
+    static PerDevice<cudaError_t> attr;
+    SK_CUDA_RET(set_smem_limit_once(attr, prefill_attn_kernel, SM_ALLOC));
 
     PrefillParams p{};
     p.out = out;

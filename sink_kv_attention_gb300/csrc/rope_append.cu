@@ -445,8 +445,8 @@ cudaError_t launch_append(AppendParams p, cudaStream_t st) {
     const size_t smem = kAppendStages * (append_stage_bytes<IO>(hq, p.Hkv, D) + size_t(p.rotary_dim / 2) * 8) +
                         2 * kAppendStages * 8;
     if (smem > 200 * 1024) return cudaErrorInvalidValue;  // more heads than the stages can hold
-    static cudaError_t attr = cudaFuncSetAttribute(kv_append_kernel<IO, KC, VC, D, NEOX, PAGED>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    static PerDevice<cudaError_t> attr_cache;
+    const cudaError_t attr = set_smem_limit_once(attr_cache, kv_append_kernel<IO, KC, VC, D, NEOX, PAGED>, 200 * 1024);
     if (attr != cudaSuccess) return attr;
     // blocks per sequence: one when a single block covers the tokens (it then also
     // advances the state), else enough blocks to fill the GPU
