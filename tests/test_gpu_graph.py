@@ -95,3 +95,59 @@ def test_two_streams_with_own_workspaces(sk):
             sk.decode_attention(l2, q2, out=o2, workspace=w2, stream=s2)
     torch.cuda.synchronize()
     assert torch.equal(o1, want1) and torch.equal(o2, want2)
+
+
+def test_captured_chunked_prefill_equals_eager(sk):
+    """Chunks of a prompt (rotate, attend over the prior ring, append the rotated keys)
+    captured as one graph give the same bits as the same calls made eagerly."""
+    from sink_kv_attention_gb300 import synth
+    B, Hq, Hkv, D, S, W, T, n = 2, 8, 2, 128, 4, 200, 96, 3
+    tbl = sk.RopeTable(D, D, 1e4, 4096)
+    q = synth.normal((n, B, T, Hq, D), 90, torch.bfloat16, device="cuda")
+    k = synth.normal((n, B, T, Hkv, D), 91, torch.bfloat16, device="cuda")
+    v = synth.normal((n, B, T, Hkv, D), 92, torch.bfloat16, device="cuda")
+    p_first = 300  # the first chunk starts after a prompt already in the cache
+
+    def fresh():
+        layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W)
+        synth.fill_normal_(layer.k, 93)
+        synth.fill_normal_(layer.v, 94)
+        layer.pos.fill_(p_first)
+        layer.count.fill_(W)
+        layer.head.fill_(17)
+        return layer
+
+    ws = torch.empty(sk.prefill_workspace_bytes(B, T, Hkv, D, sk.prefill_prior_keys(p_first + n * T, S, W)),
+                     dtype=torch.uint8, device="cuda")
+    posn = [torch.arange(p_first + i * T, p_first + (i + 1) * T, dtype=torch.int64, device="cuda").repeat(B)
+            for i in range(n)]
+
+    def run(layer, qs, ks, outs):
+        for i in range(n):
+            sk.rope_apply(tbl, qs[i].view(B * T, Hq, D), posn[i])
+            sk.rope_apply(tbl, ks[i].view(B * T, Hkv, D), posn[i])
+            sk.prefill_attention(qs[i], ks[i], v[i], p_first + i * T, S, W, out=outs[i], workspace=ws,
+                                 prior=layer, err=layer.err)
+            sk.kv_append(None, layer, None, ks[i], v[i])
+
+    eager, qe, ke = fresh(), q.clone(), k.clone()
+    out_e = torch.empty(n, B, T, Hq, D, dtype=torch.bfloat16, device="cuda")
+    run(eager, qe, ke, out_e)
+    torch.cuda.synchronize()
+    graph_layer, qg, kg = fresh(), q.clone(), k.clone()
+    out_g = torch.empty_like(out_e)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(graph_layer, qg, kg, out_g)
+    graph_layer2 = fresh()  # capture does not run: replay on fresh state and inputs
+    for f in ("k", "v", "pos", "head", "count"):
+        getattr(graph_layer, f).copy_(getattr(graph_layer2, f))
+    qg.copy_(q)
+    kg.copy_(k)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g, out_e)
+    assert torch.equal(graph_layer.k, eager.k) and torch.equal(graph_layer.v, eager.v)
+    assert graph_layer.pos.tolist() == eager.pos.tolist() == [p_first + n * T] * B
+    assert graph_layer.head.tolist() == eager.head.tolist()
+    assert eager.error_bits() == 0 and graph_layer.error_bits() == 0
