@@ -357,9 +357,10 @@ SK_API sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const voi
  * -1 for p0 < 0 or sinks < 0. */
 SK_API int64_t sk_prefill_prior_keys(int64_t p0, int32_t sinks, int32_t window);
 
-/* Workspace bytes sk_prefill_attention needs: a transposed copy of the keys' V, and
- * with prior_keys > 0 (sk_prefill_prior_keys of a call that passes a prior) a
- * combined copy of the prior's and the chunk's keys.  0 for an unsupported shape. */
+/* Workspace bytes sk_prefill_attention needs: with prior_keys > 0 (sk_prefill_prior_keys
+ * of a call that passes a prior) a combined copy of the prior's and the chunk's keys and
+ * values; without a prior no scratch is used and the answer is a token 16 bytes.  0 for
+ * an unsupported shape. */
 SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim,
                                          int64_t prior_keys);
 
@@ -380,7 +381,8 @@ SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_
  *   by T_k - T_q).  Without a prior, keys before p0 are not seen.  A ring prior must
  *   have the call's sinks and window (window > 0) and a count of
  *   min(window, p0 - min(sinks, p0)), as appends through this library leave it; a
- *   global prior needs p0 <= capacity (SK_ERR_CAPACITY otherwise).  K and V bf16, same batch, n_kv_heads and head_dim.
+ *   global prior needs p0 <= capacity (SK_ERR_CAPACITY otherwise).  K and V bf16, same
+ *   batch, n_kv_heads and head_dim.
  *   A device state that does not match p0 sets SK_DEVERR_STATE in *err; the result
  *   is then undefined, and every read stays inside the cache.
  *   workspace: device, >= sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim,

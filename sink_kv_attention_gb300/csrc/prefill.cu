@@ -12,18 +12,19 @@
 //   warps 0-3  softmax: thread r owns query row r = TMEM lane r
 //   warp 4     MMA issue (one lane)
 //   warp 5     TMA loads of Q and K (one lane)
-//   warp 6     TMA loads of V^T (one lane)
+//   warp 6     TMA loads of V (one lane)
 // Per key tile i (BN = 64 keys):
 //   S_i = Q K_i^T      tcgen05.mma M=128 N=64, into one of two TMEM S buffers
 //   softmax_i          tcgen05.ld S_i, mask, online max/sum in base 2 with a lazy
 //                      rescale of O (only when the row max grows by more than 2^8),
 //                      P_i as bf16 pairs written back over S_i with tcgen05.st
 //   O += P_i V_i       tcgen05.mma M=128 N=128 with A = P_i read from tensor memory
-//                      and B = V_i^T (V taken transposed so B is K-major)
+//                      and B = V_i as stored (MN-major: dims along the rows)
 // QK of tile i+1 runs on the tensor cores while softmax of tile i runs, and softmax no
 // longer waits for P.V of the previous tile (only a rare O rescale does); two CTAs per
 // SM overlap one CTA's softmax with the other's MMAs.
-// V is transposed once per call into the workspace ([B][Hkv][D][T_pad]).
+// V tiles are loaded as they lie ([key][dim], like K) and serve P.V as an MN-major B
+// operand, so V needs no transposed copy.
 // An optional learned sink logit per query head (a denominator-only term) enters at
 // the epilogue.
 #include <cudaTypedefs.h>
@@ -50,7 +51,7 @@ constexpr float kSinkLogitMax = 15.0f;
 constexpr int SM_Q = 0;                       // Q dims 0-63 then 64-127: 2 x 16 KB
 constexpr int SM_K = 32768;                   // 2 stages x (K lo 8 KB, K hi 8 KB)
 constexpr int K_STAGE = 16384;
-constexpr int SM_V = SM_K + 2 * K_STAGE;      // 2 stages x V^T 16 KB
+constexpr int SM_V = SM_K + 2 * K_STAGE;      // 2 stages x (V lo 8 KB, V hi 8 KB)
 constexpr int V_STAGE = 16384;
 constexpr int SM_BAR = SM_V + 2 * V_STAGE;
 constexpr int N_BARS = 16;
@@ -116,7 +117,7 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, boo
 
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmVT, PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tmV, PrefillParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
@@ -193,21 +194,23 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
     } else if (warp == 6) {
-        // ---------------------------- TMA loads: V^T -----------------------------
+        // ----------------------------- TMA loads: V ------------------------------
         if (lane == 0) {
             for (int i = 0; i < tp.n; ++i) {
                 const int s = i & 1;
                 if (i >= 2) wait_or_flag(&v_empty[s], ((i >> 1) - 1) & 1, bad);
                 const int k0 = key_tile(tp, i) * BN;
+                uint8_t* st = smem + SM_V + s * V_STAGE;
                 mbar_arrive_expect_tx(&v_full[s], V_STAGE);
-                tma_load_3d(smem + SM_V + s * V_STAGE, &tmVT, k0, 0, b * p.Hkv + g, &v_full[s]);
+                tma_load_4d(st, &tmV, 0, g, k0, b, &v_full[s]);
+                tma_load_4d(st + BN * 128, &tmV, 64, g, k0, b, &v_full[s]);
             }
         }
     } else if (warp == 4) {
         // ------------------------------- MMA issue -------------------------------
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, HD);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, HD) | (1u << 16);  // B (V) MN-major
             const uint32_t sq = smem_u32(smem + SM_Q);
             wait_or_flag(q_full, 0, bad);
             tc_fence_after_sync();
@@ -236,11 +239,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                     wait_or_flag(&p_full[s], (j >> 1) & 1, bad);
                     wait_or_flag(&v_full[s], (j >> 1) & 1, bad);
                     tc_fence_after_sync();
-                    const uint32_t svt = smem_u32(smem + SM_V + s * V_STAGE);
+                    const uint32_t sv = smem_u32(smem + SM_V + s * V_STAGE);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
-                        // A = P_j in TMEM: 16 keys = 8 columns of packed bf16 pairs
-                        const uint64_t db = desc_kmajor_sw128(svt + kk * 32);
+                        // A = P_j in TMEM: 16 keys = 8 columns of packed bf16 pairs; B = 16
+                        // key rows of V (2 KB), dims 64-127 in the second 8 KB block
+                        const uint64_t db = desc_mnmajor_sw128(sv + kk * 2048, BN * 128);
                         umma_bf16_tmem_a(tmem + 2 * BN, tmem + s * BN + kk * 8, db, idesc_pv,
                                          (j > 0 || kk > 0) ? 1u : 0u);
                     }
@@ -413,12 +417,14 @@ __device__ __forceinline__ int64_t prior_slot(const PriorView& pv, int b, int j)
     return pv.S + (cnt == pv.W ? (hd + ci) % pv.W : ci);
 }
 
-// Combined keys kc [B][Tk][Hkv][HD]: prior rows, then the chunk's k [B][T][Hkv][HD].
-// One thread per 16 bytes.  The thread of (b, j = 0, g = 0, c = 0) checks that the
-// prior's state matches the chunk's start (pos = p0; a ring holds cr recent entries).
-__global__ void __launch_bounds__(256) gather_keys_kernel(PriorView pv, const __nv_bfloat16* __restrict__ k,
-                                                          __nv_bfloat16* __restrict__ kc, int B, int T, int Tk,
-                                                          int Hkv, uint32_t* err) {
+// Combined keys and values kc, vc [B][Tk][Hkv][HD]: prior rows, then the chunk's k, v
+// [B][T][Hkv][HD].  One thread per 16 bytes of a K row and the same 16 bytes of its V
+// row.  The thread of (b, j = 0, g = 0, c = 0) checks that the prior's state matches the
+// chunk's start (pos = p0; a ring holds ring_count recent entries).
+__global__ void __launch_bounds__(256) gather_kv_kernel(PriorView pv, const __nv_bfloat16* __restrict__ k,
+                                                        const __nv_bfloat16* __restrict__ v,
+                                                        __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc,
+                                                        int B, int T, int Tk, int Hkv, uint32_t* err) {
     constexpr int CH = HD / 8;  // 16-byte chunks per row
     const int qoff = pv.s0 + pv.cr;
     const int64_t total = int64_t(B) * Tk * Hkv * CH;
@@ -428,52 +434,23 @@ __global__ void __launch_bounds__(256) gather_keys_kernel(PriorView pv, const __
         const int g = int((i / CH) % Hkv);
         const int64_t bj = i / (int64_t(CH) * Hkv);
         const int j = int(bj % Tk), b = int(bj / Tk);
-        const __nv_bfloat16* src;
+        const __nv_bfloat16 *ks, *vs;
         if (j < qoff) {
-            src = pv.k + ((int64_t(b) * Hkv + g) * pv.cap + prior_slot(pv, b, j)) * HD;
+            const int64_t row = ((int64_t(b) * Hkv + g) * pv.cap + prior_slot(pv, b, j)) * HD;
+            ks = pv.k + row;
+            vs = pv.v + row;
             if (j == 0 && g == 0 && c == 0) {
                 const bool ok = pv.pos[b] == pv.p0 && (pv.kind == SK_LAYER_GLOBAL || pv.count[b] == pv.ring_count);
                 if (!ok) set_error(err, SK_DEVERR_STATE);
             }
         } else {
-            src = k + ((int64_t(b) * T + (j - qoff)) * Hkv + g) * HD;
+            const int64_t row = ((int64_t(b) * T + (j - qoff)) * Hkv + g) * HD;
+            ks = k + row;
+            vs = v + row;
         }
-        reinterpret_cast<uint4*>(kc + (bj * Hkv + g) * HD)[c] = reinterpret_cast<const uint4*>(src)[c];
-    }
-}
-
-// v [B][T][Hkv][D] -> vt [B*Hkv][D][Tk_pad], 64 x 64 tiles through shared memory.  With
-// a prior (PRIOR), key index t < qoff reads prior row t and t >= qoff chunk row t - qoff.
-template <bool PRIOR>
-__global__ void __launch_bounds__(256) transpose_v_kernel(const __nv_bfloat16* __restrict__ v,
-                                                          __nv_bfloat16* __restrict__ vt, int T, int Tk,
-                                                          int T_pad, int Hkv, PriorView pv) {
-    __shared__ __nv_bfloat16 tile[64][66];
-    const int t0 = blockIdx.x * 64, d0 = blockIdx.y * 64, bg = blockIdx.z;
-    const int b = bg / Hkv, g = bg % Hkv;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int qoff = PRIOR ? pv.s0 + pv.cr : 0;
-    for (int i = ty; i < 64; i += 8) {
-        const int t = t0 + i;
-        if (t < Tk) {
-            const __nv_bfloat16* row =
-                PRIOR && t < qoff ? pv.v + ((int64_t(b) * Hkv + g) * pv.cap + prior_slot(pv, b, t)) * HD
-                                  : v + ((int64_t(b) * T + (t - qoff)) * Hkv + g) * HD;
-            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(row + d0 + 2 * tx);
-            tile[i][2 * tx] = x.x;
-            tile[i][2 * tx + 1] = x.y;
-        }
-    }
-    __syncthreads();
-    for (int i = ty; i < 64; i += 8) {
-        const int d = d0 + i;
-        const int t = t0 + 2 * tx;
-        if (t < Tk) {
-            __nv_bfloat162 y;
-            y.x = tile[2 * tx][i];
-            y.y = t + 1 < Tk ? tile[2 * tx + 1][i] : __float2bfloat16(0.0f);
-            *reinterpret_cast<__nv_bfloat162*>(vt + (int64_t(bg) * HD + d) * T_pad + t) = y;
-        }
+        const int64_t dst = (bj * Hkv + g) * HD;
+        reinterpret_cast<uint4*>(kc + dst)[c] = reinterpret_cast<const uint4*>(ks)[c];
+        reinterpret_cast<uint4*>(vc + dst)[c] = reinterpret_cast<const uint4*>(vs)[c];
     }
 }
 
@@ -500,8 +477,6 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-int64_t t_pad_of(int T) { return (int64_t(T) + 63) / 64 * 64; }
 
 }  // namespace
 }  // namespace sk
@@ -539,9 +514,8 @@ extern "C" size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n
     if (batch < 1 || T < 1 || n_kv_heads < 1 || head_dim != HD || prior_keys < 0) return 0;
     const int64_t Tk = int64_t(T) + prior_keys;
     if (Tk > (int64_t(1) << 30)) return 0;
-    size_t bytes = size_t(batch) * n_kv_heads * HD * t_pad_of(int(Tk)) * sizeof(__nv_bfloat16);  // V^T
-    if (prior_keys > 0) bytes += size_t(batch) * Tk * n_kv_heads * HD * sizeof(__nv_bfloat16);    // keys
-    return bytes;
+    if (prior_keys == 0) return 16;  // no scratch is used; a token size keeps 0 for "unsupported"
+    return 2 * size_t(batch) * Tk * n_kv_heads * HD * sizeof(__nv_bfloat16);  // combined keys and values
 }
 
 extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
@@ -592,12 +566,15 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     SK_RET_IF(need == 0 || ws_bytes < need, SK_ERR_ARG);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int Tk = int(Tk64);
-    const int64_t T_pad = t_pad_of(Tk);
-    __nv_bfloat16* vt = static_cast<__nv_bfloat16*>(workspace);
-    // keys: the chunk's own, or (with a prior) the combined buffer after V^T
+    // keys and values: the chunk's own, or (with a prior) the combined buffers
     const void* keys = k_rot;
-    __nv_bfloat16* kc = vt + size_t(batch) * n_kv_heads * HD * T_pad;
-    if (qoff > 0) keys = kc;
+    const void* vals = v;
+    __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(workspace);
+    __nv_bfloat16* vc = kc + size_t(batch) * Tk * n_kv_heads * HD;
+    if (qoff > 0) {
+        keys = kc;
+        vals = vc;
+    }
 
     // pack the q heads of a GQA group into one CTA (a power of two dividing n_rep, at
     // most 8): the K / V tiles are then loaded once for all of them
@@ -606,7 +583,7 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     while (nh < 8 && nrep % (2 * nh) == 0) nh *= 2;
     const int qpb = BM / nh;
 
-    CUtensorMap mq, mk, mvt;
+    CUtensorMap mq, mk, mv;
     {
         const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_q_heads), cuuint64_t(T), cuuint64_t(batch)};
         const cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(n_q_heads) * HD * 2,
@@ -620,29 +597,17 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
                                        cuuint64_t(Tk) * n_kv_heads * HD * 2};
         const cuuint32_t box[4] = {64, 1, BN, 1};
         SK_RET_IF(!make_map(&mk, keys, 4, dims, strides, box), SK_ERR_CUDA);
-    }
-    {
-        const cuuint64_t dims[3] = {cuuint64_t(Tk), cuuint64_t(HD), cuuint64_t(batch) * n_kv_heads};
-        const cuuint64_t strides[2] = {cuuint64_t(T_pad) * 2, cuuint64_t(HD) * T_pad * 2};
-        const cuuint32_t box[3] = {BN, HD, 1};
-        SK_RET_IF(!make_map(&mvt, vt, 3, dims, strides, box), SK_ERR_CUDA);
+        SK_RET_IF(!make_map(&mv, vals, 4, dims, strides, box), SK_ERR_CUDA);
     }
 
     if (qoff > 0) {
         const int64_t threads = int64_t(batch) * Tk * n_kv_heads * (HD / 8);
         const int64_t blocks = std::min<int64_t>((threads + 255) / 256, int64_t(device_sm_count()) * 16);
-        gather_keys_kernel<<<unsigned(blocks), 256, 0, st>>>(pv, static_cast<const __nv_bfloat16*>(k_rot), kc,
-                                                            batch, T, Tk, n_kv_heads, err);
+        gather_kv_kernel<<<unsigned(blocks), 256, 0, st>>>(pv, static_cast<const __nv_bfloat16*>(k_rot),
+                                                          static_cast<const __nv_bfloat16*>(v), kc, vc, batch, T,
+                                                          Tk, n_kv_heads, err);
         SK_CUDA_RET(cudaGetLastError());
     }
-    dim3 tgrid(unsigned((Tk + 63) / 64), HD / 64, unsigned(batch * n_kv_heads));
-    if (qoff > 0)
-        transpose_v_kernel<true><<<tgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(v), vt, T, Tk,
-                                                        int(T_pad), n_kv_heads, pv);
-    else
-        transpose_v_kernel<false><<<tgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(v), vt, T, Tk,
-                                                         int(T_pad), n_kv_heads, pv);
-    SK_CUDA_RET(cudaGetLastError());
 
     static PerDevice<cudaError_t> attr;
     SK_CUDA_RET(set_smem_limit_once(attr, prefill_attn_kernel, SM_ALLOC));
@@ -668,7 +633,7 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     p.nqb = (T + qpb - 1) / qpb;
     p.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
     const int64_t grid = int64_t(p.nqb) * (n_q_heads / nh) * batch;
-    prefill_attn_kernel<<<unsigned(grid), kThreads, SM_ALLOC, st>>>(mq, mk, mvt, p);
+    prefill_attn_kernel<<<unsigned(grid), kThreads, SM_ALLOC, st>>>(mq, mk, mv, p);
     SK_CUDA_RET(cudaGetLastError());
     return SK_OK;
 }

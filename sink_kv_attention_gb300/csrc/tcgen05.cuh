@@ -88,6 +88,19 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// Shared-memory descriptor of a 128-byte-swizzled MN-major operand: the MN dimension runs
+// along 128-byte rows (64 bf16), K down the rows; 8 rows form a 1 KB swizzle atom.  LBO =
+// byte stride between 64-element MN blocks, SBO = byte stride between 8-row K groups.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t smem_addr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= uint64_t((smem_addr & 0x3FFFFu) >> 4);
+    d |= uint64_t((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+    d |= uint64_t(1024u >> 4) << 32;
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(2) << 61;
+    return d;
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both K-major,
 // shape M x N (bits 4-5 D format, 7-9 A format, 10-12 B format, 15/16 A/B major,
 // 17-22 N >> 3, 24-28 M >> 4).

@@ -119,9 +119,9 @@ def test_prefill_prior_keys_are_exactly_the_old_keys_a_chunk_sees(lib):
 
 def test_prefill_workspace_and_prior_arguments_checked_on_host(lib):
     import sink_kv_attention_gb300 as sk
-    # V^T for T (+ prior keys), padded to 64 keys, plus the combined keys with a prior
-    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 0) == 2 * 8 * 128 * 128 * 2
-    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 30) == 2 * 8 * 128 * 192 * 2 + 2 * 130 * 8 * 128 * 2
+    # no scratch without a prior (a token 16 bytes); with one, the combined keys and values
+    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 0) == 16
+    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 30) == 2 * (2 * 130 * 8 * 128 * 2)
     assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, -1) == 0
     assert lib.sk_prefill_workspace_bytes(2, 100, 8, 64, 0) == 0
     fake = 1 << 20  # aligned, never dereferenced: every case below fails before a launch
