@@ -637,6 +637,98 @@ def bench_paged(args):
             "gpu_launches": steps * 3, "launch": "cuda graph of the timed steps", "clocks": clocks.summary()}
 
 
+def bench_window_i8(args):
+    """The windowed-layer decode step on an int8 K cache: the same shapes as the default
+    line (B=32, H_q=32, H_kv=8, d_h=r=128, S=4, W=4092, rings full at random heads);
+    K rows are 128 int8 codes plus one fp32 scale, V and queries bf16.  One step = RoPE +
+    append (K quantised per row) + split-K attention, the timed steps captured as one
+    CUDA graph."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    B, Hq, Hkv, D, S, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    steps, warm = args.steps, args.warmup
+    n = 2 * steps + warm
+    tbl = sk.RopeTable(D, c["r"], c["theta"], c["pos_hi"] + n + 64)
+    layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W, k_dtype=torch.int8)
+    layer.k.copy_(synth.randint(layer.k.shape, 11, -127, 128, device="cuda").to(torch.int8))
+    synth.fill_uniform_(layer.k_scale, 12, 0.5 / 127, 2.0 / 127)
+    synth.fill_normal_(layer.v, 13)
+    pos, head, count = synth.window_state(13, B, W, c["pos_lo"], c["pos_hi"])
+    layer.pos.copy_(pos)
+    layer.head.copy_(head)
+    layer.count.copy_(count)
+    qs = synth.normal((n, B, 1, Hq, D), 14, torch.bfloat16, device="cuda")
+    ks = synth.normal((n, B, 1, Hkv, D), 15, torch.bfloat16, device="cuda")
+    vs = synth.normal((n, B, 1, Hkv, D), 16, torch.bfloat16, device="cuda")
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(sk.decode_workspace_bytes(layer, Hq), dtype=torch.uint8, device="cuda")
+    zl = _learned_sinks(args, Hq)
+
+    def step(i, ev=None):
+        st = torch.cuda.current_stream()
+        sk.kv_append(tbl, layer, qs[i], ks[i], vs[i])
+        if ev is not None:
+            ev[0].record(st)
+        sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws, sink_logits=zl)
+        if ev is not None:
+            ev[1].record(st)
+
+    for i in range(warm):
+        step(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(steps):
+            step(warm + i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("end")
+    clocks.stop()
+    ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+          for _ in range(steps)]
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        for i in range(steps):
+            step(warm + steps + i, ev[i])
+    g2.replay()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    dec_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    assert layer.error_bits() == 0
+    L = S + W
+    kv_bytes = B * Hkv * L * (D + 4 + D * 2)     # int8 K row + its scale, bf16 V row
+    alg_decode = kv_bytes + 2 * (B * Hq * D * 2)
+    hbm, _, _, peak_kind = _peaks()
+    value = kv_bytes / (ms * 1e-3) / 1e9
+    achieved = alg_decode / (dec_ms * 1e-3) / 1e9
+    return {"metric": METRIC + " (int8 K cache)", "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": steps, "warmup": warm, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "dtype": "bf16 q/v, int8 K + fp32 scale", "data": "synthetic",
+            "config": {"workload": "windowed-layer decode step on an int8 K cache (RoPE + quantising append + "
+                                   "split-K attention)", "batch": B, "H_q": Hq, "H_kv": Hkv, "d_h": D, "sinks": S,
+                       "window": W, "learned_sink_logits": bool(args.learned_sink),
+                       "l2": f"inputs larger than L2 (KV {kv_bytes / 1e6:.0f} MB per step)"},
+            "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "traffic": None,
+                         "kernel": "decode attention over int8 keys (split-K + combine), per launch",
+                         "algorithmic_bytes_per_launch": alg_decode, "launch_ms": round(dec_ms, 5),
+                         "peak_source": f"{peak_kind} hbm_gbs"},
+            "gpu_launches": steps * 3, "launch": "cuda graph of the timed steps", "clocks": clocks.summary()}
+
+
 def bench_shift(args, kdt):
     """Local-position window slide: the recent keys of the windowed decode workload's
     cache (B=32, H_kv=8, d_h=r=128, S=4, W=4092, every ring full) turned by one
@@ -1030,8 +1122,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="window",
-                    choices=["window", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill", "prefill_chunk",
-                             "dynamic_bf16", "dynamic_i8", "shift_bf16", "shift_i8", "paged"])
+                    choices=["window", "window_i8", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill",
+                             "prefill_chunk", "dynamic_bf16", "dynamic_i8", "shift_bf16", "shift_i8", "paged"])
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--cpu-worker-mt", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
@@ -1095,6 +1187,8 @@ def main():
                 print(json.dumps(bench_dynamic(args, args.workload.split("_")[1])))
             elif args.workload == "paged":
                 print(json.dumps(bench_paged(args)))
+            elif args.workload == "window_i8":
+                print(json.dumps(bench_window_i8(args)))
             elif args.workload.startswith("shift"):
                 print(json.dumps(bench_shift(args, args.workload.split("_")[1])))
             else:

@@ -313,7 +313,9 @@ SK_API size_t sk_decode_workspace_bytes(const sk_kv_layer* layer, int32_t n_q_he
  *   cache").  The same value serves every sequence.
  *   workspace: device, >= sk_decode_workspace_bytes(layer, n_q_heads) bytes, 16-byte
  *   aligned; its contents need no initialisation.
- * Supported: io SK_F32 with an F32/F32 cache, io SK_BF16 with a BF16/BF16 cache;
+ * Supported: io SK_F32 with an F32/F32 cache, io SK_BF16 with a BF16/BF16 cache, and io
+ * SK_BF16 with an I8/BF16 cache (int8 K codes and one fp32 scale per row in k_scale, as
+ * sk_kv_append and sk_kv_rerotate write them; head_dim 128): a key is code * scale.
  * n_q_heads / n_kv_heads in {1, 2, 4} for head_dim 128 and {1, 2, 4, 8} for 64. */
 SK_API sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q_rot, int32_t n_q_heads,
                                      int32_t io_dtype, const float* sink_logits, void* out,

@@ -179,6 +179,19 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* gmem_src, uint32_t 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem_src), "r"(bytes) : "memory");
 }
 
+// 16 int8 codes -> 8 exact float pairs (byte permute under 2^23, subtract 2^23 + 128).
+__device__ __forceinline__ void codes16_to_pairs(const uint4& u, float2* f) {
+    const uint32_t w[4] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u, u.z ^ 0x80808080u, u.w ^ 0x80808080u};
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7540)),
+                                          __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7541))), bias);
+        f[2 * i + 1] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7542)),
+                                              __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7543))), bias);
+    }
+}
+
 // 2^x with the hardware approximation (ex2.approx.ftz.f32): -inf -> +0.
 __device__ __forceinline__ float fast_exp2_approx(float x) {
     float y;

@@ -49,6 +49,7 @@ struct DecodeParams {
     float* ws;
     const int32_t* count;
     const int64_t* pos;
+    const float* kscale;  // [B][Hkv][cap] per-row scales of an int8 K cache, else null
     uint32_t* err;
     int64_t cap;
     int B, Hkv, S, kind;
@@ -144,7 +145,8 @@ template <typename T, int D, int NREP> constexpr int decode_warps() {
 
 template <int N> constexpr int ilog2() { return N <= 1 ? 0 : 1 + ilog2<N / 2>(); }
 
-template <typename T, int D, int NREP> struct DecodeCfg {
+// KQ: the K cache holds int8 codes (D bytes per row, one fp32 scale per row); V is T.
+template <typename T, int D, int NREP, bool KQ = false> struct DecodeCfg {
     static constexpr int NWARPS = decode_warps<T, D, NREP>();
     static constexpr int LG = ilog2<NREP>();
     static constexpr int VEC = ElemIO<T>::kPerVec;    // elements per 16-byte chunk
@@ -155,8 +157,10 @@ template <typename T, int D, int NREP> struct DecodeCfg {
     static constexpr int TILE = NWARPS * RPW;         // rows per stage
     static_assert((TILE & (TILE - 1)) == 0, "tile height must be a power of two");
     static constexpr int DPV = D / 32;                // dims per lane (PV)
-    static constexpr int ROW_BYTES = D * int(sizeof(T));
-    static constexpr int STAGE_BYTES = 2 * TILE * ROW_BYTES;   // K tile then V tile
+    static constexpr int ROW_BYTES = D * int(sizeof(T));      // a V row (and a K row unless KQ)
+    static constexpr int K_ROW_BYTES = KQ ? D : ROW_BYTES;
+    static constexpr int STAGE_BYTES = TILE * (K_ROW_BYTES + ROW_BYTES);   // K tile then V tile
+    static_assert(!KQ || (D == 128 && sizeof(T) == 2), "int8 keys: head_dim 128, bf16 queries and values");
     static constexpr int STAGES_FIT = (192 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 5 ? 5 : STAGES_FIT;
     static_assert(STAGES >= 2, "stage too large");
@@ -368,9 +372,10 @@ __device__ __forceinline__ void prefetch_share(const DecodeParams& p, const int6
         const int64_t r1 = min(min(hi, st + w.len()) - st, p.cap);
         if (r1 > r0) {
             const int64_t unit = int64_t(w.b) * p.Hkv + w.g;
-            const uint32_t bytes = uint32_t(r1 - r0) * C::ROW_BYTES;
-            bulk_prefetch_l2(static_cast<const T*>(p.kc) + (unit * p.cap + r0) * D, bytes);
-            bulk_prefetch_l2(static_cast<const T*>(p.vc) + (unit * p.cap + r0) * D, bytes);
+            bulk_prefetch_l2(static_cast<const uint8_t*>(p.kc) + (unit * p.cap + r0) * C::K_ROW_BYTES,
+                             uint32_t(r1 - r0) * C::K_ROW_BYTES);
+            bulk_prefetch_l2(static_cast<const T*>(p.vc) + (unit * p.cap + r0) * D,
+                             uint32_t(r1 - r0) * C::ROW_BYTES);
         }
     } while (w.next());
 }
@@ -378,10 +383,10 @@ __device__ __forceinline__ void prefetch_share(const DecodeParams& p, const int6
 // PAGED selects the block-table producer and key-aligned tiles.  The two layouts are
 // separate instantiations: the contiguous kernel then carries none of the paged code
 // (compiled into one kernel, the contiguous path measured 3-5% slower).
-template <typename T, int D, int NREP, bool PAGED>
-__global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
+template <typename T, int D, int NREP, bool PAGED, bool KQ>
+__global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ>::THREADS, 1)
     decode_split_kernel(DecodeParams p) {
-    using C = DecodeCfg<T, D, NREP>;
+    using C = DecodeCfg<T, D, NREP, KQ>;
     constexpr int NWARPS = C::NWARPS;
     constexpr int STAGES = C::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -444,15 +449,20 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
                 if (st >= hi) break;
                 const int64_t r0 = max(lo, st) - st, r1 = min(hi, st + w.len()) - st;
                 const int64_t unit = int64_t(w.b) * p.Hkv + w.g;
-                const T* kbase = static_cast<const T*>(p.kc) + unit * p.cap * D;
+                const uint8_t* kbase = static_cast<const uint8_t*>(p.kc) + unit * p.cap * C::K_ROW_BYTES;
                 const T* vbase = static_cast<const T*>(p.vc) + unit * p.cap * D;
+                if constexpr (KQ) {  // warm L2 with the segment's row scales (16-byte aligned interior)
+                    const uintptr_t a = (reinterpret_cast<uintptr_t>(p.kscale + unit * p.cap + r0) + 15) & ~uintptr_t(15);
+                    const uintptr_t e = reinterpret_cast<uintptr_t>(p.kscale + unit * p.cap + r1) & ~uintptr_t(15);
+                    if (e > a) bulk_prefetch_l2(reinterpret_cast<const void*>(a), uint32_t(e - a));
+                }
                 for (int64_t row = r0; row < r1; row += C::TILE) {
                     const uint32_t n = uint32_t(min(int64_t(C::TILE), r1 - row));
                     if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1)) timed_out = true;
                     uint8_t* dst = stages + size_t(stage) * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full_bar[stage], 2u * n * C::ROW_BYTES);
-                    bulk_copy_g2s(dst, kbase + row * D, n * C::ROW_BYTES, &full_bar[stage], policy);
-                    bulk_copy_g2s(dst + C::TILE * C::ROW_BYTES, vbase + row * D, n * C::ROW_BYTES,
+                    mbar_arrive_expect_tx(&full_bar[stage], n * uint32_t(C::K_ROW_BYTES + C::ROW_BYTES));
+                    bulk_copy_g2s(dst, kbase + row * C::K_ROW_BYTES, n * C::K_ROW_BYTES, &full_bar[stage], policy);
+                    bulk_copy_g2s(dst + C::TILE * C::K_ROW_BYTES, vbase + row * D, n * C::ROW_BYTES,
                                   &full_bar[stage], policy);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -489,14 +499,16 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
         const int b = w.b, g = w.g;
         const int64_t unit = int64_t(b) * p.Hkv + g;
 
-        // q slice of this lane for the NREP heads in its permuted order, pre-scaled.
+        // q slice of this lane for the NREP heads in its permuted order, pre-scaled: the
+        // dims of its K chunks (chunks l8 and l8 + 8 of 8 elements; with int8 keys, dims
+        // 16 l8 .. 16 l8 + 15, one 16-code chunk)
         float2 q2[NREP][C::DPL / 2];
 #pragma unroll
         for (int hh = 0; hh < NREP; ++hh) {
             const T* qrow = qbase + (unit * NREP + (hh ^ hperm)) * D;
 #pragma unroll
             for (int i = 0; i < C::CPL; ++i) {
-                const uint4 raw = reinterpret_cast<const uint4*>(qrow)[l8 + 8 * i];
+                const uint4 raw = reinterpret_cast<const uint4*>(qrow)[KQ ? 2 * l8 + i : l8 + 8 * i];
                 float f[C::VEC];
                 ElemIO<T>::unpack(raw, f);
 #pragma unroll
@@ -513,16 +525,27 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
 #pragma unroll
             for (int d = 0; d < C::DPV / 2; ++d) acc[h][d] = make_float2(0.f, 0.f);
 
+        // int8 keys: this lane's row scale, loaded one tile ahead of its use
+        const float* srow = KQ ? p.kscale + unit * p.cap + warp * C::RPW + gi * C::RPG + rperm : nullptr;
+        float ks_next = 1.0f;
+        if constexpr (KQ) {
+            if (r0 + warp * C::RPW + gi * C::RPG + rperm < r1) ks_next = __ldg(srow + r0);
+        }
         const int64_t tph = PAGED ? tile_phase(p, b, C::TILE) : 0;
         int n = 0;
         for (int64_t row0 = r0; row0 < r1; row0 += PAGED ? n : C::TILE) {
             const int skip = PAGED ? int((row0 - tph) & (C::TILE - 1)) : 0;
             n = int(min(int64_t(C::TILE - skip), r1 - row0));
             if (!mbar_wait_bounded(&full_bar[stage], phase)) timed_out = true;
-            const T* ktile = reinterpret_cast<const T*>(stages + size_t(stage) * C::STAGE_BYTES);
-            const T* vtile = ktile + C::TILE * D;
+            const uint8_t* ktile = stages + size_t(stage) * C::STAGE_BYTES;
+            const T* vtile = reinterpret_cast<const T*>(ktile + C::TILE * C::K_ROW_BYTES);
             const int wrow0 = warp * C::RPW;
             const int nw = max(0, min(C::RPW, n - wrow0));  // valid rows of this warp
+            float kscale = 1.0f;  // int8 keys: the scale of this lane's row (used after the reduce)
+            if constexpr (KQ) {
+                kscale = ks_next;
+                if (row0 + C::TILE + wrow0 + gi * C::RPG + rperm < r1) ks_next = __ldg(srow + row0 + C::TILE);
+            }
 
             // ---- QK: slot jj*NREP + hh holds row (jj ^ rperm), head (hh ^ hperm) ----
             float part[8];
@@ -531,18 +554,22 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
                 const int lr = gi * C::RPG + (jj ^ rperm);
                 float2 kf[C::DPL / 2];
                 if (lr < nw) {
-                    const uint4* krow = reinterpret_cast<const uint4*>(ktile + (wrow0 + lr) * D);
+                    const uint4* krow = reinterpret_cast<const uint4*>(ktile + (wrow0 + lr) * C::K_ROW_BYTES);
+                    if constexpr (KQ) {
+                        codes16_to_pairs(krow[l8], kf);  // 16 codes, exact in fp32
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < C::CPL; ++i) {
-                        const uint4 raw = krow[l8 + 8 * i];
-                        if constexpr (sizeof(T) == 2) {
-                            kf[i * 4 + 0] = bf16x2_to_float2(raw.x);
-                            kf[i * 4 + 1] = bf16x2_to_float2(raw.y);
-                            kf[i * 4 + 2] = bf16x2_to_float2(raw.z);
-                            kf[i * 4 + 3] = bf16x2_to_float2(raw.w);
-                        } else {
-                            kf[i * 2 + 0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
-                            kf[i * 2 + 1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+                        for (int i = 0; i < C::CPL; ++i) {
+                            const uint4 raw = krow[l8 + 8 * i];
+                            if constexpr (sizeof(T) == 2) {
+                                kf[i * 4 + 0] = bf16x2_to_float2(raw.x);
+                                kf[i * 4 + 1] = bf16x2_to_float2(raw.y);
+                                kf[i * 4 + 2] = bf16x2_to_float2(raw.z);
+                                kf[i * 4 + 3] = bf16x2_to_float2(raw.w);
+                            } else {
+                                kf[i * 2 + 0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+                                kf[i * 2 + 1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+                            }
                         }
                     }
                 } else {
@@ -563,7 +590,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP>::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 2; ++i) part[i] += __shfl_xor_sync(kFull, part[i + 2], 2);
             part[0] += __shfl_xor_sync(kFull, part[1], 1);
-            const float s = my_row < nw ? part[0] : -INFINITY;
+            const float s = my_row < nw ? (KQ ? part[0] * kscale : part[0]) : -INFINITY;
 
             // ---- online softmax (base 2) for this lane's head ----
             float tmax = s;
@@ -727,28 +754,34 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
     }
 }
 
-template <typename T, int D, int NREP>
+// KQ: int8 keys (contiguous layers only; paged layers hold bf16 or fp32 keys).
+template <typename T, int D, int NREP, bool KQ = false>
 struct DecodeLaunch {
-    using C = DecodeCfg<T, D, NREP>;
+    using C = DecodeCfg<T, D, NREP, KQ>;
 
-    // Both instantiations (contiguous and paged) get the shared-memory limit; the grid is
-    // sized from the smaller occupancy of the two.
+    // Every instantiation launched from here (contiguous, and paged unless KQ) gets the
+    // shared-memory limit; the grid is sized from the smallest occupancy among them.
     static int blocks_per_sm() {
         static PerDevice<int> cache;
         return cache.get(
             [] {
                 int n0 = 0, n1 = 0;
-                if (cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, false>,
+                if (cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, false, KQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM)) != cudaSuccess ||
-                    cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM)) != cudaSuccess)
-                    return 0;
-                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, decode_split_kernel<T, D, NREP, false>,
-                                                                  C::THREADS, C::SMEM) != cudaSuccess ||
-                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, decode_split_kernel<T, D, NREP, true>,
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, decode_split_kernel<T, D, NREP, false, KQ>,
                                                                   C::THREADS, C::SMEM) != cudaSuccess)
                     return 0;
-                return std::min(n0, n1);
+                if constexpr (KQ) {
+                    return n0;
+                } else {
+                    if (cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, true, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(C::SMEM)) != cudaSuccess ||
+                        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, decode_split_kernel<T, D, NREP, true, false>,
+                                                                      C::THREADS, C::SMEM) != cudaSuccess)
+                        return 0;
+                    return std::min(n0, n1);
+                }
             },
             [](int n) { return n > 0; }, 0);
     }
@@ -762,25 +795,32 @@ struct DecodeLaunch {
     static cudaError_t run(DecodeParams p, const sk_kv_layer& L, cudaStream_t st) {
         if (blocks_per_sm() < 1) return cudaErrorInvalidConfiguration;
         p.n_blocks = grid();
-        cudaError_t e = p.kind == kKindPaged
-                            ? launch_pdl(decode_split_kernel<T, D, NREP, true>, dim3(p.n_blocks), dim3(C::THREADS),
-                                         C::SMEM, st, p)
-                            : launch_pdl(decode_split_kernel<T, D, NREP, false>, dim3(p.n_blocks), dim3(C::THREADS),
-                                         C::SMEM, st, p);
+        cudaError_t e;
+        if constexpr (KQ) {
+            if (p.kind == kKindPaged) return cudaErrorInvalidValue;
+            e = launch_pdl(decode_split_kernel<T, D, NREP, false, true>, dim3(p.n_blocks), dim3(C::THREADS), C::SMEM,
+                           st, p);
+        } else {
+            e = p.kind == kKindPaged
+                    ? launch_pdl(decode_split_kernel<T, D, NREP, true, false>, dim3(p.n_blocks), dim3(C::THREADS),
+                                 C::SMEM, st, p)
+                    : launch_pdl(decode_split_kernel<T, D, NREP, false, false>, dim3(p.n_blocks), dim3(C::THREADS),
+                                 C::SMEM, st, p);
+        }
         if (e != cudaSuccess) return e;
         const int warps = L.batch * L.n_kv_heads * NREP;
         return launch_pdl(decode_combine_kernel<T, D, NREP>, dim3((warps + 7) / 8), dim3(256), 0, st, p);
     }
 };
 
-template <typename T, int D>
+template <typename T, int D, bool KQ = false>
 bool dispatch(int nrep, bool want_ws, const sk_kv_layer& L, DecodeParams* p, cudaStream_t st, size_t* ws,
               cudaError_t* e) {
     switch (nrep) {
-#define SK_CASE(N)                                              \
-    case N:                                                     \
-        if (want_ws) *ws = DecodeLaunch<T, D, N>::workspace(L); \
-        else *e = DecodeLaunch<T, D, N>::run(*p, L, st);        \
+#define SK_CASE(N)                                                  \
+    case N:                                                         \
+        if (want_ws) *ws = DecodeLaunch<T, D, N, KQ>::workspace(L); \
+        else *e = DecodeLaunch<T, D, N, KQ>::run(*p, L, st);        \
         return true;
         SK_CASE(1)
         SK_CASE(2)
@@ -807,6 +847,8 @@ bool route(int io_dtype, const sk_kv_layer& L, int nrep, bool want_ws, DecodePar
     } else if (io_dtype == SK_F32 && L.k_dtype == SK_F32 && L.v_dtype == SK_F32) {
         if (L.head_dim == 128) return dispatch<float, 128>(nrep, want_ws, L, p, st, ws, e);
         if (L.head_dim == 64) return dispatch<float, 64>(nrep, want_ws, L, p, st, ws, e);
+    } else if (io_dtype == SK_BF16 && L.k_dtype == SK_I8 && L.v_dtype == SK_BF16) {
+        if (L.head_dim == 128) return dispatch<__nv_bfloat16, 128, true>(nrep, want_ws, L, p, st, ws, e);
     }
     return false;
 }
@@ -825,6 +867,8 @@ sk_status check_layer(const sk_kv_layer* layer, int32_t n_q_heads) {
         SK_RET_IF(L.kind != SK_LAYER_GLOBAL, SK_ERR_ARG);
     }
     SK_RET_IF((reinterpret_cast<uintptr_t>(L.k) | reinterpret_cast<uintptr_t>(L.v)) & 15u, SK_ERR_ARG);
+    if (L.k_dtype == SK_I8)
+        SK_RET_IF(L.k_scale == nullptr || (reinterpret_cast<uintptr_t>(L.k_scale) & 3u), SK_ERR_ARG);
     return SK_OK;
 }
 
@@ -866,6 +910,7 @@ extern "C" sk_status sk_decode_attention(const sk_kv_layer* layer, const void* q
     p.ws = static_cast<float*>(workspace);
     p.count = L.count;
     p.pos = L.pos;
+    p.kscale = L.k_dtype == SK_I8 ? L.k_scale : nullptr;
     p.err = L.err;
     p.cap = L.capacity;
     p.B = L.batch;

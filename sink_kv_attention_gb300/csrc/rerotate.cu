@@ -197,19 +197,6 @@ __global__ void __launch_bounds__(kThreads) rerotate_bf16_kernel(RerotParams p) 
 // rint(x * 127 / max|x|) = rint(t * 127 / max|t|) for t = the turned codes, and the new
 // scale is max|t| * s_old / 127.  Pairs of values go through packed fp32 arithmetic.
 
-// 16 codes -> 8 exact float pairs (byte permute under 2^23, subtract 2^23 + 128).
-__device__ __forceinline__ void codes16_to_pairs(const uint4& u, float2* f) {
-    const uint32_t w[4] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u, u.z ^ 0x80808080u, u.w ^ 0x80808080u};
-    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7540)),
-                                          __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7541))), bias);
-        f[2 * i + 1] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7542)),
-                                              __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7543))), bias);
-    }
-}
-
 // 8 float pairs -> 16 codes rint(t * inv), ties to even (|t * inv| < 127.5 by construction).
 __device__ __forceinline__ uint4 pairs_to_codes16(const float2* t, float inv) {
     const float2 inv2 = make_float2(inv, inv), magic = make_float2(12582912.0f, 12582912.0f);
