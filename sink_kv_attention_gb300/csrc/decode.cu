@@ -618,11 +618,25 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ>::THREADS, 1)
                 for (int r = 0; r < C::RPW; ++r) {
                     float2 vf[C::DPV / 2];
                     load_pv_slice<T, C::DPV>(vtile + (wrow0 + r) * D, lane, vf);
+                    if constexpr (NREP >= 2 && !KQ && !PAGED) {
+                        // the (p, p) pairs of two heads in one 16-byte load (measured: +2% on
+                        // the contiguous bf16 step, -0.5 to -1% for paged layers and int8 keys)
 #pragma unroll
-                    for (int h = 0; h < NREP; ++h) {
-                        const float2 pp = ps[r * NREP + h];
+                        for (int h = 0; h < NREP; h += 2) {
+                            const float4 pp = *reinterpret_cast<const float4*>(&ps[r * NREP + h]);
 #pragma unroll
-                        for (int d = 0; d < C::DPV / 2; ++d) acc[h][d] = __ffma2_rn(pp, vf[d], acc[h][d]);
+                            for (int d = 0; d < C::DPV / 2; ++d) {
+                                acc[h][d] = __ffma2_rn(make_float2(pp.x, pp.y), vf[d], acc[h][d]);
+                                acc[h + 1][d] = __ffma2_rn(make_float2(pp.z, pp.w), vf[d], acc[h + 1][d]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < NREP; ++h) {
+                            const float2 pp = ps[r * NREP + h];
+#pragma unroll
+                            for (int d = 0; d < C::DPV / 2; ++d) acc[h][d] = __ffma2_rn(pp, vf[d], acc[h][d]);
+                        }
                     }
                 }
             } else {
