@@ -25,6 +25,12 @@
 // back from shared memory as (p, p) pairs ready for packed fp32 FMAs.
 // A second kernel combines each unit's partials by log-sum-exp; a learned sink logit
 // (a per-head term in the softmax denominator) enters there.
+//
+// Instantiations: contiguous layers (ring or global) and paged layers (a block-table
+// producer), each for bf16 or fp32 caches, and contiguous layers with int8 keys (128
+// codes and one fp32 scale per K row, bf16 V): a lane decodes its 16 codes of a row
+// exactly to fp32, and the reduced score is multiplied by the row's scale.  Before its
+// PDL wait, a contiguous block asks L2 for the first rows of its share.
 #include <algorithm>
 #include <mutex>
 
