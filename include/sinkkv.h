@@ -474,6 +474,14 @@ SK_API sk_status sk_kv_shift_recent(const sk_kv_layer* layers, int32_t n_layers,
  * truncation; this is how a C caller hears it. */
 SK_API sk_status sk_sync_check(uint32_t* err, int32_t clear, void* stream, uint32_t* bits_out);
 
+/* Diagnostic: launch one thread that waits, through the library's bounded in-kernel
+ * wait, on an mbarrier that never completes.  After the wait's limit (about one
+ * second) it gives up, ORs SK_DEVERR_TIMEOUT into *err (device) and exits: the same
+ * path every pipelined kernel takes if a copy never lands, so a caller can check that
+ * such a failure is reported and leaves the context usable.  Asynchronous on
+ * `stream`; SK_ERR_ARG for err == NULL. */
+SK_API sk_status sk_selftest_bounded_wait(uint32_t* err, void* stream);
+
 /* A static, human-readable name for a status code. */
 SK_API const char* sk_status_str(sk_status status);
 

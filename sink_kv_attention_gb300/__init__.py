@@ -100,6 +100,7 @@ _SIGNATURES = [
     ("sk_decode_attention_noalloc", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32,
                                                    ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_prefill_prior_keys", ctypes.c_int64, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
+    ("sk_selftest_bounded_wait", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_prefill_workspace_bytes", ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                      ctypes.c_int64]),
     ("sk_prefill_attention", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
@@ -603,6 +604,12 @@ def sync_check(err: torch.Tensor, clear: bool = False, stream=None):
     bits = ctypes.c_uint32()
     st = _lib().sk_sync_check(_ptr(err), 1 if clear else 0, _stream(stream), ctypes.byref(bits))
     return int(st), int(bits.value)
+
+
+def selftest_bounded_wait(err: torch.Tensor, stream=None) -> None:
+    """Launch the bounded-wait diagnostic (sk_selftest_bounded_wait): about one second
+    later SK_DEVERR_TIMEOUT is set in `err`."""
+    _check(_lib().sk_selftest_bounded_wait(_ptr(err), _stream(stream)), "sk_selftest_bounded_wait")
 
 
 def version() -> int:

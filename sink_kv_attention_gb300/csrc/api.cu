@@ -17,7 +17,25 @@ int device_sm_count() {
     return cached[dev];
 }
 
+namespace {
+
+// One thread waits, through the library's bounded wait, on an mbarrier that nothing
+// will ever complete: the wait gives up after its limit and the error word says so.
+__global__ void bounded_wait_probe_kernel(uint32_t* err) {
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    if (!mbar_wait_bounded(&bar, 0)) set_error(err, SK_DEVERR_TIMEOUT);
+}
+
+}  // namespace
 }  // namespace sk
+
+extern "C" sk_status sk_selftest_bounded_wait(uint32_t* err, void* stream) {
+    SK_RET_IF(err == nullptr, SK_ERR_ARG);
+    sk::bounded_wait_probe_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err);
+    return cudaGetLastError() == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}
 
 extern "C" const char* sk_status_str(sk_status status) {
     switch (status) {
