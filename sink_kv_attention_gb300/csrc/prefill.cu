@@ -109,6 +109,13 @@ __device__ __forceinline__ bool tile_full(const PrefillParams& p, int q0, int k0
     return q_last - k0 < p.W || k0 + BN - 1 < p.nsk;
 }
 
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, bool& bad) {
     if (mbar_wait_bounded(bar, parity)) return true;
     bad = true;
@@ -287,14 +294,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             // row max of the raw scores: 8 independent chains, then a tree
+            // row max with three-input max: 8 chains of 8 columns, then the chains
             float mx[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx[e] = sc[e];
-#pragma unroll
-            for (int j = 8; j < 64; ++j) mx[j & 7] = fmaxf(mx[j & 7], sc[j]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], mx[e + 4]);
-            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+            for (int c = 0; c < 8; ++c) {
+                float m = fmax3(sc[c], sc[c + 8], sc[c + 16]);
+                m = fmax3(m, sc[c + 24], sc[c + 32]);
+                m = fmax3(m, sc[c + 40], sc[c + 48]);
+                mx[c] = fmaxf(m, sc[c + 56]);
+            }
+            const float m_tile =
+                fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * p.scale_log2;
             // Lazy rescale: keep the running max unless the row max grows by more than
             // 2^8.  A row that has seen only masked keys (m_run = -inf) has O = 0 and
             // l = 0, so it adopts the new max without touching O.
