@@ -293,8 +293,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     sc[j] = vis ? sc[j] : -INFINITY;
                 }
             }
-            // row max of the raw scores: 8 independent chains, then a tree
-            // row max with three-input max: 8 chains of 8 columns, then the chains
+            // row max of the raw scores with three-input max: 8 chains of 8 columns, then the chains
             float mx[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
