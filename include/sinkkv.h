@@ -262,7 +262,8 @@ SK_API void sk_rope_dynamic_destroy(sk_rope_dynamic* dyn);
  * row t at absolute position positions[t] (device int64 [n_tok]).
  * [RoPE] the rotation listing: o1 = x1 cos - x2 sin, o2 = x2 cos + x1 sin, times mu;
  * dims [r, d_h) untouched.  A row whose position is < 0 or >= max_positions is left
- * unchanged and sets SK_DEVERR_POSITION_RANGE in *err (device, may be NULL). */
+ * unchanged and sets SK_DEVERR_POSITION_RANGE in *err (device, may be NULL).
+ * n_tok = 0 launches nothing and returns SK_OK; x and positions may then be NULL. */
 SK_API sk_status sk_rope_apply(const sk_rope_table* table, void* x, int32_t dtype, int64_t n_tok,
                         int32_t n_heads, const int64_t* positions, uint32_t* err, void* stream);
 
@@ -287,7 +288,9 @@ SK_API sk_status sk_rope_apply(const sk_rope_table* table, void* x, int32_t dtyp
  * and sets SK_DEVERR_POSITION_RANGE.
  * io_dtype: SK_BF16 or SK_F32.  Supported (io, k cache, v cache): (F32,F32,F32),
  * (BF16,BF16,BF16), (BF16,I8,BF16); others return SK_ERR_UNSUPPORTED.
- * n_q_heads must be a multiple of n_kv_heads when q is given. */
+ * n_q_heads must be a multiple of n_kv_heads when q is given.
+ * T = 0 checks the layer, launches nothing (the state stays as it is) and returns
+ * SK_OK; q, k and v may then be NULL. */
 SK_API sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer* layer, void* q,
                        int32_t n_q_heads, void* k, const void* v, int32_t io_dtype, int32_t T,
                        void* stream);
@@ -361,8 +364,8 @@ SK_API int64_t sk_prefill_prior_keys(int64_t p0, int32_t sinks, int32_t window);
 
 /* Workspace bytes sk_prefill_attention needs: with prior_keys > 0 (sk_prefill_prior_keys
  * of a call that passes a prior) a combined copy of the prior's and the chunk's keys and
- * values; without a prior no scratch is used and the answer is a token 16 bytes.  0 for
- * an unsupported shape. */
+ * values; without a prior, or with T = 0, no scratch is used and the answer is a token
+ * 16 bytes.  0 for an unsupported shape. */
 SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim,
                                          int64_t prior_keys);
 
@@ -391,7 +394,9 @@ SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_
  *   prior ? sk_prefill_prior_keys(p0, sinks, window) : 0) bytes, 16-byte aligned, no
  *   initialisation needed.  err: device error word (SK_DEVERR_TIMEOUT if a bounded
  *   in-kernel wait gave up, SK_DEVERR_STATE as above), may be NULL.
- * Supported: head_dim 128, SK_BF16, T + prior keys <= 2^30. */
+ * Supported: head_dim 128, SK_BF16, T + prior keys <= 2^30.  T = 0 checks the other
+ * arguments, launches nothing and returns SK_OK; q_rot, k_rot, v, out and workspace
+ * may then be NULL. */
 SK_API sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
                                       int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                                       int64_t p0, int32_t sinks, int32_t window, const sk_kv_layer* prior,
@@ -426,7 +431,7 @@ SK_API sk_status sk_kv_rerotate(const sk_kv_layer* layers, int32_t n_layers, con
  * whose seq_lens[b] + T exceeds max_blocks * block_size, or whose positions pass the
  * table, is skipped with SK_DEVERR_CAPACITY / SK_DEVERR_POSITION_RANGE; a token whose
  * block id is outside [0, n_blocks) is not stored and sets SK_DEVERR_BLOCK_TABLE.
- * Layouts and dtypes as sk_kv_append. */
+ * Layouts, dtypes and T = 0 as sk_kv_append. */
 SK_API sk_status sk_paged_append(const sk_rope_table* table, const sk_paged_layer* layer, void* q,
                                  int32_t n_q_heads, const void* k, const void* v, int32_t io_dtype, int32_t T,
                                  void* stream);

@@ -520,10 +520,11 @@ extern "C" int64_t sk_prefill_prior_keys(int64_t p0, int32_t sinks, int32_t wind
 
 extern "C" size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim,
                                              int64_t prior_keys) {
-    if (batch < 1 || T < 1 || n_kv_heads < 1 || head_dim != HD || prior_keys < 0) return 0;
+    if (batch < 1 || T < 0 || n_kv_heads < 1 || head_dim != HD || prior_keys < 0) return 0;
     const int64_t Tk = int64_t(T) + prior_keys;
     if (Tk > (int64_t(1) << 30)) return 0;
-    if (prior_keys == 0) return 16;  // no scratch is used; a token size keeps 0 for "unsupported"
+    // no scratch is used: a token size keeps 0 for "unsupported"
+    if (prior_keys == 0 || T == 0) return 16;
     return 2 * size_t(batch) * Tk * n_kv_heads * HD * sizeof(__nv_bfloat16);  // combined keys and values
 }
 
@@ -532,9 +533,11 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
                                           int64_t p0, int32_t sinks, int32_t window, const sk_kv_layer* prior,
                                           const float* sink_logits, void* out, void* workspace, size_t ws_bytes,
                                           uint32_t* err, void* stream) {
-    SK_RET_IF(q_rot == nullptr || k_rot == nullptr || v == nullptr || out == nullptr || workspace == nullptr,
-              SK_ERR_ARG);
     SK_RET_IF(batch < 1 || T < 0 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads != 0, SK_ERR_ARG);
+    // T = 0 reads and writes nothing: the chunk, output and workspace pointers may be NULL
+    SK_RET_IF(T > 0 && (q_rot == nullptr || k_rot == nullptr || v == nullptr || out == nullptr ||
+                        workspace == nullptr),
+              SK_ERR_ARG);
     SK_RET_IF(p0 < 0 || sinks < 0, SK_ERR_ARG);
     SK_RET_IF(head_dim != HD, SK_ERR_UNSUPPORTED);
     const uintptr_t al = reinterpret_cast<uintptr_t>(q_rot) | reinterpret_cast<uintptr_t>(k_rot) |

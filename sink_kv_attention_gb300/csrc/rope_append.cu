@@ -46,22 +46,28 @@ __device__ __forceinline__ bool lane_pairs(int rotary_dim, int c, int* j0) {
 }
 
 // Rotate the VEC elements of this lane (c = lane index within its row), with the lane's
-// (cos, sin) pairs at cs (global or shared memory).  Every lane of the warp must call
-// this (it shuffles); `active` lanes update f.
-template <typename T, int D, bool NEOX>
+// (cos, sin) pairs at cs (global or shared memory).  A NeoX rotation needs the lane's
+// partner vector in the other half of the rotary part: with ROW_IN_SMEM it is loaded
+// from `row` (the row in shared memory), else every lane of the warp must call this (it
+// shuffles).  `active` lanes update f.
+template <typename T, int D, bool NEOX, bool ROW_IN_SMEM = false>
 __device__ __forceinline__ void rotate_lane(float* f, const uint4& raw, const float4* cs, int rotary_dim, int c,
-                                            int lane, bool active) {
+                                            int lane, bool active, const uint4* row = nullptr) {
     constexpr int VEC = RowLayout<T, D>::VEC;
     if constexpr (NEOX) {
         const int hc = (rotary_dim / 2) / VEC;  // vectors per half of the rotary part
         const bool rot = c < 2 * hc;
         const int partner_c = c < hc ? c + hc : c - hc;
-        const int src = lane - c + (rot ? partner_c : c);
         uint4 pr;
-        pr.x = __shfl_sync(kFull, raw.x, src);
-        pr.y = __shfl_sync(kFull, raw.y, src);
-        pr.z = __shfl_sync(kFull, raw.z, src);
-        pr.w = __shfl_sync(kFull, raw.w, src);
+        if constexpr (ROW_IN_SMEM) {
+            pr = active && rot ? row[partner_c] : raw;
+        } else {
+            const int src = lane - c + (rot ? partner_c : c);
+            pr.x = __shfl_sync(kFull, raw.x, src);
+            pr.y = __shfl_sync(kFull, raw.y, src);
+            pr.z = __shfl_sync(kFull, raw.z, src);
+            pr.w = __shfl_sync(kFull, raw.w, src);
+        }
         if (active && rot) {
             float p[VEC];
             ElemIO<T>::unpack(pr, p);
@@ -363,18 +369,34 @@ __global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p
             // this lane's (cos, sin) pairs of position pos + t, copied in with the rows
             float4 cs[TCH];
             const float4* trow = reinterpret_cast<const float4*>(stage + rows_bytes) + j0 / 2;
+            if constexpr (TCH == 4) {
+                // The 8 lanes of a quarter warp read 64-byte-strided pieces of the row, which
+                // fall on 2 of the 8 bank groups (4 wavefronts a load, in every quarter). Each
+                // lane takes its 4 chunks starting at chunk m = (piece / 2) mod 4 instead, so a
+                // load touches 8 distinct groups, and then undoes the rotation in registers
+                // (measured: the prefill-chunk append 5010-5070 -> 5590-5640 GB/s).
+                const int m = (j0 / 16) & 3;
+                float4 t[4], u[4];
 #pragma unroll
-            for (int i = 0; i < TCH; ++i) cs[i] = rot_lane ? trow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i = 0; i < 4; ++i) t[i] = rot_lane ? trow[(i + m) & 3] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) u[j] = (m & 1) ? t[(j + 3) & 3] : t[j];  // u[j] = chunk j + (m & 2)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cs[j] = (m & 2) ? u[(j + 2) & 3] : u[j];  // cs[j] = chunk j
+            } else {
+#pragma unroll
+                for (int i = 0; i < TCH; ++i) cs[i] = rot_lane ? trow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             for (int r0 = warp * L::RPW; r0 < rows_per_tok; r0 += kWarps * L::RPW) {
                 const int r = r0 + rw;  // uniform trip count per warp; lanes past the token idle
                 const bool live = r < rows_per_tok;
                 const int which = r < hq ? 0 : (r < hq + p.Hkv ? 1 : 2);
                 const int h = which == 0 ? r : (which == 1 ? r - hq : r - hq - p.Hkv);
-                const uint4 raw = live ? reinterpret_cast<const uint4*>(stage + size_t(r) * D * sizeof(IO))[c]
-                                       : make_uint4(0, 0, 0, 0);
+                const uint4* srow = reinterpret_cast<const uint4*>(stage + size_t(r) * D * sizeof(IO));
+                const uint4 raw = live ? srow[c] : make_uint4(0, 0, 0, 0);
                 float f[VEC];
                 ElemIO<IO>::unpack(raw, f);
-                rotate_lane<IO, D, NEOX>(f, raw, cs, p.rotary_dim, c, lane, live && which < 2);
+                rotate_lane<IO, D, NEOX, true>(f, raw, cs, p.rotary_dim, c, lane, live && which < 2, srow);
                 const uint4 out = ElemIO<IO>::pack(f);
                 if (live && which == 0) reinterpret_cast<uint4*>(qtok + h * D)[c] = out;
                 if (live && which == 1) reinterpret_cast<uint4*>(ktok + h * D)[c] = out;
@@ -487,11 +509,12 @@ using namespace sk;
 extern "C" sk_status sk_rope_apply(const sk_rope_table* table, void* x, int32_t dtype, int64_t n_tok,
                                    int32_t n_heads, const int64_t* positions, uint32_t* err,
                                    void* stream) {
-    SK_RET_IF(table == nullptr || x == nullptr || positions == nullptr, SK_ERR_ARG);
+    SK_RET_IF(table == nullptr, SK_ERR_ARG);
     SK_RET_IF(n_tok < 0 || n_heads < 1, SK_ERR_ARG);
     SK_RET_IF(dtype != SK_BF16 && dtype != SK_F32, SK_ERR_UNSUPPORTED);
+    if (n_tok == 0) return SK_OK;  // nothing is read: x and positions may be NULL
+    SK_RET_IF(x == nullptr || positions == nullptr, SK_ERR_ARG);
     SK_RET_IF(!aligned16(x), SK_ERR_ARG);
-    if (n_tok == 0) return SK_OK;
     const sk_rope_config& c = table_config(table);
     ApplyParams p{table_device(table), c.max_positions, c.rotary_dim, x, n_tok, n_heads, positions, err};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -533,7 +556,8 @@ sk_status run_append(const AppendParams& p, const sk_rope_config& c, int io_dtyp
 extern "C" sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer* layer, void* q,
                                   int32_t n_q_heads, void* k, const void* v, int32_t io_dtype,
                                   int32_t T, void* stream) {
-    SK_RET_IF(layer == nullptr || k == nullptr || v == nullptr, SK_ERR_ARG);
+    SK_RET_IF(layer == nullptr || T < 0, SK_ERR_ARG);
+    SK_RET_IF(T > 0 && (k == nullptr || v == nullptr), SK_ERR_ARG);  // T = 0: k, v may be NULL
     SK_RET_IF(table == nullptr && q != nullptr, SK_ERR_ARG);  // nothing would rotate q
     const sk_kv_layer& L = *layer;
     // Without a table the keys come rotated: an identity "rotation" (no rotary dims)
@@ -561,7 +585,7 @@ extern "C" sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer*
         return SK_ERR_ARG;
     }
     if (q != nullptr) SK_RET_IF(n_q_heads < 1 || n_q_heads % L.n_kv_heads != 0, SK_ERR_ARG);
-    SK_RET_IF(!aligned16(k) || !aligned16(v) || !aligned16(L.k) || !aligned16(L.v), SK_ERR_ARG);
+    SK_RET_IF(!aligned16(k) || !aligned16(v) || !aligned16(L.k) || !aligned16(L.v), SK_ERR_ARG);  // NULL passes
     SK_RET_IF(q != nullptr && !aligned16(q), SK_ERR_ARG);
     if (L.k_dtype == SK_I8) SK_RET_IF(L.k_scale == nullptr, SK_ERR_ARG);
     if (T == 0) return SK_OK;
@@ -594,7 +618,8 @@ extern "C" sk_status sk_kv_append(const sk_rope_table* table, const sk_kv_layer*
 extern "C" sk_status sk_paged_append(const sk_rope_table* table, const sk_paged_layer* layer, void* q,
                                      int32_t n_q_heads, const void* k, const void* v, int32_t io_dtype,
                                      int32_t T, void* stream) {
-    SK_RET_IF(table == nullptr || layer == nullptr || k == nullptr || v == nullptr, SK_ERR_ARG);
+    SK_RET_IF(table == nullptr || layer == nullptr || T < 0, SK_ERR_ARG);
+    SK_RET_IF(T > 0 && (k == nullptr || v == nullptr), SK_ERR_ARG);  // T = 0: k, v may be NULL
     const sk_paged_layer& L = *layer;
     const sk_rope_config& c = table_config(table);
     SK_RET_IF(paged_layer_check(L) != SK_OK, SK_ERR_ARG);

@@ -124,6 +124,8 @@ def test_prefill_workspace_and_prior_arguments_checked_on_host(lib):
     assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 30) == 2 * (2 * 130 * 8 * 128 * 2)
     assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, -1) == 0
     assert lib.sk_prefill_workspace_bytes(2, 100, 8, 64, 0) == 0
+    assert lib.sk_prefill_workspace_bytes(2, 0, 8, 128, 30) == 16   # an empty chunk
+    assert lib.sk_prefill_workspace_bytes(2, -1, 8, 128, 0) == 0
     fake = 1 << 20  # aligned, never dereferenced: every case below fails before a launch
 
     def prior(kind=sk.SK_LAYER_RING, k_dtype=sk.SK_BF16, sinks=4, window=60, capacity=64):
@@ -156,3 +158,30 @@ def test_append_without_table_takes_no_q(lib):
     s.head_dim = 96
     assert lib.sk_kv_append(None, ctypes.byref(s), None, 0, fake, fake, sk.SK_BF16, 1, None) == \
         sk.SK_ERR_UNSUPPORTED
+
+
+def test_zero_length_calls_return_ok_without_a_launch(lib):
+    """T = 0 passes the host checks and returns SK_OK with nothing launched: the
+    pointers below are aligned fakes that a launch would fault on, and no CUDA device
+    is needed."""
+    import sink_kv_attention_gb300 as sk
+    fake = 1 << 20
+    s = sk.KVLayerStruct(sk.SK_LAYER_RING, sk.SK_BF16, sk.SK_BF16, 2, 8, 128, 4, 60, 64, fake, fake, None,
+                         fake, fake, fake, None)
+    assert lib.sk_kv_append(None, ctypes.byref(s), None, 0, fake, fake, sk.SK_BF16, 0, None) == sk.SK_OK
+    assert lib.sk_kv_append(None, ctypes.byref(s), None, 0, fake, fake, sk.SK_BF16, -1, None) == sk.SK_ERR_ARG
+    assert lib.sk_prefill_attention(fake, fake, fake, 2, 0, 32, 8, 128, 0, 4, 60, None, None, fake, fake, 16,
+                                    None, None) == sk.SK_OK
+    assert lib.sk_prefill_attention(fake, fake, fake, 2, 0, 32, 8, 128, 100, 4, 60, ctypes.byref(s), None, fake,
+                                    fake, 16, None, None) == sk.SK_OK
+    assert lib.sk_prefill_attention(fake, fake, fake, 2, -1, 32, 8, 128, 0, 4, 60, None, None, fake, fake, 16,
+                                    None, None) == sk.SK_ERR_ARG
+    # an empty torch tensor has data_ptr() 0: NULL data pointers are accepted at T = 0 only
+    assert lib.sk_kv_append(None, ctypes.byref(s), None, 0, None, None, sk.SK_BF16, 0, None) == sk.SK_OK
+    assert lib.sk_kv_append(None, ctypes.byref(s), None, 0, None, None, sk.SK_BF16, 1, None) == sk.SK_ERR_ARG
+    assert lib.sk_prefill_attention(None, None, None, 2, 0, 32, 8, 128, 0, 4, 60, None, None, None, None, 0,
+                                    None, None) == sk.SK_OK
+    assert lib.sk_prefill_attention(None, None, None, 2, 1, 32, 8, 128, 0, 4, 60, None, None, None, None, 0,
+                                    None, None) == sk.SK_ERR_ARG
+    s.window = 0  # the layer is still checked at T = 0
+    assert lib.sk_kv_append(None, ctypes.byref(s), None, 0, None, None, sk.SK_BF16, 0, None) == sk.SK_ERR_ARG
