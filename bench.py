@@ -233,10 +233,18 @@ def bench_window(args, rank, world):
     # second captured pass of as many steps right after.
     graph = None
     if not args.eager:
+        state0 = [t.clone() for t in (layer.pos, layer.head, layer.count)]
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for i in range(steps):
                 step(warm + i)
+        torch.cuda.synchronize()
+        # the graph's first launch also uploads it: replay once untimed, then put the
+        # ring state back so that the timed replay makes the same appends and reads
+        graph.replay()
+        torch.cuda.synchronize()
+        for t, s0 in zip((layer.pos, layer.head, layer.count), state0):
+            t.copy_(s0)
         torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
