@@ -606,10 +606,17 @@ def bench_paged(args):
     for i in range(warm):
         step(i)
     torch.cuda.synchronize()
+    lens0 = layer.seq_lens.clone()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for i in range(steps):
             step(warm + i)
+    torch.cuda.synchronize()
+    # untimed first replay (it also uploads the graph), then the lengths are put back so
+    # that the timed replay appends the same tokens into the same blocks
+    graph.replay()
+    torch.cuda.synchronize()
+    layer.seq_lens.copy_(lens0)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -700,10 +707,18 @@ def bench_window_i8(args):
     for i in range(warm):
         step(i)
     torch.cuda.synchronize()
+    state0 = [t.clone() for t in (layer.pos, layer.head, layer.count)]
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for i in range(steps):
             step(warm + i)
+    torch.cuda.synchronize()
+    # untimed first replay (it also uploads the graph), then the ring state is put back
+    # so that the timed replay makes the same appends and reads
+    graph.replay()
+    torch.cuda.synchronize()
+    for t, s0 in zip((layer.pos, layer.head, layer.count), state0):
+        t.copy_(s0)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

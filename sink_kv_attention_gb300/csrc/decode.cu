@@ -705,6 +705,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ>::THREADS, 1)
 }
 
 // One warp per (b, q head): log-sum-exp combine of the unit's partials.
+constexpr int kCombineFew = 3;  // partials a combine warp loads in one go
+
 template <typename T, int D, int NREP>
 __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
     constexpr int DPV = D / 32;
@@ -748,21 +750,49 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
     const float z2 = has_sink
                          ? fminf(fmaxf(p.sink_logits[hq], kSinkLogitMin), kSinkLogitMax) * kLog2e
                          : -INFINITY;
-    float M = z2;
-    for (int i = 0; i < n; ++i)
-        if (owns_rows(i)) M = fmaxf(M, base[i * PF + h]);
-    const float Mu = M == -INFINITY ? 0.0f : M;
     float acc[DPV];
 #pragma unroll
     for (int d = 0; d < DPV; ++d) acc[d] = 0.0f;
-    float lsum = has_sink ? fast_exp2_approx(z2 - Mu) : 0.0f;
-    for (int i = 0; i < n; ++i) {
-        if (!owns_rows(i)) continue;
-        const float* pp = base + i * PF;
-        const float f = fast_exp2_approx(pp[h] - Mu);
-        lsum = fmaf(f, pp[NREP + h], lsum);
+    float lsum;
+    if (n <= kCombineFew) {
+        // the usual case (a unit cut between at most kCombineFew blocks): every partial's
+        // max, sum and value slice are loaded at once, one round trip to L2
+        float mv[kCombineFew], lv[kCombineFew], vv[kCombineFew][DPV];
 #pragma unroll
-        for (int d = 0; d < DPV; ++d) acc[d] = fmaf(f, pp[2 * NREP + h * D + lane * DPV + d], acc[d]);
+        for (int i = 0; i < kCombineFew; ++i) {
+            const bool own = i < n && owns_rows(i);
+            const float* pp = base + i * PF;
+            mv[i] = own ? pp[h] : -INFINITY;
+            lv[i] = own ? pp[NREP + h] : 0.0f;
+#pragma unroll
+            for (int d = 0; d < DPV; ++d) vv[i][d] = own ? pp[2 * NREP + h * D + lane * DPV + d] : 0.0f;
+        }
+        float M = z2;
+#pragma unroll
+        for (int i = 0; i < kCombineFew; ++i) M = fmaxf(M, mv[i]);
+        const float Mu = M == -INFINITY ? 0.0f : M;
+        lsum = has_sink ? fast_exp2_approx(z2 - Mu) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < kCombineFew; ++i) {
+            const float f = fast_exp2_approx(mv[i] - Mu);  // 0 for a block that wrote nothing
+            lsum = fmaf(f, lv[i], lsum);
+#pragma unroll
+            for (int d = 0; d < DPV; ++d) acc[d] = fmaf(f, vv[i][d], acc[d]);
+        }
+    } else {
+        float M = z2;
+        for (int i = 0; i < n; ++i)
+            if (owns_rows(i)) M = fmaxf(M, base[i * PF + h]);
+        const float Mu = M == -INFINITY ? 0.0f : M;
+        lsum = has_sink ? fast_exp2_approx(z2 - Mu) : 0.0f;
+        for (int i = 0; i < n; ++i) {
+            if (!owns_rows(i)) continue;
+            const float* pp = base + i * PF;
+            const float f = fast_exp2_approx(pp[h] - Mu);
+            lsum = fmaf(f, pp[NREP + h], lsum);
+#pragma unroll
+            for (int d = 0; d < DPV; ++d) acc[d] = fmaf(f, pp[2 * NREP + h * D + lane * DPV + d], acc[d]);
+        }
     }
     const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
 #pragma unroll
