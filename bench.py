@@ -550,6 +550,44 @@ def bench_rerotate(args, kdt):
             "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": args.steps, "clocks": clk}
 
 
+def bench_rope(args):
+    """Standalone RoPE (sk_rope_apply), as a chunk prefilled over a cached prefix uses it:
+    the queries and keys of the prefill chunk (T=32768, H_q=32, H_kv=8, d_h=r=128,
+    theta 5e5) rotated in place, one call for Q and one for K per step; positions
+    p0 .. p0+T-1 with p0 = 32768."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.PREFILL
+    T, Hq, Hkv, D = c["T"], c["Hq"], c["Hkv"], c["D"]
+    p0 = 32768
+    tbl = sk.RopeTable(D, c["r"], c["theta"], p0 + T)
+    q = synth.normal((T, Hq, D), 31, torch.bfloat16, device="cuda")
+    k = synth.normal((T, Hkv, D), 32, torch.bfloat16, device="cuda")
+    posn = torch.arange(p0, p0 + T, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step(i):
+        sk.rope_apply(tbl, q, posn, err=err)
+        sk.rope_apply(tbl, k, posn, err=err)
+
+    ms, clk = _timed(step, args.steps, args.warmup)
+    assert int(err.item()) == 0
+    half = c["r"] // 2
+    # rows read and written in place, plus each call's table rows (one per token)
+    alg = 2 * T * (Hq + Hkv) * D * 2 + 2 * T * half * 8
+    hbm, _, _, peak_kind = _peaks()
+    value = alg / (ms * 1e-3) / 1e9
+    return {"metric": "RoPE apply GB/s (frac of HBM peak), rows/s", "value": round(value, 2), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"Q and K of a {T}-token chunk at positions {p0}.. (H_q={Hq}, H_kv={Hkv}, "
+                                   f"d_h=r={D}), rotated in place", "algorithmic_bytes": alg,
+                       "l2": "inputs larger than L2"},
+            "frac_of_hbm_peak": round(value / hbm, 4), "rows_per_s": round(T * (Hq + Hkv) / (ms * 1e-3), 1),
+            "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": 2 * args.steps, "clocks": clk}
+
+
 def bench_paged(args):
     """The windowed-layer decode step on a paged cache: B=32, H_q=32, H_kv=8,
     d_h=r=128, request sinks S=4, window W=4092, 16-token blocks scattered over a
@@ -1160,7 +1198,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="window",
                     choices=["window", "window_i8", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill",
-                             "prefill_chunk", "dynamic_bf16", "dynamic_i8", "shift_bf16", "shift_i8", "paged"])
+                             "prefill_chunk", "dynamic_bf16", "dynamic_i8", "shift_bf16", "shift_i8", "paged",
+                             "rope"])
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--cpu-worker-mt", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
@@ -1228,6 +1267,8 @@ def main():
                 print(json.dumps(bench_window_i8(args)))
             elif args.workload.startswith("shift"):
                 print(json.dumps(bench_shift(args, args.workload.split("_")[1])))
+            elif args.workload == "rope":
+                print(json.dumps(bench_rope(args)))
             else:
                 print(json.dumps(bench_rerotate(args, args.workload.split("_")[1])))
         return

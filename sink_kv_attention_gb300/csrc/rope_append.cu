@@ -114,37 +114,49 @@ struct ApplyParams {
     uint32_t* err;
 };
 
+constexpr int kApplyPasses = 4;  // row groups of a token each warp loads before rotating
+
+// One warp per token (grid-stride): the token's position and this lane's (cos, sin)
+// pairs are read once, then the token's H rows go through in passes of kApplyPasses
+// row groups whose loads are all issued before the first rotation.
 template <typename T, int D, bool NEOX>
 __global__ void __launch_bounds__(kThreads) rope_apply_kernel(ApplyParams p) {
     using L = RowLayout<T, D>;
+    constexpr int TCH = table_chunks<T, NEOX>();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = lane % L::LPR, rw = lane / L::LPR;
     const int half = p.rotary_dim / 2;
-    const int64_t n_rows = p.n_tok * p.H;
-    const int64_t stride = int64_t(gridDim.x) * kWarps * L::RPW;
+    int j0 = 0;
+    const bool rot_lane = lane_pairs<T, D, NEOX>(p.rotary_dim, c, &j0);
     T* x = static_cast<T*>(p.x);
-    for (int64_t base = (int64_t(blockIdx.x) * kWarps + warp) * L::RPW; base < n_rows;
-         base += stride) {
-        const int64_t row = base + rw;
-        bool active = row < n_rows;
-        int64_t P = 0;
-        if (active) {
-            P = p.positions[row / p.H];
-            if (P < 0 || P >= p.max_pos) {
-                if (c == 0) set_error(p.err, SK_DEVERR_POSITION_RANGE);
-                active = false;
+    for (int64_t tok = int64_t(blockIdx.x) * kWarps + warp; tok < p.n_tok; tok += int64_t(gridDim.x) * kWarps) {
+        uint4* xt = reinterpret_cast<uint4*>(x + tok * p.H * D) + c;  // this lane's chunk of row 0
+        const int64_t P = p.positions[tok];
+        const bool ok = P >= 0 && P < p.max_pos;  // the same in every lane
+        if (!ok) {
+            if (lane == 0) set_error(p.err, SK_DEVERR_POSITION_RANGE);
+            continue;
+        }
+        float4 cs[TCH];
+        const float4* trow = reinterpret_cast<const float4*>(p.table + P * half + j0);
+#pragma unroll
+        for (int i = 0; i < TCH; ++i) cs[i] = rot_lane ? __ldg(trow + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r0 = 0; r0 < p.H; r0 += kApplyPasses * L::RPW) {
+            uint4 raw[kApplyPasses];
+#pragma unroll
+            for (int u = 0; u < kApplyPasses; ++u) {
+                const int r = r0 + u * L::RPW + rw;
+                raw[u] = r < p.H ? xt[r * (D / L::VEC)] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kApplyPasses; ++u) {
+                const int r = r0 + u * L::RPW + rw;
+                float f[L::VEC];
+                ElemIO<T>::unpack(raw[u], f);
+                rotate_lane<T, D, NEOX>(f, raw[u], cs, p.rotary_dim, c, lane, r < p.H);  // every lane shuffles
+                if (r < p.H) xt[r * (D / L::VEC)] = ElemIO<T>::pack(f);
             }
         }
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        uint4* ptr = reinterpret_cast<uint4*>(x + row * D) + c;
-        if (active) raw = *ptr;
-        float f[L::VEC];
-        ElemIO<T>::unpack(raw, f);
-        int j0 = 0;
-        lane_pairs<T, D, NEOX>(p.rotary_dim, c, &j0);
-        rotate_lane<T, D, NEOX>(f, raw, reinterpret_cast<const float4*>(p.table + (active ? P : 0) * half + j0),
-                                p.rotary_dim, c, lane, active);
-        if (active) *ptr = ElemIO<T>::pack(f);
     }
 }
 
@@ -452,9 +464,7 @@ bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 
 template <typename T, int D, bool NEOX>
 cudaError_t launch_apply(const ApplyParams& p, cudaStream_t st) {
-    using L = RowLayout<T, D>;
-    const int64_t n_rows = p.n_tok * p.H;
-    int64_t blocks = (n_rows + kWarps * L::RPW - 1) / (kWarps * L::RPW);
+    int64_t blocks = (p.n_tok + kWarps - 1) / kWarps;  // one warp per token
     blocks = std::min<int64_t>(blocks, int64_t(device_sm_count()) * 8);
     if (blocks < 1) blocks = 1;
     rope_apply_kernel<T, D, NEOX><<<unsigned(blocks), kThreads, 0, st>>>(p);
