@@ -70,6 +70,41 @@ def test_rope_apply_matches_oracle(sk, dtype, D, r, neox, factor):
         assert torch.equal(torch.from_numpy(f64(x)[..., r:]), torch.from_numpy(x_in[..., r:]))
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("neox", [True, False])
+@pytest.mark.parametrize("H", [17, 40])
+def test_rope_apply_many_heads(sk, dtype, D, neox, H):
+    """Tokens of many heads: the kernel takes a token's rows in passes of several row
+    groups, so these head counts need more than one pass and end on a partial one."""
+    from sink_kv_attention_gb300 import synth
+    max_pos = 70000
+    table = sk.RopeTable(D, D, 1e4, max_pos, neox=neox)
+    n_tok = 301
+    x = synth.normal((n_tok, H, D), seed=7, dtype=dtype).cuda()
+    pos = synth.randint((n_tok,), seed=8, lo=0, hi=max_pos)
+    x_in = f64(x)
+    sk.rope_apply(table, x, pos.cuda())
+    spec = RopeSpec(D, D, 1e4, neox)
+    want = rope_rotate(x_in, pos.numpy(), spec.omega(), spec.mscale(), D, neox)
+    assert_rows_close(f64(x), want, dtype)
+
+
+def test_rope_apply_full_chunk_sampled(sk):
+    """The Q of a 32,768-token chunk at positions 32768.. (H_q=32, d_h=r=128, theta 5e5),
+    as a chunk prefilled over a cached prefix rotates it; sampled tokens."""
+    from sink_kv_attention_gb300 import synth
+    T, H, D, p0 = 32768, 32, 128, 32768
+    table = sk.RopeTable(D, D, 5e5, p0 + T)
+    x = synth.normal((T, H, D), seed=9, dtype=torch.bfloat16, device="cuda")
+    x_in = x.cpu()
+    sk.rope_apply(table, x, torch.arange(p0, p0 + T, dtype=torch.int64, device="cuda"))
+    rows = [0, 1, 7, 8, 4095, 16384, T - 2, T - 1]
+    spec = RopeSpec(D, D, 5e5, True)
+    want = rope_rotate(f64(x_in[rows]), [p0 + t for t in rows], spec.omega(), spec.mscale(), D, True)
+    assert_rows_close(f64(x[rows]), want, torch.bfloat16)
+
+
 def test_rope_apply_position_out_of_range_is_flagged(sk):
     table = sk.RopeTable(64, 64, 1e4, 100)
     x = torch.randn(3, 2, 64, device="cuda")
