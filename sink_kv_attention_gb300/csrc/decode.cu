@@ -711,38 +711,70 @@ template <typename T, int D, int NREP>
 __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
     constexpr int DPV = D / 32;
     constexpr int PF = NREP * (D + 2);
-    __shared__ int64_t pre[kMaxBatch + 1];
+    // the row prefix from the state as read before the wait (a guess) and after it
+    __shared__ int64_t pre[2][kMaxBatch + 1];
     const int lane = threadIdx.x & 31;
     pdl_trigger();
-    pdl_wait();  // the split kernel's partials are complete
-    if (threadIdx.x < 32) unit_prefix(p, pre, lane);
+    // Before the wait the state is final unless the append ahead of the split kernel is
+    // still running. The guess only picks the partials to load as soon as the wait
+    // returns, alongside the state read after it, which decides whether they are used.
+    if (threadIdx.x < 32) unit_prefix(p, pre[0], lane);
     __syncthreads();
     const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int Hq = p.Hkv * NREP;
-    if (warp_global >= p.B * Hq) return;
-    const int b = warp_global / Hq, hq = warp_global % Hq;
+    const bool active = warp_global < p.B * Hq;
+    const int b = active ? warp_global / Hq : 0, hq = active ? warp_global % Hq : 0;
     const int g = hq / NREP, h = hq % NREP;
-    const int64_t R = pre[p.B];
-    const int64_t Lb = (pre[b + 1] - pre[b]) / p.Hkv;
+    const int64_t unit = int64_t(b) * p.Hkv + g;
+    const int P = p.n_blocks;
+    // blocks fb..fb+n-1 own the unit's rows, except blocks whose row range is empty
+    // (possible when R < P): those wrote nothing and are skipped.
+    auto owns_rows = [&](int64_t c, int64_t R) { return (c * R + P - 1) / P < ((c + 1) * R + P - 1) / P; };
+    float mv[kCombineFew], lv[kCombineFew], vv[kCombineFew][DPV];
+    // every partial's max, sum and value slice of a unit cut between at most kCombineFew
+    // blocks, at once (one round trip to L2); a block that wrote nothing gives max -inf
+    auto load_few = [&](int64_t fb, int n, int64_t R) {
+        const float* base = p.ws + (fb + unit) * PF;
+#pragma unroll
+        for (int i = 0; i < kCombineFew; ++i) {
+            const bool own = i < n && owns_rows(fb + i, R);
+            const float* pp = base + i * PF;
+            mv[i] = own ? pp[h] : -INFINITY;
+            lv[i] = own ? pp[NREP + h] : 0.0f;
+#pragma unroll
+            for (int d = 0; d < DPV; ++d) vv[i][d] = own ? pp[2 * NREP + h * D + lane * DPV + d] : 0.0f;
+        }
+    };
+    // the guessed split of the unit; n0 = 0: nothing loaded early
+    int64_t fb0 = 0, R0 = pre[0][p.B];
+    int n0 = 0;
+    {
+        const int64_t s0 = pre[0][b], e0 = pre[0][b + 1];
+        const int64_t L0 = (e0 - s0) / p.Hkv;
+        if (active && R0 > 0 && L0 > 0 && s0 >= 0 && e0 <= R0) {
+            const int64_t st0 = s0 + int64_t(g) * L0;
+            fb0 = first_block_of(st0, R0, P);
+            const int64_t lb0 = first_block_of(st0 + L0 - 1, R0, P);
+            if (fb0 >= 0 && lb0 < P && lb0 - fb0 + 1 <= kCombineFew) n0 = int(lb0 - fb0 + 1);
+        }
+    }
+    pdl_wait();  // the split kernel's partials are complete
+    if (n0 > 0) load_few(fb0, n0, R0);
+    if (threadIdx.x < 32) unit_prefix(p, pre[1], lane);
+    __syncthreads();
+    if (!active) return;
+    const int64_t R = pre[1][p.B];
+    const int64_t Lb = (pre[1][b + 1] - pre[1][b]) / p.Hkv;
     T* o = static_cast<T*>(p.out) + (int64_t(b) * Hq + hq) * D + lane * DPV;
     if (Lb == 0) {
 #pragma unroll
         for (int d = 0; d < DPV; ++d) o[d] = T(0.0f);
         return;
     }
-    const int64_t st = pre[b] + int64_t(g) * Lb;
-    const int64_t fb = first_block_of(st, R, p.n_blocks);
-    const int64_t lb = first_block_of(st + Lb - 1, R, p.n_blocks);
-    const int64_t unit = int64_t(b) * p.Hkv + g;
-    // blocks fb..lb own the unit's rows, except blocks whose row range is empty
-    // (possible when R < P): those wrote nothing and are skipped.
-    const float* base = p.ws + (fb + unit) * PF;
+    const int64_t st = pre[1][b] + int64_t(g) * Lb;
+    const int64_t fb = first_block_of(st, R, P);
+    const int64_t lb = first_block_of(st + Lb - 1, R, P);
     const int n = int(lb - fb + 1);
-    const int P = p.n_blocks;
-    auto owns_rows = [&](int i) {
-        const int64_t c = fb + i;
-        return (c * R + P - 1) / P < ((c + 1) * R + P - 1) / P;
-    };
     // A learned sink is one more logit z (scaled-score units, clamped) in the
     // denominator with no value row ("RoPE, scaling, sliding window, attention sinks",
     // "Hybrid models break the uniform-spec assumption"); in base 2 it is z log2(e).
@@ -755,18 +787,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
     for (int d = 0; d < DPV; ++d) acc[d] = 0.0f;
     float lsum;
     if (n <= kCombineFew) {
-        // the usual case (a unit cut between at most kCombineFew blocks): every partial's
-        // max, sum and value slice are loaded at once, one round trip to L2
-        float mv[kCombineFew], lv[kCombineFew], vv[kCombineFew][DPV];
-#pragma unroll
-        for (int i = 0; i < kCombineFew; ++i) {
-            const bool own = i < n && owns_rows(i);
-            const float* pp = base + i * PF;
-            mv[i] = own ? pp[h] : -INFINITY;
-            lv[i] = own ? pp[NREP + h] : 0.0f;
-#pragma unroll
-            for (int d = 0; d < DPV; ++d) vv[i][d] = own ? pp[2 * NREP + h * D + lane * DPV + d] : 0.0f;
-        }
+        // the same blocks under the same ownership rule: the early loads are the partials
+        if (!(n0 == n && fb0 == fb && R0 == R)) load_few(fb, n, R);
         float M = z2;
 #pragma unroll
         for (int i = 0; i < kCombineFew; ++i) M = fmaxf(M, mv[i]);
@@ -780,13 +802,14 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
             for (int d = 0; d < DPV; ++d) acc[d] = fmaf(f, vv[i][d], acc[d]);
         }
     } else {
+        const float* base = p.ws + (fb + unit) * PF;
         float M = z2;
         for (int i = 0; i < n; ++i)
-            if (owns_rows(i)) M = fmaxf(M, base[i * PF + h]);
+            if (owns_rows(fb + i, R)) M = fmaxf(M, base[i * PF + h]);
         const float Mu = M == -INFINITY ? 0.0f : M;
         lsum = has_sink ? fast_exp2_approx(z2 - Mu) : 0.0f;
         for (int i = 0; i < n; ++i) {
-            if (!owns_rows(i)) continue;
+            if (!owns_rows(fb + i, R)) continue;
             const float* pp = base + i * PF;
             const float f = fast_exp2_approx(pp[h] - Mu);
             lsum = fmaf(f, pp[NREP + h], lsum);
