@@ -326,6 +326,18 @@ __global__ void __launch_bounds__(kThreads + 32) kv_append_kernel(AppendParams p
         fence_barrier_init();
     }
     pdl_trigger();  // the attention after this kernel may launch and run its prologue
+    if (warp == kWarps && lane == 0 && p.T == 1 && gridDim.x == 1) {
+        // A one-token append (a decode step): warm L2 with the token's rows and, at the
+        // position the state shows now, its cos/sin row, while earlier kernels finish.
+        // Only a hint: the copies after the wait read whatever is final.
+        const int64_t tok = int64_t(b);
+        if (hq > 0) bulk_prefetch_l2(static_cast<const IO*>(p.q) + tok * p.Hq * D, uint32_t(hq * D * sizeof(IO)));
+        bulk_prefetch_l2(static_cast<const IO*>(p.k) + tok * p.Hkv * D, uint32_t(p.Hkv * D * sizeof(IO)));
+        bulk_prefetch_l2(static_cast<const IO*>(p.v) + tok * p.Hkv * D, uint32_t(p.Hkv * D * sizeof(IO)));
+        const int64_t guess = p.pos[b];
+        if (half > 0 && guess >= 0 && guess < p.max_pos)
+            bulk_prefetch_l2(p.table + guess * half, uint32_t(half * sizeof(float2)));
+    }
     pdl_wait();     // earlier kernels (the previous step's attention) are done
     __syncthreads();
     const SeqState s = load_state(p, b);
