@@ -14,10 +14,10 @@ Page names used in the citations:
 * "#2961 rope: --rope-scaling dynamic" (strata pull request, page 3)
 * "Attention Sink 与 Streaming KV Cache" (llm-glossary, page 4)
 
-Precision: float64 throughout, except where a floating-point value decides an
-integer (the int8 requantisation code).  The pages do not fix that precision, so
-the decision is taken in float32, the precision the CUDA kernel uses
-(``quantize_int8_rows``).
+Precision: float64 throughout, including where a floating-point value decides an
+integer (the int8 code rint(x / scale) of ``quantize_int8_rows``).  Parity tests
+treat values within 1e-3 of a rounding tie as undecided: there either neighbour
+is a correct rounding.
 
 Parity status: every function below is pinned by ``tests/test_oracle_*.py``
 against values the pages print, closed forms, invariants or library routines.
@@ -209,28 +209,25 @@ def rerotate(k_a: np.ndarray, positions: Sequence[int], spec_a: RopeSpec,
 
 
 # ---------------------------------------------------------------------------
-# int8 keys with one float32 scale per row.
+# int8 keys with one scale per row.
 # ---------------------------------------------------------------------------
 
 def quantize_int8_rows(x: np.ndarray):
-    """Symmetric absmax int8 codes with one scale per row (last axis).
+    """Symmetric absmax int8 codes with one scale per row (last axis), in float64.
 
     scale = max_k |x_k| / 127 (a zero row gets scale 1 and codes 0);
-    code = clamp(rint(x * (127 / max_k |x_k|)), -127, 127), rint rounding half to even.
-    The pages fix neither the rounding nor its precision ("#2961", "What it does":
-    dequantize, turn, requantize), so the decision is taken the way the CUDA kernel
-    takes it, in float32: x is rounded to float32 first, the row's reciprocal
-    127 / max|x| is one IEEE float32 division, and each code is rint of the float32
-    product.
+    code = clamp(rint(x / scale), -127, 127), rint rounding half to even.
+    "#2961 rope: --rope-scaling dynamic", "What it does": int8 keys are dequantized,
+    turned and requantized; its parity table measures errors in int8 steps (the
+    scale).  The pages fix neither the scale rule nor the rounding; the reading
+    taken is the symmetric absmax rule with one scale per row, its division and
+    rounding done on the float64 row as written here.
     """
-    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
-    amax = np.max(np.abs(x32), axis=-1, keepdims=True)
-    zero = amax == 0
-    safe = np.where(zero, np.float32(1.0), amax).astype(np.float32)
-    scale = np.where(zero, np.float32(1.0), (safe / np.float32(127.0)).astype(np.float32)).astype(np.float32)
-    inv = (np.float32(127.0) / safe).astype(np.float32)
-    q = np.rint((x32 * inv).astype(np.float32))
-    q = np.where(zero, np.float32(0.0), q)
+    x = np.asarray(x, dtype=np.float64)
+    amax = np.max(np.abs(x), axis=-1, keepdims=True)
+    zero = amax == 0.0
+    scale = np.where(zero, 1.0, amax / 127.0)
+    q = np.where(zero, 0.0, np.rint(x / scale))
     codes = np.clip(q, -127, 127).astype(np.int8)
     return codes, scale[..., 0]
 

@@ -7,7 +7,7 @@ import pytest
 
 from oracle.sinkkv_oracle import (RopeSpec, kv_bytes_per_token, rope_inv_freq, rope_rotate,
                                   yarn_correction_dim, yarn_correction_range, yarn_inv_freq,
-                                  yarn_mscale)
+                                  yarn_linear_ramp, yarn_mscale)
 
 
 def _floats(s):
@@ -142,6 +142,38 @@ def test_yarn_regions_and_degenerate_factor():
     assert np.all(y[mid] < plain[mid]) and np.all(y[mid] > plain[mid] / s)
     np.testing.assert_allclose(yarn_inv_freq(r, theta, 1.0, L0), plain, rtol=1e-15)
     assert np.array_equal(RopeSpec(r, r, theta, yarn_factor=1.0).omega(), plain)
+
+
+def test_yarn_band_is_linear_in_the_pair_index():
+    """Inside the band the page's ramp is linear in i, so omega_i * pos_freq_i =
+    1 - ramp_i (1 - 1/s) has zero second differences over pairs low .. high, and at
+    the band's midpoint i = 33 of (20, 46) it is exactly halfway between 1 and 1/s
+    ("RoPE, scaling, sliding window, attention sinks", "YaRN, precisely")."""
+    r, theta, L0, s = 128, 1e4, 4096, 8.0
+    y = yarn_inv_freq(r, theta, s, L0)
+    pos_freq = theta ** (np.arange(0, r, 2) / r)
+    rel = y * pos_freq                     # 1 below the band, 1/s above it
+    band = rel[20:47]
+    np.testing.assert_allclose(np.diff(band, 2), 0.0, atol=1e-14)
+    assert rel[33] == pytest.approx((1.0 + 1.0 / s) / 2.0, rel=1e-14)
+    # the step per pair is (1 - 1/s) / (high - low)
+    np.testing.assert_allclose(np.diff(band), -(1.0 - 1.0 / s) / 26.0, rtol=1e-12)
+
+
+def test_yarn_ramp_degenerate_band_is_a_step():
+    """low == high: the page's ramp moves high by 0.001 to avoid dividing by zero,
+    which makes the ramp a step, 0 up to and including pair low and 1 after it."""
+    assert yarn_linear_ramp(5, 5, 10).tolist() == [0.0] * 6 + [1.0] * 4
+    assert yarn_linear_ramp(0, 0, 4).tolist() == [0.0, 1.0, 1.0, 1.0]
+    # the same branch reached through the whole frequency blend: with L0 = 6 every
+    # pair turns less than once in L0 tokens, d(1) < 0 and d(32) < 0, so the band
+    # clamps to (0, 0); pair 0 keeps its frequency 1 and every other pair is divided by s
+    r, theta, L0, s = 128, 1e4, 6, 4.0
+    assert yarn_correction_range(32, 1, r, theta, L0) == (0, 0)
+    y = yarn_inv_freq(r, theta, s, L0)
+    plain = theta ** (-np.arange(0, r, 2) / r)
+    assert y[0] == 1.0
+    np.testing.assert_allclose(y[1:], plain[1:] / s, rtol=1e-15)
 
 
 def test_kv_bytes_context_numbers(golden):
