@@ -46,6 +46,29 @@ def randint(shape, seed: int, lo: int, hi: int, device="cpu") -> torch.Tensor:
     return torch.randint(lo, hi, tuple(shape), generator=g, dtype=torch.int64, device=device)
 
 
+def sparse_signs(shape, seed: int, density: float, dtype=torch.bfloat16, device="cpu") -> torch.Tensor:
+    """Values in {-1, 0, +1}: each entry is +1 or -1 with probability density / 2 each,
+    else 0.  Exact in every float format; sums of them are small integers."""
+    g = generator(seed, device)
+    u = torch.rand(*shape, generator=g, dtype=torch.float32, device=device)
+    x = torch.zeros_like(u)
+    x[u < density / 2] = 1.0
+    x[(u >= density / 2) & (u < density)] = -1.0
+    return x.to(dtype)
+
+
+def fill_sparse_signs_(t: torch.Tensor, seed: int, density: float) -> torch.Tensor:
+    """sparse_signs into a (possibly huge) device tensor, in place."""
+    g = generator(seed, t.device)
+    flat = t.view(-1)
+    step = 1 << 28
+    for i in range(0, flat.numel(), step):
+        chunk = flat[i:i + step]
+        u = torch.rand(chunk.numel(), generator=g, dtype=torch.float32, device=t.device)
+        chunk.copy_(torch.where(u < density / 2, 1.0, torch.where(u < density, -1.0, 0.0)))
+    return t
+
+
 def fill_normal_(t: torch.Tensor, seed: int) -> torch.Tensor:
     """Fill a (possibly huge) device tensor with N(0,1) draws, in place."""
     g = generator(seed, t.device)

@@ -5,9 +5,10 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.sinkkv_oracle import GlobalCache, RingCache, RopeSpec, attend, rope_rotate
+from oracle.sinkkv_oracle import GlobalCache, RingCache, RopeSpec, attend, quantize_int8_rows, rope_rotate
 from sink_kv_attention_gb300 import synth
-from tests.test_gpu_rope_append_decode import BF16_ATTN_ATOL, f64
+from tests.test_gpu_rerotate import assert_int8_requant
+from tests.test_gpu_rope_append_decode import f64, BF16_ATTN_ATOL
 
 pytestmark = pytest.mark.gpu
 
@@ -26,6 +27,61 @@ def sk():
 def _dequant_keys(layer, b):
     """[Hkv, C, D] float64 keys of sequence b: code * scale."""
     return f64(layer.k[b].to(torch.float32)) * f64(layer.k_scale[b])[..., None]
+
+
+@pytest.mark.parametrize("kind", ["ring", "global"])
+@pytest.mark.parametrize("Dh,r", [(128, 128), (128, 64), (64, 64)])
+@pytest.mark.parametrize("neox", [True, False])
+def test_int8_append_codes_match_oracle_quantisation(sk, kind, Dh, r, neox):
+    """The quantising append, code by code: every stored row's codes and scale against
+    the oracle's int8 rule on the float64 rotated key, quantize_int8_rows(rope_rotate(k))
+    ("#2961 rope: --rope-scaling dynamic", "What it does": int8 K, one scale per row).
+    Codes are exact except within 1e-3 of a rounding tie; scales within 1e-5 relative.
+    Chunks of one token (decode mode) and longer ones, ring wrap and global prefix;
+    rows of zeros get scale 1 and codes 0."""
+    B, Hq, Hkv, S, W = 2, 8, 2, 3, 29
+    chunks = [1, 4, 1, 17, 2, 40, 1, 9]
+    total = sum(chunks)
+    tbl = sk.RopeTable(Dh, r, 1e4, 512, neox=neox)
+    spec = RopeSpec(Dh, r, 1e4, neox)
+    if kind == "ring":
+        layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, Dh, sinks=S, window=W, k_dtype=torch.int8)
+        caches = [RingCache(S, W) for _ in range(B)]
+    else:
+        layer = sk.KVLayer.allocate(sk.SK_LAYER_GLOBAL, B, Hkv, Dh, capacity=total + 5, k_dtype=torch.int8)
+        caches = [GlobalCache(total + 5) for _ in range(B)]
+    k_all = synth.normal((B, total, Hkv, Dh), 43, torch.bfloat16)
+    k_all[1, 5, 0] = 0.0                      # a zero row: scale 1, codes 0
+    v_all = synth.normal((B, total, Hkv, Dh), 44, torch.bfloat16)
+    want_codes, want_scale, turned = [], [], []
+    for b in range(B):
+        kr = rope_rotate(f64(k_all[b]), np.arange(total), spec.omega(), 1.0, r, neox)   # [total, Hkv, D]
+        c_, s_ = quantize_int8_rows(kr)
+        want_codes.append(c_)
+        want_scale.append(s_)
+        turned.append(kr)
+    done = 0
+    for T in chunks:
+        sk.kv_append(tbl, layer, None, k_all[:, done:done + T].clone().cuda(), v_all[:, done:done + T].clone().cuda())
+        for b in range(B):
+            caches[b].append([done + t for t in range(T)])
+        done += T
+        torch.cuda.synchronize()
+        codes, scales = layer.k.cpu().numpy(), layer.k_scale.cpu().numpy()
+        for b in range(B):
+            if kind == "ring":
+                slots = caches[b].chronological_slots()
+                held = caches[b].chronological_positions()
+            else:
+                slots = held = list(range(done))
+            got_c = codes[b][:, slots].transpose(1, 0, 2)          # [n, Hkv, D]
+            got_s = scales[b][:, slots].transpose(1, 0)            # [n, Hkv]
+            assert_int8_requant(got_c, got_s, want_codes[b][held], want_scale[b][held], turned[b][held])
+            assert np.array_equal(f64(layer.v[b][:, slots].transpose(0, 1)), f64(v_all[b, held]))
+    assert want_scale[1][5, 0] == 1.0 and not want_codes[1][5, 0].any()
+    if kind == "global":
+        assert float(layer.k_scale[1, 0, 5]) == 1.0 and not layer.k[1, 0, 5].any()
+    assert layer.error_bits() == 0
 
 
 @pytest.mark.parametrize("kind", ["ring", "global"])

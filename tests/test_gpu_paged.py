@@ -47,7 +47,7 @@ class HostAllocator:
                 table[b, j] = -1
 
 
-def _run_paged(sk, *, dtype, D, r, Hq, Hkv, bs, S, W, n_sink_blocks, lengths, chunks, seed):
+def _run_paged(sk, *, dtype, D, r, Hq, Hkv, bs, S, W, n_sink_blocks, lengths, chunks, seed, neox=True):
     """Append raw tokens chunk by chunk through the library (allocating blocks before
     each append and freeing those the window left), then decode the last token's
     query; returns everything the oracle needs."""
@@ -67,8 +67,8 @@ def _run_paged(sk, *, dtype, D, r, Hq, Hkv, bs, S, W, n_sink_blocks, lengths, ch
         layer.sink_block_ids.copy_(torch.tensor(sink_ids, dtype=torch.int32))
         layer.k_pool[sink_ids] = sink_k.cuda()
         layer.v_pool[sink_ids] = sink_v.cuda()
-    tbl = sk.RopeTable(D, r, 1e4, total + 8)
-    spec = RopeSpec(D, r, 1e4)
+    tbl = sk.RopeTable(D, r, 1e4, total + 8, neox=neox)
+    spec = RopeSpec(D, r, 1e4, neox)
     raw_q = synth.normal((B, total, Hq, D), seed, dtype)
     raw_k = synth.normal((B, total, Hkv, D), seed + 1, dtype)
     raw_v = synth.normal((B, total, Hkv, D), seed + 2, dtype)
@@ -113,7 +113,7 @@ def _oracle_pool(layer_shape, table, sink_ids, sink_k, sink_v, raw_k, raw_v, len
         kp[blk] = f64(sink_k[j])
         vp[blk] = f64(sink_v[j])
     for b, L in enumerate(lengths):
-        kr = rope_rotate(f64(raw_k[b, :L]), np.arange(L), spec.omega(), 1.0, r)
+        kr = rope_rotate(f64(raw_k[b, :L]), np.arange(L), spec.omega(), 1.0, r, spec.neox)
         for P in range(L):
             blk = table[b, P // bs]
             if blk >= 0:
@@ -137,12 +137,19 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=[f"case{i}" for i in range(len(CASES))])
-def test_paged_append_and_decode_match_oracle(sk, case):
+# GPT-J (interleaved) pairing through the paged append: partial and full rotary, bf16
+# and fp32, with and without static sink blocks
+GPTJ_CASES = [CASES[1], CASES[2], CASES[0], CASES[5]]
+
+
+@pytest.mark.parametrize("case,neox", [(c, True) for c in CASES] + [(c, False) for c in GPTJ_CASES],
+                         ids=[f"case{i}" for i in range(len(CASES))] +
+                             [f"gptj{i}" for i in range(len(GPTJ_CASES))])
+def test_paged_append_and_decode_match_oracle(sk, case, neox):
     dtype, D, r, Hq, Hkv, bs, S, W, nsb, lengths, chunks = case
     layer, table, sink_ids, sink_k, sink_v, raw_q, raw_k, raw_v, q_last, spec = _run_paged(
         sk, dtype=dtype, D=D, r=r, Hq=Hq, Hkv=Hkv, bs=bs, S=S, W=W, n_sink_blocks=nsb, lengths=lengths,
-        chunks=chunks, seed=300)
+        chunks=chunks, seed=300, neox=neox)
     kp, vp = _oracle_pool(tuple(layer.k_pool.shape), table, sink_ids, sink_k, sink_v, raw_k, raw_v, lengths, spec,
                           bs, r)
     sink_len = nsb * bs
@@ -158,7 +165,7 @@ def test_paged_append_and_decode_match_oracle(sk, case):
     tol = F32_ATTN_ATOL if dtype == torch.float32 else BF16_ATTN_ATOL
     for b, L in enumerate(lengths):
         full_row = np.concatenate([np.array(sink_ids, dtype=np.int64), table[b]])
-        qr = rope_rotate(f64(raw_q[b, L - 1:L]), [L - 1], spec.omega(), 1.0, r)[0]
+        qr = rope_rotate(f64(raw_q[b, L - 1:L]), [L - 1], spec.omega(), 1.0, r, neox)[0]
         want = paged_decode_attention(qr, kp, vp, full_row, L + sink_len, bs, S, W if W > 0 else None)
         np.testing.assert_allclose(out[b], want, rtol=0, atol=tol)
     assert layer.error_bits() == 0

@@ -193,13 +193,18 @@ def test_decode_visible_set_probe(sk):
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("kind", ["ring", "global"])
 @pytest.mark.parametrize("D,r", [(128, 64), (64, 64), (128, 128)])
-def test_chunked_append_state_and_decode(sk, dtype, kind, D, r):
+@pytest.mark.parametrize("neox", [True, False])
+def test_chunked_append_state_and_decode(sk, dtype, kind, D, r, neox):
+    """Fused RoPE + append, chunk by chunk, in NeoX (j, j + r/2) and GPT-J (2j, 2j + 1)
+    pairing ("RoPE, scaling, sliding window, attention sinks", RoPE section: the two
+    pairings give different keys), partial rotary included: rotated Q and K, cached
+    rows and ring state against the oracle, then a decode over the cache."""
     from sink_kv_attention_gb300 import synth
     B, Hq, Hkv, S, W = 2, 8, 2, 3, 5
     chunks = [1, 2, 3, 5, 7, 1, 11, 4, 1, 6, 1, 1]
     total = sum(chunks)
-    tbl = sk.RopeTable(D, r, 1e4, 256, neox=True)
-    spec = RopeSpec(D, r, 1e4, True)
+    tbl = sk.RopeTable(D, r, 1e4, 256, neox=neox)
+    spec = RopeSpec(D, r, 1e4, neox)
     if kind == "ring":
         layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W, k_dtype=dtype, v_dtype=dtype)
         caches = [RingCache(S, W) for _ in range(B)]
@@ -217,8 +222,8 @@ def test_chunked_append_state_and_decode(sk, dtype, kind, D, r):
         sk.kv_append(tbl, layer, q, k, v)
         pos = list(range(done, done + T))
         for b in range(B):
-            qr = rope_rotate(f64(q_all[b, done:done + T]), pos, spec.omega(), 1.0, r)
-            kr = rope_rotate(f64(k_all[b, done:done + T]), pos, spec.omega(), 1.0, r)
+            qr = rope_rotate(f64(q_all[b, done:done + T]), pos, spec.omega(), 1.0, r, neox)
+            kr = rope_rotate(f64(k_all[b, done:done + T]), pos, spec.omega(), 1.0, r, neox)
             assert_rows_close(f64(q[b]), qr, dtype)
             assert_rows_close(f64(k[b]), kr, dtype)
             caches[b].append([(kr[t], f64(v_all[b, done + t])) for t in range(T)])
@@ -237,7 +242,7 @@ def test_chunked_append_state_and_decode(sk, dtype, kind, D, r):
         # decode attention of the chunk's last query over the cache
         out = sk.decode_attention(layer, q[:, -1].contiguous())
         for b in range(B):
-            qr_last = rope_rotate(f64(q_all[b, done - 1:done]), [done - 1], spec.omega(), 1.0, r)[0]
+            qr_last = rope_rotate(f64(q_all[b, done - 1:done]), [done - 1], spec.omega(), 1.0, r, neox)[0]
             want = o_decode(caches[b], qr_last)
             tol = F32_ATTN_ATOL if dtype == torch.float32 else BF16_ATTN_ATOL
             np.testing.assert_allclose(f64(out[b]), want, rtol=0, atol=tol)
