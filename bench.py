@@ -30,25 +30,50 @@ if ROOT not in sys.path:
 METRIC = "sink+window decode attn KV-read GB/s (frac of HBM peak), tokens/s, keys/s"
 
 
-def _profiled_traffic(summary="decode_split_window_b32.md"):
-    """DRAM bytes per launch of the split-K decode kernel from a committed ncu summary,
-    or None when the kernel sources changed since that capture."""
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel from one
+# ncu capture, stated here with the sha256 of every source the captured build came from.
+# A row reports it only while those sources are unchanged, else null.  "scale": the capture
+# ran a smaller case of the same kernel; the traffic grows in proportion to the units
+# processed and is scaled by that factor to one launch of the full workload.
+NCU_TRAFFIC = {
+    "decode_window_b32": dict(
+        bytes=540113408, scale=1,
+        capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --steps 5 --warmup 3 "
+                "--no-cpu-baseline (split kernel only)",
+        sources={"decode.cu": "8c96fd4d98b61f9203207f41fa2780aa91f52e775cc43f1c8f744042f1e39dca",
+                 "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}),
+    "prefill_attn_t32768": dict(
+        bytes=634700000, scale=1,
+        capture="ncu --set full -k regex:prefill_attn -s 2 -c 1, python bench.py --workload prefill "
+                "--steps 3 --warmup 2",
+        sources={"prefill.cu": "3f102412d55ba7e80eb45b10daa6829898fddb2114ab587302e021dd8c040a46"}),
+    "rerotate_bf16_48l": dict(
+        bytes=2358400000, scale=12,
+        capture="ncu --set full -k regex:rerotate_bf16 -s 2 -c 1, python bench.py --workload rerotate_bf16 "
+                "--layers 4 --steps 3 --warmup 2 (4 of 48 layers, x12)",
+        sources={"rerotate.cu": "d3577ee983e461c227d117bf96e81fbb3eb4d59417b4704116cc72c317f3b411"}),
+    "rerotate_i8_48l": dict(
+        bytes=2421800000, scale=12,
+        capture="ncu --set full -k regex:rerotate_i8 -s 2 -c 1, python bench.py --workload rerotate_i8 "
+                "--layers 4 --steps 3 --warmup 2 (4 of 48 layers, x12)",
+        sources={"rerotate.cu": "d3577ee983e461c227d117bf96e81fbb3eb4d59417b4704116cc72c317f3b411"}),
+}
+
+
+def _traffic(name):
+    """Per-launch DRAM bytes of NCU_TRAFFIC[name] while its sources are unchanged, else None."""
     import hashlib
-    import re
-    try:
-        with open(os.path.join(ROOT, "profiles", summary)) as f:
-            text = f.read()
-        m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-        pairs = re.findall(r"(\w+\.cuh?) sha256 ([0-9a-f]{64})", text)
-        if not m or not pairs:
-            return None
-        for name, digest in pairs:
-            with open(os.path.join(ROOT, "sink_kv_attention_gb300", "csrc", name), "rb") as f:
+    ent = NCU_TRAFFIC.get(name)
+    if ent is None:
+        return None
+    for fname, digest in ent["sources"].items():
+        try:
+            with open(os.path.join(ROOT, "sink_kv_attention_gb300", "csrc", fname), "rb") as f:
                 if hashlib.sha256(f.read()).hexdigest() != digest:
                     return None
-        return int(m.group(1))
-    except OSError:
-        return None
+        except OSError:
+            return None
+    return int(ent["bytes"] * ent["scale"])
 
 
 def _peaks():
@@ -204,7 +229,7 @@ def bench_window(args, rank, world):
     steps, warm = args.steps, args.warmup
     tbl, layer, c = window_setup(seed_base=replica_seed_base(rank), steps=2 * steps + warm + 2)
     B, Hq, Hkv, D, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["W"]
-    n = 2 * steps + warm
+    n = steps + warm
     # one fresh token per sequence per step, resident in HBM before timing
     qs = synth.normal((n, B, 1, Hq, D), 14, torch.bfloat16, device="cuda")
     ks = synth.normal((n, B, 1, Hkv, D), 15, torch.bfloat16, device="cuda")
@@ -214,179 +239,137 @@ def bench_window(args, rank, world):
     stream = torch.cuda.current_stream()
     zl = _learned_sinks(args, Hq)
 
-    def step(i, ev=None):
-        st = torch.cuda.current_stream()  # the capture stream while a graph is captured
+    def step(i):
         sk.kv_append(tbl, layer, qs[i], ks[i], vs[i])
-        if ev is not None:
-            ev[0].record(st)
         sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws, sink_logits=zl)
-        if ev is not None:
-            ev[1].record(st)
 
     for i in range(warm):
         step(i)
     torch.cuda.synchronize()
     # The timed steps run as one captured CUDA graph, the way a serving loop runs decode
-    # (the library's calls keep all state on the device, so they capture).  That graph
-    # holds no timing events between the kernels: an event node would serialise the
-    # programmatic-dependent launches.  The decode launches are timed with events in a
-    # second captured pass of as many steps right after.
-    graph = None
-    if not args.eager:
-        state0 = [t.clone() for t in (layer.pos, layer.head, layer.count)]
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for i in range(steps):
-                step(warm + i)
-        torch.cuda.synchronize()
-        # the graph's first launch also uploads it: replay once untimed, then put the
-        # ring state back so that the timed replay makes the same appends and reads
-        graph.replay()
-        torch.cuda.synchronize()
-        for t, s0 in zip((layer.pos, layer.head, layer.count), state0):
-            t.copy_(s0)
-        torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # (the library's calls keep all state on the device, so they capture).  The graph is
+    # replayed until the timed region lasts at least TARGET_MS; after every replay the
+    # ring counters are put back, so every replay makes the same appends and reads.
+    reset = _state_saver([layer])
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     if rank == 0:
         clocks.start()
         time.sleep(0.3)
-    _barrier(world)
-    torch.cuda.synchronize()
-    clocks.mark("start")
-    t_start.record(stream)
-    if graph is not None:
-        graph.replay()
+    if args.eager:
+        graph = None
+        per = []
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+        _barrier(world)
+        torch.cuda.synchronize()
+        clocks.mark("start")
+        t0 = time.perf_counter()
+        for a, b in ev:
+            a.record(stream)
+            for i in range(steps):
+                step(warm + i)
+            b.record(stream)
+            reset()
+        torch.cuda.synchronize()
+        clocks.mark("end")
+        per = [a.elapsed_time(b) / steps for a, b in ev]
+        region_ms, R = (time.perf_counter() - t0) * 1e3, len(ev)
     else:
-        for i in range(steps):
-            step(warm + i)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clocks.mark("end")
-    _barrier(world)
+        graph = _capture(step, warm, steps)
+        per, region_ms, R = _replays(graph, steps, TARGET_MS, reset=reset, clocks=clocks, world=world)
     if rank == 0:
         clocks.stop()
-    # per-launch timing of the decode attention call
-    dec_ev = None
-    if graph is not None:
-        try:
-            dec_ev = [(torch.cuda.Event(enable_timing=True, external=True),
-                       torch.cuda.Event(enable_timing=True, external=True)) for _ in range(steps)]
-            g2 = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g2):
-                for i in range(steps):
-                    step(warm + steps + i, dec_ev[i])
-            g2.replay()
-        except TypeError:
-            dec_ev = None
-    if dec_ev is None:
-        dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for i in range(steps):
-            step(warm + steps + i, dec_ev[i])
-    torch.cuda.synchronize()
-    ms = t_start.elapsed_time(t_end)
-    ms = _max_over_ranks(ms, world)
-    dec_ms = sum(a.elapsed_time(b) for a, b in dec_ev) / steps
     assert layer.error_bits() == 0
+    ms_step = _max_over_ranks(statistics.median(per), world)
 
     L = c["S"] + W  # visible keys per sequence (ring full)
     kv_bytes = B * Hkv * L * D * 2 * 2
     alg_bytes_decode = kv_bytes + 2 * (B * Hq * D * 2)          # + q read, out write
-    ms_step = ms / steps
     value = weak_scaling_value(kv_bytes, ms_step, world)
+    # the dominant kernel, decode attention: its launches back to back in one graph
+    roof = _launch_roofline(lambda i: sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws, sink_logits=zl),
+                            steps, alg_bytes_decode, "decode_window_b32",
+                            "decode attention (split-K + combine); its launches back to back in one graph",
+                            "K+V of 4096 visible rows x 32 sequences x 8 kv heads + q + out")
 
     # end to end through the public API with host buffers: pinned inputs copied in,
     # the output copied out, every step.  A serving loop overlaps the copies of the next
     # step with the current step's kernels: the device inputs and outputs are double
     # buffered and the copies run on a second stream, ordered by events.
-    e2e = None
-    if True:
-        hq = torch.empty((steps, B, 1, Hq, D), dtype=torch.bfloat16).pin_memory()
-        hk = torch.empty((steps, B, 1, Hkv, D), dtype=torch.bfloat16).pin_memory()
-        hv = torch.empty((steps, B, 1, Hkv, D), dtype=torch.bfloat16).pin_memory()
-        hq.copy_(qs[:steps].cpu()); hk.copy_(ks[:steps].cpu()); hv.copy_(vs[:steps].cpu())
-        hout = torch.empty((steps, B, Hq, D), dtype=torch.bfloat16).pin_memory()
-        dq = [torch.empty_like(qs[0]) for _ in range(2)]
-        dk = [torch.empty_like(ks[0]) for _ in range(2)]
-        dv = [torch.empty_like(vs[0]) for _ in range(2)]
-        dout = [torch.empty_like(out) for _ in range(2)]
-        tbl2, layer2, _ = window_setup(seed_base=100 * rank + 7, steps=steps + 2)
-        copy_stream = torch.cuda.Stream()
+    hq = torch.empty((steps, B, 1, Hq, D), dtype=torch.bfloat16).pin_memory()
+    hk = torch.empty((steps, B, 1, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty((steps, B, 1, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    hq.copy_(qs[:steps].cpu()); hk.copy_(ks[:steps].cpu()); hv.copy_(vs[:steps].cpu())
+    hout = torch.empty((steps, B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    dq = [torch.empty_like(qs[0]) for _ in range(2)]
+    dk = [torch.empty_like(ks[0]) for _ in range(2)]
+    dv = [torch.empty_like(vs[0]) for _ in range(2)]
+    dout = [torch.empty_like(out) for _ in range(2)]
+    tbl2, layer2, _ = window_setup(seed_base=100 * rank + 7, steps=steps + 2)
+    copy_stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def e2e_steps():
+        comp = torch.cuda.current_stream()
+        # event lists per step: inputs landed, step computed, output read back
+        landed = [torch.cuda.Event() for _ in range(steps)]
+        computed = [torch.cuda.Event() for _ in range(steps)]
+        read = [torch.cuda.Event() for _ in range(steps)]
+
+        def h2d(i):
+            j = i % 2
+            copy_stream.wait_stream(comp) if i == 0 else None
+            if i >= 2:
+                copy_stream.wait_event(computed[i - 2])   # buffers j free again
+            with torch.cuda.stream(copy_stream):
+                dq[j].copy_(hq[i], non_blocking=True)
+                dk[j].copy_(hk[i], non_blocking=True)
+                dv[j].copy_(hv[i], non_blocking=True)
+                landed[i].record(copy_stream)
+
+        h2d(0)
+        for i in range(steps):
+            j = i % 2
+            if i + 1 < steps:
+                h2d(i + 1)
+            comp.wait_event(landed[i])
+            if i >= 2:
+                comp.wait_event(read[i - 2])   # out buffer j read back
+            sk.kv_append(tbl2, layer2, dq[j], dk[j], dv[j])
+            sk.decode_attention(layer2, dq[j][:, 0], out=dout[j], workspace=ws, sink_logits=zl)
+            computed[i].record(comp)
+            copy_stream.wait_event(computed[i])
+            with torch.cuda.stream(copy_stream):
+                hout[i].copy_(dout[j], non_blocking=True)
+                read[i].record(copy_stream)
+        comp.wait_stream(copy_stream)
+
+    reset2 = _state_saver([layer2])
+    if graph is not None:  # the same calls, host copies included, as one captured graph
+        g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_e2e):
+            e2e_steps()
         torch.cuda.synchronize()
-
-        def e2e_steps():
-            comp = torch.cuda.current_stream()
-            # event lists per step: inputs landed, step computed, output read back
-            landed = [torch.cuda.Event() for _ in range(steps)]
-            computed = [torch.cuda.Event() for _ in range(steps)]
-            read = [torch.cuda.Event() for _ in range(steps)]
-
-            def h2d(i):
-                j = i % 2
-                copy_stream.wait_stream(comp) if i == 0 else None
-                if i >= 2:
-                    copy_stream.wait_event(computed[i - 2])   # buffers j free again
-                with torch.cuda.stream(copy_stream):
-                    dq[j].copy_(hq[i], non_blocking=True)
-                    dk[j].copy_(hk[i], non_blocking=True)
-                    dv[j].copy_(hv[i], non_blocking=True)
-                    landed[i].record(copy_stream)
-
-            h2d(0)
-            for i in range(steps):
-                j = i % 2
-                if i + 1 < steps:
-                    h2d(i + 1)
-                comp.wait_event(landed[i])
-                if i >= 2:
-                    comp.wait_event(read[i - 2])   # out buffer j read back
-                sk.kv_append(tbl2, layer2, dq[j], dk[j], dv[j])
-                sk.decode_attention(layer2, dq[j][:, 0], out=dout[j], workspace=ws, sink_logits=zl)
-                computed[i].record(comp)
-                copy_stream.wait_event(computed[i])
-                with torch.cuda.stream(copy_stream):
-                    hout[i].copy_(dout[j], non_blocking=True)
-                    read[i].record(copy_stream)
-            comp.wait_stream(copy_stream)
-
-        state0 = [t.clone() for t in (layer2.pos, layer2.head, layer2.count)]
-        g_e2e = None
-        if not args.eager:  # the same calls, host copies included, as one captured graph
-            g_e2e = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_e2e):
-                e2e_steps()
+        per_e, _, _ = _replays(g_e2e, steps, TARGET_MS / 2, reset=reset2, world=world)
+    else:
+        per_e = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            e2e_steps()
+            e1.record(stream)
             torch.cuda.synchronize()
-        # One untimed pass first (the graph's first launch uploads it; the copy engines
-        # first touch the pinned pages), then the ring state is put back, so the timed
-        # pass makes exactly the same appends and reads.
-        if g_e2e is not None:
-            g_e2e.replay()
-        else:
-            e2e_steps()
-        torch.cuda.synchronize()
-        for t, s0 in zip((layer2.pos, layer2.head, layer2.count), state0):
-            t.copy_(s0)
-        torch.cuda.synchronize()
-        _barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        if g_e2e is not None:
-            g_e2e.replay()
-        else:
-            e2e_steps()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world) / steps
-        if layer2.error_bits() != 0:  # a skipped append would make the timed pass do less work
-            raise RuntimeError(f"end-to-end pass set device error bits {layer2.error_bits():#x}")
-        h2d_bytes = (hq[0].numel() + hk[0].numel() + hv[0].numel()) * 2
-        e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": hout[0].numel() * 2,
-               "ms_per_step": round(e2e_ms, 5),
-               "overlap": "next step's inputs copied in on a second stream during this step"}
+            reset2()
+            per_e.append(e0.elapsed_time(e1) / steps)
+    e2e_ms = _max_over_ranks(statistics.median(per_e), world)
+    if layer2.error_bits() != 0:  # a skipped append would make the timed pass do less work
+        raise RuntimeError(f"end-to-end pass set device error bits {layer2.error_bits():#x}")
+    h2d_bytes = (hq[0].numel() + hk[0].numel() + hv[0].numel()) * 2
+    e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": hout[0].numel() * 2,
+           "ms_per_step": round(e2e_ms, 5),
+           "overlap": "next step's inputs copied in on a second stream during this step"}
 
     hbm, _, _, peak_kind = _peaks()
-    achieved = alg_bytes_decode / (dec_ms * 1e-3) / 1e9
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -401,14 +384,14 @@ def bench_window(args, rank, world):
         "frac_of_hbm_peak": round(value / world / hbm, 4),
         "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
         "keys_per_s": round(world * B * L / (ms_step * 1e-3), 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": _profiled_traffic(),
-                     "kernel": "decode attention (split-K + combine), per launch, events in a second captured pass of the same steps",
-                     "algorithmic_bytes_per_launch": alg_bytes_decode,
-                     "launch_ms": round(dec_ms, 5), "peak_source": f"{peak_kind} hbm_gbs"},
+        "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": steps * 3,
-        "launch": "eager" if graph is None else "cuda graph of the timed steps",
+        "timing": {"replays": R, "steps_per_replay": steps, "timed_steps": R * steps,
+                   "timed_ms": round(region_ms, 2), "ms_per_step": "median over replays",
+                   "ms_per_step_mean": round(statistics.fmean(per), 5),
+                   "ms_per_step_min": round(min(per), 5), "ms_per_step_max": round(max(per), 5)},
+        "gpu_launches": R * steps * 3,
+        "launch": "eager" if graph is None else "cuda graph of the steps, replayed",
     }
     if rank == 0:
         result["clocks"] = clocks.summary()
@@ -419,32 +402,125 @@ def bench_window(args, rank, world):
 # other rows of the hot path (measured with --workload)
 # ---------------------------------------------------------------------------
 
-def _timed(fn, steps, warm):
-    """Run fn(i) warm times, then time exactly `steps` calls with CUDA events."""
+TARGET_MS = 300.0        # the shortest timed region: replays of a captured graph of the steps
+MAX_REPLAYS = 2000
+
+
+def _capture(fn, first, n):
+    """One CUDA graph of fn(first) .. fn(first + n - 1) (the library's calls keep all
+    state on the device, so they capture)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            fn(first + i)
+    torch.cuda.synchronize()
+    return g
+
+
+def _replays(graph, n_steps, target_ms=TARGET_MS, reset=None, clocks=None, world=1, max_replays=MAX_REPLAYS):
+    """Replay a captured graph of n_steps steps until the timed region lasts at least
+    target_ms: one untimed replay first (it also uploads the graph), then R timed
+    replays, each between two events on the launching stream.  reset(), when given,
+    runs after every replay, outside the per-replay events (it puts back state such as
+    a ring's counters).  Returns the per-step times of the replays (ms), the whole
+    region's time (ms) and R."""
+    import torch
+    stream = torch.cuda.current_stream()
+    graph.replay()
+    if reset is not None:
+        reset()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    if reset is not None:
+        reset()
+    torch.cuda.synchronize()
+    est = max(e0.elapsed_time(e1), 1e-3)
+    R = int(min(max_replays, max(3, -(-target_ms // est))))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark("start")
+    t0.record(stream)
+    for a, b in ev:
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        if reset is not None:
+            reset()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark("end")
+    _barrier(world)
+    per_step = [a.elapsed_time(b) / n_steps for a, b in ev]
+    return per_step, t0.elapsed_time(t1), R
+
+
+def _timed(fn, steps, warm, target_ms=TARGET_MS, reset=None):
+    """Run fn(i) warm times, capture fn(warm) .. fn(warm + steps - 1) as one CUDA graph
+    and replay it until at least target_ms are timed; returns the median time per step
+    (ms), the clocks sampled over the timed region and the timing record."""
     import torch
     for i in range(warm):
         fn(i)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if reset is not None:
+        reset()
+    g = _capture(fn, warm, steps)
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     clocks.start()
     time.sleep(0.3)
-    torch.cuda.synchronize()
-    clocks.mark("start")
-    e0.record()
-    for i in range(steps):
-        fn(warm + i)
-    e1.record()
-    torch.cuda.synchronize()
-    clocks.mark("end")
+    per, total, R = _replays(g, steps, target_ms, reset=reset, clocks=clocks)
     clocks.stop()
-    return e0.elapsed_time(e1) / steps, clocks.summary()
+    ms = statistics.median(per)
+    return ms, clocks.summary(), {"replays": R, "steps_per_replay": steps, "timed_ms": round(total, 2),
+                                  "ms_per_step_mean": round(statistics.fmean(per), 5),
+                                  "ms_per_step_min": round(min(per), 5), "ms_per_step_max": round(max(per), 5)}
+
+
+def _state_saver(layers):
+    """reset() that puts back the layers' pos (and ring head/count) as they are now,
+    with device-to-device copies (no kernels)."""
+    saved = []
+    for L in layers:
+        for t in (L.pos, L.head, L.count):
+            if t is not None:
+                saved.append((t, t.clone()))
+
+    def reset():
+        for t, s0 in saved:
+            t.copy_(s0)
+    return reset
+
+
+def _launch_roofline(fn, n, alg_bytes, name, kernel, unit_note, target_ms=TARGET_MS / 2):
+    """Roofline of an HBM-bound kernel: fn(i) for i < n (launches of that kernel alone,
+    back to back in one graph, programmatic dependent launch between them, as in a
+    decode loop over layers) replayed for target_ms; achieved = algorithmic bytes per
+    launch / median time per launch."""
+    hbm, _, _, peak_kind = _peaks()
+    g = _capture(fn, 0, n)
+    per, total, R = _replays(g, n, target_ms)
+    ms = statistics.median(per)
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": _traffic(name) if name else None,
+            "kernel": kernel, "algorithmic_bytes_per_launch": int(alg_bytes), "algorithmic_bytes": unit_note,
+            "launch_ms": round(ms, 5), "launches_timed": R * n, "peak_source": f"{peak_kind} hbm_gbs (of measured)"
+            if peak_kind == "measured" else f"{peak_kind} hbm_gbs"}
 
 
 def bench_hybrid(args):
     """Llama-3-8B-shaped hybrid decode: 32 layers (every 4th global with a 131072-token
     prefix, the rest S=4 + W=4096 rings), B=16; one step = append + attention on all
-    32 layers."""
+    32 layers.  The layers' counters are put back after every replay of the captured
+    steps, so each replay makes the same appends and reads."""
     import torch
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
@@ -479,15 +555,27 @@ def bench_hybrid(args):
             sk.kv_append(tbl, L, qs[i, j], ks[i, j], vs[i, j])
             sk.decode_attention(L, qs[i, j, :, 0], out=out, workspace=ws, sink_logits=zl)
 
-    ms, clk = _timed(step, steps, warm)
+    for i in range(warm):
+        step(i)
+    torch.cuda.synchronize()
+    ms, clk, rec = _timed(lambda i: step(warm + i), steps, 0, reset=_state_saver(layers))
+    assert all(L.error_bits() == 0 for L in layers)
     n_glob = sum(1 for i in range(c["layers"]) if synth.hybrid_layer_is_global(i))
     n_slid = c["layers"] - n_glob
-    # visible rows grow by one per step on global layers; use the mean over the timed steps
+    # visible rows grow by one per step on global layers; use the mean over the captured steps
     mean_glob = prefix + 1 + warm + (steps - 1) / 2
     kv_bytes = (n_glob * mean_glob + n_slid * (S + W)) * B * Hkv * D * 2 * 2
     hbm, _, _, peak_kind = _peaks()
     value = kv_bytes / (ms * 1e-3) / 1e9
-    assert all(L.error_bits() == 0 for L in layers)
+    # the dominant kernel: decode attention over a global layer (131,073+ visible rows per
+    # (sequence, kv head)), the 8 global layers' calls back to back
+    glob = [L for L in layers if L.kind == sk.SK_LAYER_GLOBAL]
+    rows_g = int(glob[0].pos[0])
+    alg = B * Hkv * rows_g * D * 2 * 2 + 2 * B * Hq * D * 2
+    roof = _launch_roofline(lambda i: sk.decode_attention(glob[i % len(glob)], qs[0, 0, :, 0], out=out, workspace=ws,
+                                                          sink_logits=zl),
+                            len(glob), alg, None, "decode attention over a global layer (split-K + combine), "
+                            "8 launches back to back", f"K+V of {rows_g} rows x 16 sequences x 8 kv heads + q + out")
     return {"metric": "hybrid decode step KV-read GB/s (frac of HBM peak), tokens/s", "value": round(value, 2),
             "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": warm, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
@@ -496,7 +584,9 @@ def bench_hybrid(args):
                        "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.1f} GB per step)",
                        "learned_sink_logits": bool(args.learned_sink)},
             "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
-            "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": steps * c["layers"] * 3, "clocks": clk}
+            "roofline": roof, "timing": rec,
+            "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": rec["replays"] * steps * c["layers"] * 3,
+            "clocks": clk}
 
 
 def bench_rerotate(args, kdt):
@@ -534,20 +624,29 @@ def bench_rerotate(args, kdt):
         else:
             sk.kv_rerotate(layers, tB, tA)
 
-    ms, clk = _timed(step, args.steps, args.warmup)
+    steps = args.steps + (args.steps % 2)     # an even number of turns: the keys come back
+    ms, clk, rec = _timed(step, steps, args.warmup)
     rows = nl * Hkv * N
     alg = rows * (r * 2 * 2 if kdt == "bf16" else (D + 4) * 2)
     hbm, _, _, peak_kind = _peaks()
     value = alg / (ms * 1e-3) / 1e9
     assert all(L.error_bits() == 0 for L in layers)
+    traffic = _traffic(f"rerotate_{kdt}_48l") if nl == 48 else None
+    roof = {"bound": "hbm", "achieved": round(value, 2), "peak": hbm, "unit": "GB/s", "frac": round(value / hbm, 4),
+            "traffic": traffic, "kernel": f"rerotate_{kdt}_kernel, one launch per step (all layers)",
+            "algorithmic_bytes_per_launch": alg,
+            "algorithmic_bytes": ("rows x r x 2 B, read and written (only the rotary half)" if kdt == "bf16" else
+                                  "rows x (d_h codes + 4 B scale), read and written"),
+            "launch_ms": round(ms, 5), "peak_source": f"{peak_kind} hbm_gbs"}
     return {"metric": f"cached-key rerotation ({kdt}) GB/s (frac of HBM peak), keys/s", "value": round(value, 2),
-            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "dtype": kdt, "data": "synthetic",
             "config": {"workload": f"{nl} layers x 4 kv heads x 524288 positions, d_h=128, r=64, YaRN 1<->2",
                        "algorithmic_bytes": alg, "l2": "inputs larger than L2"},
             "frac_of_hbm_peak": round(value / hbm, 4), "keys_per_s": round(rows / (ms * 1e-3), 1),
             "table_build_ms": round(table_ms, 1), "table_rebuild_ms": round(rebuild_ms, 1),
-            "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": args.steps, "clocks": clk}
+            "roofline": roof, "timing": rec,
+            "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": rec["replays"] * steps, "clocks": clk}
 
 
 def bench_rope(args):
@@ -571,7 +670,7 @@ def bench_rope(args):
         sk.rope_apply(tbl, q, posn, err=err)
         sk.rope_apply(tbl, k, posn, err=err)
 
-    ms, clk = _timed(step, args.steps, args.warmup)
+    ms, clk, rec = _timed(step, args.steps, args.warmup)
     assert int(err.item()) == 0
     half = c["r"] // 2
     # rows read and written in place, plus each call's table rows (one per token)
@@ -585,7 +684,8 @@ def bench_rope(args):
                                    f"d_h=r={D}), rotated in place", "algorithmic_bytes": alg,
                        "l2": "inputs larger than L2"},
             "frac_of_hbm_peak": round(value / hbm, 4), "rows_per_s": round(T * (Hq + Hkv) / (ms * 1e-3), 1),
-            "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": 2 * args.steps, "clocks": clk}
+            "timing": rec, "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": 2 * args.steps * rec["replays"],
+            "clocks": clk}
 
 
 def bench_paged(args):
@@ -697,7 +797,7 @@ def bench_paged(args):
             "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4),
-                         "traffic": _profiled_traffic("paged_decode_window_b32_bs16.md"),
+                         "traffic": None,
                          "kernel": "paged decode attention (split-K + combine), per launch",
                          "algorithmic_bytes_per_launch": alg_decode, "launch_ms": round(dec_ms, 5),
                          "peak_source": f"{peak_kind} hbm_gbs"},
@@ -835,20 +935,22 @@ def bench_shift(args, kdt):
     def step(i):
         sk.kv_shift_recent(layers, table, -1 if i % 2 == 0 else 1)
 
-    ms, clk = _timed(step, args.steps, args.warmup)
+    steps = args.steps + (args.steps % 2)     # as many -1 as +1 turns per replay
+    ms, clk, rec = _timed(step, steps, args.warmup)
     rows = nl * B * Hkv * W
     alg = rows * (r * 2 * 2 if kdt == "bf16" else (D + 4) * 2)
     hbm, _, _, peak_kind = _peaks()
     value = alg / (ms * 1e-3) / 1e9
     assert all(l.error_bits() == 0 for l in layers)
     return {"metric": f"recent-key shift ({kdt}) GB/s (frac of HBM peak)", "value": round(value, 2),
-            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "dtype": kdt, "data": "synthetic",
             "config": {"workload": f"windowed decode cache x {nl} layer(s): B=32, H_kv=8, d_h=r=128, S=4, "
                                    "W=4092, rings full; recent keys turned by one position", "layers": nl,
                        "algorithmic_bytes": alg, "l2": "inputs larger than L2" if alg > 129e6 else "fits L2"},
             "frac_of_hbm_peak": round(value / hbm, 4), "keys_per_s": round(rows / (ms * 1e-3), 1),
-            "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": args.steps, "clocks": clk}
+            "timing": rec, "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": steps * rec["replays"],
+            "clocks": clk}
 
 
 DYNAMIC_CHAIN = (1.125, 1.25, 1.5, 1.625, 1.75, 1.875, 2.0)
@@ -953,16 +1055,17 @@ def _prefill_tiles(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64):
 
 def bench_prefill(args):
     """Prefill chunk: B=1, T=32768, H_q=32, H_kv=8, d_h=r=128, bf16, S=4, W=4092: RoPE +
-    ring append of the chunk, then masked attention of the chunk over itself."""
+    ring append of the chunk, then masked attention of the chunk over itself.  The
+    appends of a replay go into one fresh ring per captured step; the rings are
+    emptied again after every replay."""
     import torch
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
     c = synth.PREFILL
     B, T, Hq, Hkv, D, S, W = c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    steps, warm = args.steps, args.warmup
     tbl = sk.RopeTable(D, c["r"], c["theta"], T + 8)
-    # a fresh ring per append step, so every step appends the chunk at positions 0..T-1
-    layers = [sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W)
-              for _ in range(args.steps + args.warmup)]
+    layers = [sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W) for _ in range(steps + warm)]
     q0 = synth.normal((B, T, Hq, D), 63, torch.bfloat16, device="cuda")
     k0 = synth.normal((B, T, Hkv, D), 64, torch.bfloat16, device="cuda")
     v = synth.normal((B, T, Hkv, D), 65, torch.bfloat16, device="cuda")
@@ -978,9 +1081,10 @@ def bench_prefill(args):
     def attend(i):
         sk.prefill_attention(q, k, v, 0, S, W, out=out, workspace=ws, err=err, sink_logits=zl)
 
-    ms_append, clk_a = _timed(append, args.steps, args.warmup)
-    ms_attn, clk = _timed(attend, args.steps, args.warmup)
-    assert int(err.item()) == 0
+    empty = _state_saver(layers)            # every ring as allocated: empty
+    ms_append, clk_a, rec_a = _timed(append, steps, warm, reset=empty)
+    ms_attn, clk, rec = _timed(attend, steps, warm)
+    assert int(err.item()) == 0 and all(L.error_bits() == 0 for L in layers)
     _, bf16_peak, bf16_sust, peak_kind = _peaks()
     hbm = _peaks()[0]
     vis_pairs = sum(min(t + 1, S + W) for t in range(T))      # (query, key) pairs per head
@@ -989,20 +1093,39 @@ def bench_prefill(args):
     tile_flops = tiles * (Hq // nh) * B * 4 * 128 * 64 * D
     append_bytes = B * T * (Hq + 2 * Hkv) * D * 2 + B * T * (Hq + Hkv) * D * 2 + B * Hkv * (S + W) * D * 2 * 2
     tf = tile_flops / (ms_attn * 1e-3) / 1e12
+    tf_alg = alg_flops / (ms_attn * 1e-3) / 1e12
+    append_gbs = append_bytes / (ms_append * 1e-3) / 1e9
+    roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+            "frac": round(tf / bf16_peak, 4), "traffic": _traffic("prefill_attn_t32768"),
+            "kernel": "prefill_attn_kernel (tcgen05, one launch per step)",
+            "flops_per_launch": tile_flops, "flops": "4 d_h x 128 x 64 per visited (128-row, 64-key) tile and "
+                                                     "group of q heads (the tiles the mask does not rule out)",
+            "algorithmic": {"achieved": round(tf_alg, 1), "frac": round(tf_alg / bf16_peak, 4),
+                            "flops_per_launch": alg_flops,
+                            "flops": "4 d_h per visible (query, key) pair and q head"},
+            "launch_ms": round(ms_attn, 5), "peak_source": f"{peak_kind} bf16_tflops (burst: the kernel is timed "
+                                                            f"alone)"}
+    append_roof = {"bound": "hbm", "achieved": round(append_gbs, 1), "peak": hbm, "unit": "GB/s",
+                   "frac": round(append_gbs / hbm, 4), "traffic": None,
+                   "kernel": "kv_append_kernel (RoPE on Q and K + ring write of the chunk's last W rows)",
+                   "algorithmic_bytes_per_launch": append_bytes,
+                   "algorithmic_bytes": "read Q, K, V + write Q_rot, K_rot + write the ring's S + W rows of K and V",
+                   "launch_ms": round(ms_append, 5), "peak_source": f"{peak_kind} hbm_gbs"}
     return {"metric": "prefill attention TFLOP/s on visited tiles (frac of dense bf16 peak); append GB/s",
-            "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": steps, "warmup": warm,
             "ms_per_step": round(ms_attn, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "prefill chunk: B=1, T=32768, H_q=32, H_kv=8, d_h=128, S=4, W=4092",
                        "visited_tiles_per_head_group": tiles, "heads_per_cta": nh,
                        "tile": f"128 rows ({nh} heads x {128 // nh} queries) x 64 keys",
                        "learned_sink_logits": bool(args.learned_sink)},
             "frac_of_bf16_peak": round(tf / bf16_peak, 4),
-            "algorithmic_tflops": round(alg_flops / (ms_attn * 1e-3) / 1e12, 1),
+            "algorithmic_tflops": round(tf_alg, 1), "algorithmic_frac_of_bf16_peak": round(tf_alg / bf16_peak, 4),
             "algorithmic_flops": alg_flops, "tile_flops": tile_flops,
-            "append_ms": round(ms_append, 4), "append_gbs": round(append_bytes / (ms_append * 1e-3) / 1e9, 1),
-            "append_frac_of_hbm_peak": round(append_bytes / (ms_append * 1e-3) / 1e9 / hbm, 4),
+            "append_ms": round(ms_append, 4), "append_gbs": round(append_gbs, 1),
+            "append_frac_of_hbm_peak": round(append_gbs / hbm, 4),
+            "roofline": roof, "append_roofline": append_roof, "timing": rec, "append_timing": rec_a,
             "peak_source": f"{peak_kind} bf16_tflops {bf16_peak} / hbm_gbs {hbm}",
-            "gpu_launches": args.steps * 2, "clocks": clk}
+            "gpu_launches": steps * rec["replays"], "clocks": clk, "append_clocks": clk_a}
 
 
 def bench_prefill_chunk(args):
@@ -1033,7 +1156,7 @@ def bench_prefill_chunk(args):
     def attend(i):
         sk.prefill_attention(q, k, v, p0, S, W, out=out, workspace=ws, err=layer.err, sink_logits=zl, prior=layer)
 
-    ms, clk = _timed(attend, args.steps, args.warmup)
+    ms, clk, rec = _timed(attend, args.steps, args.warmup)
     assert layer.error_bits() == 0
     _, bf16_peak, _, peak_kind = _peaks()
     alg_flops = T * (S + W) * Hq * B * 4 * D          # every query sees S + W keys here
@@ -1051,8 +1174,119 @@ def bench_prefill_chunk(args):
             "frac_of_bf16_peak": round(tf / bf16_peak, 4),
             "algorithmic_tflops": round(alg_flops / (ms * 1e-3) / 1e12, 1),
             "algorithmic_flops": alg_flops, "tile_flops": tile_flops,
-            "peak_source": f"{peak_kind} bf16_tflops {bf16_peak}",
-            "gpu_launches": args.steps * 3, "clocks": clk}
+            "peak_source": f"{peak_kind} bf16_tflops {bf16_peak}", "timing": rec,
+            "gpu_launches": args.steps * 3 * rec["replays"], "clocks": clk}
+
+
+# ---------------------------------------------------------------------------
+# the configurations beside the headline: the tiny case and single-stream decode
+# ---------------------------------------------------------------------------
+
+def bench_tiny(args):
+    """The tiny case: 1 sequence, H_q=8, H_kv=4, d_h=r=64, theta=1e4, fp32, C=6 with S=2
+    sinks, 10 tokens decoded one at a time (RoPE + append + attention per token).  A
+    replay of the captured graph decodes the 10 tokens; the ring is emptied after it."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.TINY
+    T, Hq, Hkv, D = c["T"], c["Hq"], c["Hkv"], c["D"]
+    tbl = sk.RopeTable(D, c["r"], c["theta"], 64)
+    layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, 1, Hkv, D, sinks=c["S"], window=c["W"], k_dtype=torch.float32,
+                                v_dtype=torch.float32)
+    q_all = synth.normal((1, T, Hq, D), 0)
+    k_all = synth.normal((1, T, Hkv, D), 1)
+    v_all = synth.normal((1, T, Hkv, D), 2)
+    qs = [q_all[:, t:t + 1].contiguous().cuda() for t in range(T)]
+    ks = [k_all[:, t:t + 1].contiguous().cuda() for t in range(T)]
+    vs = [v_all[:, t:t + 1].contiguous().cuda() for t in range(T)]
+    out = torch.empty(1, Hq, D, device="cuda")
+    ws = torch.empty(sk.decode_workspace_bytes(layer, Hq), dtype=torch.uint8, device="cuda")
+    empty = _state_saver([layer])
+
+    def step(t):
+        sk.kv_append(tbl, layer, qs[t % T], ks[t % T], vs[t % T])
+        sk.decode_attention(layer, qs[t % T][:, 0], out=out, workspace=ws)
+
+    for t in range(T):
+        step(t)
+    torch.cuda.synchronize()
+    empty()
+    g = _capture(step, 0, T)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    per, total, R = _replays(g, T, TARGET_MS / 3, reset=empty, clocks=clocks)
+    clocks.stop()
+    assert layer.error_bits() == 0
+    us = statistics.median(per) * 1e3
+    return {"metric": "tiny case: microseconds per decode step (RoPE + append + attention of one token)",
+            "value": round(us, 3), "unit": "us/step", "higher_is_better": False, "dtype": "f32",
+            "config": {"workload": "tiny: 1 sequence, H_q=8, H_kv=4, d_h=r=64, theta=1e4, fp32, C=6, S=2, "
+                                   "10 tokens one at a time"},
+            "roofline": {"bound": "latency", "achieved": round(us, 3), "unit": "us/step", "peak": None,
+                         "frac": None, "kernel": "append + split + combine per token (3 launches)",
+                         "note": "a parity case: 3 KB of cache, far from any throughput roofline"},
+            "timing": {"replays": R, "steps_per_replay": T, "timed_ms": round(total, 2)},
+            "gpu_launches": 3 * T * R, "clocks": clocks.summary()}
+
+
+def bench_window_b1(args):
+    """Single-stream decode: one sequence through 32 windowed layers (each H_q=32,
+    H_kv=8, d_h=r=128, S=4, W=4092, ring full at a random head), one token per step:
+    RoPE + append + split-K attention over 4096 visible keys on every layer.  The
+    32 layers' caches (537 MB) exceed L2, as a model's layers do."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    Hq, Hkv, D, S, W = c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    nl = 32
+    steps, warm = args.steps, args.warmup
+    tbl = sk.RopeTable(D, c["r"], c["theta"], c["pos_hi"] + steps + warm + 8)
+    pos, head, count = synth.window_state(43, nl, W, c["pos_lo"], c["pos_hi"])
+    layers = []
+    for j in range(nl):
+        L = sk.KVLayer.allocate(sk.SK_LAYER_RING, 1, Hkv, D, sinks=S, window=W)
+        synth.fill_normal_(L.k, 4100 + j)
+        synth.fill_normal_(L.v, 4200 + j)
+        L.pos.fill_(int(pos[0]))
+        L.head.fill_(int(head[j]))
+        L.count.fill_(W)
+        layers.append(L)
+    n = steps + warm
+    qs = synth.normal((n, nl, 1, 1, Hq, D), 44, torch.bfloat16, device="cuda")
+    ks = synth.normal((n, nl, 1, 1, Hkv, D), 45, torch.bfloat16, device="cuda")
+    vs = synth.normal((n, nl, 1, 1, Hkv, D), 46, torch.bfloat16, device="cuda")
+    out = torch.empty(1, Hq, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(sk.decode_workspace_bytes(layers[0], Hq), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        for j, L in enumerate(layers):
+            sk.kv_append(tbl, L, qs[i, j], ks[i, j], vs[i, j])
+            sk.decode_attention(L, qs[i, j, :, 0], out=out, workspace=ws)
+
+    for i in range(warm):
+        step(i)
+    torch.cuda.synchronize()
+    ms, clk, rec = _timed(lambda i: step(warm + i), steps, 0, reset=_state_saver(layers))
+    assert all(L.error_bits() == 0 for L in layers)
+    kv_layer = Hkv * (S + W) * D * 2 * 2
+    hbm, _, _, peak_kind = _peaks()
+    value = nl * kv_layer / (ms * 1e-3) / 1e9
+    roof = _launch_roofline(lambda i: sk.decode_attention(layers[i % nl], qs[0, i % nl, :, 0], out=out,
+                                                          workspace=ws), nl,
+                            kv_layer + 2 * Hq * D * 2, None,
+                            "decode attention at batch 1 (split-K + combine); the 32 layers' launches back to "
+                            "back in one graph", "K+V of 4096 visible rows x 8 kv heads + q + out, per layer")
+    return {"metric": "single-stream decode over 32 windowed layers: us per token, tokens/s, KV-read GB/s",
+            "value": round(ms * 1e3, 2), "unit": "us/token", "higher_is_better": False, "dtype": "bf16",
+            "config": {"workload": "batch 1 through 32 windowed layers (H_q=32, H_kv=8, d_h=r=128, S=4, W=4092, "
+                                   "rings full): RoPE + append + attention per layer",
+                       "l2": f"inputs larger than L2 (KV {nl * kv_layer / 1e6:.0f} MB per step)"},
+            "tokens_per_s": round(1.0 / (ms * 1e-3), 1), "gbs": round(value, 2),
+            "frac_of_hbm_peak": round(value / hbm, 4), "us_per_layer": round(ms * 1e3 / nl, 3),
+            "roofline": roof, "timing": rec, "gpu_launches": 3 * nl * steps * rec["replays"], "clocks": clk}
 
 
 # ---------------------------------------------------------------------------
@@ -1174,6 +1408,165 @@ def cpu_baseline_all_cores(n_seq=32):
                       f"process {d['secs']:.2f} s)"}
 
 
+# ---------------------------------------------------------------------------
+# oracle baselines of the other configurations (float64 numpy, single thread, in a
+# subprocess); where the whole configuration would take minutes, a bounded sample is
+# timed and the configuration's time extrapolated from it (said so in "sample")
+# ---------------------------------------------------------------------------
+
+def _cpu_tiny():
+    import numpy as np
+    from oracle.sinkkv_oracle import RingCache, RopeSpec, decode_attention, rope_rotate
+    from sink_kv_attention_gb300 import synth
+    c = synth.TINY
+    T, D = c["T"], c["D"]
+    om = RopeSpec(D, c["r"], c["theta"]).omega()
+    q = synth.normal((T, c["Hq"], D), 0).double().numpy()
+    k = synth.normal((T, c["Hkv"], D), 1).double().numpy()
+    v = synth.normal((T, c["Hkv"], D), 2).double().numpy()
+    secs, steps = 0.0, 0
+    while secs < 2.0:
+        t0 = time.perf_counter()
+        ring = RingCache(c["S"], c["W"])
+        for t in range(T):
+            qr = rope_rotate(q[t:t + 1], [t], om, 1.0, c["r"])
+            kr = rope_rotate(k[t:t + 1], [t], om, 1.0, c["r"])
+            ring.append([(kr[0], v[t])])
+            decode_attention(ring, qr[0])
+        secs += time.perf_counter() - t0
+        steps += T
+    return {"value": round(secs / steps * 1e6, 2), "unit": "us/step",
+            "sample": f"the whole case, {steps // T} times ({steps} decode steps, {secs:.2f} s)"}
+
+
+def _cpu_window_b1():
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    secs, reps = 0.0, 0
+    while secs < 5.0:
+        s_, _ = cpu_oracle_window(1, seed_base=reps)
+        secs, reps = secs + s_, reps + 1
+    per_layer = secs / reps
+    kv = c["Hkv"] * (c["S"] + c["W"]) * c["D"] * 2 * 2
+    return {"value": round(per_layer * 32 * 1e6, 1), "unit": "us/token", "gbs": round(kv / per_layer / 1e9, 4),
+            "sample": f"{reps} single-sequence windowed decode steps of one layer ({secs:.2f} s), x 32 layers "
+                      "(extrapolated)"}
+
+
+def _cpu_hybrid():
+    import numpy as np
+    from oracle.sinkkv_oracle import GlobalCache, RingCache, RopeSpec, decode_attention, rope_rotate
+    from sink_kv_attention_gb300 import synth
+    c = synth.HYBRID
+    B, Hq, Hkv, D, S, W, prefix = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"], c["prefix"]
+    om = RopeSpec(D, c["r"], c["theta"]).omega()
+    t_glob, t_slid = [], []
+    for b, kind in [(0, "g"), (1, "g")] + [(b, "s") for b in range(8)]:
+        n = prefix if kind == "g" else S + W
+        kb = synth.normal((n, Hkv, D), 7000 + b, torch_dtype()).double().numpy()
+        vb = synth.normal((n, Hkv, D), 7100 + b, torch_dtype()).double().numpy()
+        q = synth.normal((1, Hq, D), 7200 + b, torch_dtype()).double().numpy()
+        k = synth.normal((1, Hkv, D), 7300 + b, torch_dtype()).double().numpy()
+        v = synth.normal((Hkv, D), 7400 + b, torch_dtype()).double().numpy()
+        t0 = time.perf_counter()
+        if kind == "g":
+            cache = GlobalCache(prefix + 1)
+            cache.append([(kb[s], vb[s]) for s in range(prefix)])
+        else:
+            cache = RingCache(S, W)
+            cache.pos, cache.head, cache.count = prefix, (97 * b) % W, W
+            for s in range(S + W):
+                cache.slots[s] = (kb[s], vb[s])
+        qr = rope_rotate(q, [prefix], om, 1.0, D)
+        kr = rope_rotate(k, [prefix], om, 1.0, D)
+        cache.append([(kr[0], v)])
+        decode_attention(cache, qr[0])
+        (t_glob if kind == "g" else t_slid).append(time.perf_counter() - t0)
+    tg, ts = sum(t_glob) / len(t_glob), sum(t_slid) / len(t_slid)
+    step_s = B * (8 * tg + 24 * ts)
+    kv = (8 * (prefix + 1) + 24 * (S + W)) * B * Hkv * D * 2 * 2
+    return {"value": round(kv / step_s / 1e9, 4), "unit": "GB/s", "ms_per_step": round(step_s * 1e3, 1),
+            "sample": f"one global layer for {len(t_glob)} sequences ({sum(t_glob):.2f} s) and one sliding layer "
+                      f"for {len(t_slid)} sequences ({sum(t_slid):.2f} s); the 32-layer, 16-sequence step "
+                      "extrapolated as 16 x (8 global + 24 sliding)"}
+
+
+def torch_dtype():
+    import torch
+    return torch.bfloat16
+
+
+def _cpu_prefill():
+    import numpy as np
+    from oracle.sinkkv_oracle import prefill_attention
+    from sink_kv_attention_gb300 import synth
+    c = synth.PREFILL
+    T, Hq, Hkv, D, S, W = c["T"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    q = synth.normal((T, Hq, D), 63, torch_dtype()).double().numpy()
+    k = synth.normal((T, Hkv, D), 64, torch_dtype()).double().numpy()
+    v = synth.normal((T, Hkv, D), 65, torch_dtype()).double().numpy()
+    rows = sorted(np.random.default_rng(5).choice(T, 256, replace=False).tolist())
+    t0 = time.perf_counter()
+    prefill_attention(q, k, v, 0, S, W, rows=rows)
+    secs = time.perf_counter() - t0
+    pairs = lambda ts: sum(min(t + 1, S + W) for t in ts)
+    full_s = secs * pairs(range(T)) / pairs(rows)
+    flops = pairs(range(T)) * Hq * 4 * D
+    return {"value": round(flops / full_s / 1e12, 6), "unit": "TFLOP/s", "ms_per_step": round(full_s * 1e3, 1),
+            "sample": f"256 sampled query rows, all 32 heads ({secs:.2f} s); the chunk's time extrapolated by "
+                      "its visible (query, key) pairs"}
+
+
+def _cpu_rerotate(kdt):
+    import numpy as np
+    from oracle.sinkkv_oracle import RopeSpec, rerotate, rerotate_int8
+    c = synth_cfg("REROTATE")
+    D, r, Hkv, N = c["D"], c["r"], c["Hkv"], c["positions"]
+    a = RopeSpec(D, r, c["theta"], True, c["factor_a"], c["orig_ctx"])
+    b = a.with_factor(c["factor_b"])
+    rng = np.random.default_rng(6)
+    secs, rows = 0.0, 0
+    while secs < 6.0:
+        pos = rng.integers(0, N, 16384)
+        if kdt == "bf16":
+            x = rng.uniform(-1, 1, (len(pos), Hkv, D))
+            t0 = time.perf_counter()
+            rerotate(x, pos, a, b)
+        else:
+            codes = rng.integers(-127, 128, (len(pos), Hkv, D)).astype(np.int8)
+            sc = rng.uniform(1 / 127, 2 / 127, (len(pos), Hkv))
+            t0 = time.perf_counter()
+            rerotate_int8(codes, sc, pos, a, b)
+        secs += time.perf_counter() - t0
+        rows += len(pos) * Hkv
+    per_row = r * 2 * 2 if kdt == "bf16" else (D + 4) * 2
+    total_rows = c["layers"] * Hkv * N
+    return {"value": round(rows * per_row / secs / 1e9, 4), "unit": "GB/s",
+            "ms_per_step": round(secs / rows * total_rows * 1e3, 1),
+            "sample": f"{rows} key rows at random positions ({secs:.2f} s); the 48-layer step "
+                      f"({total_rows} rows) extrapolated by the row count"}
+
+
+def synth_cfg(name):
+    from sink_kv_attention_gb300 import synth
+    return getattr(synth, name)
+
+
+CPU_ROWS = {"tiny": _cpu_tiny, "window_b1": _cpu_window_b1, "hybrid": _cpu_hybrid, "prefill": _cpu_prefill,
+            "rerotate_bf16": lambda: _cpu_rerotate("bf16"), "rerotate_i8": lambda: _cpu_rerotate("i8")}
+
+
+def cpu_row(name):
+    """The oracle baseline of configuration `name`, single-threaded in a subprocess."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-row", name],
+                       capture_output=True, text=True, env=env, timeout=900)
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d.update({"cores": 1, "kind": "oracle", "cpu": _cpu_model()})
+    return d
+
+
 def cpu_baseline(n_seq=32):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
@@ -1190,17 +1583,50 @@ def cpu_baseline(n_seq=32):
 # main
 # ---------------------------------------------------------------------------
 
+ROWS = (("tiny", bench_tiny), ("window_b1", bench_window_b1), ("hybrid", bench_hybrid),
+        ("prefill", bench_prefill), ("rerotate_bf16", lambda a: bench_rerotate(a, "bf16")),
+        ("rerotate_i8", lambda a: bench_rerotate(a, "i8")))
+
+
+def bench_rows(args):
+    """Every other configuration of the path on this GPU, each with its roofline and
+    its oracle baseline: the tiny case, single-stream decode, the hybrid 32-layer step,
+    the prefill chunk and the two rerotations."""
+    import gc
+    import torch
+    rows = {}
+    for name, fn in ROWS:
+        try:
+            r = fn(args)
+            for key in ("n_gpus", "data", "peak_source"):
+                r.pop(key, None)
+        except Exception as e:  # reported, never fatal to the headline
+            r = {"error": f"{type(e).__name__}: {str(e)[:300]}"}
+        gc.collect()
+        torch.cuda.empty_cache()
+        if not args.no_cpu_baseline:
+            try:
+                r["cpu_baseline"] = cpu_row(name)
+            except Exception as e:
+                r["cpu_baseline"] = {"value": None, "error": str(e)[:200]}
+        rows[name] = r
+    return rows
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="window",
                     choices=["window", "window_i8", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill",
                              "prefill_chunk", "dynamic_bf16", "dynamic_i8", "shift_bf16", "shift_i8", "paged",
                              "rope"])
     ap.add_argument("--cpu-worker", type=int, default=0)
+    ap.add_argument("--cpu-row", default="", choices=[""] + sorted(CPU_ROWS))
+    ap.add_argument("--no-rows", action="store_true",
+                    help="the headline line only, without the other configurations")
     ap.add_argument("--cpu-worker-mt", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="rerotate: layer count (default 48)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1211,6 +1637,9 @@ def main():
 
     if args.cpu_worker:
         _cpu_worker(args.cpu_worker)
+        return
+    if args.cpu_row:
+        print(json.dumps(CPU_ROWS[args.cpu_row]()))
         return
     if args.cpu_worker_mt:
         _cpu_worker_mt(args.cpu_worker_mt)
@@ -1274,6 +1703,8 @@ def main():
         return
     result = bench_window(args, rank, world_)
     if rank == 0:
+        if not args.no_rows and world_ == 1:
+            result["rows"] = bench_rows(args)
         if not args.no_cpu_baseline and world_ == 1:
             try:
                 result["cpu_baseline"] = cpu_baseline()
