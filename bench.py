@@ -1622,7 +1622,7 @@ def main():
     ap.add_argument("--workload", default="window",
                     choices=["window", "window_i8", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill",
                              "prefill_chunk", "dynamic_bf16", "dynamic_i8", "shift_bf16", "shift_i8", "paged",
-                             "rope"])
+                             "rope", "tiny", "window_b1"])
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--cpu-row", default="", choices=[""] + sorted(CPU_ROWS))
     ap.add_argument("--no-rows", action="store_true",
@@ -1698,6 +1698,10 @@ def main():
                 print(json.dumps(bench_shift(args, args.workload.split("_")[1])))
             elif args.workload == "rope":
                 print(json.dumps(bench_rope(args)))
+            elif args.workload == "tiny":
+                print(json.dumps(bench_tiny(args)))
+            elif args.workload == "window_b1":
+                print(json.dumps(bench_window_b1(args)))
             else:
                 print(json.dumps(bench_rerotate(args, args.workload.split("_")[1])))
         return

@@ -60,6 +60,7 @@ struct DecodeParams {
     int64_t cap;
     int B, Hkv, S, kind;
     int n_blocks;  // P: blocks of the split kernel
+    int combine_wpu;  // warps per (b, q head) in the combine kernel
     float qscale;  // log2(e) / sqrt(D)
     // paged layers (kind kKindPaged): pools in kc / vc, request lengths in pos
     const int32_t* block_table;
@@ -704,7 +705,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ>::THREADS, 1)
     if (timed_out) set_error(p.err, SK_DEVERR_TIMEOUT);
 }
 
-// One warp per (b, q head): log-sum-exp combine of the unit's partials.
+// Log-sum-exp combine of each unit's partials, one warp per (b, q head): the kernel for
+// batches whose units meet one to three blocks each.
 constexpr int kCombineFew = 3;  // partials a combine warp loads in one go
 
 template <typename T, int D, int NREP>
@@ -802,20 +804,49 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
             for (int d = 0; d < DPV; ++d) acc[d] = fmaf(f, vv[i][d], acc[d]);
         }
     } else {
+        // A unit cut between more blocks than usual (a long sequence among short ones):
+        // the lanes take the partials 32 at a time for the max and the sum, then every
+        // lane adds its dims of each partial, the weights broadcast by shuffle, several
+        // partials' loads in flight at once.
         const float* base = p.ws + (fb + unit) * PF;
         float M = z2;
-        for (int i = 0; i < n; ++i)
-            if (owns_rows(fb + i, R)) M = fmaxf(M, base[i * PF + h]);
-        const float Mu = M == -INFINITY ? 0.0f : M;
-        lsum = has_sink ? fast_exp2_approx(z2 - Mu) : 0.0f;
-        for (int i = 0; i < n; ++i) {
-            if (!owns_rows(fb + i, R)) continue;
-            const float* pp = base + i * PF;
-            const float f = fast_exp2_approx(pp[h] - Mu);
-            lsum = fmaf(f, pp[NREP + h], lsum);
-#pragma unroll
-            for (int d = 0; d < DPV; ++d) acc[d] = fmaf(f, pp[2 * NREP + h * D + lane * DPV + d], acc[d]);
+        for (int i0 = 0; i0 < n; i0 += 32) {
+            const int i = i0 + lane;
+            if (i < n && owns_rows(fb + i, R)) M = fmaxf(M, base[i * PF + h]);
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        const float Mu = M == -INFINITY ? 0.0f : M;
+        float lpart = 0.0f;
+        for (int i0 = 0; i0 < n; i0 += 32) {
+            const int i = i0 + lane;
+            // a block that owns none of the unit's rows wrote nothing here: weight 0,
+            // and its (stale) slot is never read
+            const bool own = i < n && owns_rows(fb + i, R);
+            const float f = own ? fast_exp2_approx(base[i * PF + h] - Mu) : 0.0f;
+            if (own) lpart = fmaf(f, base[i * PF + NREP + h], lpart);
+            const int cnt = min(32, n - i0);
+            constexpr int U = 4;
+            for (int j0 = 0; j0 < cnt; j0 += U) {
+                float fj[U], vj[U][DPV];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    fj[u] = __shfl_sync(kFull, f, (j0 + u) & 31);
+                    const bool use = j0 + u < cnt && fj[u] != 0.0f;
+                    const float* pp = base + (i0 + j0 + u) * PF + 2 * NREP + h * D + lane * DPV;
+#pragma unroll
+                    for (int d = 0; d < DPV; ++d) vj[u][d] = use ? pp[d] : 0.0f;
+                    if (!use) fj[u] = 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int d = 0; d < DPV; ++d) acc[d] = fmaf(fj[u], vj[u][d], acc[d]);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lpart += __shfl_xor_sync(kFull, lpart, o);
+        lsum = lpart + (has_sink ? fast_exp2_approx(z2 - Mu) : 0.0f);
     }
     const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
 #pragma unroll
@@ -825,6 +856,174 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
         else
             o[d] = acc[d] * inv;
     }
+}
+
+// KQ: int8 keys (contiguous layers only; paged layers hold bf16 or fp32 keys).
+
+// Log-sum-exp combine for few, long units (a single sequence or a few): a group of
+// p.combine_wpu warps (2, 4 or 8, all in one block) per (b, q head).  Warp `sub` of the group takes the partials
+// [sub n / wpu, (sub + 1) n / wpu) of the n blocks that met the unit, kCombineBatch at a
+// time, folding them into a running (max, sum, values); the group's warps then merge
+// through shared memory.  The host picks wpu from the partials a unit meets on average,
+// so that a warp's share is one batch: a single round trip to L2 after the wait (a
+// single sequence of 8 kv heads meets about 20 blocks per unit).
+constexpr int kCombineBatch = 4;  // partials a combine warp loads in one go
+
+template <typename T, int D, int NREP>
+__global__ void __launch_bounds__(256) decode_combine_group_kernel(DecodeParams p) {
+    constexpr int DPV = D / 32;
+    constexpr int PF = NREP * (D + 2);
+    constexpr int KB = kCombineBatch;
+    // the row prefix from the state as read before the wait (a guess) and after it
+    __shared__ int64_t pre[2][kMaxBatch + 1];
+    __shared__ float mrg[8][2 + D];  // per warp: running max, sum and its lanes' values
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_trigger();
+    // Before the wait the state is final unless the append ahead of the split kernel is
+    // still running. The guess only picks the partials to load as soon as the wait
+    // returns, alongside the state read after it, which decides whether they are used.
+    if (threadIdx.x < 32) unit_prefix(p, pre[0], lane);
+    __syncthreads();
+    const int wpu = p.combine_wpu;
+    const int wg = blockIdx.x * 8 + warp;
+    const int item = wg / wpu, sub = wg % wpu;
+    const int Hq = p.Hkv * NREP;
+    const bool active = item < p.B * Hq;
+    const int b = active ? item / Hq : 0, hq = active ? item % Hq : 0;
+    const int g = hq / NREP, h = hq % NREP;
+    const int64_t unit = int64_t(b) * p.Hkv + g;
+    const int P = p.n_blocks;
+    // blocks fb..fb+n-1 meet the unit's rows, except blocks whose row range is empty
+    // (possible when R < P): those wrote nothing and are skipped.
+    auto owns_rows = [&](int64_t c, int64_t R) { return (c * R + P - 1) / P < ((c + 1) * R + P - 1) / P; };
+    auto share = [&](int n, int* j0, int* j1) {
+        *j0 = int(int64_t(sub) * n / wpu);
+        *j1 = int(int64_t(sub + 1) * n / wpu);
+    };
+    float mv[KB], lv[KB], vv[KB][DPV];
+    // max, sum and value slice of partials j0 .. j1-1 (at most KB) at once; a block
+    // that wrote nothing gives max -inf and is never read
+    auto load = [&](int64_t fb, int64_t R, int j0, int j1) {
+        const float* base = p.ws + (fb + unit) * PF;
+#pragma unroll
+        for (int i = 0; i < KB; ++i) {
+            const int j = j0 + i;
+            const bool own = j < j1 && owns_rows(fb + j, R);
+            const float* pp = base + j * PF;
+            mv[i] = own ? pp[h] : -INFINITY;
+            lv[i] = own ? pp[NREP + h] : 0.0f;
+#pragma unroll
+            for (int d = 0; d < DPV; ++d) vv[i][d] = own ? pp[2 * NREP + h * D + lane * DPV + d] : 0.0f;
+        }
+    };
+    // the guessed split of the unit and this warp's first batch of it; n0 = 0: nothing
+    // loaded early
+    int64_t fb0 = 0, R0 = pre[0][p.B];
+    int n0 = 0, g0 = 0, g1 = 0;
+    {
+        const int64_t s0 = pre[0][b], e0 = pre[0][b + 1];
+        const int64_t L0 = (e0 - s0) / p.Hkv;
+        if (active && R0 > 0 && L0 > 0 && s0 >= 0 && e0 <= R0) {
+            const int64_t st0 = s0 + int64_t(g) * L0;
+            fb0 = first_block_of(st0, R0, P);
+            const int64_t lb0 = first_block_of(st0 + L0 - 1, R0, P);
+            if (fb0 >= 0 && lb0 < P && lb0 >= fb0) n0 = int(lb0 - fb0 + 1);
+        }
+        if (n0 > 0) share(n0, &g0, &g1);
+    }
+    pdl_wait();  // the split kernel's partials are complete
+    if (n0 > 0) load(fb0, R0, g0, min(g1, g0 + KB));
+    if (threadIdx.x < 32) unit_prefix(p, pre[1], lane);
+    __syncthreads();
+    const int64_t R = pre[1][p.B];
+    const int64_t Lb = active ? (pre[1][b + 1] - pre[1][b]) / p.Hkv : 0;
+    float m_loc = -INFINITY, l_loc = 0.0f, acc[DPV];
+#pragma unroll
+    for (int d = 0; d < DPV; ++d) acc[d] = 0.0f;
+    if (Lb > 0) {
+        const int64_t st = pre[1][b] + int64_t(g) * Lb;
+        const int64_t fb = first_block_of(st, R, P);
+        const int n = int(first_block_of(st + Lb - 1, R, P) - fb + 1);
+        int j0, j1;
+        share(n, &j0, &j1);
+        // the same blocks under the same ownership rule: the early loads are this batch
+        const bool early = n0 == n && fb0 == fb && R0 == R;
+        for (int jb = j0; jb < j1; jb += KB) {
+            if (!(early && jb == j0)) load(fb, R, jb, min(j1, jb + KB));
+            float Mb = m_loc;
+#pragma unroll
+            for (int i = 0; i < KB; ++i) Mb = fmaxf(Mb, mv[i]);
+            const float Mu = Mb == -INFINITY ? 0.0f : Mb;
+            const float alpha = fast_exp2_approx(m_loc - Mu);  // 0 while nothing is folded in
+            l_loc *= alpha;
+#pragma unroll
+            for (int d = 0; d < DPV; ++d) acc[d] *= alpha;
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                const float f = fast_exp2_approx(mv[i] - Mu);  // 0 for a block that wrote nothing
+                l_loc = fmaf(f, lv[i], l_loc);
+#pragma unroll
+                for (int d = 0; d < DPV; ++d) acc[d] = fmaf(f, vv[i][d], acc[d]);
+            }
+            m_loc = Mb;
+        }
+    }
+    // A learned sink is one more logit z (scaled-score units, clamped) in the
+    // denominator with no value row ("RoPE, scaling, sliding window, attention sinks",
+    // "Hybrid models break the uniform-spec assumption"); in base 2 it is z log2(e).
+    const bool has_sink = p.sink_logits != nullptr;
+    const float z2 = has_sink && active
+                         ? fminf(fmaxf(p.sink_logits[hq], kSinkLogitMin), kSinkLogitMax) * kLog2e
+                         : -INFINITY;
+    float lsum;
+    if (wpu > 1) {
+        if (lane == 0) {
+            mrg[warp][0] = m_loc;
+            mrg[warp][1] = l_loc;
+        }
+#pragma unroll
+        for (int d = 0; d < DPV; ++d) mrg[warp][2 + lane * DPV + d] = acc[d];
+        __syncthreads();
+        if (sub != 0 || !active) return;
+        float M = z2;
+        for (int s = 0; s < wpu; ++s) M = fmaxf(M, mrg[warp + s][0]);
+        const float Mu = M == -INFINITY ? 0.0f : M;
+        lsum = has_sink ? fast_exp2_approx(z2 - Mu) : 0.0f;
+#pragma unroll
+        for (int d = 0; d < DPV; ++d) acc[d] = 0.0f;
+        for (int s = 0; s < wpu; ++s) {
+            const float f = fast_exp2_approx(mrg[warp + s][0] - Mu);
+            lsum = fmaf(f, mrg[warp + s][1], lsum);
+#pragma unroll
+            for (int d = 0; d < DPV; ++d) acc[d] = fmaf(f, mrg[warp + s][2 + lane * DPV + d], acc[d]);
+        }
+    } else {
+        if (!active) return;
+        const float M = fmaxf(z2, m_loc);
+        const float Mu = M == -INFINITY ? 0.0f : M;
+        const float f = fast_exp2_approx(m_loc - Mu);
+        lsum = fmaf(f, l_loc, has_sink ? fast_exp2_approx(z2 - Mu) : 0.0f);
+#pragma unroll
+        for (int d = 0; d < DPV; ++d) acc[d] *= f;
+    }
+    T* o = static_cast<T*>(p.out) + (int64_t(b) * Hq + hq) * D + lane * DPV;
+    const float inv = (Lb > 0 && lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+#pragma unroll
+    for (int d = 0; d < DPV; ++d) {
+        if constexpr (sizeof(T) == 2)
+            o[d] = __float2bfloat16_rn(acc[d] * inv);
+        else
+            o[d] = acc[d] * inv;
+    }
+}
+
+// Warps per (b, q head) of the combine: enough that a warp's share of the partials a
+// unit meets on average (about P / units + 1) is one batch.
+inline int combine_wpu(int P, int64_t units) {
+    const int64_t avg = int64_t(P) / std::max<int64_t>(1, units) + 1;
+    int w = 1;
+    while (w < 8 && (avg + w - 1) / w > kCombineBatch) w <<= 1;
+    return w;
 }
 
 // KQ: int8 keys (contiguous layers only; paged layers hold bf16 or fp32 keys).
@@ -868,6 +1067,12 @@ struct DecodeLaunch {
     static cudaError_t run(DecodeParams p, const sk_kv_layer& L, cudaStream_t st) {
         if (blocks_per_sm() < 1) return cudaErrorInvalidConfiguration;
         p.n_blocks = grid();
+        if (p.kind != kKindPaged) {
+            // no more blocks than rows the cache can hold: blocks without rows would only
+            // add partials for the combine to skip
+            const int64_t rows = int64_t(L.batch) * L.n_kv_heads * L.capacity;
+            p.n_blocks = int(std::max<int64_t>(1, std::min<int64_t>(p.n_blocks, rows)));
+        }
         cudaError_t e;
         if constexpr (KQ) {
             if (p.kind == kKindPaged) return cudaErrorInvalidValue;
@@ -881,8 +1086,13 @@ struct DecodeLaunch {
                                  C::SMEM, st, p);
         }
         if (e != cudaSuccess) return e;
-        const int warps = L.batch * L.n_kv_heads * NREP;
-        return launch_pdl(decode_combine_kernel<T, D, NREP>, dim3((warps + 7) / 8), dim3(256), 0, st, p);
+        p.combine_wpu = combine_wpu(p.n_blocks, int64_t(L.batch) * L.n_kv_heads);
+        const int64_t warps = int64_t(L.batch) * L.n_kv_heads * NREP * p.combine_wpu;
+        return p.combine_wpu == 1
+                   ? launch_pdl(decode_combine_kernel<T, D, NREP>, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, st,
+                                p)
+                   : launch_pdl(decode_combine_group_kernel<T, D, NREP>, dim3(unsigned((warps + 7) / 8)), dim3(256),
+                                0, st, p);
     }
 };
 
