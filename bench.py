@@ -732,60 +732,29 @@ def bench_paged(args):
     ws = torch.empty(sk.paged_decode_workspace_bytes(layer, Hq), dtype=torch.uint8, device="cuda")
     zl = _learned_sinks(args, Hq)
 
-    def step(i, ev=None):
-        st = torch.cuda.current_stream()
+    def step(i):
         sk.paged_append(tbl, layer, qs[i], ks[i], vs[i])
-        if ev is not None:
-            ev[0].record(st)
         sk.paged_decode_attention(layer, qs[i, :, 0], out=out, workspace=ws, sink_logits=zl)
-        if ev is not None:
-            ev[1].record(st)
 
     for i in range(warm):
         step(i)
     torch.cuda.synchronize()
     lens0 = layer.seq_lens.clone()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for i in range(steps):
-            step(warm + i)
-    torch.cuda.synchronize()
-    # untimed first replay (it also uploads the graph), then the lengths are put back so
-    # that the timed replay appends the same tokens into the same blocks
-    graph.replay()
-    torch.cuda.synchronize()
-    layer.seq_lens.copy_(lens0)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
-    clocks.start()
-    time.sleep(0.3)
-    torch.cuda.synchronize()
-    clocks.mark("start")
-    t0.record(stream)
-    graph.replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    clocks.mark("end")
-    clocks.stop()
-    ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
-          for _ in range(steps)]
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2):
-        for i in range(steps):
-            step(warm + steps + i, ev[i])
-    g2.replay()
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
-    dec_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    def reset():  # the lengths put back: every replay appends the same tokens into the same blocks
+        layer.seq_lens.copy_(lens0)
+
+    ms, clk, rec = _timed(lambda i: step(warm + i), steps, 0, reset=reset)
     assert layer.error_bits() == 0
     L = S + W
     kv_bytes = B * Hkv * L * D * 2 * 2
     alg_decode = kv_bytes + 2 * (B * Hq * D * 2)
     hbm, _, _, peak_kind = _peaks()
     value = kv_bytes / (ms * 1e-3) / 1e9
-    achieved = alg_decode / (dec_ms * 1e-3) / 1e9
+    roof = _launch_roofline(lambda i: sk.paged_decode_attention(layer, qs[i, :, 0], out=out, workspace=ws,
+                                                                sink_logits=zl), steps, alg_decode, None,
+                            "paged decode attention (split-K + combine); its launches back to back in one graph",
+                            "K+V of 4096 visible rows x 32 sequences x 8 kv heads + q + out")
     return {"metric": METRIC + " (paged cache)", "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
             "steps": steps, "warmup": warm, "ms_per_step": round(ms, 5), "higher_is_better": True,
             "dtype": "bf16", "data": "synthetic",
@@ -795,28 +764,23 @@ def bench_paged(args):
                        "learned_sink_logits": bool(args.learned_sink),
                        "l2": f"inputs larger than L2 (KV {kv_bytes / 1e6:.0f} MB per step)"},
             "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
-                         "frac": round(achieved / hbm, 4),
-                         "traffic": None,
-                         "kernel": "paged decode attention (split-K + combine), per launch",
-                         "algorithmic_bytes_per_launch": alg_decode, "launch_ms": round(dec_ms, 5),
-                         "peak_source": f"{peak_kind} hbm_gbs"},
-            "gpu_launches": steps * 3, "launch": "cuda graph of the timed steps", "clocks": clocks.summary()}
+            "roofline": roof, "timing": rec,
+            "gpu_launches": steps * 3 * rec["replays"], "clocks": clk}
 
 
 def bench_window_i8(args):
     """The windowed-layer decode step on an int8 K cache: the same shapes as the default
     line (B=32, H_q=32, H_kv=8, d_h=r=128, S=4, W=4092, rings full at random heads);
     K rows are 128 int8 codes plus one fp32 scale, V and queries bf16.  One step = RoPE +
-    append (K quantised per row) + split-K attention, the timed steps captured as one
-    CUDA graph."""
+    append (K quantised per row) + split-K attention, the steps captured as one CUDA
+    graph and replayed (ring counters put back after each replay)."""
     import torch
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
     c = synth.WINDOW
     B, Hq, Hkv, D, S, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
     steps, warm = args.steps, args.warmup
-    n = 2 * steps + warm
+    n = steps + warm
     tbl = sk.RopeTable(D, c["r"], c["theta"], c["pos_hi"] + n + 64)
     layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W, k_dtype=torch.int8)
     layer.k.copy_(synth.randint(layer.k.shape, 11, -127, 128, device="cuda").to(torch.int8))
@@ -833,61 +797,25 @@ def bench_window_i8(args):
     ws = torch.empty(sk.decode_workspace_bytes(layer, Hq), dtype=torch.uint8, device="cuda")
     zl = _learned_sinks(args, Hq)
 
-    def step(i, ev=None):
-        st = torch.cuda.current_stream()
+    def step(i):
         sk.kv_append(tbl, layer, qs[i], ks[i], vs[i])
-        if ev is not None:
-            ev[0].record(st)
         sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws, sink_logits=zl)
-        if ev is not None:
-            ev[1].record(st)
 
     for i in range(warm):
         step(i)
     torch.cuda.synchronize()
-    state0 = [t.clone() for t in (layer.pos, layer.head, layer.count)]
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for i in range(steps):
-            step(warm + i)
-    torch.cuda.synchronize()
-    # untimed first replay (it also uploads the graph), then the ring state is put back
-    # so that the timed replay makes the same appends and reads
-    graph.replay()
-    torch.cuda.synchronize()
-    for t, s0 in zip((layer.pos, layer.head, layer.count), state0):
-        t.copy_(s0)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
-    clocks.start()
-    time.sleep(0.3)
-    torch.cuda.synchronize()
-    clocks.mark("start")
-    t0.record(stream)
-    graph.replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    clocks.mark("end")
-    clocks.stop()
-    ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
-          for _ in range(steps)]
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2):
-        for i in range(steps):
-            step(warm + steps + i, ev[i])
-    g2.replay()
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
-    dec_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    ms, clk, rec = _timed(lambda i: step(warm + i), steps, 0, reset=_state_saver([layer]))
     assert layer.error_bits() == 0
     L = S + W
     kv_bytes = B * Hkv * L * (D + 4 + D * 2)     # int8 K row + its scale, bf16 V row
     alg_decode = kv_bytes + 2 * (B * Hq * D * 2)
     hbm, _, _, peak_kind = _peaks()
     value = kv_bytes / (ms * 1e-3) / 1e9
-    achieved = alg_decode / (dec_ms * 1e-3) / 1e9
+    roof = _launch_roofline(lambda i: sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws,
+                                                          sink_logits=zl), steps, alg_decode, None,
+                            "decode attention over int8 keys (split-K + combine); its launches back to back in "
+                            "one graph", "int8 K + fp32 scale + bf16 V of 4096 rows x 32 sequences x 8 kv heads "
+                                         "+ q + out")
     return {"metric": METRIC + " (int8 K cache)", "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
             "steps": steps, "warmup": warm, "ms_per_step": round(ms, 5), "higher_is_better": True,
             "dtype": "bf16 q/v, int8 K + fp32 scale", "data": "synthetic",
@@ -896,12 +824,8 @@ def bench_window_i8(args):
                        "window": W, "learned_sink_logits": bool(args.learned_sink),
                        "l2": f"inputs larger than L2 (KV {kv_bytes / 1e6:.0f} MB per step)"},
             "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
-                         "frac": round(achieved / hbm, 4), "traffic": None,
-                         "kernel": "decode attention over int8 keys (split-K + combine), per launch",
-                         "algorithmic_bytes_per_launch": alg_decode, "launch_ms": round(dec_ms, 5),
-                         "peak_source": f"{peak_kind} hbm_gbs"},
-            "gpu_launches": steps * 3, "launch": "cuda graph of the timed steps", "clocks": clocks.summary()}
+            "roofline": roof, "timing": rec,
+            "gpu_launches": steps * 3 * rec["replays"], "clocks": clk}
 
 
 def bench_shift(args, kdt):
@@ -1585,13 +1509,15 @@ def cpu_baseline(n_seq=32):
 
 ROWS = (("tiny", bench_tiny), ("window_b1", bench_window_b1), ("hybrid", bench_hybrid),
         ("prefill", bench_prefill), ("rerotate_bf16", lambda a: bench_rerotate(a, "bf16")),
-        ("rerotate_i8", lambda a: bench_rerotate(a, "i8")))
+        ("rerotate_i8", lambda a: bench_rerotate(a, "i8")), ("window_i8", bench_window_i8),
+        ("paged", bench_paged))
 
 
 def bench_rows(args):
     """Every other configuration of the path on this GPU, each with its roofline and
     its oracle baseline: the tiny case, single-stream decode, the hybrid 32-layer step,
-    the prefill chunk and the two rerotations."""
+    the prefill chunk and the two rerotations; then the windowed step over int8 keys
+    and over a paged cache (the oracle's arithmetic there is the windowed line's)."""
     import gc
     import torch
     rows = {}
@@ -1604,7 +1530,7 @@ def bench_rows(args):
             r = {"error": f"{type(e).__name__}: {str(e)[:300]}"}
         gc.collect()
         torch.cuda.empty_cache()
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and name in CPU_ROWS:
             try:
                 r["cpu_baseline"] = cpu_row(name)
             except Exception as e:

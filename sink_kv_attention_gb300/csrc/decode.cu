@@ -154,7 +154,9 @@ template <int N> constexpr int ilog2() { return N <= 1 ? 0 : 1 + ilog2<N / 2>();
 
 // KQ: the K cache holds int8 codes (D bytes per row, one fp32 scale per row); V is T.
 template <typename T, int D, int NREP, bool KQ = false> struct DecodeCfg {
-    static constexpr int NWARPS = decode_warps<T, D, NREP>();
+    // int8 keys at n_rep 4: 12 consumer warps (3 per scheduler; the kernel is bound by
+    // the consumers' issue and latency, and its 128 registers allow them)
+    static constexpr int NWARPS = (KQ && NREP == 4) ? 12 : decode_warps<T, D, NREP>();
     static constexpr int LG = ilog2<NREP>();
     static constexpr int VEC = ElemIO<T>::kPerVec;    // elements per 16-byte chunk
     static constexpr int CPL = (D / VEC) / 8;         // chunks per lane (QK)
@@ -162,7 +164,8 @@ template <typename T, int D, int NREP, bool KQ = false> struct DecodeCfg {
     static constexpr int RPG = 8 / NREP;              // rows per 8-lane group
     static constexpr int RPW = 4 * RPG;               // rows per warp per stage
     static constexpr int TILE = NWARPS * RPW;         // rows per stage
-    static_assert((TILE & (TILE - 1)) == 0, "tile height must be a power of two");
+    // paged tiles start at multiples of the tile height; int8-key layers are never paged
+    static_assert(KQ || (TILE & (TILE - 1)) == 0, "tile height must be a power of two");
     static constexpr int DPV = D / 32;                // dims per lane (PV)
     static constexpr int ROW_BYTES = D * int(sizeof(T));      // a V row (and a K row unless KQ)
     static constexpr int K_ROW_BYTES = KQ ? D : ROW_BYTES;
@@ -507,20 +510,62 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ>::THREADS, 1)
         const int64_t unit = int64_t(b) * p.Hkv + g;
 
         // q slice of this lane for the NREP heads in its permuted order, pre-scaled: the
-        // dims of its K chunks (chunks l8 and l8 + 8 of 8 elements; with int8 keys, dims
-        // 16 l8 .. 16 l8 + 15, one 16-code chunk)
-        float2 q2[NREP][C::DPL / 2];
+        // dims of its K chunks (chunks l8 and l8 + 8 of 8 elements).  With int8 keys the
+        // lane's dims are 16 l8 .. 16 l8 + 15 (one 16-code chunk), and q is held as int16
+        // pairs with one scale per head: the dot product with the codes is then exact
+        // integer arithmetic (dp2a), with no conversion of the codes.
+        float2 q2[NREP][KQ ? 1 : C::DPL / 2];
+        uint32_t q16[NREP][KQ ? 8 : 1];
+        float qsc = p.qscale;  // int8 keys: the scale of this lane's head (slot 0) times qscale
+        if constexpr (KQ) {
+            float qf[NREP][16];
+            float am[NREP];
 #pragma unroll
-        for (int hh = 0; hh < NREP; ++hh) {
-            const T* qrow = qbase + (unit * NREP + (hh ^ hperm)) * D;
+            for (int hh = 0; hh < NREP; ++hh) {
+                const T* qrow = qbase + (unit * NREP + (hh ^ hperm)) * D;
+                am[hh] = 0.0f;
 #pragma unroll
-            for (int i = 0; i < C::CPL; ++i) {
-                const uint4 raw = reinterpret_cast<const uint4*>(qrow)[KQ ? 2 * l8 + i : l8 + 8 * i];
-                float f[C::VEC];
-                ElemIO<T>::unpack(raw, f);
+                for (int i = 0; i < 2; ++i) {
+                    const uint4 raw = reinterpret_cast<const uint4*>(qrow)[2 * l8 + i];
+                    ElemIO<T>::unpack(raw, qf[hh] + 8 * i);
+                }
 #pragma unroll
-                for (int e = 0; e < C::VEC / 2; ++e)
-                    q2[hh][i * C::VEC / 2 + e] = make_float2(f[2 * e] * p.qscale, f[2 * e + 1] * p.qscale);
+                for (int e = 0; e < 16; ++e) am[hh] = fmaxf(am[hh], fabsf(qf[hh][e]));
+            }
+            // max |q| of each head over its 128 dims: the 8 lanes of the group hold 16 dims
+            // each; slot hh of the partner at xor distance x holds this lane's slot
+            // hh ^ (x & (NREP - 1)) head
+#pragma unroll
+            for (int x = 1; x < 8; x <<= 1) {
+                float t[NREP];
+#pragma unroll
+                for (int hh = 0; hh < NREP; ++hh) t[hh] = __shfl_xor_sync(kFull, am[hh ^ (x & (NREP - 1))], x);
+#pragma unroll
+                for (int hh = 0; hh < NREP; ++hh) am[hh] = fmaxf(am[hh], t[hh]);
+            }
+#pragma unroll
+            for (int hh = 0; hh < NREP; ++hh) {
+                const float inv = am[hh] > 0.0f ? 32767.0f / am[hh] : 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int lo = __float2int_rn(qf[hh][2 * e] * inv), hi = __float2int_rn(qf[hh][2 * e + 1] * inv);
+                    q16[hh][e] = (uint32_t(lo) & 0xFFFFu) | (uint32_t(hi) << 16);
+                }
+            }
+            qsc = (am[0] > 0.0f ? am[0] / 32767.0f : 0.0f) * p.qscale;
+        } else {
+#pragma unroll
+            for (int hh = 0; hh < NREP; ++hh) {
+                const T* qrow = qbase + (unit * NREP + (hh ^ hperm)) * D;
+#pragma unroll
+                for (int i = 0; i < C::CPL; ++i) {
+                    const uint4 raw = reinterpret_cast<const uint4*>(qrow)[l8 + 8 * i];
+                    float f[C::VEC];
+                    ElemIO<T>::unpack(raw, f);
+#pragma unroll
+                    for (int e = 0; e < C::VEC / 2; ++e)
+                        q2[hh][i * C::VEC / 2 + e] = make_float2(f[2 * e] * p.qscale, f[2 * e + 1] * p.qscale);
+                }
             }
         }
 
@@ -556,15 +601,39 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ>::THREADS, 1)
 
             // ---- QK: slot jj*NREP + hh holds row (jj ^ rperm), head (hh ^ hperm) ----
             float part[8];
+            if constexpr (KQ) {
+                // int8 codes against int16 q: 8 dp2a per (row, head), exact int32 sums
+                int ipart[8];
 #pragma unroll
-            for (int jj = 0; jj < C::RPG; ++jj) {
-                const int lr = gi * C::RPG + (jj ^ rperm);
-                float2 kf[C::DPL / 2];
-                if (lr < nw) {
-                    const uint4* krow = reinterpret_cast<const uint4*>(ktile + (wrow0 + lr) * C::K_ROW_BYTES);
-                    if constexpr (KQ) {
-                        codes16_to_pairs(krow[l8], kf);  // 16 codes, exact in fp32
-                    } else {
+                for (int jj = 0; jj < C::RPG; ++jj) {
+                    const int lr = gi * C::RPG + (jj ^ rperm);
+                    const uint4 kw = lr < nw ? reinterpret_cast<const uint4*>(ktile + (wrow0 + lr) * C::K_ROW_BYTES)[l8]
+                                             : make_uint4(0, 0, 0, 0);
+                    const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+                    for (int hh = 0; hh < NREP; ++hh) {
+                        int a = 0;
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            a = __dp2a_lo(int(q16[hh][2 * wi]), int(w4[wi]), a);
+                            a = __dp2a_hi(int(q16[hh][2 * wi + 1]), int(w4[wi]), a);
+                        }
+                        ipart[jj * NREP + hh] = a;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ipart[i] += __shfl_xor_sync(kFull, ipart[i + 4], 4);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) ipart[i] += __shfl_xor_sync(kFull, ipart[i + 2], 2);
+                ipart[0] += __shfl_xor_sync(kFull, ipart[1], 1);
+                part[0] = float(ipart[0]) * qsc;
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < C::RPG; ++jj) {
+                    const int lr = gi * C::RPG + (jj ^ rperm);
+                    float2 kf[C::DPL / 2];
+                    if (lr < nw) {
+                        const uint4* krow = reinterpret_cast<const uint4*>(ktile + (wrow0 + lr) * C::K_ROW_BYTES);
 #pragma unroll
                         for (int i = 0; i < C::CPL; ++i) {
                             const uint4 raw = krow[l8 + 8 * i];
@@ -578,25 +647,25 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ>::THREADS, 1)
                                 kf[i * 2 + 1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
                             }
                         }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < C::DPL / 2; ++e) kf[e] = make_float2(0.f, 0.f);
                     }
-                } else {
 #pragma unroll
-                    for (int e = 0; e < C::DPL / 2; ++e) kf[e] = make_float2(0.f, 0.f);
+                    for (int hh = 0; hh < NREP; ++hh) {
+                        float2 a = __fmul2_rn(q2[hh][0], kf[0]);
+#pragma unroll
+                        for (int e = 1; e < C::DPL / 2; ++e) a = __ffma2_rn(q2[hh][e], kf[e], a);
+                        part[jj * NREP + hh] = a.x + a.y;
+                    }
                 }
+                // ---- butterfly reduce-scatter: slot i of lane L holds value i ^ L ----
 #pragma unroll
-                for (int hh = 0; hh < NREP; ++hh) {
-                    float2 a = __fmul2_rn(q2[hh][0], kf[0]);
+                for (int i = 0; i < 4; ++i) part[i] += __shfl_xor_sync(kFull, part[i + 4], 4);
 #pragma unroll
-                    for (int e = 1; e < C::DPL / 2; ++e) a = __ffma2_rn(q2[hh][e], kf[e], a);
-                    part[jj * NREP + hh] = a.x + a.y;
-                }
+                for (int i = 0; i < 2; ++i) part[i] += __shfl_xor_sync(kFull, part[i + 2], 2);
+                part[0] += __shfl_xor_sync(kFull, part[1], 1);
             }
-            // ---- butterfly reduce-scatter: slot i of lane L holds value i ^ L ----
-#pragma unroll
-            for (int i = 0; i < 4; ++i) part[i] += __shfl_xor_sync(kFull, part[i + 4], 4);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) part[i] += __shfl_xor_sync(kFull, part[i + 2], 2);
-            part[0] += __shfl_xor_sync(kFull, part[1], 1);
             const float s = my_row < nw ? (KQ ? part[0] * kscale : part[0]) : -INFINITY;
 
             // ---- online softmax (base 2) for this lane's head ----
