@@ -153,10 +153,14 @@ template <typename T, int D, int NREP> constexpr int decode_warps() {
 template <int N> constexpr int ilog2() { return N <= 1 ? 0 : 1 + ilog2<N / 2>(); }
 
 // KQ: the K cache holds int8 codes (D bytes per row, one fp32 scale per row); V is T.
-template <typename T, int D, int NREP, bool KQ = false> struct DecodeCfg {
-    // int8 keys at n_rep 4: 12 consumer warps (3 per scheduler; the kernel is bound by
-    // the consumers' issue and latency, and its 128 registers allow them)
-    static constexpr int NWARPS = (KQ && NREP == 4) ? 12 : decode_warps<T, D, NREP>();
+// PAGED: the block-table producer, whose tiles start at multiples of the tile height.
+template <typename T, int D, int NREP, bool KQ = false, bool PAGED = false> struct DecodeCfg {
+    // Contiguous bf16 layers at n_rep 4 and d_h 128 (bf16 or int8 keys) run 12 consumer
+    // warps, 3 per scheduler: the consumers' issue and latency bound these kernels
+    // (measured against 8 warps: bf16 keys +2.4% on the windowed step with 3 stages,
+    // int8 keys +13%).  Paged tiles keep a power-of-two height.
+    static constexpr bool WIDE = !PAGED && NREP == 4 && D == 128 && sizeof(T) == 2;
+    static constexpr int NWARPS = WIDE ? 12 : decode_warps<T, D, NREP>();
     static constexpr int LG = ilog2<NREP>();
     static constexpr int VEC = ElemIO<T>::kPerVec;    // elements per 16-byte chunk
     static constexpr int CPL = (D / VEC) / 8;         // chunks per lane (QK)
@@ -164,18 +168,19 @@ template <typename T, int D, int NREP, bool KQ = false> struct DecodeCfg {
     static constexpr int RPG = 8 / NREP;              // rows per 8-lane group
     static constexpr int RPW = 4 * RPG;               // rows per warp per stage
     static constexpr int TILE = NWARPS * RPW;         // rows per stage
-    // paged tiles start at multiples of the tile height; int8-key layers are never paged
-    static_assert(KQ || (TILE & (TILE - 1)) == 0, "tile height must be a power of two");
+    static_assert(!PAGED || (TILE & (TILE - 1)) == 0, "paged tile height must be a power of two");
     static constexpr int DPV = D / 32;                // dims per lane (PV)
     static constexpr int ROW_BYTES = D * int(sizeof(T));      // a V row (and a K row unless KQ)
     static constexpr int K_ROW_BYTES = KQ ? D : ROW_BYTES;
     static constexpr int STAGE_BYTES = TILE * (K_ROW_BYTES + ROW_BYTES);   // K tile then V tile
     static_assert(!KQ || (D == 128 && sizeof(T) == 2), "int8 keys: head_dim 128, bf16 queries and values");
-    static constexpr int STAGES_FIT = (192 * 1024) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 5 ? 5 : STAGES_FIT;
-    static_assert(STAGES >= 2, "stage too large");
     static constexpr int MERGE_FLOATS = NWARPS * NREP * (D + 2);
     static constexpr int PS_F2 = NWARPS * (RPW * NREP + NREP);  // (p, p) pairs + (alpha, alpha)
+    // as many stages (at most 5) as fit beside the rest in 227 KB, less 1 KB of slack
+    static constexpr size_t OTHER_BYTES = size_t(MERGE_FLOATS) * 4 + size_t(PS_F2) * 8 + (kMaxBatch + 1) * 8 + 2 * 5 * 8;
+    static constexpr int STAGES_FIT = int((232448 - 1024 - OTHER_BYTES) / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_FIT > 5 ? 5 : STAGES_FIT;
+    static_assert(STAGES >= 2, "stage too large");
     static constexpr size_t OFF_MERGE = size_t(STAGES) * STAGE_BYTES;
     static constexpr size_t OFF_PS = OFF_MERGE + size_t(MERGE_FLOATS) * 4;
     static constexpr size_t OFF_PRE = OFF_PS + size_t(PS_F2) * 8;
@@ -394,9 +399,9 @@ __device__ __forceinline__ void prefetch_share(const DecodeParams& p, const int6
 // separate instantiations: the contiguous kernel then carries none of the paged code
 // (compiled into one kernel, the contiguous path measured 3-5% slower).
 template <typename T, int D, int NREP, bool PAGED, bool KQ>
-__global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ>::THREADS, 1)
+__global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ, PAGED>::THREADS, 1)
     decode_split_kernel(DecodeParams p) {
-    using C = DecodeCfg<T, D, NREP, KQ>;
+    using C = DecodeCfg<T, D, NREP, KQ, PAGED>;
     constexpr int NWARPS = C::NWARPS;
     constexpr int STAGES = C::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1098,9 +1103,10 @@ inline int combine_wpu(int P, int64_t units) {
 // KQ: int8 keys (contiguous layers only; paged layers hold bf16 or fp32 keys).
 template <typename T, int D, int NREP, bool KQ = false>
 struct DecodeLaunch {
-    using C = DecodeCfg<T, D, NREP, KQ>;
+    using C = DecodeCfg<T, D, NREP, KQ, false>;   // contiguous layers
+    using CP = DecodeCfg<T, D, NREP, KQ, true>;   // paged layers (never with int8 keys)
 
-    // Every instantiation launched from here (contiguous, and paged unless KQ) gets the
+    // Every instantiation launched from here (contiguous, and paged unless KQ) gets its
     // shared-memory limit; the grid is sized from the smallest occupancy among them.
     static int blocks_per_sm() {
         static PerDevice<int> cache;
@@ -1117,9 +1123,9 @@ struct DecodeLaunch {
                 } else {
                     if (cudaFuncSetAttribute(decode_split_kernel<T, D, NREP, true, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(C::SMEM)) != cudaSuccess ||
+                                             int(CP::SMEM)) != cudaSuccess ||
                         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, decode_split_kernel<T, D, NREP, true, false>,
-                                                                      C::THREADS, C::SMEM) != cudaSuccess)
+                                                                      CP::THREADS, CP::SMEM) != cudaSuccess)
                         return 0;
                     return std::min(n0, n1);
                 }
@@ -1149,8 +1155,8 @@ struct DecodeLaunch {
                            st, p);
         } else {
             e = p.kind == kKindPaged
-                    ? launch_pdl(decode_split_kernel<T, D, NREP, true, false>, dim3(p.n_blocks), dim3(C::THREADS),
-                                 C::SMEM, st, p)
+                    ? launch_pdl(decode_split_kernel<T, D, NREP, true, false>, dim3(p.n_blocks), dim3(CP::THREADS),
+                                 CP::SMEM, st, p)
                     : launch_pdl(decode_split_kernel<T, D, NREP, false, false>, dim3(p.n_blocks), dim3(C::THREADS),
                                  C::SMEM, st, p);
         }
