@@ -37,10 +37,16 @@ METRIC = "sink+window decode attn KV-read GB/s (frac of HBM peak), tokens/s, key
 # processed and is scaled by that factor to one launch of the full workload.
 NCU_TRAFFIC = {
     "decode_window_b32": dict(
-        bytes=540113408, scale=1,
-        capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --steps 5 --warmup 3 "
-                "--no-cpu-baseline (split kernel only)",
-        sources={"decode.cu": "8c96fd4d98b61f9203207f41fa2780aa91f52e775cc43f1c8f744042f1e39dca",
+        bytes=542278400, scale=1,
+        capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --no-rows --no-cpu-baseline "
+                "--steps 5 --warmup 3 (split kernel only)",
+        sources={"decode.cu": "55c52f9e7df83499bc4fbcc79d689e224d9861abf0c768cfc5f9b179acc35f02",
+                 "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}),
+    "decode_window_b32_int8": dict(
+        bytes=410712576, scale=1,
+        capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload window_i8 "
+                "--steps 5 --warmup 3 (split kernel only)",
+        sources={"decode.cu": "55c52f9e7df83499bc4fbcc79d689e224d9861abf0c768cfc5f9b179acc35f02",
                  "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}),
     "prefill_attn_t32768": dict(
         bytes=634700000, scale=1,
@@ -812,7 +818,7 @@ def bench_window_i8(args):
     hbm, _, _, peak_kind = _peaks()
     value = kv_bytes / (ms * 1e-3) / 1e9
     roof = _launch_roofline(lambda i: sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws,
-                                                          sink_logits=zl), steps, alg_decode, None,
+                                                          sink_logits=zl), steps, alg_decode, "decode_window_b32_int8",
                             "decode attention over int8 keys (split-K + combine); its launches back to back in "
                             "one graph", "int8 K + fp32 scale + bf16 V of 4096 rows x 32 sequences x 8 kv heads "
                                          "+ q + out")
