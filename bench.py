@@ -1026,7 +1026,9 @@ def bench_prefill(args):
     tf_alg = alg_flops / (ms_attn * 1e-3) / 1e12
     append_gbs = append_bytes / (ms_append * 1e-3) / 1e9
     roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-            "frac": round(tf / bf16_peak, 4), "traffic": _traffic("prefill_attn_t32768"),
+            "frac": round(tf / bf16_peak, 4), "peak_sustained": bf16_sust,
+            "frac_sustained": round(tf / bf16_sust, 4) if bf16_sust else None,
+            "traffic": _traffic("prefill_attn_t32768"),
             "kernel": "prefill_attn_kernel (tcgen05, one launch per step)",
             "flops_per_launch": tile_flops, "flops": "4 d_h x 128 x 64 per visited (128-row, 64-key) tile and "
                                                      "group of q heads (the tiles the mask does not rule out)",
