@@ -1025,18 +1025,24 @@ def bench_prefill(args):
     tf = tile_flops / (ms_attn * 1e-3) / 1e12
     tf_alg = alg_flops / (ms_attn * 1e-3) / 1e12
     append_gbs = append_bytes / (ms_append * 1e-3) / 1e9
-    roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-            "frac": round(tf / bf16_peak, 4), "peak_sustained": bf16_sust,
+    # The peak: the sustained bf16 figure (a seconds-long matmul loop under the power cap)
+    # when the clock record shows the power cap active over this region, else the burst
+    # figure; both fractions are reported.
+    capped = "sw_power_cap" in (clk.get("reasons") or []) and bool(bf16_sust)
+    peak = bf16_sust if capped else bf16_peak
+    roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(tf / peak, 4), "frac_burst": round(tf / bf16_peak, 4),
             "frac_sustained": round(tf / bf16_sust, 4) if bf16_sust else None,
             "traffic": _traffic("prefill_attn_t32768"),
             "kernel": "prefill_attn_kernel (tcgen05, one launch per step)",
             "flops_per_launch": tile_flops, "flops": "4 d_h x 128 x 64 per visited (128-row, 64-key) tile and "
                                                      "group of q heads (the tiles the mask does not rule out)",
-            "algorithmic": {"achieved": round(tf_alg, 1), "frac": round(tf_alg / bf16_peak, 4),
+            "algorithmic": {"achieved": round(tf_alg, 1), "frac": round(tf_alg / peak, 4),
                             "flops_per_launch": alg_flops,
                             "flops": "4 d_h per visible (query, key) pair and q head"},
-            "launch_ms": round(ms_attn, 5), "peak_source": f"{peak_kind} bf16_tflops (burst: the kernel is timed "
-                                                            f"alone)"}
+            "launch_ms": round(ms_attn, 5),
+            "peak_source": (f"{peak_kind} bf16_tflops_sustained: the region ran under the power cap" if capped
+                            else f"{peak_kind} bf16_tflops (burst)")}
     append_roof = {"bound": "hbm", "achieved": round(append_gbs, 1), "peak": hbm, "unit": "GB/s",
                    "frac": round(append_gbs / hbm, 4), "traffic": None,
                    "kernel": "kv_append_kernel (RoPE on Q and K + ring write of the chunk's last W rows)",
@@ -1050,8 +1056,8 @@ def bench_prefill(args):
                        "visited_tiles_per_head_group": tiles, "heads_per_cta": nh,
                        "tile": f"128 rows ({nh} heads x {128 // nh} queries) x 64 keys",
                        "learned_sink_logits": bool(args.learned_sink)},
-            "frac_of_bf16_peak": round(tf / bf16_peak, 4),
-            "algorithmic_tflops": round(tf_alg, 1), "algorithmic_frac_of_bf16_peak": round(tf_alg / bf16_peak, 4),
+            "frac_of_bf16_peak": round(tf / peak, 4),
+            "algorithmic_tflops": round(tf_alg, 1), "algorithmic_frac_of_bf16_peak": round(tf_alg / peak, 4),
             "algorithmic_flops": alg_flops, "tile_flops": tile_flops,
             "append_ms": round(ms_append, 4), "append_gbs": round(append_gbs, 1),
             "append_frac_of_hbm_peak": round(append_gbs / hbm, 4),
