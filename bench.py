@@ -963,14 +963,19 @@ def _prefill_heads_per_cta(n_rep):
     return nh
 
 
-def _prefill_tiles(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64):
+PREFILL_SINK_STRIP = 16   # keys of the strip a sink tile below the window is visited as
+
+
+def _prefill_tiles(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64, strips=False):
     """(128-row x 64-key) tiles the prefill kernel visits per (sequence, group of nh q
     heads), and nh: the kernel's plan (blocks of BM / nh queries of nh heads; per block
     the sink tiles below the window, then the window's tiles).  qoff > 0: a chunk over
-    a prior cache, whose qoff keys come first (the leading S of them sinks)."""
+    a prior cache, whose qoff keys come first (the leading S of them sinks).  strips=True
+    also returns how many of those tiles are visited as a 16-key sink strip (a single
+    sink tile below the window whose sinks fit in the strip)."""
     nh = _prefill_heads_per_cta(n_rep)
     qpb = BM // nh
-    n_total = 0
+    n_total = n_strip = 0
     Tk = T + qoff
     nsk = S if qoff > 0 else max(0, S - p0)
     for q0 in range(0, T, qpb):
@@ -980,7 +985,8 @@ def _prefill_tiles(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64):
         sink_keys = min(Tk, nsk) if W > 0 else 0
         n_sink = min(first, (sink_keys + BN - 1) // BN)
         n_total += n_sink + (last - first + 1)
-    return n_total, nh
+        n_strip += 1 if (n_sink == 1 and nsk <= PREFILL_SINK_STRIP) else 0
+    return (n_total, nh, n_strip) if strips else (n_total, nh)
 
 
 def bench_prefill(args):
@@ -1019,8 +1025,10 @@ def bench_prefill(args):
     hbm = _peaks()[0]
     vis_pairs = sum(min(t + 1, S + W) for t in range(T))      # (query, key) pairs per head
     alg_flops = vis_pairs * Hq * B * 4 * D
-    tiles, nh = _prefill_tiles(T, S, W, Hq // Hkv)
-    tile_flops = tiles * (Hq // nh) * B * 4 * 128 * 64 * D
+    tiles, nh, strips = _prefill_tiles(T, S, W, Hq // Hkv, strips=True)
+    # visited tiles at 64 keys each, the sink strips at 16
+    tile_keys = (tiles - strips) * 64 + strips * PREFILL_SINK_STRIP
+    tile_flops = tile_keys * (Hq // nh) * B * 4 * 128 * D
     append_bytes = B * T * (Hq + 2 * Hkv) * D * 2 + B * T * (Hq + Hkv) * D * 2 + B * Hkv * (S + W) * D * 2 * 2
     tf = tile_flops / (ms_attn * 1e-3) / 1e12
     tf_alg = alg_flops / (ms_attn * 1e-3) / 1e12
@@ -1036,7 +1044,8 @@ def bench_prefill(args):
             "traffic": _traffic("prefill_attn_t32768"),
             "kernel": "prefill_attn_kernel (tcgen05, one launch per step)",
             "flops_per_launch": tile_flops, "flops": "4 d_h x 128 x 64 per visited (128-row, 64-key) tile and "
-                                                     "group of q heads (the tiles the mask does not rule out)",
+                                                     "group of q heads (the tiles the mask does not rule out), "
+                                                     "x 16 for a sink strip",
             "algorithmic": {"achieved": round(tf_alg, 1), "frac": round(tf_alg / peak, 4),
                             "flops_per_launch": alg_flops,
                             "flops": "4 d_h per visible (query, key) pair and q head"},
@@ -1053,7 +1062,8 @@ def bench_prefill(args):
             "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": steps, "warmup": warm,
             "ms_per_step": round(ms_attn, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "prefill chunk: B=1, T=32768, H_q=32, H_kv=8, d_h=128, S=4, W=4092",
-                       "visited_tiles_per_head_group": tiles, "heads_per_cta": nh,
+                       "visited_tiles_per_head_group": tiles, "sink_strips_per_head_group": strips,
+                       "heads_per_cta": nh,
                        "tile": f"128 rows ({nh} heads x {128 // nh} queries) x 64 keys",
                        "learned_sink_logits": bool(args.learned_sink)},
             "frac_of_bf16_peak": round(tf / peak, 4),
@@ -1098,8 +1108,9 @@ def bench_prefill_chunk(args):
     assert layer.error_bits() == 0
     _, bf16_peak, _, peak_kind = _peaks()
     alg_flops = T * (S + W) * Hq * B * 4 * D          # every query sees S + W keys here
-    tiles, nh = _prefill_tiles(T, S, W, Hq // Hkv, qoff=qoff)
-    tile_flops = tiles * (Hq // nh) * B * 4 * 128 * 64 * D
+    tiles, nh, strips = _prefill_tiles(T, S, W, Hq // Hkv, qoff=qoff, strips=True)
+    tile_keys = (tiles - strips) * 64 + strips * PREFILL_SINK_STRIP
+    tile_flops = tile_keys * (Hq // nh) * B * 4 * 128 * D
     tf = tile_flops / (ms * 1e-3) / 1e12
     return {"metric": "chunked prefill attention over a prior ring, TFLOP/s on visited tiles (frac of dense bf16 "
                       "peak)",

@@ -5,7 +5,8 @@
 // query t sees key k iff k <= t and (p0 + k < S or t - k < W); W <= 0 is a global
 // layer (causal only).  "Inference & 128K Long Context", prefill vs decode: masking a
 // dense score matrix does not cut FLOPs, so here only key tiles the mask leaves (at
-// least partly) visible are visited: the sink tile(s) and the tiles of the window.
+// least partly) visible are visited: the sink tile(s) and the tiles of the window.  A
+// sink tile below the window whose sinks fit in 16 keys is visited as a 16-key strip.
 //
 // One CTA = one (sequence, group of nh q heads sharing a kv head, block of qpb = 128 / nh
 // queries): BM = 128 tile rows, row r = head r / qpb, query r % qpb.
@@ -43,6 +44,7 @@ constexpr int HD = 128;
 constexpr int kThreads = 7 * 32;
 constexpr uint32_t kTmemCols = 256;  // S0 [0, 64), S1 [64, 128), O [128, 256)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kSinkStrip = 16;
 // Bounds of a learned sink logit ("Inference & 128K Long Context", "Sink clamp cache").
 constexpr float kSinkLogitMin = -10.0f;
 constexpr float kSinkLogitMax = 15.0f;
@@ -157,6 +159,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q0 = qb * p.qpb;
     const int g = h0 / (p.Hq / p.Hkv);
     const TilePlan tp = plan_tiles(p, q0);
+    // a sink tile below the window whose sinks fit in kSinkStrip keys is visited as a
+    // strip: Q K^T with N = kSinkStrip, P.V with K = kSinkStrip, kSinkStrip softmax columns
+    const int n_strip = (tp.n_sink == 1 && p.nsk <= kSinkStrip) ? 1 : 0;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -217,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ------------------------------- MMA issue -------------------------------
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN);
+            constexpr uint32_t idesc_qk_strip = idesc_bf16_f32(BM, kSinkStrip);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, HD) | (1u << 16);  // B (V) MN-major
             const uint32_t sq = smem_u32(smem + SM_Q);
             wait_or_flag(q_full, 0, bad);
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const uint32_t off = (kk & 3) * 32;        // 16 dims = 32 bytes
                         const uint64_t da = desc_kmajor_sw128(sq + half * (BM * 128) + off);
                         const uint64_t db = desc_kmajor_sw128(sk + half * (BN * 128) + off);
-                        umma_bf16(tmem + s * BN, da, db, idesc_qk, kk > 0 ? 1u : 0u);
+                        umma_bf16(tmem + s * BN, da, db, i < n_strip ? idesc_qk_strip : idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&s_full[s]);
                     umma_commit(&k_empty[s]);
@@ -247,13 +253,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                     wait_or_flag(&v_full[s], (j >> 1) & 1, bad);
                     tc_fence_after_sync();
                     const uint32_t sv = smem_u32(smem + SM_V + s * V_STAGE);
+                    if (j < n_strip) {
+                        // the sink strip: its 16 keys, one K step (P_j in 8 TMEM columns)
+                        const uint64_t db = desc_mnmajor_sw128(sv, BN * 128);
+                        umma_bf16_tmem_a(tmem + 2 * BN, tmem + s * BN, db, idesc_pv, j > 0 ? 1u : 0u);
+                    } else {
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        // A = P_j in TMEM: 16 keys = 8 columns of packed bf16 pairs; B = 16
-                        // key rows of V (2 KB), dims 64-127 in the second 8 KB block
-                        const uint64_t db = desc_mnmajor_sw128(sv + kk * 2048, BN * 128);
-                        umma_bf16_tmem_a(tmem + 2 * BN, tmem + s * BN + kk * 8, db, idesc_pv,
-                                         (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            // A = P_j in TMEM: 16 keys = 8 columns of packed bf16 pairs; B = 16
+                            // key rows of V (2 KB), dims 64-127 in the second 8 KB block
+                            const uint64_t db = desc_mnmajor_sw128(sv + kk * 2048, BN * 128);
+                            umma_bf16_tmem_a(tmem + 2 * BN, tmem + s * BN + kk * 8, db, idesc_pv,
+                                             (j > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit(&pv_done[s]);
                     umma_commit(&v_empty[s]);
@@ -267,7 +279,39 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int t = q0 + r % p.qpb;        // its query
         const uint32_t lane_base = uint32_t(warp * 32) << 16;
         float m_run = -INFINITY, l_run = 0.0f;
-        for (int i = 0; i < tp.n; ++i) {
+        if (n_strip) {
+            // tile 0, the sink strip: only sinks are visible (the window starts above it)
+            wait_or_flag(&s_full[0], 0, bad);
+            tc_fence_after_sync();
+            uint32_t raw[kSinkStrip];
+            tmem_ld_32x16(tmem + lane_base, raw);
+            tmem_ld_wait();
+            float sc[kSinkStrip];
+#pragma unroll
+            for (int j = 0; j < kSinkStrip; ++j) sc[j] = j < p.nsk ? __uint_as_float(raw[j]) : -INFINITY;
+            float mx = fmax3(sc[0], sc[1], sc[2]);
+#pragma unroll
+            for (int j = 3; j < kSinkStrip; j += 2) mx = fmax3(mx, sc[j], sc[j + 1 < kSinkStrip ? j + 1 : j]);
+            m_run = mx * p.scale_log2;
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm2 = make_float2(-m_run, -m_run);
+            uint32_t pk[kSinkStrip / 2];
+            float2 ls = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < kSinkStrip; e += 2) {
+                const float2 x = __ffma2_rn(make_float2(sc[e], sc[e + 1]), sc2, nm2);
+                const float p0 = fast_exp2_approx(x.x), p1 = fast_exp2_approx(x.y);
+                ls = __fadd2_rn(ls, make_float2(p0, p1));
+                pk[e >> 1] = float2_to_bf16x2(p0, p1);
+            }
+            tmem_st_32x8(tmem + lane_base, pk);
+            l_run = ls.x + ls.y;
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[0]);
+        }
+        for (int i = n_strip; i < tp.n; ++i) {
             const int s = i & 1;
             wait_or_flag(&s_full[s], (i >> 1) & 1, bad);
             tc_fence_after_sync();

@@ -48,3 +48,34 @@ def test_prefill_tiles_chunk_over_prior(T, S, W, n_rep, p0):
     s0 = min(S, p0) if W > 0 else 0
     qoff = s0 + (min(W - 1, p0 - s0) if W > 0 else p0)
     assert bench._prefill_tiles(T, S, W, n_rep, p0=p0, qoff=qoff) == _brute_tiles(T, S, W, n_rep, p0=p0, qoff=qoff)
+
+
+def _brute_strips(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64, strip=16):
+    """Query blocks whose key tile 0 holds visible pairs, all of them sink keys that fit in
+    one strip: the blocks whose tile 0 the kernel visits as a 16-key strip."""
+    nh = bench._prefill_heads_per_cta(n_rep)
+    qpb = BM // nh
+    Tk = T + qoff
+    if qoff:
+        s0 = min(S, p0)
+        pos = list(range(s0)) + list(range(p0 - (qoff - s0), p0)) + list(range(p0, p0 + T))
+        nsk = S
+    else:
+        pos = list(range(p0, p0 + T))
+        nsk = max(0, S - p0)
+    win = W if W > 0 else None
+    count = 0
+    for q0 in range(0, T, qpb):
+        vis = [j for t in range(q0, min(q0 + qpb, T)) for j in range(min(BN, Tk))
+               if mask_allows(p0 + t, pos[j], S, win)]
+        if vis and W > 0 and max(vis) < nsk and nsk <= strip:
+            count += 1
+    return count
+
+
+@pytest.mark.parametrize("T,S,W,n_rep,p0", [
+    (300, 4, 100, 4, 0), (300, 0, 100, 4, 0), (300, 4, 0, 4, 0), (513, 3, 130, 1, 1),
+    (1000, 4, 300, 2, 0), (700, 20, 100, 4, 0),
+])
+def test_prefill_sink_strips(T, S, W, n_rep, p0):
+    assert bench._prefill_tiles(T, S, W, n_rep, p0=p0, strips=True)[2] == _brute_strips(T, S, W, n_rep, p0=p0)
