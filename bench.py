@@ -971,19 +971,30 @@ def _prefill_tiles(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64, strips=False):
     """(128-row x 64-key) tiles the prefill kernel visits per (sequence, group of nh q
     heads), and nh: the kernel's plan (blocks of BM / nh queries of nh heads; per block
     the sink tiles below the window, then the window's tiles).  qoff > 0: a chunk over
-    a prior cache, whose qoff keys come first (the leading S of them sinks).  strips=True
-    also returns how many of those tiles are visited as a 16-key sink strip (a single
-    sink tile below the window whose sinks fit in the strip)."""
+    a prior cache; its qoff keys come first, padded to a multiple of BN (the padding is
+    never visible), then the chunk's keys.  strips=True also returns how many of those
+    tiles are visited as a 16-key sink strip (a single sink tile below the window whose
+    sinks fit in the strip)."""
     nh = _prefill_heads_per_cta(n_rep)
     qpb = BM // nh
+    qpad = -(-qoff // BN) * BN
+    Tk = T + qpad
+    chunk_sinks = max(0, S - p0)
+    if qoff > 0:
+        nsk = min(S, p0)
+        nskc = qpad + min(T, chunk_sinks)
+        sink_end = nskc if chunk_sinks > 0 else nsk
+    else:
+        nsk = sink_end = min(T, chunk_sinks)
     n_total = n_strip = 0
-    Tk = T + qoff
-    nsk = S if qoff > 0 else max(0, S - p0)
     for q0 in range(0, T, qpb):
-        q_last = min(q0 + qpb, T) - 1 + qoff
-        win_lo = max(0, q0 + qoff - W + 1) if W > 0 else 0
+        q_last = min(q0 + qpb, T) - 1 + qpad
+        win_lo = 0
+        if W > 0:
+            prior_lo = q0 + qoff - W + 1
+            win_lo = max(0, prior_lo) if prior_lo < qoff else q0 + qpad - W + 1
         first, last = win_lo // BN, q_last // BN
-        sink_keys = min(Tk, nsk) if W > 0 else 0
+        sink_keys = min(Tk, sink_end) if W > 0 else 0
         n_sink = min(first, (sink_keys + BN - 1) // BN)
         n_total += n_sink + (last - first + 1)
         n_strip += 1 if (n_sink == 1 and nsk <= PREFILL_SINK_STRIP) else 0
@@ -1080,8 +1091,9 @@ def bench_prefill(args):
 def bench_prefill_chunk(args):
     """A later chunk of a long prompt: B=1, T=8192 new tokens at p0=32768 attending over
     the full, wrapped ring a first chunk left (S=4, W=4092) and over themselves;
-    H_q=32, H_kv=8, d_h=128, bf16.  One step = the prior-key gather, the V transpose
-    and the attention (sk_prefill_attention with a prior)."""
+    H_q=32, H_kv=8, d_h=128, bf16.  One step = the gather of the prior's keys and
+    values and the attention (sk_prefill_attention with a prior), which reads the chunk's
+    own keys and values in place."""
     import torch
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
@@ -1109,7 +1121,7 @@ def bench_prefill_chunk(args):
     assert layer.error_bits() == 0
     _, bf16_peak, _, peak_kind = _peaks()
     alg_flops = T * (S + W) * Hq * B * 4 * D          # every query sees S + W keys here
-    tiles, nh, strips = _prefill_tiles(T, S, W, Hq // Hkv, qoff=qoff, strips=True)
+    tiles, nh, strips = _prefill_tiles(T, S, W, Hq // Hkv, p0=p0, qoff=qoff, strips=True)
     tile_keys = (tiles - strips) * 64 + strips * PREFILL_SINK_STRIP
     tile_flops = tile_keys * (Hq // nh) * B * 4 * 128 * D
     tf = tile_flops / (ms * 1e-3) / 1e12
@@ -1125,7 +1137,7 @@ def bench_prefill_chunk(args):
             "algorithmic_tflops": round(alg_flops / (ms * 1e-3) / 1e12, 1),
             "algorithmic_flops": alg_flops, "tile_flops": tile_flops,
             "peak_source": f"{peak_kind} bf16_tflops {bf16_peak}", "timing": rec,
-            "gpu_launches": args.steps * 3 * rec["replays"], "clocks": clk}
+            "gpu_launches": args.steps * 2 * rec["replays"], "clocks": clk}
 
 
 # ---------------------------------------------------------------------------

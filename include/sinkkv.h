@@ -363,9 +363,10 @@ SK_API sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const voi
 SK_API int64_t sk_prefill_prior_keys(int64_t p0, int32_t sinks, int32_t window);
 
 /* Workspace bytes sk_prefill_attention needs: with prior_keys > 0 (sk_prefill_prior_keys
- * of a call that passes a prior) a combined copy of the prior's and the chunk's keys and
- * values; without a prior, or with T = 0, no scratch is used and the answer is a token
- * 16 bytes.  0 for an unsupported shape. */
+ * of a call that passes a prior) a copy of the prior's keys and values, padded with zero
+ * rows to a multiple of 64 (the chunk's own keys and values are read in place); without
+ * a prior, or with T = 0, no scratch is used and the answer is a token 16 bytes.  0 for
+ * an unsupported shape. */
 SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim,
                                          int64_t prior_keys);
 
@@ -394,7 +395,7 @@ SK_API size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_
  *   prior ? sk_prefill_prior_keys(p0, sinks, window) : 0) bytes, 16-byte aligned, no
  *   initialisation needed.  err: device error word (SK_DEVERR_TIMEOUT if a bounded
  *   in-kernel wait gave up, SK_DEVERR_STATE as above), may be NULL.
- * Supported: head_dim 128, SK_BF16, T + prior keys <= 2^30.  T = 0 checks the other
+ * Supported: head_dim 128, SK_BF16, T + prior keys (padded to a multiple of 64) <= 2^30.  T = 0 checks the other
  * arguments, launches nothing and returns SK_OK; q_rot, k_rot, v, out and workspace
  * may then be NULL. */
 SK_API sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,

@@ -65,16 +65,22 @@ constexpr int SM_BYTES = SM_TMEM + 16;
 constexpr int SM_ALLOC = SM_BYTES + 1024;
 static_assert(SM_ALLOC >= SM_BYTES + 896, "no room to align the shared-memory base");
 
-// Queries and keys live in one index space: query t is key index t + qoff (the
-// chunk's own key), keys [0, qoff) come from a prior cache.  Key j is visible to
-// query t iff j <= t + qoff and (j < nsk or t + qoff - j < W).
+// Queries and keys live in one index space.  Without a prior cache it is the chunk's:
+// query t is key t, key j is visible to query t iff j <= t and (j < nsk or t - j < W).
+// With one, keys [0, qoff) are the prior's (gathered into the workspace, padded with
+// zero rows to qpad, a multiple of BN, so that no tile mixes prior and chunk keys) and
+// key qpad + t is the chunk's key t, read in place.  Prior key j (j < qoff) is visible
+// to query t iff j < nsk or t + qoff - j < W (all of them with W <= 0); padding is never
+// visible; chunk key qpad + k is visible iff k <= t and (qpad + k < nskc or t - k < W).
 struct PrefillParams {
     void* out;
     const float* sink_logits;  // [Hq] learned sinks or null
     uint32_t* err;
     int T, Hq, Hkv, B;
-    int Tk, qoff;              // keys in the key buffer; key index of query 0
-    int nsk, W;                // leading sink keys; window (<= 0: global)
+    int Tk, qoff, qpad;        // keys in the index space; prior keys; padded prior keys
+    int nsk, W;                // leading sink keys (prior keys with a prior); window (<= 0: global)
+    int nskc;                  // chunk sink keys end below this index (qpad + sinks - p0)
+    int sink_end;              // index past the last sink key (the plan's sink tiles)
     int nqb;           // query blocks of qpb queries
     int nh, qpb;       // q heads packed per CTA (one GQA group's), queries per block: nh * qpb = BM
     float scale_log2;  // log2(e) / sqrt(head_dim)
@@ -88,11 +94,15 @@ struct TilePlan {
 
 __device__ __forceinline__ TilePlan plan_tiles(const PrefillParams& p, int q0) {
     TilePlan tp;
-    const int q_last = min(q0 + p.qpb, p.T) - 1 + p.qoff;  // in key index space
-    const int win_lo = p.W > 0 ? max(0, q0 + p.qoff - p.W + 1) : 0;
+    const int q_last = min(q0 + p.qpb, p.T) - 1 + p.qpad;  // the last query's own key
+    int win_lo = 0;                                          // the first query's oldest key
+    if (p.W > 0) {
+        const int prior_lo = q0 + p.qoff - p.W + 1;          // as a prior index
+        win_lo = prior_lo < p.qoff ? max(0, prior_lo) : q0 + p.qpad - p.W + 1;
+    }
     tp.first_win = win_lo / BN;
     const int last = q_last / BN;
-    const int sink_keys = p.W > 0 ? min(p.Tk, p.nsk) : 0;
+    const int sink_keys = p.W > 0 ? min(p.Tk, p.sink_end) : 0;
     tp.n_sink = min(tp.first_win, (sink_keys + BN - 1) / BN);
     tp.n = tp.n_sink + (last - tp.first_win + 1);
     return tp;
@@ -104,11 +114,31 @@ __device__ __forceinline__ int key_tile(const TilePlan& tp, int i) {
 
 // Every (query, key) of the tile visible to every query of the block?
 __device__ __forceinline__ bool tile_full(const PrefillParams& p, int q0, int k0) {
-    const int q_last = min(q0 + p.qpb, p.T) - 1 + p.qoff;
     if (q0 + p.qpb > p.T) return false;
-    if (k0 + BN - 1 > q0 + p.qoff || k0 + BN > p.Tk) return false;
+    const int t_last = q0 + p.qpb - 1;
+    if (k0 < p.qpad) {  // prior keys (and padding)
+        if (k0 + BN > p.qoff) return false;
+        if (p.W <= 0) return true;
+        return t_last + p.qoff - k0 < p.W || k0 + BN - 1 < p.nsk;
+    }
+    if (k0 + BN - 1 > q0 + p.qpad || k0 + BN > p.Tk) return false;
     if (p.W <= 0) return true;
-    return q_last - k0 < p.W || k0 + BN - 1 < p.nsk;
+    return t_last + p.qpad - k0 < p.W || k0 + BN - 1 < p.nskc;
+}
+
+// Visibility bounds of a boundary tile at key k0 for a query whose own key is qpad + tq:
+// tile column j is visible iff j <= jmax and (j >= jwin or j < jsink).
+__device__ __forceinline__ void tile_bounds(const PrefillParams& p, int tq, int k0, int& jmax, int& jwin,
+                                            int& jsink) {
+    if (k0 < p.qpad) {
+        jmax = p.qoff - 1 - k0;  // padding never
+        jwin = p.W > 0 ? tq + p.qoff - p.W + 1 - k0 : -(1 << 30);
+        jsink = p.W > 0 ? p.nsk - k0 : -(1 << 30);
+    } else {
+        jmax = tq + p.qpad - k0;
+        jwin = p.W > 0 ? tq + p.qpad - p.W + 1 - k0 : -(1 << 30);
+        jsink = p.W > 0 ? p.nskc - k0 : -(1 << 30);
+    }
 }
 
 // max of three floats in one instruction
@@ -126,7 +156,8 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, boo
 
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKc,
+                        const __grid_constant__ CUtensorMap tmVc, PrefillParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
@@ -201,8 +232,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int k0 = key_tile(tp, i) * BN;
                 uint8_t* st = smem + SM_K + s * K_STAGE;
                 mbar_arrive_expect_tx(&k_full[s], K_STAGE);
-                tma_load_4d(st, &tmK, 0, g, k0, b, &k_full[s]);
-                tma_load_4d(st + BN * 128, &tmK, 64, g, k0, b, &k_full[s]);
+                // prior keys from the workspace, chunk keys in place
+                const CUtensorMap* m = k0 < p.qpad ? &tmK : &tmKc;
+                const int kr = k0 < p.qpad ? k0 : k0 - p.qpad;
+                tma_load_4d(st, m, 0, g, kr, b, &k_full[s]);
+                tma_load_4d(st + BN * 128, m, 64, g, kr, b, &k_full[s]);
             }
         }
     } else if (warp == 6) {
@@ -214,8 +248,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int k0 = key_tile(tp, i) * BN;
                 uint8_t* st = smem + SM_V + s * V_STAGE;
                 mbar_arrive_expect_tx(&v_full[s], V_STAGE);
-                tma_load_4d(st, &tmV, 0, g, k0, b, &v_full[s]);
-                tma_load_4d(st + BN * 128, &tmV, 64, g, k0, b, &v_full[s]);
+                const CUtensorMap* m = k0 < p.qpad ? &tmV : &tmVc;
+                const int kr = k0 < p.qpad ? k0 : k0 - p.qpad;
+                tma_load_4d(st, m, 0, g, kr, b, &v_full[s]);
+                tma_load_4d(st + BN * 128, m, 64, g, kr, b, &v_full[s]);
             }
         }
     } else if (warp == 4) {
@@ -288,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_ld_wait();
             float sc[kSinkStrip];
 #pragma unroll
-            for (int j = 0; j < kSinkStrip; ++j) sc[j] = j < p.nsk ? __uint_as_float(raw[j]) : -INFINITY;
+            for (int j = 0; j < kSinkStrip; ++j) sc[j] = j < p.nsk ? __uint_as_float(raw[j]) : -INFINITY;  // nsk <= qoff
             float mx = fmax3(sc[0], sc[1], sc[2]);
 #pragma unroll
             for (int j = 3; j < kSinkStrip; j += 2) mx = fmax3(mx, sc[j], sc[j + 1 < kSinkStrip ? j + 1 : j]);
@@ -327,10 +363,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < 64; ++j) sc[j] = __uint_as_float(raw[j]);
             if (!full) {
                 // key k0 + j visible iff j <= jmax and (j >= jwin or j < jsink): branch-free
-                const int tq = min(t, p.T - 1) + p.qoff;  // the query's own key index
-                const int jmax = tq - k0;
-                const int jwin = p.W > 0 ? tq - p.W + 1 - k0 : -(1 << 30);
-                const int jsink = p.W > 0 ? p.nsk - k0 : -(1 << 30);
+                int jmax, jwin, jsink;
+                tile_bounds(p, min(t, p.T - 1), k0, jmax, jwin, jsink);
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
                     const bool vis = (j <= jmax) && (j >= jwin || j < jsink);
@@ -444,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // The keys a chunk takes from a prior cache, in order: the first s0 positions (sink
 // slots, or the prefix of a global layer), then the last cr positions before p0 (the
 // newest cr entries of the ring in chronological order, or the global rows at those
-// positions).  Key index j < s0 + cr of the combined key buffer is prior row j.  A
+// positions).  Key index j < s0 + cr of the gathered prior keys is prior row j.  A
 // ring at position p0 holds ring_count = min(W, p0 - s0) entries; the chunk needs
 // the newest cr <= ring_count of them.
 struct PriorView {
@@ -470,40 +504,38 @@ __device__ __forceinline__ int64_t prior_slot(const PriorView& pv, int b, int j)
     return pv.S + (cnt == pv.W ? (hd + ci) % pv.W : ci);
 }
 
-// Combined keys and values kc, vc [B][Tk][Hkv][HD]: prior rows, then the chunk's k, v
-// [B][T][Hkv][HD].  One thread per 16 bytes of a K row and the same 16 bytes of its V
-// row.  The thread of (b, j = 0, g = 0, c = 0) checks that the prior's state matches the
-// chunk's start (pos = p0; a ring holds ring_count recent entries).
-__global__ void __launch_bounds__(256) gather_kv_kernel(PriorView pv, const __nv_bfloat16* __restrict__ k,
-                                                        const __nv_bfloat16* __restrict__ v,
-                                                        __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc,
-                                                        int B, int T, int Tk, int Hkv, uint32_t* err) {
+// The prior's keys and values kc, vc [B][qpad][Hkv][HD]: prior rows j < qoff in the
+// order of the key index space (sinks, then recent positions oldest first), then zero
+// rows up to qpad (never visible; zero so that no stale value meets a zero weight).  The
+// chunk's own keys are not copied: the attention kernel reads them in place.  One thread
+// per 16 bytes of a K row and the same 16 bytes of its V row.  The thread of (b, j = 0,
+// g = 0, c = 0) checks that the prior's state matches the chunk's start (pos = p0; a ring
+// holds ring_count recent entries).
+__global__ void __launch_bounds__(256) gather_prior_kernel(PriorView pv, __nv_bfloat16* __restrict__ kc,
+                                                           __nv_bfloat16* __restrict__ vc, int B, int qpad, int Hkv,
+                                                           uint32_t* err) {
     constexpr int CH = HD / 8;  // 16-byte chunks per row
     const int qoff = pv.s0 + pv.cr;
-    const int64_t total = int64_t(B) * Tk * Hkv * CH;
+    const int64_t total = int64_t(B) * qpad * Hkv * CH;
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * blockDim.x) {
         const int c = int(i % CH);
         const int g = int((i / CH) % Hkv);
         const int64_t bj = i / (int64_t(CH) * Hkv);
-        const int j = int(bj % Tk), b = int(bj / Tk);
-        const __nv_bfloat16 *ks, *vs;
+        const int j = int(bj % qpad), b = int(bj / qpad);
+        const int64_t dst = (bj * Hkv + g) * HD;
         if (j < qoff) {
             const int64_t row = ((int64_t(b) * Hkv + g) * pv.cap + prior_slot(pv, b, j)) * HD;
-            ks = pv.k + row;
-            vs = pv.v + row;
             if (j == 0 && g == 0 && c == 0) {
                 const bool ok = pv.pos[b] == pv.p0 && (pv.kind == SK_LAYER_GLOBAL || pv.count[b] == pv.ring_count);
                 if (!ok) set_error(err, SK_DEVERR_STATE);
             }
+            reinterpret_cast<uint4*>(kc + dst)[c] = reinterpret_cast<const uint4*>(pv.k + row)[c];
+            reinterpret_cast<uint4*>(vc + dst)[c] = reinterpret_cast<const uint4*>(pv.v + row)[c];
         } else {
-            const int64_t row = ((int64_t(b) * T + (j - qoff)) * Hkv + g) * HD;
-            ks = k + row;
-            vs = v + row;
+            reinterpret_cast<uint4*>(kc + dst)[c] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(vc + dst)[c] = make_uint4(0, 0, 0, 0);
         }
-        const int64_t dst = (bj * Hkv + g) * HD;
-        reinterpret_cast<uint4*>(kc + dst)[c] = reinterpret_cast<const uint4*>(ks)[c];
-        reinterpret_cast<uint4*>(vc + dst)[c] = reinterpret_cast<const uint4*>(vs)[c];
     }
 }
 
@@ -562,14 +594,17 @@ extern "C" int64_t sk_prefill_prior_keys(int64_t p0, int32_t sinks, int32_t wind
     return s0 + cr;
 }
 
+// Prior keys padded to a whole number of key tiles.
+static int64_t padded_prior(int64_t prior_keys) { return (prior_keys + BN - 1) / BN * BN; }
+
 extern "C" size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n_kv_heads, int32_t head_dim,
                                              int64_t prior_keys) {
     if (batch < 1 || T < 0 || n_kv_heads < 1 || head_dim != HD || prior_keys < 0) return 0;
-    const int64_t Tk = int64_t(T) + prior_keys;
-    if (Tk > (int64_t(1) << 30)) return 0;
+    const int64_t qpad = padded_prior(prior_keys);
+    if (int64_t(T) + qpad > (int64_t(1) << 30)) return 0;
     // no scratch is used: a token size keeps 0 for "unsupported"
     if (prior_keys == 0 || T == 0) return 16;
-    return 2 * size_t(batch) * Tk * n_kv_heads * HD * sizeof(__nv_bfloat16);  // combined keys and values
+    return 2 * size_t(batch) * qpad * n_kv_heads * HD * sizeof(__nv_bfloat16);  // the prior's keys and values
 }
 
 extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
@@ -616,21 +651,16 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
                        int(ring_count)};
     }
     if (T == 0) return SK_OK;
-    const int64_t Tk64 = int64_t(T) + qoff;
+    const int64_t qpad = padded_prior(qoff);
+    const int64_t Tk64 = int64_t(T) + qpad;
     SK_RET_IF(Tk64 > (int64_t(1) << 30), SK_ERR_UNSUPPORTED);
     const size_t need = sk_prefill_workspace_bytes(batch, T, n_kv_heads, head_dim, qoff);
     SK_RET_IF(need == 0 || ws_bytes < need, SK_ERR_ARG);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int Tk = int(Tk64);
-    // keys and values: the chunk's own, or (with a prior) the combined buffers
-    const void* keys = k_rot;
-    const void* vals = v;
+    // the prior's keys and values (gathered, padded to qpad rows) in the workspace
     __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(workspace);
-    __nv_bfloat16* vc = kc + size_t(batch) * Tk * n_kv_heads * HD;
-    if (qoff > 0) {
-        keys = kc;
-        vals = vc;
-    }
+    __nv_bfloat16* vc = kc + size_t(batch) * qpad * n_kv_heads * HD;
 
     // pack the q heads of a GQA group into one CTA (a power of two dividing n_rep, at
     // most 8): the K / V tiles are then loaded once for all of them
@@ -639,7 +669,7 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     while (nh < 8 && nrep % (2 * nh) == 0) nh *= 2;
     const int qpb = BM / nh;
 
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mkc, mvc;
     {
         const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_q_heads), cuuint64_t(T), cuuint64_t(batch)};
         const cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(n_q_heads) * HD * 2,
@@ -647,22 +677,27 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
         const cuuint32_t box[4] = {64, 1, cuuint32_t(qpb), 1};
         SK_RET_IF(!make_map(&mq, q_rot, 4, dims, strides, box), SK_ERR_CUDA);
     }
-    {
-        const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_kv_heads), cuuint64_t(Tk), cuuint64_t(batch)};
+    const cuuint32_t kv_box[4] = {64, 1, BN, 1};
+    {  // the chunk's keys and values, read in place
+        const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_kv_heads), cuuint64_t(T), cuuint64_t(batch)};
         const cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(n_kv_heads) * HD * 2,
-                                       cuuint64_t(Tk) * n_kv_heads * HD * 2};
-        const cuuint32_t box[4] = {64, 1, BN, 1};
-        SK_RET_IF(!make_map(&mk, keys, 4, dims, strides, box), SK_ERR_CUDA);
-        SK_RET_IF(!make_map(&mv, vals, 4, dims, strides, box), SK_ERR_CUDA);
+                                       cuuint64_t(T) * n_kv_heads * HD * 2};
+        SK_RET_IF(!make_map(&mkc, k_rot, 4, dims, strides, kv_box), SK_ERR_CUDA);
+        SK_RET_IF(!make_map(&mvc, v, 4, dims, strides, kv_box), SK_ERR_CUDA);
     }
-
-    if (qoff > 0) {
-        const int64_t threads = int64_t(batch) * Tk * n_kv_heads * (HD / 8);
+    if (qoff > 0) {  // the prior's, gathered
+        const cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(n_kv_heads), cuuint64_t(qpad), cuuint64_t(batch)};
+        const cuuint64_t strides[3] = {cuuint64_t(HD) * 2, cuuint64_t(n_kv_heads) * HD * 2,
+                                       cuuint64_t(qpad) * n_kv_heads * HD * 2};
+        SK_RET_IF(!make_map(&mk, kc, 4, dims, strides, kv_box), SK_ERR_CUDA);
+        SK_RET_IF(!make_map(&mv, vc, 4, dims, strides, kv_box), SK_ERR_CUDA);
+        const int64_t threads = int64_t(batch) * qpad * n_kv_heads * (HD / 8);
         const int64_t blocks = std::min<int64_t>((threads + 255) / 256, int64_t(device_sm_count()) * 16);
-        gather_kv_kernel<<<unsigned(blocks), 256, 0, st>>>(pv, static_cast<const __nv_bfloat16*>(k_rot),
-                                                          static_cast<const __nv_bfloat16*>(v), kc, vc, batch, T,
-                                                          Tk, n_kv_heads, err);
+        gather_prior_kernel<<<unsigned(blocks), 256, 0, st>>>(pv, kc, vc, batch, int(qpad), n_kv_heads, err);
         SK_CUDA_RET(cudaGetLastError());
+    } else {
+        mk = mkc;  // no prior: every key tile is the chunk's
+        mv = mvc;
     }
 
     static PerDevice<cudaError_t> attr;
@@ -675,11 +710,19 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     p.T = T;
     p.Tk = Tk;
     p.qoff = int(qoff);
-    // sinks in key index space: without a prior, chunk key k has position p0 + k; with
-    // one, the combined buffer starts with the positions 0 .. s0-1 (all of the sinks
-    // when the ring has dropped keys, else positions equal indices)
-    p.nsk = window > 0 ? int(std::min<int64_t>(Tk, std::max<int64_t>(0, qoff > 0 ? sinks : int64_t(sinks) - p0)))
-                       : 0;
+    p.qpad = int(qpad);
+    // Sinks in the key index space.  Without a prior, chunk key k has position p0 + k:
+    // keys below sinks - p0 are sinks.  With one, prior keys 0 .. min(sinks, p0) - 1 are
+    // the positions below p0 that are sinks, and chunk keys (at qpad + k) whose position
+    // p0 + k is below sinks are sinks too.
+    const int64_t chunk_sinks = std::max<int64_t>(0, int64_t(sinks) - p0);
+    if (window > 0) {
+        p.nsk = int(qoff > 0 ? std::min<int64_t>(sinks, p0) : std::min<int64_t>(T, chunk_sinks));
+        p.nskc = int(qpad + std::min<int64_t>(T, chunk_sinks));
+        p.sink_end = int(chunk_sinks > 0 ? p.nskc : p.nsk);
+    } else {
+        p.nsk = p.nskc = p.sink_end = 0;
+    }
     p.W = window;
     p.Hq = n_q_heads;
     p.Hkv = n_kv_heads;
@@ -689,7 +732,7 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     p.nqb = (T + qpb - 1) / qpb;
     p.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
     const int64_t grid = int64_t(p.nqb) * (n_q_heads / nh) * batch;
-    prefill_attn_kernel<<<unsigned(grid), kThreads, SM_ALLOC, st>>>(mq, mk, mv, p);
+    prefill_attn_kernel<<<unsigned(grid), kThreads, SM_ALLOC, st>>>(mq, mk, mv, mkc, mvc, p);
     SK_CUDA_RET(cudaGetLastError());
     return SK_OK;
 }

@@ -121,7 +121,10 @@ def test_prefill_workspace_and_prior_arguments_checked_on_host(lib):
     import sink_kv_attention_gb300 as sk
     # no scratch without a prior (a token 16 bytes); with one, the combined keys and values
     assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 0) == 16
-    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 30) == 2 * (2 * 130 * 8 * 128 * 2)
+    # the prior's 30 keys, padded to 64 rows, of K and of V (the chunk is read in place)
+    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 30) == 2 * (2 * 64 * 8 * 128 * 2)
+    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 64) == 2 * (2 * 64 * 8 * 128 * 2)
+    assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, 65) == 2 * (2 * 128 * 8 * 128 * 2)
     assert lib.sk_prefill_workspace_bytes(2, 100, 8, 128, -1) == 0
     assert lib.sk_prefill_workspace_bytes(2, 100, 8, 64, 0) == 0
     assert lib.sk_prefill_workspace_bytes(2, 0, 8, 128, 30) == 16   # an empty chunk

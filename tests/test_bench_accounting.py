@@ -11,25 +11,32 @@ from oracle.sinkkv_oracle import mask_allows
 
 def _brute_tiles(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64):
     """Tiles with a visible pair: rows are (head, query) of a block of BM // nh queries;
-    the key index space is [prior keys][chunk keys] (positions as the prefill defines)."""
+    the key index space is [prior keys, padded to a multiple of BN][chunk keys]
+    (positions as the prefill defines; padding has none)."""
     nh = bench._prefill_heads_per_cta(n_rep)
     qpb = BM // nh
-    Tk = T + qoff
-    # absolute positions of the key buffer: sinks, then the recent keys before p0, then the chunk
-    if qoff:
-        s0 = min(S, p0)
-        pos = list(range(s0)) + list(range(p0 - (qoff - s0), p0)) + list(range(p0, p0 + T))
-    else:
-        pos = list(range(p0, p0 + T))
+    pos = _key_positions(T, S, p0, qoff, BN)
+    Tk = len(pos)
     win = W if W > 0 else None
     count = 0
     for q0 in range(0, T, qpb):
         queries = range(q0, min(q0 + qpb, T))
         for k0 in range(0, Tk, BN):
             keys = range(k0, min(k0 + BN, Tk))
-            if any(mask_allows(p0 + t, pos[j], S, win) for t in queries for j in keys):
+            if any(pos[j] is not None and mask_allows(p0 + t, pos[j], S, win) for t in queries for j in keys):
                 count += 1
     return count, nh
+
+
+def _key_positions(T, S, p0, qoff, BN):
+    """Absolute position of every key index: the prior's sinks, then its recent keys
+    before p0, then padding (None) up to a multiple of BN, then the chunk."""
+    if not qoff:
+        return list(range(p0, p0 + T))
+    s0 = min(S, p0)
+    qpad = -(-qoff // BN) * BN
+    return (list(range(s0)) + list(range(p0 - (qoff - s0), p0)) + [None] * (qpad - qoff)
+            + list(range(p0, p0 + T)))
 
 
 @pytest.mark.parametrize("T,S,W,n_rep,p0", [
@@ -42,7 +49,7 @@ def test_prefill_tiles_chunk_alone(T, S, W, n_rep, p0):
 
 @pytest.mark.parametrize("T,S,W,n_rep,p0", [
     (300, 4, 100, 4, 250), (300, 4, 100, 4, 50), (129, 0, 61, 1, 1000), (260, 3, 300, 8, 700),
-    (200, 4, 0, 4, 300),
+    (200, 4, 0, 4, 300), (400, 4, 100, 4, 2), (300, 16, 40, 4, 9),
 ])
 def test_prefill_tiles_chunk_over_prior(T, S, W, n_rep, p0):
     s0 = min(S, p0) if W > 0 else 0
@@ -55,27 +62,27 @@ def _brute_strips(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64, strip=16):
     one strip: the blocks whose tile 0 the kernel visits as a 16-key strip."""
     nh = bench._prefill_heads_per_cta(n_rep)
     qpb = BM // nh
-    Tk = T + qoff
-    if qoff:
-        s0 = min(S, p0)
-        pos = list(range(s0)) + list(range(p0 - (qoff - s0), p0)) + list(range(p0, p0 + T))
-        nsk = S
-    else:
-        pos = list(range(p0, p0 + T))
-        nsk = max(0, S - p0)
+    pos = _key_positions(T, S, p0, qoff, BN)
+    Tk = len(pos)
     win = W if W > 0 else None
     count = 0
     for q0 in range(0, T, qpb):
-        vis = [j for t in range(q0, min(q0 + qpb, T)) for j in range(min(BN, Tk))
-               if mask_allows(p0 + t, pos[j], S, win)]
-        if vis and W > 0 and max(vis) < nsk and nsk <= strip:
+        pure = []   # tiles below the window: visible keys only as sinks
+        for k0 in range(0, Tk, BN):
+            pairs = [(t, j) for t in range(q0, min(q0 + qpb, T)) for j in range(k0, min(k0 + BN, Tk))
+                     if pos[j] is not None and mask_allows(p0 + t, pos[j], S, win)]
+            if pairs and not any(mask_allows(p0 + t, pos[j], 0, win) for t, j in pairs):
+                pure.append((k0, max(j for _, j in pairs)))
+        # tile 0 is the one tile of sinks alone, and its sinks fit in a strip
+        if W > 0 and len(pure) == 1 and pure[0][0] == 0 and pure[0][1] < strip:
             count += 1
     return count
 
 
-@pytest.mark.parametrize("T,S,W,n_rep,p0", [
-    (300, 4, 100, 4, 0), (300, 0, 100, 4, 0), (300, 4, 0, 4, 0), (513, 3, 130, 1, 1),
-    (1000, 4, 300, 2, 0), (700, 20, 100, 4, 0),
+@pytest.mark.parametrize("T,S,W,n_rep,p0,qoff", [
+    (300, 4, 100, 4, 0, 0), (300, 0, 100, 4, 0, 0), (300, 4, 0, 4, 0, 0), (513, 3, 130, 1, 1, 0),
+    (1000, 4, 300, 2, 0, 0), (700, 20, 100, 4, 0, 0), (300, 4, 100, 4, 250, 103), (400, 4, 100, 4, 2, 2),
 ])
-def test_prefill_sink_strips(T, S, W, n_rep, p0):
-    assert bench._prefill_tiles(T, S, W, n_rep, p0=p0, strips=True)[2] == _brute_strips(T, S, W, n_rep, p0=p0)
+def test_prefill_sink_strips(T, S, W, n_rep, p0, qoff):
+    assert (bench._prefill_tiles(T, S, W, n_rep, p0=p0, qoff=qoff, strips=True)[2]
+            == _brute_strips(T, S, W, n_rep, p0=p0, qoff=qoff))
