@@ -49,10 +49,10 @@ NCU_TRAFFIC = {
         sources={"decode.cu": "55c52f9e7df83499bc4fbcc79d689e224d9861abf0c768cfc5f9b179acc35f02",
                  "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}),
     "prefill_attn_t32768": dict(
-        bytes=637162752, scale=1,
+        bytes=634040064, scale=1,
         capture="ncu --set full -k regex:prefill_attn -s 2 -c 1, python bench.py --workload prefill "
                 "--steps 3 --warmup 2",
-        sources={"prefill.cu": "deea7740a8510f6b30ceb2719b3cfe931910b7cd5577ba59fde1b806fbf8f604",
+        sources={"prefill.cu": "62d9edd81ca0d37ead7e9a63e3364208ac8f18f651fbe2abb81122236ca872f2",
                  "tcgen05.cuh": "351b9597267c8e6efeb86d6fc37090095dc2b99a351b47884061cba635ae854d"}),
     "rerotate_bf16_48l": dict(
         bytes=2358400000, scale=12,
