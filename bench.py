@@ -42,6 +42,12 @@ NCU_TRAFFIC = {
                 "--steps 5 --warmup 3 (split kernel only)",
         sources={"decode.cu": "55c52f9e7df83499bc4fbcc79d689e224d9861abf0c768cfc5f9b179acc35f02",
                  "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}),
+    "decode_paged_window_b32_bs16": dict(
+        bytes=540817152, scale=1,
+        capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload paged "
+                "--steps 5 --warmup 3 (split kernel only)",
+        sources={"decode.cu": "55c52f9e7df83499bc4fbcc79d689e224d9861abf0c768cfc5f9b179acc35f02",
+                 "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}),
     "decode_window_b32_int8": dict(
         bytes=410712576, scale=1,
         capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload window_i8 "
@@ -759,7 +765,8 @@ def bench_paged(args):
     hbm, _, _, peak_kind = _peaks()
     value = kv_bytes / (ms * 1e-3) / 1e9
     roof = _launch_roofline(lambda i: sk.paged_decode_attention(layer, qs[i, :, 0], out=out, workspace=ws,
-                                                                sink_logits=zl), steps, alg_decode, None,
+                                                                sink_logits=zl), steps, alg_decode,
+                            "decode_paged_window_b32_bs16",
                             "paged decode attention (split-K + combine); its launches back to back in one graph",
                             "K+V of 4096 visible rows x 32 sequences x 8 kv heads + q + out")
     return {"metric": METRIC + " (paged cache)", "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
