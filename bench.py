@@ -512,14 +512,15 @@ def _state_saver(layers):
     return reset
 
 
-def _launch_roofline(fn, n, alg_bytes, name, kernel, unit_note, target_ms=TARGET_MS / 2):
+def _launch_roofline(fn, n, alg_bytes, name, kernel, unit_note, target_ms=TARGET_MS / 2, reset=None):
     """Roofline of an HBM-bound kernel: fn(i) for i < n (launches of that kernel alone,
     back to back in one graph, programmatic dependent launch between them, as in a
     decode loop over layers) replayed for target_ms; achieved = algorithmic bytes per
-    launch / median time per launch."""
+    launch / median time per launch.  reset() (outside the timed replays) puts back
+    state the launches advance."""
     hbm, _, _, peak_kind = _peaks()
     g = _capture(fn, 0, n)
-    per, total, R = _replays(g, n, target_ms)
+    per, total, R = _replays(g, n, target_ms, reset=reset)
     ms = statistics.median(per)
     achieved = alg_bytes / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
@@ -1153,7 +1154,8 @@ def bench_prefill_chunk(args):
 
 def bench_tiny(args):
     """The tiny case: 1 sequence, H_q=8, H_kv=4, d_h=r=64, theta=1e4, fp32, C=6 with S=2
-    sinks, 10 tokens decoded one at a time (RoPE + append + attention per token).  A
+    sinks, 10 tokens decoded one at a time (RoPE + append + attention per token, as the
+    decode step sk_decode_step; sk_kv_append + sk_decode_attention timed beside it).  A
     replay of the captured graph decodes the 10 tokens; the ring is emptied after it."""
     import torch
     import sink_kv_attention_gb300 as sk
@@ -1170,10 +1172,14 @@ def bench_tiny(args):
     ks = [k_all[:, t:t + 1].contiguous().cuda() for t in range(T)]
     vs = [v_all[:, t:t + 1].contiguous().cuda() for t in range(T)]
     out = torch.empty(1, Hq, D, device="cuda")
-    ws = torch.empty(sk.decode_workspace_bytes(layer, Hq), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(sk.decode_workspace_bytes(layer, Hq), sk.decode_step_workspace_bytes(layer, Hq)),
+                     dtype=torch.uint8, device="cuda")
     empty = _state_saver([layer])
 
-    def step(t):
+    def step(t):  # q, k, v are read only
+        sk.decode_step(tbl, layer, qs[t % T][:, 0], ks[t % T][:, 0], vs[t % T][:, 0], out=out, workspace=ws)
+
+    def step_two_calls(t):  # rotates q and k in place
         sk.kv_append(tbl, layer, qs[t % T], ks[t % T], vs[t % T])
         sk.decode_attention(layer, qs[t % T][:, 0], out=out, workspace=ws)
 
@@ -1189,22 +1195,31 @@ def bench_tiny(args):
     clocks.stop()
     assert layer.error_bits() == 0
     us = statistics.median(per) * 1e3
+    g2 = _capture(step_two_calls, 0, T)
+    per2, _, _ = _replays(g2, T, TARGET_MS / 6, reset=empty)
+    assert layer.error_bits() == 0
     return {"metric": "tiny case: microseconds per decode step (RoPE + append + attention of one token)",
             "value": round(us, 3), "unit": "us/step", "higher_is_better": False, "dtype": "f32",
             "config": {"workload": "tiny: 1 sequence, H_q=8, H_kv=4, d_h=r=64, theta=1e4, fp32, C=6, S=2, "
                                    "10 tokens one at a time"},
             "roofline": {"bound": "latency", "achieved": round(us, 3), "unit": "us/step", "peak": None,
-                         "frac": None, "kernel": "append + split + combine per token (3 launches)",
+                         "frac": None, "kernel": "split (with the token's RoPE + append) + combine per token "
+                                                 "(2 launches)",
                          "note": "a parity case: 3 KB of cache, far from any throughput roofline"},
             "timing": {"replays": R, "steps_per_replay": T, "timed_ms": round(total, 2)},
-            "gpu_launches": 3 * T * R, "clocks": clocks.summary()}
+            "two_calls": {"us_per_step": round(statistics.median(per2) * 1e3, 3),
+                          "calls": "sk_kv_append + sk_decode_attention, three launches per token"},
+            "gpu_launches": 2 * T * R, "clocks": clocks.summary()}
 
 
 def bench_window_b1(args):
     """Single-stream decode: one sequence through 32 windowed layers (each H_q=32,
     H_kv=8, d_h=r=128, S=4, W=4092, ring full at a random head), one token per step:
-    RoPE + append + split-K attention over 4096 visible keys on every layer.  The
-    32 layers' caches (537 MB) exceed L2, as a model's layers do."""
+    RoPE + append + split-K attention over 4096 visible keys on every layer, as the
+    decode step (sk_decode_step: the append folded into the attention's two kernels).
+    The same steps as sk_kv_append + sk_decode_attention (three launches per layer) are
+    timed beside it on the same state.  The 32 layers' caches (537 MB) exceed L2, as a
+    model's layers do."""
     import torch
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
@@ -1228,9 +1243,15 @@ def bench_window_b1(args):
     ks = synth.normal((n, nl, 1, 1, Hkv, D), 45, torch.bfloat16, device="cuda")
     vs = synth.normal((n, nl, 1, 1, Hkv, D), 46, torch.bfloat16, device="cuda")
     out = torch.empty(1, Hq, D, dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(sk.decode_workspace_bytes(layers[0], Hq), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(sk.decode_workspace_bytes(layers[0], Hq), sk.decode_step_workspace_bytes(layers[0], Hq)),
+                     dtype=torch.uint8, device="cuda")
+    reset = _state_saver(layers)
 
-    def step(i):
+    def step(i):  # q, k, v are read only
+        for j, L in enumerate(layers):
+            sk.decode_step(tbl, L, qs[i, j, :, 0], ks[i, j, :, 0], vs[i, j, :, 0], out=out, workspace=ws)
+
+    def step_two_calls(i):  # rotates q and k in place
         for j, L in enumerate(layers):
             sk.kv_append(tbl, L, qs[i, j], ks[i, j], vs[i, j])
             sk.decode_attention(L, qs[i, j, :, 0], out=out, workspace=ws)
@@ -1238,24 +1259,32 @@ def bench_window_b1(args):
     for i in range(warm):
         step(i)
     torch.cuda.synchronize()
-    ms, clk, rec = _timed(lambda i: step(warm + i), steps, 0, reset=_state_saver(layers))
+    ms, clk, rec = _timed(lambda i: step(warm + i), steps, 0, reset=reset)
     assert all(L.error_bits() == 0 for L in layers)
     kv_layer = Hkv * (S + W) * D * 2 * 2
     hbm, _, _, peak_kind = _peaks()
     value = nl * kv_layer / (ms * 1e-3) / 1e9
-    roof = _launch_roofline(lambda i: sk.decode_attention(layers[i % nl], qs[0, i % nl, :, 0], out=out,
-                                                          workspace=ws), nl,
-                            kv_layer + 2 * Hq * D * 2, None,
-                            "decode attention at batch 1 (split-K + combine); the 32 layers' launches back to "
-                            "back in one graph", "K+V of 4096 visible rows x 8 kv heads + q + out, per layer")
+    tok_bytes = 4 * Hkv * D * 2  # the token's k and v read, then written to the cache
+    roof = _launch_roofline(lambda i: sk.decode_step(tbl, layers[i % nl], qs[0, i % nl, :, 0], ks[0, i % nl, :, 0],
+                                                     vs[0, i % nl, :, 0], out=out, workspace=ws), nl,
+                            kv_layer + 2 * Hq * D * 2 + tok_bytes, None,
+                            "decode step at batch 1 (split-K with the token's RoPE + append, combine); the 32 "
+                            "layers' launches back to back in one graph",
+                            "K+V of 4096 visible rows x 8 kv heads + q + out + the token's k, v in and out, "
+                            "per layer", reset=reset)
+    reset()
+    ms_two, _, rec_two = _timed(lambda i: step_two_calls(warm + i), steps, 0, reset=reset)
+    assert all(L.error_bits() == 0 for L in layers)
     return {"metric": "single-stream decode over 32 windowed layers: us per token, tokens/s, KV-read GB/s",
             "value": round(ms * 1e3, 2), "unit": "us/token", "higher_is_better": False, "dtype": "bf16",
             "config": {"workload": "batch 1 through 32 windowed layers (H_q=32, H_kv=8, d_h=r=128, S=4, W=4092, "
-                                   "rings full): RoPE + append + attention per layer",
+                                   "rings full): RoPE + append + attention per layer (sk_decode_step)",
                        "l2": f"inputs larger than L2 (KV {nl * kv_layer / 1e6:.0f} MB per step)"},
             "tokens_per_s": round(1.0 / (ms * 1e-3), 1), "gbs": round(value, 2),
             "frac_of_hbm_peak": round(value / hbm, 4), "us_per_layer": round(ms * 1e3 / nl, 3),
-            "roofline": roof, "timing": rec, "gpu_launches": 3 * nl * steps * rec["replays"], "clocks": clk}
+            "two_calls": {"us_per_token": round(ms_two * 1e3, 2), "calls": "sk_kv_append + sk_decode_attention, "
+                          "three launches per layer, same state", "timing": rec_two},
+            "roofline": roof, "timing": rec, "gpu_launches": 2 * nl * steps * rec["replays"], "clocks": clk}
 
 
 # ---------------------------------------------------------------------------

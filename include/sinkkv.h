@@ -354,6 +354,39 @@ SK_API sk_status sk_decode_attention_noalloc(const sk_kv_layer* layer, const voi
                                              int32_t n_q_heads, int32_t io_dtype,
                                              const float* sink_logits, void* out, void* stream);
 
+/* ---- Decode step: RoPE + append + attention in two kernels ------------------------- */
+
+/* Workspace bytes sk_decode_step needs for `layer` and n_q_heads (0: unsupported). */
+SK_API size_t sk_decode_step_workspace_bytes(const sk_kv_layer* layer, int32_t n_q_heads);
+
+/* One decode token per sequence: sk_kv_append with T = 1 followed by
+ * sk_decode_attention, with the append folded into the attention's two kernels, so a
+ * step is one split kernel and one combine instead of three launches ([MIXED] 4.3-4.4:
+ * at decode the step is bound by the KV bytes it streams; the separate append was a
+ * launch and a hand-off of its own for a few KB).  The results are the same bits as
+ * those two calls: the key is rotated and stored with the append's arithmetic and its
+ * state rules (slot, head, count, pos, the SK_DEVERR_POSITION_RANGE and
+ * SK_DEVERR_CAPACITY refusals), q is rotated the same way, and the attention reads the
+ * same rows in the same order.  Differences: q and k are NOT rotated in place (they are
+ * read only), and a ring head outside [0, window) is refused with SK_DEVERR_STATE
+ * instead of being written through.
+ *   table: the RoPE table (head_dim as the layer's); NULL: q and k come rotated and are
+ *      used as given (no position limit but the counter's own).
+ *   q: [batch][n_q_heads][head_dim] of io_dtype, device, read only.
+ *   k, v: [batch][n_kv_heads][head_dim] of io_dtype, device, read only.
+ *   out: [batch][n_q_heads][head_dim] of io_dtype, device; may alias q.
+ *   sink_logits, workspace: as sk_decode_attention, with
+ *      sk_decode_step_workspace_bytes(layer, n_q_heads) bytes of workspace.
+ * The state (head, count, pos) changes in the second kernel; until the call's work is
+ * done on the stream nothing else may read or write this layer.
+ * Supported: ring and global layers with io SK_BF16 and a BF16/BF16 cache, or io
+ * SK_F32 and an F32/F32 cache (int8 K caches: sk_kv_append + sk_decode_attention);
+ * n_q_heads / n_kv_heads as sk_decode_attention. */
+SK_API sk_status sk_decode_step(const sk_rope_table* table, const sk_kv_layer* layer, const void* q,
+                                int32_t n_q_heads, const void* k, const void* v, int32_t io_dtype,
+                                const float* sink_logits, void* out, void* workspace, size_t ws_bytes,
+                                void* stream);
+
 /* ---- Prefill attention (causal + window + sinks) ---------------------------------- */
 
 /* Keys a chunk starting at position p0 takes from a prior cache: with window > 0 the

@@ -12,6 +12,7 @@ sk_rope_dynamic_*      DynamicRope (+ dynamic_factor)
 sk_rope_apply          rope_apply
 sk_kv_append           kv_append
 sk_decode_attention    decode_attention (+ decode_workspace_bytes, decode_attention_noalloc)
+sk_decode_step         decode_step (+ decode_step_workspace_bytes)
 sk_prefill_attention   prefill_attention
 sk_kv_rerotate         kv_rerotate
 sk_kv_shift_recent     kv_shift_recent
@@ -99,6 +100,10 @@ _SIGNATURES = [
                                            ctypes.c_void_p]),
     ("sk_decode_attention_noalloc", ctypes.c_int, [ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32,
                                                    ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    ("sk_decode_step_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(KVLayerStruct), ctypes.c_int32]),
+    ("sk_decode_step", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(KVLayerStruct), ctypes.c_void_p, ctypes.c_int32,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     ("sk_prefill_prior_keys", ctypes.c_int64, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
     ("sk_selftest_bounded_wait", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_prefill_workspace_bytes", ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -449,6 +454,34 @@ def decode_attention_noalloc(layer: KVLayer, q_rot: torch.Tensor, out: torch.Ten
                                               _sk_dtype(q_rot.dtype), _sink_logits(sink_logits, q_rot.shape[1]),
                                               _ptr(out), _stream(stream)),
            "sk_decode_attention_noalloc")
+    return out
+
+
+def decode_step_workspace_bytes(layer: KVLayer, n_q_heads: int) -> int:
+    s = layer.struct()
+    return int(_lib().sk_decode_step_workspace_bytes(ctypes.byref(s), n_q_heads))
+
+
+def decode_step(table: Optional[RopeTable], layer: KVLayer, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None,
+                sink_logits: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode token per sequence: RoPE + append + attention in two kernels
+    (sk_decode_step).  q [B, Hq, D], k and v [B, Hkv, D], unrotated and left as they are
+    (unlike kv_append); returns out [B, Hq, D].  table None: q and k come rotated."""
+    _need_contig(q, k, v)
+    Hq = q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    s = layer.struct()
+    need = int(_lib().sk_decode_step_workspace_bytes(ctypes.byref(s), Hq))
+    if need == 0:
+        raise SinkKVError(SK_ERR_UNSUPPORTED, "sk_decode_step_workspace_bytes")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(_lib().sk_decode_step(None if table is None else table.handle, ctypes.byref(s), _ptr(q), Hq, _ptr(k),
+                                 _ptr(v), _sk_dtype(q.dtype), _sink_logits(sink_logits, Hq), _ptr(out),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "sk_decode_step")
     return out
 
 

@@ -92,6 +92,8 @@ def test_bad_arguments_rejected_on_host(lib):
     assert lib.sk_prefill_attention(None, None, None, 1, 1, 1, 1, 128, 0, 0, 0, None, None, None, None, 0, None,
                                     None) == sk.SK_ERR_ARG
     assert lib.sk_decode_workspace_bytes(None, 8) == 0
+    assert lib.sk_decode_step(None, None, None, 8, None, None, 0, None, None, None, 0, None) == sk.SK_ERR_ARG
+    assert lib.sk_decode_step_workspace_bytes(None, 8) == 0
     assert lib.sk_kv_rerotate(None, 1, None, None, None) == sk.SK_ERR_ARG
     assert lib.sk_rope_apply(None, None, 0, 1, 1, None, None, None) == sk.SK_ERR_ARG
     assert lib.sk_paged_append(None, None, None, 0, None, None, 0, 1, None) == sk.SK_ERR_ARG
