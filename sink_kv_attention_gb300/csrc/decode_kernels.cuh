@@ -618,31 +618,6 @@ __device__ __forceinline__ void write_new_rows(const DecodeParams& p, int b, int
     }
 }
 
-// FUSED, before the PDL wait: ask L2 for the table rows the step's rotations read, at
-// each sequence's position as the state shows now and the one after it (the state may
-// still be a step behind).  A hint only: the rows are read after the wait.
-__device__ __forceinline__ void prefetch_table_rows(const DecodeParams& p, const int64_t* pre) {
-    const int P = gridDim.x, c = blockIdx.x;
-    const int64_t R = pre[p.B];
-    if (R <= 0 || p.rotary_dim <= 0) return;
-    const int64_t lo = (int64_t(c) * R + P - 1) / P;
-    const int64_t hi = (int64_t(c + 1) * R + P - 1) / P;
-    if (lo >= hi) return;
-    const uint32_t bytes = uint32_t(p.rotary_dim / 2) * uint32_t(sizeof(float2));
-    UnitWalk w{pre, p.B, p.Hkv, 0, 0};
-    w.seek(lo);
-    int last_b = -1;
-    do {
-        if (w.start() >= hi) break;
-        if (w.b != last_b) {
-            last_b = w.b;
-            const int64_t pos = p.pos[w.b];
-            for (int64_t q = pos; q <= pos + 1; ++q)
-                if (q >= 0 && q < p.max_pos) bulk_prefetch_l2(p.table + q * (p.rotary_dim / 2), bytes);
-        }
-    } while (w.next());
-}
-
 // Rows of K and V per block that the split kernel asks L2 to fetch before its PDL wait
 // (128 KB per block at d_h = 128, bf16).  Measured on the 32 x 4096-row windowed step:
 // 128 to 384 rows gave the same gain (about 5%); 768 and more gave less.
@@ -726,10 +701,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ, PAGED, FUSED>::THREA
         // (Paged layers take no prefetch: per-block table reads made it a loss there.)
         unit_prefix<ROWS>(p, pre, lane);
         __syncwarp();
-        if (lane == 0) {
-            if constexpr (FUSED) prefetch_table_rows(p, pre);
-            prefetch_share<C, T, D>(p, pre);
-        }
+        if (lane == 0) prefetch_share<C, T, D>(p, pre);
         __syncwarp();
     }
     pdl_wait();  // the append before this kernel has written the state, q and the new rows
