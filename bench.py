@@ -35,25 +35,26 @@ METRIC = "sink+window decode attn KV-read GB/s (frac of HBM peak), tokens/s, key
 # A row reports it only while those sources are unchanged, else null.  "scale": the capture
 # ran a smaller case of the same kernel; the traffic grows in proportion to the units
 # processed and is scaled by that factor to one launch of the full workload.
+DECODE_SOURCES = {"decode.cu": "e6c7c2686de1a89eeb4a8c18ed6f37b833011124de96333c41c2fea3ae08a2b3",
+                  "decode_kernels.cuh": "bfa9cfec93c71e425fdc5b9296b39d112da8f7687d6fda00b01f738c1d03282d",
+                  "rope_lane.cuh": "92cd7898465a1776e0e3f9e32707943dca4d074e80246d99524d949885102532",
+                  "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}
 NCU_TRAFFIC = {
     "decode_window_b32": dict(
-        bytes=542278400, scale=1,
+        bytes=542267136, scale=1,
         capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --no-rows --no-cpu-baseline "
                 "--steps 5 --warmup 3 (split kernel only)",
-        sources={"decode.cu": "55c52f9e7df83499bc4fbcc79d689e224d9861abf0c768cfc5f9b179acc35f02",
-                 "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}),
+        sources=DECODE_SOURCES),
     "decode_paged_window_b32_bs16": dict(
-        bytes=540817152, scale=1,
+        bytes=540717824, scale=1,
         capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload paged "
                 "--steps 5 --warmup 3 (split kernel only)",
-        sources={"decode.cu": "55c52f9e7df83499bc4fbcc79d689e224d9861abf0c768cfc5f9b179acc35f02",
-                 "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}),
+        sources=DECODE_SOURCES),
     "decode_window_b32_int8": dict(
-        bytes=410712576, scale=1,
+        bytes=410813440, scale=1,
         capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload window_i8 "
                 "--steps 5 --warmup 3 (split kernel only)",
-        sources={"decode.cu": "55c52f9e7df83499bc4fbcc79d689e224d9861abf0c768cfc5f9b179acc35f02",
-                 "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}),
+        sources=DECODE_SOURCES),
     "prefill_attn_t32768": dict(
         bytes=634040064, scale=1,
         capture="ncu --set full -k regex:prefill_attn -s 2 -c 1, python bench.py --workload prefill "
@@ -248,7 +249,8 @@ def bench_window(args, rank, world):
     ks = synth.normal((n, B, 1, Hkv, D), 15, torch.bfloat16, device="cuda")
     vs = synth.normal((n, B, 1, Hkv, D), 16, torch.bfloat16, device="cuda")
     out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(sk.decode_workspace_bytes(layer, Hq), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(sk.decode_workspace_bytes(layer, Hq), sk.decode_step_workspace_bytes(layer, Hq)),
+                     dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     zl = _learned_sinks(args, Hq)
 
@@ -293,6 +295,16 @@ def bench_window(args, rank, world):
         clocks.stop()
     assert layer.error_bits() == 0
     ms_step = _max_over_ranks(statistics.median(per), world)
+    # the same steps as the decode step (sk_decode_step: the append folded into the
+    # attention's two kernels), on the same state
+    ms_fused = None
+    if graph is not None:
+        def step_fused(i):
+            sk.decode_step(tbl, layer, qs[i, :, 0], ks[i, :, 0], vs[i, :, 0], out=out, workspace=ws, sink_logits=zl)
+        g_f = _capture(step_fused, warm, steps)
+        per_f, _, _ = _replays(g_f, steps, TARGET_MS / 2, reset=reset, world=world)
+        assert layer.error_bits() == 0
+        ms_fused = _max_over_ranks(statistics.median(per_f), world)
 
     L = c["S"] + W  # visible keys per sequence (ring full)
     kv_bytes = B * Hkv * L * D * 2 * 2
@@ -399,6 +411,10 @@ def bench_window(args, rank, world):
         "keys_per_s": round(world * B * L / (ms_step * 1e-3), 1),
         "roofline": roof,
         "e2e": e2e,
+        "decode_step": None if ms_fused is None else {
+            "ms_per_step": round(ms_fused, 5), "gbs": round(world * kv_bytes / (ms_fused * 1e-3) / 1e9, 2),
+            "calls": "sk_decode_step: the same steps in two launches (split with the token's RoPE + append, "
+                     "combine), same state; not the headline, which times sk_kv_append + sk_decode_attention"},
         "timing": {"replays": R, "steps_per_replay": steps, "timed_steps": R * steps,
                    "timed_ms": round(region_ms, 2), "ms_per_step": "median over replays",
                    "ms_per_step_mean": round(statistics.fmean(per), 5),
@@ -532,9 +548,10 @@ def _launch_roofline(fn, n, alg_bytes, name, kernel, unit_note, target_ms=TARGET
 
 def bench_hybrid(args):
     """Llama-3-8B-shaped hybrid decode: 32 layers (every 4th global with a 131072-token
-    prefix, the rest S=4 + W=4096 rings), B=16; one step = append + attention on all
-    32 layers.  The layers' counters are put back after every replay of the captured
-    steps, so each replay makes the same appends and reads."""
+    prefix, the rest S=4 + W=4096 rings), B=16; one step = RoPE + append + attention on
+    all 32 layers as sk_kv_append + sk_decode_attention; the decode step (sk_decode_step)
+    timed beside it on the same state.  The layers' counters are put back after every
+    replay of the captured steps, so each replay makes the same appends and reads."""
     import torch
     import sink_kv_attention_gb300 as sk
     from sink_kv_attention_gb300 import synth
@@ -561,18 +578,25 @@ def bench_hybrid(args):
     ks = synth.normal((n, nl, B, 1, Hkv, D), 4, torch.bfloat16, device="cuda")
     vs = synth.normal((n, nl, B, 1, Hkv, D), 5, torch.bfloat16, device="cuda")
     out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(max(sk.decode_workspace_bytes(L, Hq) for L in layers), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(max(sk.decode_workspace_bytes(L, Hq), sk.decode_step_workspace_bytes(L, Hq))
+                         for L in layers), dtype=torch.uint8, device="cuda")
     zl = _learned_sinks(args, Hq)
 
-    def step(i):
+    def step(i):  # rotates q and k in place
         for j, L in enumerate(layers):
             sk.kv_append(tbl, L, qs[i, j], ks[i, j], vs[i, j])
             sk.decode_attention(L, qs[i, j, :, 0], out=out, workspace=ws, sink_logits=zl)
 
+    def step_fused(i):  # q, k, v are read only
+        for j, L in enumerate(layers):
+            sk.decode_step(tbl, L, qs[i, j, :, 0], ks[i, j, :, 0], vs[i, j, :, 0], out=out, workspace=ws,
+                           sink_logits=zl)
+
     for i in range(warm):
         step(i)
     torch.cuda.synchronize()
-    ms, clk, rec = _timed(lambda i: step(warm + i), steps, 0, reset=_state_saver(layers))
+    reset = _state_saver(layers)
+    ms, clk, rec = _timed(lambda i: step(warm + i), steps, 0, reset=reset)
     assert all(L.error_bits() == 0 for L in layers)
     n_glob = sum(1 for i in range(c["layers"]) if synth.hybrid_layer_is_global(i))
     n_slid = c["layers"] - n_glob
@@ -590,6 +614,9 @@ def bench_hybrid(args):
                                                           sink_logits=zl),
                             len(glob), alg, None, "decode attention over a global layer (split-K + combine), "
                             "8 launches back to back", f"K+V of {rows_g} rows x 16 sequences x 8 kv heads + q + out")
+    reset()
+    ms_fused, _, rec_fused = _timed(lambda i: step_fused(warm + i), steps, 0, reset=reset)
+    assert all(L.error_bits() == 0 for L in layers)
     return {"metric": "hybrid decode step KV-read GB/s (frac of HBM peak), tokens/s", "value": round(value, 2),
             "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": warm, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
@@ -598,6 +625,8 @@ def bench_hybrid(args):
                        "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.1f} GB per step)",
                        "learned_sink_logits": bool(args.learned_sink)},
             "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+            "decode_step": {"ms_per_step": round(ms_fused, 4), "gbs": round(kv_bytes / (ms_fused * 1e-3) / 1e9, 2),
+                            "calls": "sk_decode_step, two launches per layer, same state", "timing": rec_fused},
             "roofline": roof, "timing": rec,
             "peak_source": f"{peak_kind} hbm_gbs", "gpu_launches": rec["replays"] * steps * c["layers"] * 3,
             "clocks": clk}
