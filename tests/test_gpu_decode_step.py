@@ -193,7 +193,7 @@ def test_step_in_a_cuda_graph(sk):
         _assert_same_layer(L, E)
 
 
-@pytest.mark.parametrize("B", [1, 4])
+@pytest.mark.parametrize("B", [1, 4, 32])
 def test_windowed_step_against_the_oracle(sk, B):
     """The windowed workload's shapes (H_q=32, H_kv=8, d_h=128, S=4, W=4092, full rings at
     random heads) through decode_step, against the oracle's append + decode: heads
