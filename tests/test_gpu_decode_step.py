@@ -167,6 +167,43 @@ def test_step_without_table_and_with_learned_sinks(sk):
         _assert_same_layer(layer, ref)
 
 
+@pytest.mark.parametrize("kind,B,S,W,cap", [
+    ("ring", 64, 4, 8, None),     # 512 units of at most 12 rows: 3-5 units per block
+    ("ring", 200, 2, 3, None),    # 1600 units of at most 5 rows: about 50 per block
+    ("global", 96, 0, 0, 24),     # 768 units of at most 24 rows
+])
+def test_many_units_per_block(sk, kind, B, S, W, cap):
+    """Blocks that meet many (sequence, kv head) units: the token warp's q ring (two
+    slots) wraps many times, its writes of later units wait for the consumers to free a
+    slot, and a block writes the token rows of several units.  Random states (filling
+    sinks, filling and full rings; global prefixes), three steps, bit for bit."""
+    D, Hq, Hkv = 64, 16, 8
+    table = sk.RopeTable(D, D, 1e4, 1 << 20)
+    g = torch.Generator().manual_seed(B * 7 + W)
+    if kind == "ring":
+        layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, B, Hkv, D, sinks=S, window=W)
+        pos = torch.randint(0, S + 3 * W, (B,), generator=g)
+        cnt = torch.clamp(pos - S, min=0, max=W)
+        full = cnt == W
+        head = torch.where(full, torch.randint(0, W, (B,), generator=g), cnt % W)
+        layer.pos.copy_(pos)
+        layer.count.copy_(cnt.to(torch.int32))
+        layer.head.copy_(head.to(torch.int32))
+    else:
+        layer = sk.KVLayer.allocate(sk.SK_LAYER_GLOBAL, B, Hkv, D, capacity=cap)
+        layer.pos.copy_(torch.randint(0, cap - 3, (B,), generator=g))
+    synth.fill_normal_(layer.k, 601)
+    synth.fill_normal_(layer.v, 602)
+    for step in range(3):
+        q = synth.normal((B, Hq, D), 610 + step, torch.bfloat16).cuda()
+        k = synth.normal((B, Hkv, D), 620 + step, torch.bfloat16).cuda()
+        v = synth.normal((B, Hkv, D), 630 + step, torch.bfloat16).cuda()
+        ref, got, want = _both_paths(sk, table, layer, q, k, v)
+        assert torch.equal(got, want), step
+        _assert_same_layer(layer, ref)
+    assert layer.error_bits() == 0
+
+
 def test_step_in_a_cuda_graph(sk):
     """Three steps through two layers captured in one CUDA graph and replayed: the same
     bits as the steps taken eagerly (the state changes on the device, at replay)."""
