@@ -34,13 +34,15 @@
 //
 // FUSED kernels fold the token's RoPE + append into the step (contiguous bf16 or fp32
 // layers).  The split kernel works on the rows visible after the append, computed from
-// the state as it stands (the append's rules, below).  The one block whose share holds
-// the new token's slot writes the rotated key and the value there from an extra warp
-// before its producer copies that tile; no other block reads that slot, because the
-// visible set after the append no longer holds the entry the token replaces.  Every
-// consumer rotates its q slice with the append's arithmetic.  The state itself is
-// advanced by the combine kernel, from a copy the split kernel took, so that no block
-// of either kernel reads a state another block is changing.
+// the state as it stands (the append's rules, below).  An extra warp per block (the
+// token warp) rotates q of every unit the block meets, with the append's arithmetic,
+// into a two-slot ring in shared memory that the consumers read instead of q in global
+// memory; and the one block whose share holds a unit's new slot has it write the rotated
+// key and the value there before the producer copies that tile.  No other block reads
+// that slot, because the visible set after the append no longer holds the entry the
+// token replaces.  The state itself is advanced by the combine kernel, from a copy the
+// split kernel took, so that no block of either kernel reads a state another block is
+// changing.
 #pragma once
 
 #include <algorithm>
@@ -618,6 +620,19 @@ __device__ __forceinline__ void write_new_rows(const DecodeParams& p, int b, int
     }
 }
 
+// FUSED: this block's share of the copy of the state (as it stands during the split
+// kernel) that the combine kernel advances: block c writes sequences c, c + P, c + 2P, ...
+// (one warp; every block of the grid writes its share, so each sequence once).
+__device__ __forceinline__ void snapshot_share(const DecodeParams& p, int lane) {
+    for (int b = blockIdx.x + lane * int(gridDim.x); b < p.B; b += 32 * int(gridDim.x)) {
+        int64_t* sn = p.snap + 4 * int64_t(b);
+        sn[0] = p.pos[b];
+        sn[1] = p.count != nullptr ? p.count[b] : 0;
+        sn[2] = p.head != nullptr ? p.head[b] : 0;
+        sn[3] = 0;
+    }
+}
+
 // Rows of K and V per block that the split kernel asks L2 to fetch before its PDL wait
 // (128 KB per block at d_h = 128, bf16).  Measured on the 32 x 4096-row windowed step:
 // 128 to 384 rows gave the same gain (about 5%); 768 and more gave less.
@@ -707,26 +722,18 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ, PAGED, FUSED>::THREA
     pdl_wait();  // the append before this kernel has written the state, q and the new rows
     __syncthreads();  // the producer has finished with the guessed split
     if (warp == 0) unit_prefix<ROWS>(p, pre, lane);
-    if constexpr (FUSED) {
-        // the state as read here, for the combine kernel that advances it
-        if (blockIdx.x == 0 && warp == 1) {
-            for (int b = lane; b < p.B; b += 32) {
-                int64_t* sn = p.snap + 4 * int64_t(b);
-                sn[0] = p.pos[b];
-                sn[1] = p.count != nullptr ? p.count[b] : 0;
-                sn[2] = p.head != nullptr ? p.head[b] : 0;
-                sn[3] = 0;
-            }
-        }
-    }
     __syncthreads();
 
     const int P = gridDim.x, c = blockIdx.x;
     const int64_t R = pre[p.B];
-    if (R == 0) return;
     const int64_t lo = (int64_t(c) * R + P - 1) / P;
     const int64_t hi = (int64_t(c + 1) * R + P - 1) / P;
-    if (lo >= hi) return;
+    if (R == 0 || lo >= hi) {  // no rows here (the token warp still writes its share of the state copy)
+        if constexpr (FUSED) {
+            if (warp == NWARPS + 1) snapshot_share(p, lane);
+        }
+        return;
+    }
     bool timed_out = false;
 
     if constexpr (PAGED) {
@@ -778,6 +785,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ, PAGED, FUSED>::THREA
                 if (lane == 0) mbar_arrive(&q_full[slot]);
                 ++k;
             }
+            snapshot_share(p, lane);
             if (timed_out) set_error(p.err, SK_DEVERR_TIMEOUT);
             return;
         }
