@@ -105,6 +105,30 @@ def test_bad_arguments_rejected_on_host(lib):
     lib.sk_rope_table_destroy(None)  # NULL is ignored
 
 
+def test_decode_step_refusals_on_host(lib):
+    """sk_decode_step refuses before any launch: an int8 K cache (its step is the two
+    calls), mixed io and cache types, a ring layer without its head array, a misaligned
+    q.  The device pointers are never dereferenced on these paths."""
+    import sink_kv_attention_gb300 as sk
+    A = 1 << 20  # aligned stand-in addresses, never read
+
+    def layer(k_dtype=sk.SK_BF16, head=A + 4096):
+        return sk.KVLayerStruct(sk.SK_LAYER_RING, k_dtype, sk.SK_BF16, 2, 8, 128, 4, 60, 64, A, A + 16,
+                                A + 32 if k_dtype == sk.SK_I8 else None, head, A + 8192, A + 12288, None)
+
+    def step(L, io=sk.SK_BF16, q=A + 64):
+        return lib.sk_decode_step(None, ctypes.byref(L), q, 32, A + 128, A + 256, io, None, A + 512, A + 1024,
+                                  1 << 30, None)
+
+    assert step(layer(sk.SK_I8)) == sk.SK_ERR_UNSUPPORTED
+    assert lib.sk_decode_step_workspace_bytes(ctypes.byref(layer(sk.SK_I8)), 32) == 0
+    assert step(layer(), io=sk.SK_F32) == sk.SK_ERR_UNSUPPORTED
+    assert step(layer(head=None)) == sk.SK_ERR_ARG
+    assert step(layer(), q=A + 72) == sk.SK_ERR_ARG
+    assert lib.sk_decode_step(None, ctypes.byref(layer()), None, 32, A, A, sk.SK_BF16, None, A, A, 1 << 30,
+                              None) == sk.SK_ERR_ARG
+
+
 def test_prefill_prior_keys_are_exactly_the_old_keys_a_chunk_sees(lib):
     """sk_prefill_prior_keys(p0, S, W) is the number of positions before p0 that any
     query of a chunk starting at p0 may see under the oracle's mask (its first query

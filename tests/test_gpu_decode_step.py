@@ -268,3 +268,15 @@ def test_windowed_step_against_the_oracle(sk, B):
     assert layer.pos.tolist() == [int(x) + 1 for x in pos]
     assert layer.count.tolist() == [W] * B
     assert layer.head.tolist() == [(int(h) + 1) % W for h in head]
+
+
+def test_step_refuses_a_table_of_another_head_dim(sk):
+    """A table built for d_h = 64 against a d_h = 128 layer: SK_ERR_ARG, nothing launched,
+    the state as it was."""
+    table = sk.RopeTable(64, 64, 1e4, 1024)
+    layer = sk.KVLayer.allocate(sk.SK_LAYER_RING, 1, 2, 128, sinks=4, window=16)
+    q = torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 2, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sk.SinkKVError):
+        sk.decode_step(table, layer, q, k, k.clone())
+    assert layer.pos.tolist() == [0] and layer.error_bits() == 0
