@@ -55,6 +55,11 @@ NCU_TRAFFIC = {
         capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload window_i8 "
                 "--steps 5 --warmup 3 (split kernel only)",
         sources=DECODE_SOURCES),
+    "decode_step_window_b32": dict(
+        bytes=541921536, scale=1,
+        capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload window_step "
+                "--steps 5 --warmup 3 (fused split kernel only)",
+        sources=dict(DECODE_SOURCES, **{"decode_step.cu": "ccf687b9b226f8b64abc0f4dc079d32f1dbdcc27c072859308f1e00ad42dff18"})),
     "prefill_attn_t32768": dict(
         bytes=634040064, scale=1,
         capture="ncu --set full -k regex:prefill_attn -s 2 -c 1, python bench.py --workload prefill "
@@ -1241,6 +1246,64 @@ def bench_tiny(args):
             "gpu_launches": 2 * T * R, "clocks": clocks.summary()}
 
 
+def bench_window_step(args):
+    """The windowed decode step (B=32, H_q=32, H_kv=8, d_h=r=128, S=4, W=4092, rings full at
+    random heads) through sk_decode_step: the token's RoPE + append folded into the split
+    kernel, two launches per step; sk_kv_append + sk_decode_attention (the headline's
+    calls) timed beside it on the same state.  Roofline: the step's launches back to back
+    (split with the token, combine), the counters put back after every replay."""
+    import torch
+    import sink_kv_attention_gb300 as sk
+    from sink_kv_attention_gb300 import synth
+    steps, warm = args.steps, args.warmup
+    tbl, layer, c = window_setup(seed_base=0, steps=2 * steps + warm + 2)
+    B, Hq, Hkv, D, S, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    n = steps + warm
+    qs = synth.normal((n, B, 1, Hq, D), 14, torch.bfloat16, device="cuda")
+    ks = synth.normal((n, B, 1, Hkv, D), 15, torch.bfloat16, device="cuda")
+    vs = synth.normal((n, B, 1, Hkv, D), 16, torch.bfloat16, device="cuda")
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(sk.decode_workspace_bytes(layer, Hq), sk.decode_step_workspace_bytes(layer, Hq)),
+                     dtype=torch.uint8, device="cuda")
+
+    def step(i):  # q, k, v are read only
+        sk.decode_step(tbl, layer, qs[i, :, 0], ks[i, :, 0], vs[i, :, 0], out=out, workspace=ws)
+
+    def step_two_calls(i):  # rotates q and k in place
+        sk.kv_append(tbl, layer, qs[i], ks[i], vs[i])
+        sk.decode_attention(layer, qs[i, :, 0], out=out, workspace=ws)
+
+    for i in range(warm):
+        step(i)
+    torch.cuda.synchronize()
+    reset = _state_saver([layer])
+    ms, clk, rec = _timed(lambda i: step(warm + i), steps, 0, reset=reset)
+    assert layer.error_bits() == 0
+    kv_bytes = B * Hkv * (S + W) * D * 2 * 2
+    hbm, _, _, peak_kind = _peaks()
+    value = kv_bytes / (ms * 1e-3) / 1e9
+    alg = kv_bytes + 2 * B * Hq * D * 2 + 4 * B * Hkv * D * 2
+    roof = _launch_roofline(lambda i: step(i % n), steps, alg, "decode_step_window_b32",
+                            "decode step (split-K with the token's RoPE + append, combine); its launches back "
+                            "to back in one graph",
+                            "K+V of 4096 visible rows x 32 sequences x 8 kv heads + q + out + the token's k, v "
+                            "in and out", reset=reset)
+    reset()
+    ms_two, _, rec_two = _timed(lambda i: step_two_calls(warm + i), steps, 0, reset=reset)
+    assert layer.error_bits() == 0
+    return {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "dtype": "bf16",
+            "config": {"workload": "windowed-layer decode step (RoPE + append + split-K attention) through "
+                                   "sk_decode_step, B=32, H_q=32, H_kv=8, d_h=r=128, S=4, W=4092",
+                       "l2": f"inputs larger than L2 (KV {kv_bytes / 1e6:.0f} MB per step)"},
+            "frac_of_hbm_peak": round(value / hbm, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+            "two_calls": {"ms_per_step": round(ms_two, 5), "gbs": round(kv_bytes / (ms_two * 1e-3) / 1e9, 2),
+                          "calls": "sk_kv_append + sk_decode_attention (the headline's), same state",
+                          "timing": rec_two},
+            "roofline": roof, "timing": rec, "peak_source": f"{peak_kind} hbm_gbs",
+            "gpu_launches": 2 * steps * rec["replays"], "clocks": clk}
+
+
 def bench_window_b1(args):
     """Single-stream decode: one sequence through 32 windowed layers (each H_q=32,
     H_kv=8, d_h=r=128, S=4, W=4092, ring full at a random head), one token per step:
@@ -1651,7 +1714,7 @@ def main():
     ap.add_argument("--workload", default="window",
                     choices=["window", "window_i8", "hybrid", "rerotate_bf16", "rerotate_i8", "prefill",
                              "prefill_chunk", "dynamic_bf16", "dynamic_i8", "shift_bf16", "shift_i8", "paged",
-                             "rope", "tiny", "window_b1"])
+                             "rope", "tiny", "window_b1", "window_step"])
     ap.add_argument("--cpu-worker", type=int, default=0)
     ap.add_argument("--cpu-row", default="", choices=[""] + sorted(CPU_ROWS))
     ap.add_argument("--no-rows", action="store_true",
@@ -1731,6 +1794,8 @@ def main():
                 print(json.dumps(bench_tiny(args)))
             elif args.workload == "window_b1":
                 print(json.dumps(bench_window_b1(args)))
+            elif args.workload == "window_step":
+                print(json.dumps(bench_window_step(args)))
             else:
                 print(json.dumps(bench_rerotate(args, args.workload.split("_")[1])))
         return
