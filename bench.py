@@ -1676,14 +1676,15 @@ def cpu_baseline(n_seq=32):
 ROWS = (("tiny", bench_tiny), ("window_b1", bench_window_b1), ("hybrid", bench_hybrid),
         ("prefill", bench_prefill), ("rerotate_bf16", lambda a: bench_rerotate(a, "bf16")),
         ("rerotate_i8", lambda a: bench_rerotate(a, "i8")), ("window_i8", bench_window_i8),
-        ("paged", bench_paged))
+        ("paged", bench_paged), ("window_step", bench_window_step))
 
 
 def bench_rows(args):
     """Every other configuration of the path on this GPU, each with its roofline and
     its oracle baseline: the tiny case, single-stream decode, the hybrid 32-layer step,
-    the prefill chunk and the two rerotations; then the windowed step over int8 keys
-    and over a paged cache (the oracle's arithmetic there is the windowed line's)."""
+    the prefill chunk and the two rerotations; then the windowed step over int8 keys,
+    over a paged cache and through sk_decode_step (the oracle's arithmetic there is the
+    windowed line's)."""
     import gc
     import torch
     rows = {}
