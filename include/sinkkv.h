@@ -521,6 +521,22 @@ SK_API sk_status sk_sync_check(uint32_t* err, int32_t clear, void* stream, uint3
  * `stream`; SK_ERR_ARG for err == NULL. */
 SK_API sk_status sk_selftest_bounded_wait(uint32_t* err, void* stream);
 
+/* Diagnostic: run sk_prefill_attention's pipeline on a global causal chunk (p0 = 0, no
+ * sinks, no window, no prior) in which the softmax warps never signal that P of tile
+ * stall_tile (0-based, in each block's visiting order) is ready.  Every block that
+ * visits that tile stalls: its P.V issuer's bounded wait gives up after about one
+ * second, every later wait of the block gives up within a few polls, the MMAs and
+ * copies already issued drain (each drain wait bounded), the block frees its tensor
+ * memory and ORs SK_DEVERR_TIMEOUT into *err (device).  Blocks with fewer tiles finish
+ * normally.  The output is undefined.  Same arguments, layouts and checks as
+ * sk_prefill_attention (workspace >= sk_prefill_workspace_bytes(batch, T, n_kv_heads,
+ * head_dim, 0)); SK_ERR_ARG for err == NULL or stall_tile < 0.  Asynchronous on
+ * `stream`. */
+SK_API sk_status sk_selftest_prefill_stall(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
+                                           int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                           void* out, void* workspace, size_t ws_bytes, int32_t stall_tile,
+                                           uint32_t* err, void* stream);
+
 /* A static, human-readable name for a status code. */
 SK_API const char* sk_status_str(sk_status status);
 

@@ -106,6 +106,10 @@ _SIGNATURES = [
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     ("sk_prefill_prior_keys", ctypes.c_int64, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
     ("sk_selftest_bounded_wait", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    ("sk_selftest_prefill_stall", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32,
+                                                 ctypes.c_void_p, ctypes.c_void_p]),
     ("sk_prefill_workspace_bytes", ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                      ctypes.c_int64]),
     ("sk_prefill_attention", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
@@ -643,6 +647,26 @@ def selftest_bounded_wait(err: torch.Tensor, stream=None) -> None:
     """Launch the bounded-wait diagnostic (sk_selftest_bounded_wait): about one second
     later SK_DEVERR_TIMEOUT is set in `err`."""
     _check(_lib().sk_selftest_bounded_wait(_ptr(err), _stream(stream)), "sk_selftest_bounded_wait")
+
+
+def selftest_prefill_stall(q_rot: torch.Tensor, k_rot: torch.Tensor, v: torch.Tensor, stall_tile: int,
+                           err: torch.Tensor, stream=None) -> torch.Tensor:
+    """Run the prefill pipeline on a global causal chunk whose P of tile `stall_tile` is
+    never signalled ready (sk_selftest_prefill_stall): the blocks that reach it give up
+    after about one second and set SK_DEVERR_TIMEOUT in `err`.  Returns the (undefined)
+    output buffer."""
+    _need_contig(q_rot, k_rot, v)
+    B, T, Hq, D = q_rot.shape
+    Hkv = k_rot.shape[2]
+    out = torch.empty_like(q_rot)
+    need = prefill_workspace_bytes(B, T, Hkv, D, 0)
+    if need == 0:
+        raise SinkKVError(SK_ERR_UNSUPPORTED, "sk_prefill_workspace_bytes")
+    ws = torch.empty(need, dtype=torch.uint8, device=q_rot.device)
+    _check(_lib().sk_selftest_prefill_stall(_ptr(q_rot), _ptr(k_rot), _ptr(v), B, T, Hq, Hkv, D, _ptr(out), _ptr(ws),
+                                            need, int(stall_tile), _ptr(err), _stream(stream)),
+           "sk_selftest_prefill_stall")
+    return out
 
 
 def version() -> int:

@@ -32,6 +32,8 @@
 // operand, so V needs no transposed copy.
 // An optional learned sink logit per query head (a denominator-only term) enters at
 // the epilogue.
+// Every wait is bounded; a timeout sets SK_DEVERR_TIMEOUT in the error word (see
+// wait_or_flag for how the block then ends).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -60,7 +62,7 @@ constexpr int K_STAGE = 16384;
 constexpr int SM_V = SM_K + 2 * K_STAGE;      // 2 stages x (V lo 8 KB, V hi 8 KB)
 constexpr int V_STAGE = 16384;
 constexpr int SM_BAR = SM_V + 2 * V_STAGE;
-constexpr int N_BARS = 16;
+constexpr int N_BARS = 18;  // 17 used
 constexpr int SM_TMEM = SM_BAR + N_BARS * 8;
 constexpr int SM_BYTES = SM_TMEM + 16;
 // Two CTAs per SM fit comfortably (2 x (SM_ALLOC + 1 KB reserved) < 228 KB), with
@@ -88,6 +90,7 @@ struct PrefillParams {
     int nqb;           // query blocks of qpb queries
     int nh, qpb;       // q heads packed per CTA (one GQA group's), queries per block: nh * qpb = BM
     float scale_log2;  // log2(e) / sqrt(head_dim)
+    int stall_tile;    // -1; otherwise (self-test) P of this tile is never signalled ready
 };
 
 struct TilePlan {
@@ -152,9 +155,26 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, bool& bad) {
-    if (mbar_wait_bounded(bar, parity)) return true;
+// Bounded wait (about one second) that also gives up, after a few polls, once any role
+// of the block has timed out (the abort flag in shared memory).  The fast path is the
+// plain try_wait; the hot loops carry no extra exit tests, because each one measurably
+// slowed the pipeline.  After a timeout the roles run out their loops without waiting
+// (every wait fails within a few polls), so a stalled block ends within about a second
+// of its first timeout rather than a second per remaining wait; its results are then
+// undefined, every address stays inside its buffer, and the block drains the MMAs and
+// copies it issued (bounded waits) before it frees its tensor memory.
+__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, bool& bad,
+                                             volatile uint32_t* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort != 0u || global_timer_ns() - t0 > 1000000000ull) break;
+    }
     bad = true;
+    *abort = 1u;
     return false;
 }
 
@@ -181,7 +201,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t* s_full = bars + 9;    // [2] S_i = Q K_i^T in TMEM buffer i & 1
     uint64_t* p_full = bars + 11;   // [2] P_i (bf16) written over S_i
     uint64_t* pv_done = bars + 13;  // [2] O += P_i V_i done
+    uint64_t* drain = bars + 15;    // [2] after a timeout: each issuing thread's MMAs done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_TMEM);
+    volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(smem + SM_TMEM + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // block -> (query block, descending so the long blocks start first; head group;
@@ -200,6 +222,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
+        *abort = 0u;
         for (int s = 0; s < 2; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -232,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             for (int i = 0; i < tp.n; ++i) {
                 const int s = i & 1;
-                if (i >= 2) wait_or_flag(&k_empty[s], ((i >> 1) - 1) & 1, bad);
+                if (i >= 2) wait_or_flag(&k_empty[s], ((i >> 1) - 1) & 1, bad, abort);
                 const int k0 = key_tile(tp, i) * BN;
                 uint8_t* st = smem + SM_K + s * K_STAGE;
                 mbar_arrive_expect_tx(&k_full[s], K_STAGE);
@@ -242,13 +267,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tma_load_4d(st, m, 0, g, kr, b, &k_full[s]);
                 tma_load_4d(st + BN * 128, m, 64, g, kr, b, &k_full[s]);
             }
+            if (bad) {  // the copies in flight land before the block leaves
+                mbar_wait_bounded(q_full, 0);
+                for (int i = max(0, tp.n - 2); i < tp.n; ++i) mbar_wait_bounded(&k_full[i & 1], (i >> 1) & 1);
+            }
         }
     } else if (warp == 6) {
         // ----------------------------- TMA loads: V ------------------------------
         if (lane == 0) {
             for (int i = 0; i < tp.n; ++i) {
                 const int s = i & 1;
-                if (i >= 2) wait_or_flag(&v_empty[s], ((i >> 1) - 1) & 1, bad);
+                if (i >= 2) wait_or_flag(&v_empty[s], ((i >> 1) - 1) & 1, bad, abort);
                 const int k0 = key_tile(tp, i) * BN;
                 uint8_t* st = smem + SM_V + s * V_STAGE;
                 mbar_arrive_expect_tx(&v_full[s], V_STAGE);
@@ -257,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tma_load_4d(st, m, 0, g, kr, b, &v_full[s]);
                 tma_load_4d(st + BN * 128, m, 64, g, kr, b, &v_full[s]);
             }
+            if (bad)
+                for (int i = max(0, tp.n - 2); i < tp.n; ++i) mbar_wait_bounded(&v_full[i & 1], (i >> 1) & 1);
         }
     } else if (warp == 4) {
         // ------------------------------- Q K^T issue -------------------------------
@@ -264,13 +295,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN);
             constexpr uint32_t idesc_qk_strip = idesc_bf16_f32(BM, kSinkStrip);
             const uint32_t sq = smem_u32(smem + SM_Q);
-            wait_or_flag(q_full, 0, bad);
+            wait_or_flag(q_full, 0, bad, abort);
             tc_fence_after_sync();
             for (int i = 0; i < tp.n; ++i) {
                 const int s = i & 1;
-                wait_or_flag(&k_full[s], (i >> 1) & 1, bad);
+                wait_or_flag(&k_full[s], (i >> 1) & 1, bad, abort);
                 // S buffer s last held P_{i-2}: its P.V must be done before QK_i overwrites it
-                if (i >= 2) wait_or_flag(&pv_done[s], ((i >> 1) - 1) & 1, bad);
+                if (i >= 2) wait_or_flag(&pv_done[s], ((i >> 1) - 1) & 1, bad, abort);
                 tc_fence_after_sync();
                 const uint32_t sk = smem_u32(smem + SM_K + s * K_STAGE);
 #pragma unroll
@@ -284,6 +315,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 umma_commit(&s_full[s]);
                 umma_commit(&k_empty[s]);
             }
+            if (bad) {  // this thread's MMAs done before the block frees tensor memory
+                umma_commit(&drain[0]);
+                mbar_wait_bounded(&drain[0], 0);
+            }
         }
     } else if (warp == 7) {
         // -------------------------------- P V issue --------------------------------
@@ -293,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, HD) | (1u << 16);  // B (V) MN-major
             for (int j = 0; j < tp.n; ++j) {
                 const int s = j & 1;
-                wait_or_flag(&p_full[s], (j >> 1) & 1, bad);
-                wait_or_flag(&v_full[s], (j >> 1) & 1, bad);
+                wait_or_flag(&p_full[s], (j >> 1) & 1, bad, abort);
+                wait_or_flag(&v_full[s], (j >> 1) & 1, bad, abort);
                 tc_fence_after_sync();
                 const uint32_t sv = smem_u32(smem + SM_V + s * V_STAGE);
                 if (j < n_strip) {
@@ -314,6 +349,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 umma_commit(&pv_done[s]);
                 umma_commit(&v_empty[s]);
             }
+            if (bad) {
+                umma_commit(&drain[1]);
+                mbar_wait_bounded(&drain[1], 0);
+            }
         }
     } else if (warp < 4) {
         // ------------------------------- softmax ---------------------------------
@@ -324,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float m_run = -INFINITY, l_run = 0.0f;
         if (n_strip) {
             // tile 0, the sink strip: only sinks are visible (the window starts above it)
-            wait_or_flag(&s_full[0], 0, bad);
+            wait_or_flag(&s_full[0], 0, bad, abort);
             tc_fence_after_sync();
             uint32_t raw[kSinkStrip];
             tmem_ld_32x16(tmem + lane_base, raw);
@@ -356,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         for (int i = n_strip; i < tp.n; ++i) {
             const int s = i & 1;
-            wait_or_flag(&s_full[s], (i >> 1) & 1, bad);
+            wait_or_flag(&s_full[s], (i >> 1) & 1, bad, abort);
             tc_fence_after_sync();
             uint32_t raw[64];
             tmem_ld_32x32(tmem + lane_base + s * BN, raw);
@@ -396,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (m_run == -INFINITY) m_run = m_tile;
             if (__any_sync(0xffffffffu, grow)) {
                 // O += P_{i-1} V_{i-1} must be done before O is rescaled
-                wait_or_flag(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, bad);
+                wait_or_flag(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, bad, abort);
                 tc_fence_after_sync();
                 const float alpha = grow ? fast_exp2_approx(m_run - m_tile) : 1.0f;
 #pragma unroll 1
@@ -435,10 +474,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[s]);
+            if (lane == 0 && i != p.stall_tile) mbar_arrive(&p_full[s]);
         }
         // ---- epilogue: O / l -> bf16 rows ----
-        wait_or_flag(&pv_done[(tp.n - 1) & 1], ((tp.n - 1) >> 1) & 1, bad);
+        wait_or_flag(&pv_done[(tp.n - 1) & 1], ((tp.n - 1) >> 1) & 1, bad, abort);
         tc_fence_after_sync();
         float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
         if (p.sink_logits != nullptr) {
@@ -614,11 +653,11 @@ extern "C" size_t sk_prefill_workspace_bytes(int32_t batch, int32_t T, int32_t n
     return 2 * size_t(batch) * qpad * n_kv_heads * HD * sizeof(__nv_bfloat16);  // the prior's keys and values
 }
 
-extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
-                                          int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                          int64_t p0, int32_t sinks, int32_t window, const sk_kv_layer* prior,
-                                          const float* sink_logits, void* out, void* workspace, size_t ws_bytes,
-                                          uint32_t* err, void* stream) {
+// sk_prefill_attention with a stall tile for the self-test (-1: none).
+static sk_status prefill_launch(const void* q_rot, const void* k_rot, const void* v, int32_t batch, int32_t T,
+                                int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int64_t p0, int32_t sinks,
+                                int32_t window, const sk_kv_layer* prior, const float* sink_logits, void* out,
+                                void* workspace, size_t ws_bytes, uint32_t* err, void* stream, int stall_tile) {
     SK_RET_IF(batch < 1 || T < 0 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads != 0, SK_ERR_ARG);
     // T = 0 reads and writes nothing: the chunk, output and workspace pointers may be NULL
     SK_RET_IF(T > 0 && (q_rot == nullptr || k_rot == nullptr || v == nullptr || out == nullptr ||
@@ -738,8 +777,27 @@ extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, 
     p.qpb = qpb;
     p.nqb = (T + qpb - 1) / qpb;
     p.scale_log2 = 1.4426950408889634f / sqrtf(float(HD));
+    p.stall_tile = stall_tile;
     const int64_t grid = int64_t(p.nqb) * (n_q_heads / nh) * batch;
     prefill_attn_kernel<<<unsigned(grid), kThreads, SM_ALLOC, st>>>(mq, mk, mv, mkc, mvc, p);
     SK_CUDA_RET(cudaGetLastError());
     return SK_OK;
+}
+
+extern "C" sk_status sk_prefill_attention(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
+                                          int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                          int64_t p0, int32_t sinks, int32_t window, const sk_kv_layer* prior,
+                                          const float* sink_logits, void* out, void* workspace, size_t ws_bytes,
+                                          uint32_t* err, void* stream) {
+    return prefill_launch(q_rot, k_rot, v, batch, T, n_q_heads, n_kv_heads, head_dim, p0, sinks, window, prior,
+                          sink_logits, out, workspace, ws_bytes, err, stream, -1);
+}
+
+extern "C" sk_status sk_selftest_prefill_stall(const void* q_rot, const void* k_rot, const void* v, int32_t batch,
+                                               int32_t T, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                               void* out, void* workspace, size_t ws_bytes, int32_t stall_tile,
+                                               uint32_t* err, void* stream) {
+    SK_RET_IF(err == nullptr || stall_tile < 0, SK_ERR_ARG);
+    return prefill_launch(q_rot, k_rot, v, batch, T, n_q_heads, n_kv_heads, head_dim, 0, 0, 0, nullptr, nullptr,
+                          out, workspace, ws_bytes, err, stream, stall_tile);
 }

@@ -176,6 +176,20 @@ def test_prefill_workspace_and_prior_arguments_checked_on_host(lib):
     assert call(bad) == sk.SK_ERR_ARG                                     # batch differs
 
 
+def test_prefill_stall_selftest_arguments_checked_on_host(lib):
+    import sink_kv_attention_gb300 as sk
+    fake = 1 << 20  # aligned, never dereferenced: every case below fails before a launch
+
+    def call(stall=2, err=fake, T=256, D=128, ws=16):
+        return lib.sk_selftest_prefill_stall(fake, fake, fake, 1, T, 8, 2, D, fake, fake, ws, stall, err, None)
+
+    assert call(err=None) == sk.SK_ERR_ARG            # the error word is the test's result
+    assert call(stall=-1) == sk.SK_ERR_ARG            # -1 is the product call's "no stall"
+    assert call(D=64) == sk.SK_ERR_UNSUPPORTED        # the prefill's own checks apply
+    assert call(ws=0) == sk.SK_ERR_ARG
+    assert call(T=0) == sk.SK_OK                      # an empty chunk launches nothing
+
+
 def test_append_without_table_takes_no_q(lib):
     """sk_kv_append with no table appends rotated keys as given; a q would stay
     unrotated, so it is refused on the host (before any launch)."""

@@ -1,6 +1,8 @@
 """Failure detection on the GPU without a fault: an in-kernel wait that can never be
 satisfied gives up after its limit, reports SK_DEVERR_TIMEOUT through the device error
-word, and the context keeps working."""
+word, and the context keeps working.  The same for the prefill pipeline, whose softmax
+warps are told (by the self-test entry point) never to signal one tile's P: the blocks
+that reach it stop every role, drain what they issued and report."""
 import time
 
 import pytest
@@ -44,3 +46,44 @@ def test_unsatisfiable_wait_times_out_and_reports(sk):
 
 def test_selftest_argument_check(sk):
     assert sk._lib().sk_selftest_bounded_wait(None, None) == sk.SK_ERR_ARG
+
+
+def _chunk(T, seed):
+    from sink_kv_attention_gb300 import synth
+    q = synth.normal((1, T, 8, 128), seed, torch.bfloat16, device="cuda")
+    k = synth.normal((1, T, 2, 128), seed + 1, torch.bfloat16, device="cuda")
+    v = synth.normal((1, T, 2, 128), seed + 2, torch.bfloat16, device="cuda")
+    return q, k, v
+
+
+def test_prefill_stall_times_out_drains_and_reports(sk):
+    # T = 512, 4 q heads per block (32 queries), causal: blocks 4..15 of each head group
+    # visit 3 or more key tiles and stall at tile 2; blocks 0..3 finish normally
+    q, k, v = _chunk(512, 31)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    sk.selftest_prefill_stall(q, k, v, 2, err)
+    status, bits = sk.sync_check(err, clear=True)
+    elapsed = time.perf_counter() - t0
+    assert bits == sk.SK_DEVERR_TIMEOUT and status == sk.SK_ERR_CUDA
+    # every stalled block gives up after one wait's limit (the roles stop together),
+    # not after one limit per remaining wait
+    assert 0.9 < elapsed < 10.0
+    # the context is still usable and the kernel still right: a normal call afterwards
+    # equals a fresh one bit for bit and reports nothing
+    a = sk.prefill_attention(q, k, v, 0, 0, 0, err=err)
+    b = sk.prefill_attention(q, k, v, 0, 0, 0, err=err)
+    status, bits = sk.sync_check(err, clear=True)
+    assert status == sk.SK_OK and bits == 0
+    assert torch.equal(a, b) and torch.isfinite(a.float()).all()
+
+
+def test_prefill_stall_past_every_tile_changes_nothing(sk):
+    # a stall tile no block reaches: the pipeline runs as the product call does
+    q, k, v = _chunk(512, 37)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = sk.selftest_prefill_stall(q, k, v, 1 << 20, err)
+    want = sk.prefill_attention(q, k, v, 0, 0, 0, err=err)
+    status, bits = sk.sync_check(err, clear=True)
+    assert status == sk.SK_OK and bits == 0
+    assert torch.equal(got, want)
