@@ -61,10 +61,10 @@ NCU_TRAFFIC = {
                 "--steps 5 --warmup 3 (fused split kernel only)",
         sources=dict(DECODE_SOURCES, **{"decode_step.cu": "ccf687b9b226f8b64abc0f4dc079d32f1dbdcc27c072859308f1e00ad42dff18"})),
     "prefill_attn_t32768": dict(
-        bytes=633968896, scale=1,
+        bytes=633978880, scale=1,
         capture="ncu --set full -k regex:prefill_attn -s 2 -c 1, python bench.py --workload prefill "
                 "--steps 3 --warmup 2",
-        sources={"prefill.cu": "9294ab081a2fa50b9fabac10c006519ecf10f30f208a8104c9b4dea6bbaf8940",
+        sources={"prefill.cu": "bf63f0ca63cd9186c7cb6bee43620de94930b33e1d74b6e801213dd5b5d633b1",
                  "tcgen05.cuh": "351b9597267c8e6efeb86d6fc37090095dc2b99a351b47884061cba635ae854d"}),
     "rerotate_bf16_48l": dict(
         bytes=2358400000, scale=12,
