@@ -1637,13 +1637,116 @@ def _cpu_rerotate(kdt):
                       f"({total_rows} rows) extrapolated by the row count"}
 
 
+def _cpu_window_step():
+    """The decode step's arithmetic is the windowed line's (RoPE + append + attention):
+    single sequences of that workload, about 5 s of oracle time."""
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    secs, n = 0.0, 0
+    while secs < 5.0:
+        s_, _ = cpu_oracle_window(1, seed_base=0, first=n % c["B"])
+        secs, n = secs + s_, n + 1
+    kv = c["Hkv"] * (c["S"] + c["W"]) * c["D"] * 2 * 2
+    return {"value": round(n * kv / secs / 1e9, 4), "unit": "GB/s",
+            "ms_per_step": round(secs / n * c["B"] * 1e3, 1),
+            "sample": f"{n} single-sequence windowed decode steps ({secs:.2f} s); the {c['B']}-sequence step "
+                      "extrapolated by the sequence count"}
+
+
+def _cpu_window_i8():
+    """The windowed step over int8 keys: the cached codes dequantized (code x row
+    scale), the new key rotated and quantized by the int8 rule, then attention over the
+    dequantized keys; single sequences, about 5 s of oracle time."""
+    import numpy as np
+    from oracle.sinkkv_oracle import (RingCache, RopeSpec, decode_attention, dequantize_int8_rows,
+                                      quantize_int8_rows, rope_rotate)
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    B, Hq, Hkv, D, S, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    pos, head, count = synth.window_state(13, B, W, c["pos_lo"], c["pos_hi"])
+    om = RopeSpec(D, c["r"], c["theta"]).omega()
+    rng = np.random.default_rng(8)
+    secs, n = 0.0, 0
+    while secs < 5.0:
+        b = n % B
+        codes = rng.integers(-127, 128, (Hkv, S + W, D)).astype(np.int8)
+        scale = rng.uniform(0.5 / 127, 2.0 / 127, (Hkv, S + W))
+        vb = synth.normal((Hkv, S + W, D), 2000 + b, torch_dtype()).double().numpy()
+        q = synth.normal((1, Hq, D), 3000 + b, torch_dtype()).double().numpy()
+        k = synth.normal((1, Hkv, D), 4000 + b, torch_dtype()).double().numpy()
+        v = synth.normal((Hkv, D), 5000 + b, torch_dtype()).double().numpy()
+        t0 = time.perf_counter()
+        kb = dequantize_int8_rows(codes, scale)
+        ring = RingCache(S, W)
+        ring.pos, ring.head, ring.count = int(pos[b]), int(head[b]), int(count[b])
+        for s_ in range(S + W):
+            ring.slots[s_] = (kb[:, s_], vb[:, s_])
+        P = int(pos[b])
+        qr = rope_rotate(q, [P], om, 1.0, D)
+        kr = rope_rotate(k, [P], om, 1.0, D)
+        kc, ks = quantize_int8_rows(kr[0])
+        ring.append([(dequantize_int8_rows(kc, ks), v)])
+        decode_attention(ring, qr[0])
+        secs += time.perf_counter() - t0
+        n += 1
+    kv = Hkv * (S + W) * (D + 4 + 2 * D)  # codes + scale + bf16 V per row
+    return {"value": round(n * kv / secs / 1e9, 4), "unit": "GB/s", "ms_per_step": round(secs / n * B * 1e3, 1),
+            "sample": f"{n} single-sequence windowed decode steps over int8 keys ({secs:.2f} s); the "
+                      f"{B}-sequence step extrapolated by the sequence count"}
+
+
+def _cpu_paged():
+    """The windowed step over a paged cache (16-token blocks): the token's rotated key
+    and value written at its block and offset, then paged decode attention over the
+    sink block and the window's blocks (every other table entry -1); single sequences,
+    about 5 s of oracle time."""
+    import numpy as np
+    from oracle.sinkkv_oracle import RopeSpec, paged_decode_attention, rope_rotate
+    from sink_kv_attention_gb300 import synth
+    c = synth.WINDOW
+    B, Hq, Hkv, D, S, W = c["B"], c["Hq"], c["Hkv"], c["D"], c["S"], c["W"]
+    bs = 16
+    pos = synth.window_state(13, B, W, c["pos_lo"], c["pos_hi"])[0]
+    om = RopeSpec(D, c["r"], c["theta"]).omega()
+    rng = np.random.default_rng(9)
+    secs, n = 0.0, 0
+    while secs < 5.0:
+        b = n % B
+        P = int(pos[b])
+        first_win = P - W + 1   # the oldest recent key the new token's query sees
+        logical = sorted({0} | set(range(first_win // bs, P // bs + 1)))
+        perm = rng.permutation(len(logical))
+        table = np.full(P // bs + 1, -1, dtype=np.int64)
+        for j, lb in enumerate(logical):
+            table[lb] = perm[j]
+        kp = rng.standard_normal((len(logical), Hkv, bs, D))
+        vp = rng.standard_normal((len(logical), Hkv, bs, D))
+        q = synth.normal((1, Hq, D), 3000 + b, torch_dtype()).double().numpy()
+        k = synth.normal((1, Hkv, D), 4000 + b, torch_dtype()).double().numpy()
+        v = synth.normal((Hkv, D), 5000 + b, torch_dtype()).double().numpy()
+        t0 = time.perf_counter()
+        qr = rope_rotate(q, [P], om, 1.0, D)
+        kr = rope_rotate(k, [P], om, 1.0, D)
+        blk = int(table[P // bs])
+        kp[blk, :, P % bs] = kr[0]
+        vp[blk, :, P % bs] = v
+        paged_decode_attention(qr[0], kp, vp, table, P + 1, bs, S, W)
+        secs += time.perf_counter() - t0
+        n += 1
+    kv = Hkv * (S + W) * D * 2 * 2
+    return {"value": round(n * kv / secs / 1e9, 4), "unit": "GB/s", "ms_per_step": round(secs / n * B * 1e3, 1),
+            "sample": f"{n} single-sequence windowed decode steps over 16-token blocks ({secs:.2f} s); the "
+                      f"{B}-sequence step extrapolated by the sequence count"}
+
+
 def synth_cfg(name):
     from sink_kv_attention_gb300 import synth
     return getattr(synth, name)
 
 
 CPU_ROWS = {"tiny": _cpu_tiny, "window_b1": _cpu_window_b1, "hybrid": _cpu_hybrid, "prefill": _cpu_prefill,
-            "rerotate_bf16": lambda: _cpu_rerotate("bf16"), "rerotate_i8": lambda: _cpu_rerotate("i8")}
+            "rerotate_bf16": lambda: _cpu_rerotate("bf16"), "rerotate_i8": lambda: _cpu_rerotate("i8"),
+            "window_i8": _cpu_window_i8, "paged": _cpu_paged, "window_step": _cpu_window_step}
 
 
 def cpu_row(name):
@@ -1683,8 +1786,7 @@ def bench_rows(args):
     """Every other configuration of the path on this GPU, each with its roofline and
     its oracle baseline: the tiny case, single-stream decode, the hybrid 32-layer step,
     the prefill chunk and the two rerotations; then the windowed step over int8 keys,
-    over a paged cache and through sk_decode_step (the oracle's arithmetic there is the
-    windowed line's)."""
+    over a paged cache and through sk_decode_step."""
     import gc
     import torch
     rows = {}

@@ -86,3 +86,9 @@ def _brute_strips(T, S, W, n_rep, p0=0, qoff=0, BM=128, BN=64, strip=16):
 def test_prefill_sink_strips(T, S, W, n_rep, p0, qoff):
     assert (bench._prefill_tiles(T, S, W, n_rep, p0=p0, qoff=qoff, strips=True)[2]
             == _brute_strips(T, S, W, n_rep, p0=p0, qoff=qoff))
+
+
+def test_every_bench_row_times_the_oracle_beside_it():
+    """Each row of the default run carries an oracle baseline: a timed CPU function
+    exists for every row name."""
+    assert {name for name, _ in bench.ROWS} <= set(bench.CPU_ROWS)
