@@ -36,27 +36,27 @@ METRIC = "sink+window decode attn KV-read GB/s (frac of HBM peak), tokens/s, key
 # ran a smaller case of the same kernel; the traffic grows in proportion to the units
 # processed and is scaled by that factor to one launch of the full workload.
 DECODE_SOURCES = {"decode.cu": "e6c7c2686de1a89eeb4a8c18ed6f37b833011124de96333c41c2fea3ae08a2b3",
-                  "decode_kernels.cuh": "18965169977b75be84fd3daf73de539914faa0f9be20251324676c60ff76c4b5",
+                  "decode_kernels.cuh": "ca32eb46afc019674dcaf78784becae5d1234f61e3683aec9364237854cca0cf",
                   "rope_lane.cuh": "92cd7898465a1776e0e3f9e32707943dca4d074e80246d99524d949885102532",
                   "common.cuh": "b851c4f7d4f058ac8da61a6434a86b4bf5523a2512acac6795794a145dcd4fa0"}
 NCU_TRAFFIC = {
     "decode_window_b32": dict(
-        bytes=542700800, scale=1,
+        bytes=542240000, scale=1,
         capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --no-rows --no-cpu-baseline "
                 "--steps 5 --warmup 3 (split kernel only)",
         sources=DECODE_SOURCES),
     "decode_paged_window_b32_bs16": dict(
-        bytes=540964864, scale=1,
+        bytes=540921088, scale=1,
         capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload paged "
                 "--steps 5 --warmup 3 (split kernel only)",
         sources=DECODE_SOURCES),
     "decode_window_b32_int8": dict(
-        bytes=410752000, scale=1,
+        bytes=410360032, scale=1,
         capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload window_i8 "
                 "--steps 5 --warmup 3 (split kernel only)",
         sources=DECODE_SOURCES),
     "decode_step_window_b32": dict(
-        bytes=541921536, scale=1,
+        bytes=541355520, scale=1,
         capture="ncu --set full -k regex:decode_split -s 3 -c 1, python bench.py --workload window_step "
                 "--steps 5 --warmup 3 (fused split kernel only)",
         sources=dict(DECODE_SOURCES, **{"decode_step.cu": "ccf687b9b226f8b64abc0f4dc079d32f1dbdcc27c072859308f1e00ad42dff18"})),

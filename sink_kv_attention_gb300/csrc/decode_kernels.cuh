@@ -1048,20 +1048,33 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, NREP, KQ, PAGED, FUSED>::THREA
             for (int o = NREP; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
             const float m_new = fmaxf(m_run, tmax);
             const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-            const float alpha = fast_exp2_approx(m_run - m_use);
             const float pr = fast_exp2_approx(s - m_use);
+            // Lazy rescale (bf16 / fp32 keys, contiguous or paged, two-call path): the
+            // accumulators are rescaled only in tiles where some head's running max grew
+            // (warp-uniform); otherwise every head's factor would be exactly 1.  Measured:
+            // windowed step +1.1%, paged +3.2%; int8 keys -0.4% and the decode step -0.4%,
+            // which keep the rescale in every tile.
+            constexpr bool kLazy = !KQ && !FUSED;
+            const bool grew = kLazy ? __any_sync(kFull, m_new > m_run) : true;
+            if (grew) {
+                const float alpha = fast_exp2_approx(m_run - m_use);
+                l_run = fmaf(l_run, alpha, pr);
+                if (lane < NREP) ps[C::RPW * NREP + lane] = make_float2(alpha, alpha);  // lane h: head h
+            } else {
+                l_run += pr;
+            }
             m_run = m_new;
-            l_run = fmaf(l_run, alpha, pr);
             ps[my_row * NREP + my_h] = make_float2(pr, pr);
-            if (lane < NREP) ps[C::RPW * NREP + lane] = make_float2(alpha, alpha);  // lane h: head h
             __syncwarp();
 
             // ---- PV ----
+            if (grew) {
 #pragma unroll
-            for (int h = 0; h < NREP; ++h) {
-                const float2 a2 = ps[C::RPW * NREP + h];
+                for (int h = 0; h < NREP; ++h) {
+                    const float2 a2 = ps[C::RPW * NREP + h];
 #pragma unroll
-                for (int d = 0; d < C::DPV / 2; ++d) acc[h][d] = __fmul2_rn(acc[h][d], a2);
+                    for (int d = 0; d < C::DPV / 2; ++d) acc[h][d] = __fmul2_rn(acc[h][d], a2);
+                }
             }
             if (nw == C::RPW) {
 #pragma unroll
