@@ -1116,6 +1116,7 @@ def bench_prefill(args):
             "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": steps, "warmup": warm,
             "ms_per_step": round(ms_attn, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "prefill chunk: B=1, T=32768, H_q=32, H_kv=8, d_h=128, S=4, W=4092",
+                       "l2": "inputs larger than L2 (Q, K, V 403 MB per call)",
                        "visited_tiles_per_head_group": tiles, "sink_strips_per_head_group": strips,
                        "heads_per_cta": nh,
                        "tile": f"128 rows ({nh} heads x {128 // nh} queries) x 64 keys",
@@ -1148,16 +1149,21 @@ def bench_prefill_chunk(args):
     layer.pos.fill_(p0)
     layer.count.fill_(W)
     layer.head.fill_(1234)
-    q = synth.normal((B, T, Hq, D), 68, torch.bfloat16, device="cuda")
-    k = synth.normal((B, T, Hkv, D), 69, torch.bfloat16, device="cuda")
-    v = synth.normal((B, T, Hkv, D), 70, torch.bfloat16, device="cuda")
-    out = torch.empty_like(q)
+    # three sets of chunk inputs and outputs in rotation (168 MB each): a call's inputs
+    # have left L2 by the time they come round again
+    n_sets = 3
+    qs = [synth.normal((B, T, Hq, D), 68 + 10 * j, torch.bfloat16, device="cuda") for j in range(n_sets)]
+    ks = [synth.normal((B, T, Hkv, D), 69 + 10 * j, torch.bfloat16, device="cuda") for j in range(n_sets)]
+    vs = [synth.normal((B, T, Hkv, D), 70 + 10 * j, torch.bfloat16, device="cuda") for j in range(n_sets)]
+    outs = [torch.empty_like(qs[0]) for _ in range(n_sets)]
     qoff = sk.prefill_prior_keys(p0, S, W)
     ws = torch.empty(sk.prefill_workspace_bytes(B, T, Hkv, D, qoff), dtype=torch.uint8, device="cuda")
     zl = _learned_sinks(args, Hq)
 
     def attend(i):
-        sk.prefill_attention(q, k, v, p0, S, W, out=out, workspace=ws, err=layer.err, sink_logits=zl, prior=layer)
+        j = i % n_sets
+        sk.prefill_attention(qs[j], ks[j], vs[j], p0, S, W, out=outs[j], workspace=ws, err=layer.err,
+                             sink_logits=zl, prior=layer)
 
     ms, clk, rec = _timed(attend, args.steps, args.warmup)
     assert layer.error_bits() == 0
@@ -1173,6 +1179,7 @@ def bench_prefill_chunk(args):
             "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "prompt chunk over a prior ring: B=1, T=8192 at p0=32768, H_q=32, H_kv=8, "
                                    "d_h=128, S=4, W=4092 (ring full, wrapped)",
+                       "l2": "inputs larger than L2: three sets of q, k, v and out (168 MB each) in rotation",
                        "prior_keys": qoff, "visited_tiles_per_head_group": tiles, "heads_per_cta": nh,
                        "learned_sink_logits": bool(args.learned_sink)},
             "frac_of_bf16_peak": round(tf / bf16_peak, 4),
@@ -1221,29 +1228,60 @@ def bench_tiny(args):
         step(t)
     torch.cuda.synchronize()
     empty()
-    g = _capture(step, 0, T)
+
+    # Each timed step starts with L2 flushed: a 512 MB buffer rewritten (longer than the host needs
+    # to queue the step behind it, so the step's launches run back to back) precedes the
+    # step, outside its events; the ring is emptied after every T steps, also outside.
+    flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device="cuda")
+
+    def flushed(fn, n_iter):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_iter)]
+        for it in range(n_iter):
+            if it % T == 0:
+                empty()
+            flush.add_(1.0)
+            ev[it][0].record()
+            fn(it % T)
+            ev[it][1].record()
+        torch.cuda.synchronize()
+        empty()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    flushed(step, 2 * T)  # warm-up
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     clocks.start()
     time.sleep(0.3)
-    per, total, R = _replays(g, T, TARGET_MS / 3, reset=empty, clocks=clocks)
+    t0 = time.perf_counter()
+    clocks.mark("start")
+    per = flushed(step, 120 * T)  # synchronizes before it returns
+    clocks.mark("end")
+    wall = time.perf_counter() - t0
     clocks.stop()
     assert layer.error_bits() == 0
     us = statistics.median(per) * 1e3
-    g2 = _capture(step_two_calls, 0, T)
-    per2, _, _ = _replays(g2, T, TARGET_MS / 6, reset=empty)
+    per2 = flushed(step_two_calls, 30 * T)
+    assert layer.error_bits() == 0
+    # beside it: the same steps back to back in one captured graph, L2 warm
+    g = _capture(step, 0, T)
+    per_w, _, _ = _replays(g, T, TARGET_MS / 6, reset=empty)
     assert layer.error_bits() == 0
     return {"metric": "tiny case: microseconds per decode step (RoPE + append + attention of one token)",
             "value": round(us, 3), "unit": "us/step", "higher_is_better": False, "dtype": "f32",
             "config": {"workload": "tiny: 1 sequence, H_q=8, H_kv=4, d_h=r=64, theta=1e4, fp32, C=6, S=2, "
-                                   "10 tokens one at a time"},
+                                   "10 tokens one at a time",
+                       "l2": "flushed before every timed step (a 512 MB buffer rewritten between steps, outside "
+                             "the events)"},
             "roofline": {"bound": "latency", "achieved": round(us, 3), "unit": "us/step", "peak": None,
                          "frac": None, "kernel": "split (with the token's RoPE + append) + combine per token "
                                                  "(2 launches)",
                          "note": "a parity case: 3 KB of cache, far from any throughput roofline"},
-            "timing": {"replays": R, "steps_per_replay": T, "timed_ms": round(total, 2)},
+            "timing": {"steps_timed": len(per), "us_per_step": "median of per-step CUDA events",
+                       "us_per_step_min": round(min(per) * 1e3, 3), "wall_s": round(wall, 2)},
             "two_calls": {"us_per_step": round(statistics.median(per2) * 1e3, 3),
                           "calls": "sk_kv_append + sk_decode_attention, three launches per token"},
-            "gpu_launches": 2 * T * R, "clocks": clocks.summary()}
+            "warm_graph": {"us_per_step": round(statistics.median(per_w) * 1e3, 3),
+                           "how": "the 10 steps back to back in one captured graph, replayed, L2 warm"},
+            "gpu_launches": 2 * len(per), "clocks": clocks.summary()}
 
 
 def bench_window_step(args):
