@@ -1675,13 +1675,16 @@ def _cpu_rerotate(kdt):
                       f"({total_rows} rows) extrapolated by the row count"}
 
 
+CPU_ROW_SECS = 5.0  # oracle time of the single-sequence samples below
+
+
 def _cpu_window_step():
     """The decode step's arithmetic is the windowed line's (RoPE + append + attention):
     single sequences of that workload, about 5 s of oracle time."""
     from sink_kv_attention_gb300 import synth
     c = synth.WINDOW
     secs, n = 0.0, 0
-    while secs < 5.0:
+    while n == 0 or secs < CPU_ROW_SECS:
         s_, _ = cpu_oracle_window(1, seed_base=0, first=n % c["B"])
         secs, n = secs + s_, n + 1
     kv = c["Hkv"] * (c["S"] + c["W"]) * c["D"] * 2 * 2
@@ -1705,7 +1708,7 @@ def _cpu_window_i8():
     om = RopeSpec(D, c["r"], c["theta"]).omega()
     rng = np.random.default_rng(8)
     secs, n = 0.0, 0
-    while secs < 5.0:
+    while n == 0 or secs < CPU_ROW_SECS:
         b = n % B
         codes = rng.integers(-127, 128, (Hkv, S + W, D)).astype(np.int8)
         scale = rng.uniform(0.5 / 127, 2.0 / 127, (Hkv, S + W))
@@ -1748,7 +1751,7 @@ def _cpu_paged():
     om = RopeSpec(D, c["r"], c["theta"]).omega()
     rng = np.random.default_rng(9)
     secs, n = 0.0, 0
-    while secs < 5.0:
+    while n == 0 or secs < CPU_ROW_SECS:
         b = n % B
         P = int(pos[b])
         first_win = P - W + 1   # the oldest recent key the new token's query sees

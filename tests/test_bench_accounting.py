@@ -92,3 +92,12 @@ def test_every_bench_row_times_the_oracle_beside_it():
     """Each row of the default run carries an oracle baseline: a timed CPU function
     exists for every row name."""
     assert {name for name, _ in bench.ROWS} <= set(bench.CPU_ROWS)
+
+
+@pytest.mark.parametrize("row", ["window_step", "window_i8", "paged"])
+def test_single_sequence_oracle_baselines_run(row, monkeypatch):
+    """The oracle baselines of the decode-step, int8-key and paged rows run on the host
+    and report the row's unit (a minimal sample)."""
+    monkeypatch.setattr(bench, "CPU_ROW_SECS", 0.0)
+    r = bench.CPU_ROWS[row]()
+    assert r["unit"] == "GB/s" and r["value"] > 0 and "extrapolated" in r["sample"]
